@@ -1,0 +1,266 @@
+/*
+ * libditstream — bounded-activation forward pass of one video-DiT block on
+ * NVIDIA GB300 (sm_103a).  Plain C ABI: device pointers, sizes and a CUDA
+ * stream handle; no C++ or framework types cross this boundary.
+ *
+ * The method.  "LayerStream: H3 Chunking" (section "How the slicing works"):
+ * norm, modulation, the projections and the MLP are token-wise and run on
+ * token slices that add into the residual stream in place; attention runs in
+ * two passes — pass one keeps only K and V for all tokens, pass two
+ * recomputes the queries of one slice, attends them to the full K/V,
+ * projects and adds into the residual.  "Proposal: Generic memory-aware
+ * streaming execution for transformer models" (section "MLP planning"): a
+ * gated MLP may also be cut along its FFN feature axis, each slice passing
+ * through the matching slice of the down projection and accumulating into
+ * the output.  Section "The two numbers you set" of the first page defines
+ * the two knobs: mlp_chunk_tokens and attn_chunk_tokens (0 = unchunked
+ * attention).
+ *
+ * What one block computes (all matrices row-major, weights [out, in]):
+ *   a  = LN(x) * (1 + scale1) + shift1                     -> bf16
+ *   K, V = a Wk^T, a Wv^T   (all tokens, kept)             -> bf16
+ *   Q_s  = a_s Wq^T         (per attention slab s)         -> bf16
+ *   O_s  = softmax(Q_s K^T / sqrt(d)) V   per head         -> bf16
+ *   x_s += gate1 * (O_s Wo^T)                              (fp32, in place)
+ *   b  = LN(x) * (1 + scale2) + shift2  (per MLP chunk)    -> bf16
+ *   h_f = silu(b Wg_f^T) * (b Wu_f^T)   (per FFN slice f)  -> bf16
+ *   x_c += gate2 * sum_f h_f Wd[:, f]^T                    (fp32, in place)
+ * LN is LayerNorm over D, biased variance, eps 1e-6, no affine.
+ * modulation is float [6, D] with rows shift1, scale1, gate1, shift2,
+ * scale2, gate2.  Accumulation is fp32 throughout.
+ *
+ * Exactness.  Every kernel computes a token's row with the same operations
+ * in the same order whatever the chunk sizes, so the output is bit-identical
+ * for every (mlp_chunk_tokens, attn_chunk_tokens) and every ffn_slice.
+ *
+ * Errors.  No function aborts, traps or prints.  Host-side checks return a
+ * negative dit_status_t without launching anything.  Device waits are
+ * bounded: a wait that runs out records DIT_ERR_TIMEOUT in the plan's device
+ * status word and the kernel returns; dit_block_sync_status() reports it.
+ *
+ * Threading.  A plan is not re-entrant: one forward at a time per plan (it
+ * owns one workspace).  Different plans may run concurrently on different
+ * streams.
+ */
+#ifndef DITSTREAM_H
+#define DITSTREAM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define DITSTREAM_ABI_VERSION 1
+
+#if defined(__GNUC__)
+#define DIT_API __attribute__((visibility("default")))
+#else
+#define DIT_API
+#endif
+
+typedef int dit_status_t;
+
+#define DIT_OK 0
+#define DIT_ERR_INVALID_ARG (-1)        /* bad size, NULL pointer, bad mode */
+#define DIT_ERR_CHUNK_ALIGN (-2)        /* chunk not 0 and not a multiple of 128 */
+#define DIT_ERR_ALIGN (-3)              /* device pointer not 16-byte aligned */
+#define DIT_ERR_NO_WORKSPACE (-4)       /* forward before bind_workspace */
+#define DIT_ERR_WORKSPACE_TOO_SMALL (-5)
+#define DIT_ERR_CUDA (-6)               /* launch / runtime error: see dit_last_cuda_error() */
+#define DIT_ERR_TIMEOUT (-7)            /* a bounded device wait ran out */
+#define DIT_ERR_UNSUPPORTED_ARCH (-8)   /* current device is not sm_103 */
+
+/* CUDA stream handle (a cudaStream_t); NULL = the legacy default stream. */
+typedef void *dit_stream_t;
+
+/* Weight element types. */
+#define DIT_W_BF16 0
+#define DIT_W_INT8 1
+
+/* One block's weights: borrowed, read-only device pointers, row-major
+ * [out, in] (the nn.Linear.weight layout), 16-byte aligned.
+ *   wqkv  [3D, D]  rows 0..D-1 = Wq, D..2D-1 = Wk, 2D..3D-1 = Wv;
+ *                  head h owns rows h*d .. h*d+d-1 of each third
+ *   wo    [D, D]
+ *   wgate [F, D]   (SwiGLU gate projection: silu is applied to it)
+ *   wup   [F, D]
+ *   wdown [D, F]
+ * dtype DIT_W_BF16: bf16 elements.  dtype DIT_W_INT8: int8 elements q and
+ * one fp32 scale per output row in the matching *_scale pointer; the weight
+ * is W[r, :] = scale[r] * q[r, :] ("MiniMax-H3-Comfy-NPU", section 2.2: one
+ * weight_scale per output row, sliced with the rows).  Scales are ignored
+ * for bf16. */
+typedef struct {
+    int dtype;
+    const void *wqkv;
+    const void *wo;
+    const void *wgate;
+    const void *wup;
+    const void *wdown;
+    const float *wqkv_scale;
+    const float *wo_scale;
+    const float *wgate_scale;
+    const float *wup_scale;
+    const float *wdown_scale;
+} dit_block_weights_t;
+
+typedef struct dit_plan dit_plan_t;
+
+/* Plan one block: T tokens, hidden D, `heads` heads of d = D/heads, SwiGLU
+ * width ffn.  Pure host work; allocates no device memory.
+ *   T >= 1; D % 128 == 0; d in {64, 128}; ffn % 64 == 0 and ffn >= 64.
+ *   mlp_chunk_tokens, attn_chunk_tokens: 0 (one slab of all T tokens) or a
+ *   multiple of 128; values >= T are clamped to T ("The two numbers you set":
+ *   attn_chunk_tokens = 0 turns the two-pass slicing off; the MLP half is
+ *   still chunked by mlp_chunk_tokens).
+ * The FFN is not feature-sliced (slice width = ffn); see dit_block_plan_ex.
+ * No CUDA call is made here (the device is checked when a workspace is
+ * bound).  On success *out receives a plan owned by the caller
+ * (dit_block_plan_destroy).  Errors: DIT_ERR_INVALID_ARG,
+ * DIT_ERR_CHUNK_ALIGN. */
+DIT_API dit_status_t dit_block_plan(int64_t T, int D, int heads, int ffn,
+                            int mlp_chunk_tokens, int attn_chunk_tokens,
+                            dit_plan_t **out);
+
+/* As dit_block_plan, plus ffn_slice: 0 (= ffn) or a multiple of 64 that is
+ * <= ffn — the FFN feature-slice width ("MLP planning").  With a slice width
+ * below ffn the down projection's fp32 accumulator is carried across slices
+ * in the workspace, so the result stays bit-identical to ffn_slice = ffn. */
+DIT_API dit_status_t dit_block_plan_ex(int64_t T, int D, int heads, int ffn,
+                               int mlp_chunk_tokens, int attn_chunk_tokens,
+                               int ffn_slice, dit_plan_t **out);
+
+DIT_API void dit_block_plan_destroy(dit_plan_t *plan);
+
+/* Effective sizes of a plan after clamping: fills any non-NULL pointer. */
+DIT_API dit_status_t dit_block_plan_info(const dit_plan_t *plan, int64_t *T, int *D,
+                                 int *heads, int *ffn, int *mlp_chunk,
+                                 int *attn_chunk, int *ffn_slice);
+
+/* Exact device workspace bytes the plan needs:
+ *   256 (status words) + K [T, D] bf16 + V^T [D, roundup(T, 128)] bf16
+ *   + max(attention phase 4 * C_a * D,
+ *         MLP phase 2 * C_m * D + 2 * C_m * F_s + (F_s < F ? 4 * C_m * D : 0))
+ * each region rounded up to 1 KiB.  K/V for all tokens is the floor that
+ * grows with T ("Where people get burned": K and V of the whole sequence
+ * stay resident); everything else is bounded by the chunk sizes. */
+DIT_API size_t dit_block_workspace_bytes(const dit_plan_t *plan);
+
+/* Bind caller-owned device memory (>= dit_block_workspace_bytes, 256-byte
+ * aligned) as the plan's workspace and clear its status words.  The current
+ * device must be of compute capability 10.3.  The library never allocates
+ * device memory itself.  Errors: DIT_ERR_INVALID_ARG, DIT_ERR_ALIGN,
+ * DIT_ERR_WORKSPACE_TOO_SMALL, DIT_ERR_UNSUPPORTED_ARCH, DIT_ERR_CUDA. */
+DIT_API dit_status_t dit_block_bind_workspace(dit_plan_t *plan, void *dev_ptr,
+                                      size_t bytes);
+
+/* One block forward, in place on x [T, D] fp32 (device, caller-owned,
+ * 16-byte aligned).  modulation: device float [6, D].  Asynchronous on
+ * `stream`; returns the launch-time status.  Device-side errors are read by
+ * dit_block_sync_status().  Errors: DIT_ERR_INVALID_ARG, DIT_ERR_ALIGN,
+ * DIT_ERR_NO_WORKSPACE, DIT_ERR_CUDA. */
+DIT_API dit_status_t dit_block_forward(const dit_plan_t *plan, float *x,
+                               const dit_block_weights_t *w,
+                               const float *modulation, dit_stream_t stream);
+
+/* Synchronise `stream`, read and clear the plan's device status word.
+ * Returns DIT_OK, DIT_ERR_TIMEOUT or DIT_ERR_CUDA. */
+DIT_API dit_status_t dit_block_sync_status(const dit_plan_t *plan, dit_stream_t stream);
+
+/* Final layer (output head), fp32 arithmetic, unsliced:
+ *   out[t, :] = (LN(x[t]) * (1 + scale_f) + shift_f) W_f^T
+ * x [T, D] fp32; mod_f [2, D] fp32 (shift_f, scale_f); W_f [64, D] fp32 when
+ * wf_scale == NULL, else int8 with fp32 scales [64]; out [T, 64] fp32.
+ * "LayerStream: H3 Chunking" ("How the slicing works"): the fp32 output head
+ * runs stock.  Uses the plan's T and D only; needs no workspace. */
+DIT_API dit_status_t dit_final_forward(const dit_plan_t *plan, const float *x,
+                               const void *wf, const float *wf_scale,
+                               const float *mod_f, float *out,
+                               dit_stream_t stream);
+
+DIT_API const char *dit_status_string(dit_status_t s);
+/* Text of the last CUDA error seen by this thread's calls ("" if none). */
+DIT_API const char *dit_last_cuda_error(void);
+DIT_API int dit_abi_version(void);
+
+/* ----------------------------------------------------------------------
+ * Stage entry points: the individual kernels of the block, for per-stage
+ * checks.  Same conventions as above.  `dev_status` is an optional device
+ * int (NULL allowed) that receives DIT_ERR_TIMEOUT if a bounded wait ran
+ * out.  bf16 data is passed as raw 16-bit patterns (void *).
+ * ---------------------------------------------------------------------- */
+
+/* Norm + modulation + cast ("How the slicing works": norms and modulation
+ * are token-wise).  out[r, c] = bf16_rne((x[r,c] - mu_r) * rsqrt(var_r +
+ * 1e-6) * (1 + scale[c]) + shift[c]) for r < rows; x fp32 [rows, D] row-major;
+ * out bf16 [rows, D].  D % 128 == 0. */
+DIT_API dit_status_t dit_modln_cast(const float *x, int64_t rows, int D,
+                            const float *shift, const float *scale,
+                            void *out_bf16, dit_stream_t stream);
+
+/* Epilogues of the tensor-core GEMM  acc[M, N] = A[M, K] B[N, K]^T
+ * (A bf16, B bf16 or int8 with per-row fp32 scale applied to acc). */
+#define DIT_EPI_STORE_BF16 0  /* out bf16 [M, N], row stride ldo             */
+#define DIT_EPI_STORE_F32 1   /* out fp32 [M, N], row stride ldo             */
+#define DIT_EPI_KV 2          /* n < split_n: out (K) bf16 [row_offset+m, n],
+                                 stride ldo; n >= split_n: out2 (V^T) bf16
+                                 [n - split_n, row_offset + m], stride ldo2 */
+#define DIT_EPI_RESID 3       /* x[m, n] += gate[n] * acc  (fp32, stride ldx) */
+#define DIT_EPI_SWIGLU 4      /* two B operands b0 (gate) and b1 (up), each
+                                 [N, K]: out bf16 [m, n] = silu(acc0) * acc1 */
+#define DIT_EPI_DOWN 5        /* accumulate over FFN slices: if acc_load the
+                                 fp32 accumulator starts from acc[m, n], else
+                                 from 0; if acc_final x[m, n] += gate[n]*acc,
+                                 else acc[m, n] = acc (fp32, stride ldacc)    */
+
+typedef struct {
+    int mode;               /* DIT_EPI_* */
+    int64_t M;              /* rows of A (tokens) */
+    int N;                  /* output columns, N % 32 == 0 */
+    int K;                  /* contraction, K % 64 == 0 */
+    const void *a;          /* bf16 [M, K], row stride lda elements */
+    int64_t lda;
+    const void *b0;         /* [N, K], row stride ldb elements */
+    const void *b1;         /* second B (SWIGLU only) */
+    int64_t ldb;
+    int b_dtype;            /* DIT_W_BF16 or DIT_W_INT8 */
+    const float *b0_scale;  /* per-row scales [N] (int8 only) */
+    const float *b1_scale;
+    void *out;              /* STORE_*, KV (K), SWIGLU */
+    int64_t ldo;
+    void *out2;             /* KV: V^T */
+    int64_t ldo2;
+    int64_t row_offset;     /* KV: token index of A's row 0 */
+    int split_n;            /* KV: first V column */
+    float *x;               /* RESID, DOWN */
+    int64_t ldx;
+    const float *gate;      /* RESID, DOWN: [N] */
+    float *acc;             /* DOWN: fp32 carry [M, N] */
+    int64_t ldacc;
+    int acc_load;
+    int acc_final;
+} dit_gemm_args_t;
+
+DIT_API dit_status_t dit_gemm(const dit_gemm_args_t *args, int *dev_status,
+                      dit_stream_t stream);
+
+/* Non-causal multi-head attention of Tq queries against T keys:
+ *   o[i, h*d:(h+1)*d] = softmax(q_h[i] . k_h^T / sqrt(d)) v_h
+ * q bf16 [Tq, H*d] (stride ldq), k bf16 [T, H*d] (stride ldk), V given
+ * transposed: vt bf16 [H*d, ldvt] with vt[c, j] = V[j, c] (ldvt >= T,
+ * ldvt % 8 == 0), o bf16 [Tq, H*d] (stride ldo).  head_dim in {64, 128}.
+ * The key loop visits key tiles in one fixed order, so a query row's result
+ * does not depend on Tq or on the other queries. */
+DIT_API dit_status_t dit_attention(const void *q, int64_t Tq, int64_t ldq,
+                           const void *k, int64_t ldk, const void *vt,
+                           int64_t ldvt, int64_t T, int heads, int head_dim,
+                           void *o, int64_t ldo, int *dev_status,
+                           dit_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DITSTREAM_H */

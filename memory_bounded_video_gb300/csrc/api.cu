@@ -1,0 +1,397 @@
+// libditstream C ABI: plans, workspace layout, the bounded block schedule
+// and the stage entry points.  Host code only; kernels live in modln.cu,
+// gemm.cu, attention.cu and final.cu.
+//
+// Block schedule ("LayerStream: H3 Chunking", "How the slicing works";
+// "Proposal: Generic memory-aware streaming execution for transformer
+// models", attention streaming plan and "MLP planning"), all on one stream:
+//   pass 1, per attention slab s:  modln(x_s; shift1, scale1) -> a_s
+//                                  [K | V^T] rows s  = a_s Wkv^T       (KV)
+//   pass 2, per attention slab s:  modln(x_s; shift1, scale1) -> a_s
+//                                  Q_s = a_s Wq^T                     (STORE)
+//                                  O_s = attention(Q_s, K, V)
+//                                  x_s += gate1 * O_s Wo^T            (RESID)
+//   MLP, per token chunk c:        modln(x_c; shift2, scale2) -> b_c
+//     per FFN slice f:             h_f = silu(b_c Wg_f^T) * b_c Wu_f^T (SWIGLU)
+//                                  acc (+)= h_f Wd_f^T; on the last slice
+//                                  x_c += gate2 * acc                  (DOWN)
+// Pass 2 reads x_s before writing it, and K/V come from pass 1, so every
+// query attends to the pre-attention keys and values of all tokens.
+#include <cstdio>
+#include <cstring>
+#include <new>
+
+#include "internal.h"
+
+struct dit_plan {
+    int64_t T;
+    int D, heads, head_dim, F;
+    int cm, ca, fs;  // effective mlp chunk, attention chunk, FFN slice
+    int64_t t_pad;   // row stride of V^T
+    // workspace layout (byte offsets)
+    size_t off_k, off_vt, off_a, off_q, off_b, off_h, off_acc, total;
+    uint8_t *ws;
+    size_t ws_bytes;
+};
+
+namespace ds {
+
+namespace {
+thread_local char g_err[256] = "";
+
+size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// Signature of the driver's cuTensorMapEncodeTiled (fetched at run time so
+// the library needs no link-time dependency on libcuda).
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+
+bool load_encode() {
+    if (g_encode) return true;
+    void *fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !fn)
+        return false;
+    g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+    return true;
+}
+
+bool modln_supports(int D) {
+    if (D <= 0 || D % 128) return false;
+    switch (D / 128) {
+        case 1: case 2: case 3: case 4: case 5: case 6: case 8: case 10: case 12:
+        case 16: case 20: case 24: case 32:
+            return true;
+        default:
+            return false;
+    }
+}
+
+}  // namespace
+
+dit_status_t cuda_fail(cudaError_t e) {
+    snprintf(g_err, sizeof(g_err), "%s: %s", cudaGetErrorName(e), cudaGetErrorString(e));
+    return DIT_ERR_CUDA;
+}
+
+dit_status_t check_launch() {
+    const cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? DIT_OK : cuda_fail(e);
+}
+
+int sm_count() {
+    static int cache[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+    if (!cache[dev]) {
+        int n = 0;
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        cache[dev] = n > 0 ? n : 148;
+    }
+    return cache[dev];
+}
+
+bool make_tmap_2d(CUtensorMap *m, CUtensorMapDataType dt, const void *base, uint64_t inner,
+                  uint64_t outer, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer) {
+    if (!load_encode()) return false;
+    if (inner == 0 || outer == 0 || row_bytes % 16 || !aligned16(base)) return false;
+    const cuuint64_t dims[2] = {inner, outer};
+    const cuuint64_t strides[1] = {row_bytes};
+    const cuuint32_t box[2] = {box_inner, box_outer};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = g_encode(m, dt, 2, const_cast<void *>(base), dims, strides, box, estr,
+                                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+}  // namespace ds
+
+using namespace ds;
+
+extern "C" {
+
+int dit_abi_version(void) { return DITSTREAM_ABI_VERSION; }
+
+const char *dit_last_cuda_error(void) { return g_err; }
+
+const char *dit_status_string(dit_status_t s) {
+    switch (s) {
+        case DIT_OK: return "ok";
+        case DIT_ERR_INVALID_ARG: return "invalid argument";
+        case DIT_ERR_CHUNK_ALIGN: return "chunk size must be 0 or a multiple of 128";
+        case DIT_ERR_ALIGN: return "device pointer not 16-byte aligned";
+        case DIT_ERR_NO_WORKSPACE: return "no workspace bound to the plan";
+        case DIT_ERR_WORKSPACE_TOO_SMALL: return "workspace smaller than dit_block_workspace_bytes";
+        case DIT_ERR_CUDA: return "CUDA error";
+        case DIT_ERR_TIMEOUT: return "a bounded device wait timed out";
+        case DIT_ERR_UNSUPPORTED_ARCH: return "device is not sm_103";
+        default: return "unknown status";
+    }
+}
+
+dit_status_t dit_block_plan_ex(int64_t T, int D, int heads, int ffn, int mlp_chunk_tokens,
+                               int attn_chunk_tokens, int ffn_slice, dit_plan_t **out) {
+    if (!out) return DIT_ERR_INVALID_ARG;
+    *out = nullptr;
+    if (T <= 0 || T > (int64_t(1) << 30) || heads <= 0 || D <= 0 || D % heads ||
+        !modln_supports(D))
+        return DIT_ERR_INVALID_ARG;
+    const int hd = D / heads;
+    if (hd != 64 && hd != 128) return DIT_ERR_INVALID_ARG;
+    if (ffn < 64 || ffn % 64) return DIT_ERR_INVALID_ARG;
+    if (mlp_chunk_tokens < 0 || attn_chunk_tokens < 0 || ffn_slice < 0)
+        return DIT_ERR_INVALID_ARG;
+    if (mlp_chunk_tokens % 128 || attn_chunk_tokens % 128) return DIT_ERR_CHUNK_ALIGN;
+    if (ffn_slice % 64 || ffn_slice > ffn) return DIT_ERR_INVALID_ARG;
+
+    dit_plan *p = new (std::nothrow) dit_plan();
+    if (!p) return DIT_ERR_INVALID_ARG;
+    p->T = T;
+    p->D = D;
+    p->heads = heads;
+    p->head_dim = hd;
+    p->F = ffn;
+    auto clamp = [&](int c) -> int { return (c == 0 || c >= T) ? int(T) : c; };
+    p->cm = clamp(mlp_chunk_tokens);
+    p->ca = clamp(attn_chunk_tokens);
+    p->fs = ffn_slice == 0 ? ffn : ffn_slice;
+    p->t_pad = int64_t(round_up(size_t(T), 128));
+    const size_t A = 1024;
+    const size_t Dz = size_t(D);
+    p->off_k = A;  // [0, 256): device status words
+    p->off_vt = round_up(p->off_k + 2 * size_t(T) * Dz, A);
+    const size_t phase = round_up(p->off_vt + 2 * Dz * size_t(p->t_pad), A);
+    // attention phase: a_s / O_s share one region (a_s is dead once Q_s exists)
+    p->off_a = phase;
+    p->off_q = round_up(p->off_a + 2 * size_t(p->ca) * Dz, A);
+    const size_t attn_end = round_up(p->off_q + 2 * size_t(p->ca) * Dz, A);
+    // MLP phase (aliases the attention phase: the two never overlap in time)
+    p->off_b = phase;
+    p->off_h = round_up(p->off_b + 2 * size_t(p->cm) * Dz, A);
+    p->off_acc = round_up(p->off_h + 2 * size_t(p->cm) * size_t(p->fs), A);
+    size_t mlp_end = p->off_acc;
+    if (p->fs < p->F) mlp_end = round_up(p->off_acc + 4 * size_t(p->cm) * Dz, A);
+    p->total = attn_end > mlp_end ? attn_end : mlp_end;
+    p->ws = nullptr;
+    p->ws_bytes = 0;
+    *out = p;
+    return DIT_OK;
+}
+
+dit_status_t dit_block_plan(int64_t T, int D, int heads, int ffn, int mlp_chunk_tokens,
+                            int attn_chunk_tokens, dit_plan_t **out) {
+    return dit_block_plan_ex(T, D, heads, ffn, mlp_chunk_tokens, attn_chunk_tokens, 0, out);
+}
+
+void dit_block_plan_destroy(dit_plan_t *plan) { delete plan; }
+
+dit_status_t dit_block_plan_info(const dit_plan_t *p, int64_t *T, int *D, int *heads, int *ffn,
+                                 int *mlp_chunk, int *attn_chunk, int *ffn_slice) {
+    if (!p) return DIT_ERR_INVALID_ARG;
+    if (T) *T = p->T;
+    if (D) *D = p->D;
+    if (heads) *heads = p->heads;
+    if (ffn) *ffn = p->F;
+    if (mlp_chunk) *mlp_chunk = p->cm;
+    if (attn_chunk) *attn_chunk = p->ca;
+    if (ffn_slice) *ffn_slice = p->fs;
+    return DIT_OK;
+}
+
+size_t dit_block_workspace_bytes(const dit_plan_t *p) { return p ? p->total : 0; }
+
+dit_status_t dit_block_bind_workspace(dit_plan_t *p, void *dev_ptr, size_t bytes) {
+    if (!p || !dev_ptr) return DIT_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(dev_ptr) & 255u) return DIT_ERR_ALIGN;
+    if (bytes < p->total) return DIT_ERR_WORKSPACE_TOO_SMALL;
+    int dev = 0, major = 0, minor = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (major != 10 || minor != 3) return DIT_ERR_UNSUPPORTED_ARCH;
+    e = cudaMemset(dev_ptr, 0, 256);
+    if (e != cudaSuccess) return cuda_fail(e);
+    p->ws = static_cast<uint8_t *>(dev_ptr);
+    p->ws_bytes = bytes;
+    return DIT_OK;
+}
+
+dit_status_t dit_block_forward(const dit_plan_t *p, float *x, const dit_block_weights_t *w,
+                               const float *mod, dit_stream_t stream) {
+    if (!p || !x || !w || !mod) return DIT_ERR_INVALID_ARG;
+    if (!p->ws) return DIT_ERR_NO_WORKSPACE;
+    if (!w->wqkv || !w->wo || !w->wgate || !w->wup || !w->wdown) return DIT_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(mod) || !aligned16(w->wqkv) || !aligned16(w->wo) ||
+        !aligned16(w->wgate) || !aligned16(w->wup) || !aligned16(w->wdown))
+        return DIT_ERR_ALIGN;
+    if (w->dtype != DIT_W_BF16) return DIT_ERR_INVALID_ARG;
+
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const int64_t T = p->T;
+    const int D = p->D, F = p->F;
+    const int64_t Dl = D;
+    int *status = reinterpret_cast<int *>(p->ws);
+    void *K = p->ws + p->off_k;
+    void *Vt = p->ws + p->off_vt;
+    void *a = p->ws + p->off_a;
+    void *Q = p->ws + p->off_q;
+    void *b = p->ws + p->off_b;
+    void *h = p->ws + p->off_h;
+    float *acc = reinterpret_cast<float *>(p->ws + p->off_acc);
+    const float *shift1 = mod, *scale1 = mod + Dl, *gate1 = mod + 2 * Dl;
+    const float *shift2 = mod + 3 * Dl, *scale2 = mod + 4 * Dl, *gate2 = mod + 5 * Dl;
+    const uint16_t *wqkv = static_cast<const uint16_t *>(w->wqkv);
+    dit_status_t r;
+
+    // pass 1: K and V of every token
+    for (int64_t s = 0; s < T; s += p->ca) {
+        const int64_t rows = (T - s < p->ca) ? T - s : p->ca;
+        if ((r = launch_modln(x + s * Dl, rows, D, shift1, scale1, a, st)) != DIT_OK) return r;
+        dit_gemm_args_t g{};
+        g.mode = DIT_EPI_KV;
+        g.M = rows;
+        g.N = 2 * D;
+        g.K = D;
+        g.a = a;
+        g.lda = D;
+        g.b0 = wqkv + Dl * Dl;  // rows D..3D-1: Wk then Wv
+        g.ldb = D;
+        g.b_dtype = DIT_W_BF16;
+        g.out = K;
+        g.ldo = D;
+        g.out2 = Vt;
+        g.ldo2 = p->t_pad;
+        g.row_offset = s;
+        g.split_n = D;
+        if ((r = launch_gemm(g, status, st)) != DIT_OK) return r;
+    }
+    // pass 2: Q per slab, attention against all keys, O-projection into x
+    for (int64_t s = 0; s < T; s += p->ca) {
+        const int64_t rows = (T - s < p->ca) ? T - s : p->ca;
+        if ((r = launch_modln(x + s * Dl, rows, D, shift1, scale1, a, st)) != DIT_OK) return r;
+        dit_gemm_args_t g{};
+        g.mode = DIT_EPI_STORE_BF16;
+        g.M = rows;
+        g.N = D;
+        g.K = D;
+        g.a = a;
+        g.lda = D;
+        g.b0 = wqkv;
+        g.ldb = D;
+        g.b_dtype = DIT_W_BF16;
+        g.out = Q;
+        g.ldo = D;
+        if ((r = launch_gemm(g, status, st)) != DIT_OK) return r;
+        // O_s overwrites a_s (dead once Q_s exists)
+        if ((r = launch_attention(Q, rows, D, K, D, Vt, p->t_pad, T, p->heads, p->head_dim, a,
+                                  D, status, st)) != DIT_OK)
+            return r;
+        dit_gemm_args_t o{};
+        o.mode = DIT_EPI_RESID;
+        o.M = rows;
+        o.N = D;
+        o.K = D;
+        o.a = a;
+        o.lda = D;
+        o.b0 = w->wo;
+        o.ldb = D;
+        o.b_dtype = DIT_W_BF16;
+        o.x = x + s * Dl;
+        o.ldx = D;
+        o.gate = gate1;
+        if ((r = launch_gemm(o, status, st)) != DIT_OK) return r;
+    }
+    // MLP: token chunks x FFN feature slices
+    const uint16_t *wg = static_cast<const uint16_t *>(w->wgate);
+    const uint16_t *wu = static_cast<const uint16_t *>(w->wup);
+    const uint16_t *wd = static_cast<const uint16_t *>(w->wdown);
+    for (int64_t c = 0; c < T; c += p->cm) {
+        const int64_t rows = (T - c < p->cm) ? T - c : p->cm;
+        if ((r = launch_modln(x + c * Dl, rows, D, shift2, scale2, b, st)) != DIT_OK) return r;
+        for (int f = 0; f < F; f += p->fs) {
+            const int fw = (F - f < p->fs) ? F - f : p->fs;
+            dit_gemm_args_t g{};
+            g.mode = DIT_EPI_SWIGLU;
+            g.M = rows;
+            g.N = fw;
+            g.K = D;
+            g.a = b;
+            g.lda = D;
+            g.b0 = wg + int64_t(f) * Dl;
+            g.b1 = wu + int64_t(f) * Dl;
+            g.ldb = D;
+            g.b_dtype = DIT_W_BF16;
+            g.out = h;
+            g.ldo = p->fs;
+            if ((r = launch_gemm(g, status, st)) != DIT_OK) return r;
+            dit_gemm_args_t d{};
+            d.mode = DIT_EPI_DOWN;
+            d.M = rows;
+            d.N = D;
+            d.K = fw;
+            d.a = h;
+            d.lda = p->fs;
+            d.b0 = wd + f;  // columns f .. f+fw-1 of Wdown [D, F]
+            d.ldb = F;
+            d.b_dtype = DIT_W_BF16;
+            d.acc = acc;
+            d.ldacc = D;
+            d.acc_load = f > 0;
+            d.acc_final = f + fw >= F;
+            d.x = x + c * Dl;
+            d.ldx = D;
+            d.gate = gate2;
+            if ((r = launch_gemm(d, status, st)) != DIT_OK) return r;
+        }
+    }
+    return DIT_OK;
+}
+
+dit_status_t dit_block_sync_status(const dit_plan_t *p, dit_stream_t stream) {
+    if (!p) return DIT_ERR_INVALID_ARG;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (!p->ws) return DIT_OK;
+    int v = 0;
+    e = cudaMemcpyAsync(&v, p->ws, sizeof(int), cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess && v != 0) e = cudaMemsetAsync(p->ws, 0, sizeof(int), st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return cuda_fail(e);
+    return v == 0 ? DIT_OK : (v == DIT_ERR_TIMEOUT ? DIT_ERR_TIMEOUT : DIT_ERR_CUDA);
+}
+
+dit_status_t dit_final_forward(const dit_plan_t *p, const float *x, const void *wf,
+                               const float *wf_scale, const float *mod_f, float *out,
+                               dit_stream_t stream) {
+    if (!p) return DIT_ERR_INVALID_ARG;
+    return launch_final(x, p->T, p->D, wf, wf_scale, mod_f, out,
+                        static_cast<cudaStream_t>(stream));
+}
+
+dit_status_t dit_modln_cast(const float *x, int64_t rows, int D, const float *shift,
+                            const float *scale, void *out_bf16, dit_stream_t stream) {
+    return launch_modln(x, rows, D, shift, scale, out_bf16, static_cast<cudaStream_t>(stream));
+}
+
+dit_status_t dit_gemm(const dit_gemm_args_t *args, int *dev_status, dit_stream_t stream) {
+    if (!args) return DIT_ERR_INVALID_ARG;
+    return launch_gemm(*args, dev_status, static_cast<cudaStream_t>(stream));
+}
+
+dit_status_t dit_attention(const void *q, int64_t Tq, int64_t ldq, const void *k, int64_t ldk,
+                           const void *vt, int64_t ldvt, int64_t T, int heads, int head_dim,
+                           void *o, int64_t ldo, int *dev_status, dit_stream_t stream) {
+    return launch_attention(q, Tq, ldq, k, ldk, vt, ldvt, T, heads, head_dim, o, ldo, dev_status,
+                            static_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"

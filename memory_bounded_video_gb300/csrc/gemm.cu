@@ -1,0 +1,474 @@
+// Tensor-core GEMM for sm_103a:  acc[M, N] = A[M, K] * B[N, K]^T
+// (bf16 operands, fp32 accumulation in tensor memory) with the block's fused
+// epilogues: K/V store, Q store, gated fp32 residual add, SwiGLU, and the
+// down projection's accumulate-across-FFN-slices.
+//
+// Structure (one CTA per SM, persistent over 128 x BN output tiles):
+//   warp 0      TMA producer: A and B k-blocks (64 wide, 128-byte swizzle)
+//               into a 4-stage shared-memory ring
+//   warp 1      allocates TMEM; one lane issues tcgen05.mma (M=128, N=BN,
+//               K=16) into one of two TMEM accumulators
+//   warps 2..5  epilogue: tcgen05.ld of the accumulator (one token row per
+//               thread), the fused math, stores to global
+// The accumulator is double-buffered, so the epilogue of tile i overlaps the
+// main loop of tile i+1.
+//
+// Per-row exactness: every output element is the same fp32 accumulation over
+// K in the same order (k-blocks of 64, MMAs of 16), whatever M, the tile
+// schedule or the grid — so results do not depend on how tokens are chunked.
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace ds {
+
+namespace {
+
+constexpr int kBM = 128;
+constexpr int kBK = 64;
+constexpr int kStages = 4;
+constexpr int kThreads = 192;
+
+struct GemmParams {
+    int64_t M;
+    int N, K;
+    int num_m, num_n, num_k;
+    void *out;
+    int64_t ldo;
+    void *out2;
+    int64_t ldo2;
+    int64_t row_offset;
+    int split_n;
+    float *x;
+    int64_t ldx;
+    const float *gate;
+    float *acc;
+    int64_t ldacc;
+    int acc_load, acc_final;
+    int *status;
+};
+
+template <int MODE>
+struct Cfg {
+    static constexpr int NB = (MODE == DIT_EPI_SWIGLU) ? 2 : 1;  // B operands
+    static constexpr int BN = (MODE == DIT_EPI_SWIGLU) ? 128 : 256;
+    static constexpr int A_BYTES = kBM * kBK * 2;
+    static constexpr int B_BYTES = BN * kBK * 2;
+    static constexpr int STAGE_BYTES = A_BYTES + NB * B_BYTES;
+    static constexpr int ACC_COLS = NB * BN;  // fp32 TMEM columns per accumulator
+    static constexpr int TMEM_COLS = 2 * ACC_COLS;
+    static constexpr int OUT_COLS = BN;       // output columns per tile
+    static constexpr int BAR_BYTES = 256;
+    static constexpr int SMEM_BYTES = kStages * STAGE_BYTES + BAR_BYTES + 1024;
+};
+
+DEV void store_bf16x32(__nv_bfloat16 *dst, const float (&f)[32]) {
+    uint4 *d = reinterpret_cast<uint4 *>(dst);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        uint4 v;
+        v.x = pack_bf16x2(f[8 * i + 0], f[8 * i + 1]);
+        v.y = pack_bf16x2(f[8 * i + 2], f[8 * i + 3]);
+        v.z = pack_bf16x2(f[8 * i + 4], f[8 * i + 5]);
+        v.w = pack_bf16x2(f[8 * i + 6], f[8 * i + 7]);
+        d[i] = v;
+    }
+}
+
+// x[0..31] += gate[0..31] * f[0..31], one fp32 rounding per element.
+DEV void gated_residual32(float *x, const float *gate, const float (&f)[32]) {
+    float4 *xv = reinterpret_cast<float4 *>(x);
+    const float4 *gv = reinterpret_cast<const float4 *>(gate);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        float4 a = xv[i];
+        const float4 g = __ldg(gv + i);
+        a.x = __fmaf_rn(g.x, f[4 * i + 0], a.x);
+        a.y = __fmaf_rn(g.y, f[4 * i + 1], a.y);
+        a.z = __fmaf_rn(g.z, f[4 * i + 2], a.z);
+        a.w = __fmaf_rn(g.w, f[4 * i + 3], a.w);
+        xv[i] = a;
+    }
+}
+
+DEV float silu(float z) { return z / (1.0f + __expf(-z)); }
+
+template <int MODE>
+DEV void epilogue_tile(const GemmParams &p, uint32_t taddr, int64_t m, int nb) {
+    using C = Cfg<MODE>;
+    const bool row_ok = m < p.M;
+#pragma unroll 1
+    for (int c0 = 0; c0 < C::OUT_COLS; c0 += 32) {
+        __syncwarp();
+        uint32_t r[32];
+        tmem_ld32(taddr + c0, r);
+        uint32_t u[32];
+        if constexpr (MODE == DIT_EPI_SWIGLU) {
+            tmem_ld32(taddr + C::BN + c0, u);
+            tmem_ld_wait(u);
+        }
+        tmem_ld_wait(r);
+        const int n = nb * C::BN + c0;
+        if (!row_ok || n >= p.N) continue;
+        float f[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) f[j] = __uint_as_float(r[j]);
+        if constexpr (MODE == DIT_EPI_STORE_BF16) {
+            store_bf16x32(reinterpret_cast<__nv_bfloat16 *>(p.out) + m * p.ldo + n, f);
+        } else if constexpr (MODE == DIT_EPI_STORE_F32) {
+            float4 *d = reinterpret_cast<float4 *>(reinterpret_cast<float *>(p.out) +
+                                                   m * p.ldo + n);
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                d[i] = make_float4(f[4 * i], f[4 * i + 1], f[4 * i + 2], f[4 * i + 3]);
+        } else if constexpr (MODE == DIT_EPI_KV) {
+            const int64_t tok = p.row_offset + m;
+            if (n < p.split_n) {
+                store_bf16x32(reinterpret_cast<__nv_bfloat16 *>(p.out) + tok * p.ldo + n, f);
+            } else {
+                __nv_bfloat16 *vt = reinterpret_cast<__nv_bfloat16 *>(p.out2) +
+                                    int64_t(n - p.split_n) * p.ldo2 + tok;
+#pragma unroll
+                for (int j = 0; j < 32; ++j) vt[int64_t(j) * p.ldo2] = __float2bfloat16_rn(f[j]);
+            }
+        } else if constexpr (MODE == DIT_EPI_RESID) {
+            gated_residual32(p.x + m * p.ldx + n, p.gate + n, f);
+        } else if constexpr (MODE == DIT_EPI_SWIGLU) {
+            float h[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) h[j] = silu(f[j]) * __uint_as_float(u[j]);
+            store_bf16x32(reinterpret_cast<__nv_bfloat16 *>(p.out) + m * p.ldo + n, h);
+        } else if constexpr (MODE == DIT_EPI_DOWN) {
+            if (p.acc_final) {
+                gated_residual32(p.x + m * p.ldx + n, p.gate + n, f);
+            } else {
+                float4 *d = reinterpret_cast<float4 *>(p.acc + m * p.ldacc + n);
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    d[i] = make_float4(f[4 * i], f[4 * i + 1], f[4 * i + 2], f[4 * i + 3]);
+            }
+        }
+    }
+}
+
+// DOWN with acc_load: write the carried fp32 accumulator of tile t into the
+// TMEM buffer before the tile's MMAs start (they then accumulate onto it).
+DEV void preload_tile(const GemmParams &p, uint32_t taddr, int64_t m, int nb) {
+    using C = Cfg<DIT_EPI_DOWN>;
+    const bool row_ok = m < p.M;
+#pragma unroll 1
+    for (int c0 = 0; c0 < C::OUT_COLS; c0 += 32) {
+        const int n = nb * C::BN + c0;
+        uint32_t r[32];
+        if (row_ok && n < p.N) {
+            const float4 *s = reinterpret_cast<const float4 *>(p.acc + m * p.ldacc + n);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const float4 v = s[i];
+                r[4 * i] = __float_as_uint(v.x);
+                r[4 * i + 1] = __float_as_uint(v.y);
+                r[4 * i + 2] = __float_as_uint(v.z);
+                r[4 * i + 3] = __float_as_uint(v.w);
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) r[j] = 0u;
+        }
+        __syncwarp();
+        tmem_st32_sync(taddr + c0, r);
+    }
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
+                   const __grid_constant__ CUtensorMap tmB0,
+                   const __grid_constant__ CUtensorMap tmB1, const GemmParams p) {
+    using C = Cfg<MODE>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *tiles = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t *bars = reinterpret_cast<uint64_t *>(tiles + kStages * C::STAGE_BYTES);
+    // bars: full[kStages], empty[kStages], tfull[2], tempty[2], drain
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * kStages + 5);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+    const int warp = warp_id();
+    const int lane = lane_id();
+    const uint32_t bar0 = smem_u32(bars);
+    auto full_bar = [&](int s) { return bar0 + 8u * s; };
+    auto empty_bar = [&](int s) { return bar0 + 8u * (kStages + s); };
+    auto tfull_bar = [&](int b) { return bar0 + 8u * (2 * kStages + b); };
+    auto tempty_bar = [&](int b) { return bar0 + 8u * (2 * kStages + 2 + b); };
+    const uint32_t drain_bar = bar0 + 8u * (2 * kStages + 4);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(tfull_bar(b), 1);
+            mbar_init(tempty_bar(b), 128);
+        }
+        mbar_init(drain_bar, 1);
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmB0);
+        if (C::NB == 2) tma_prefetch_desc(&tmB1);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const WaitCtx wc{abort_flag, p.status};
+    const int num_tiles = p.num_m * p.num_n;
+    const bool preload = (MODE == DIT_EPI_DOWN) && p.acc_load;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ---------------------------------------------- TMA producer
+            int stage = 0;
+            uint32_t ph = 0;
+            int64_t issued = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+                const int mb = t / p.num_n, nb = t % p.num_n;
+                for (int kb = 0; kb < p.num_k; ++kb) {
+                    if (!mbar_wait(empty_bar(stage), ph ^ 1u, wc)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t sA = smem_u32(tiles + stage * C::STAGE_BYTES);
+                    mbar_arrive_expect_tx(full_bar(stage), C::STAGE_BYTES);
+                    tma_load_2d(sA, &tmA, full_bar(stage), kb * kBK, mb * kBM);
+                    tma_load_2d(sA + C::A_BYTES, &tmB0, full_bar(stage), kb * kBK, nb * C::BN);
+                    if (C::NB == 2)
+                        tma_load_2d(sA + C::A_BYTES + C::B_BYTES, &tmB1, full_bar(stage),
+                                    kb * kBK, nb * C::BN);
+                    ++issued;
+                    if (++stage == kStages) {
+                        stage = 0;
+                        ph ^= 1u;
+                    }
+                }
+            }
+            if (!ok) {  // let the copies already in flight land before exit
+                const int64_t first = issued > kStages ? issued - kStages : 0;
+                for (int64_t i = first; i < issued; ++i)
+                    mbar_wait_quiet(full_bar(int(i % kStages)), uint32_t((i / kStages) & 1),
+                                    kWaitLimitNs);
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ---------------------------------------------- MMA issuer
+            constexpr uint32_t IDESC = idesc_bf16_f32(kBM, C::BN);
+            int stage = 0;
+            uint32_t ph = 0;
+            int buf = 0;
+            uint32_t bph = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+                if (!mbar_wait(tempty_bar(buf), preload ? bph : (bph ^ 1u), wc)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d = tmem + uint32_t(buf * C::ACC_COLS);
+                for (int kb = 0; kb < p.num_k; ++kb) {
+                    if (!mbar_wait(full_bar(stage), ph, wc)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sA = smem_u32(tiles + stage * C::STAGE_BYTES);
+#pragma unroll
+                    for (int k = 0; k < kBK / 16; ++k) {
+                        const uint64_t ad = desc_sw128(sA + 32u * k);
+                        const uint32_t accum = (kb | k) != 0 || preload;
+                        mma_bf16_ss(d, ad, desc_sw128(sA + C::A_BYTES + 32u * k), IDESC, accum);
+                        if (C::NB == 2)
+                            mma_bf16_ss(d + C::BN, ad,
+                                        desc_sw128(sA + C::A_BYTES + C::B_BYTES + 32u * k),
+                                        IDESC, accum);
+                    }
+                    mma_commit(empty_bar(stage));
+                    if (++stage == kStages) {
+                        stage = 0;
+                        ph ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                mma_commit(tfull_bar(buf));
+                if (++buf == 2) {
+                    buf = 0;
+                    bph ^= 1u;
+                }
+            }
+            if (!ok) {  // every issued MMA must finish before TMEM is freed
+                mma_commit(drain_bar);
+                mbar_wait_quiet(drain_bar, 0, kWaitLimitNs);
+            }
+        }
+    } else {
+        // -------------------------------------------------- epilogue
+        const int q = warp & 3;  // TMEM lane quadrant this warp may access
+        const uint32_t lane_base = tmem + (uint32_t(q * 32) << 16);
+        int buf = 0;
+        uint32_t bph = 0;
+        int t = blockIdx.x;
+        if (preload && t < num_tiles) {
+            preload_tile(p, lane_base, int64_t(t / p.num_n) * kBM + q * 32 + lane, t % p.num_n);
+            tc_fence_before();
+            mbar_arrive(tempty_bar(0));
+        }
+        for (; t < num_tiles; t += gridDim.x) {
+            if (preload) {
+                const int tn = t + gridDim.x;
+                if (tn < num_tiles) {
+                    preload_tile(p, lane_base + uint32_t((buf ^ 1) * C::ACC_COLS),
+                                 int64_t(tn / p.num_n) * kBM + q * 32 + lane, tn % p.num_n);
+                    tc_fence_before();
+                    mbar_arrive(tempty_bar(buf ^ 1));
+                }
+            }
+            bool ok = mbar_wait(tfull_bar(buf), bph, wc);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
+            tc_fence_after();
+            const int mb = t / p.num_n, nb = t % p.num_n;
+            epilogue_tile<MODE>(p, lane_base + uint32_t(buf * C::ACC_COLS),
+                                int64_t(mb) * kBM + q * 32 + lane, nb);
+            if (!preload) {
+                tc_fence_before();
+                mbar_arrive(tempty_bar(buf));
+            }
+            if (++buf == 2) {
+                buf = 0;
+                bph ^= 1u;
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, C::TMEM_COLS);
+    }
+}
+
+template <int MODE>
+dit_status_t run(const dit_gemm_args_t &a, int *dev_status, cudaStream_t s) {
+    using C = Cfg<MODE>;
+    const CUtensorMapDataType bf16 = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    CUtensorMap tA, tB0, tB1;
+    if (!make_tmap_2d(&tA, bf16, a.a, uint64_t(a.K), uint64_t(a.M), uint64_t(a.lda) * 2, kBK,
+                      kBM))
+        return DIT_ERR_INVALID_ARG;
+    if (!make_tmap_2d(&tB0, bf16, a.b0, uint64_t(a.K), uint64_t(a.N), uint64_t(a.ldb) * 2, kBK,
+                      C::BN))
+        return DIT_ERR_INVALID_ARG;
+    tB1 = tB0;
+    if (C::NB == 2 && !make_tmap_2d(&tB1, bf16, a.b1, uint64_t(a.K), uint64_t(a.N),
+                                    uint64_t(a.ldb) * 2, kBK, C::BN))
+        return DIT_ERR_INVALID_ARG;
+
+    GemmParams p{};
+    p.M = a.M;
+    p.N = a.N;
+    p.K = a.K;
+    p.num_m = int((a.M + kBM - 1) / kBM);
+    p.num_n = (a.N + C::BN - 1) / C::BN;
+    p.num_k = a.K / kBK;
+    p.out = a.out;
+    p.ldo = a.ldo;
+    p.out2 = a.out2;
+    p.ldo2 = a.ldo2;
+    p.row_offset = a.row_offset;
+    p.split_n = a.split_n;
+    p.x = a.x;
+    p.ldx = a.ldx;
+    p.gate = a.gate;
+    p.acc = a.acc;
+    p.ldacc = a.ldacc;
+    p.acc_load = a.acc_load;
+    p.acc_final = a.acc_final;
+    p.status = dev_status;
+
+    static bool attr_done = false;  // per instantiation
+    if (!attr_done) {
+        cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<MODE>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             C::SMEM_BYTES);
+        if (e != cudaSuccess) return cuda_fail(e);
+        attr_done = true;
+    }
+    const int tiles = p.num_m * p.num_n;
+    const int grid = tiles < sm_count() ? tiles : sm_count();
+    gemm_tc_kernel<MODE><<<grid, kThreads, C::SMEM_BYTES, s>>>(tA, tB0, tB1, p);
+    return check_launch();
+}
+
+bool ld_ok(int64_t ld, int64_t min_ld, int elem_bytes) {
+    return ld >= min_ld && (ld * elem_bytes) % 16 == 0;
+}
+
+}  // namespace
+
+dit_status_t launch_gemm(const dit_gemm_args_t &a, int *dev_status, cudaStream_t s) {
+    if (a.M < 0 || a.N <= 0 || a.K <= 0 || a.N % 32 || a.K % kBK) return DIT_ERR_INVALID_ARG;
+    if (a.M > (int64_t(1) << 31) - kBM) return DIT_ERR_INVALID_ARG;
+    if (a.b_dtype != DIT_W_BF16) return DIT_ERR_INVALID_ARG;
+    if (!a.a || !a.b0) return DIT_ERR_INVALID_ARG;
+    if (!aligned16(a.a) || !aligned16(a.b0)) return DIT_ERR_ALIGN;
+    if (!ld_ok(a.lda, a.K, 2) || !ld_ok(a.ldb, a.K, 2)) return DIT_ERR_INVALID_ARG;
+    if (a.M == 0) return DIT_OK;
+    switch (a.mode) {
+        case DIT_EPI_STORE_BF16:
+            if (!a.out || !aligned16(a.out)) return DIT_ERR_ALIGN;
+            if (!ld_ok(a.ldo, a.N, 2)) return DIT_ERR_INVALID_ARG;
+            return run<DIT_EPI_STORE_BF16>(a, dev_status, s);
+        case DIT_EPI_STORE_F32:
+            if (!a.out || !aligned16(a.out)) return DIT_ERR_ALIGN;
+            if (!ld_ok(a.ldo, a.N, 4)) return DIT_ERR_INVALID_ARG;
+            return run<DIT_EPI_STORE_F32>(a, dev_status, s);
+        case DIT_EPI_KV:
+            if (!a.out || !a.out2 || !aligned16(a.out)) return DIT_ERR_ALIGN;
+            if (a.split_n < 0 || a.split_n % 32 || a.split_n > a.N || a.row_offset < 0)
+                return DIT_ERR_INVALID_ARG;
+            if (!ld_ok(a.ldo, a.split_n, 2) || a.ldo2 < a.row_offset + a.M)
+                return DIT_ERR_INVALID_ARG;
+            return run<DIT_EPI_KV>(a, dev_status, s);
+        case DIT_EPI_RESID:
+            if (!a.x || !a.gate || !aligned16(a.x) || !aligned16(a.gate)) return DIT_ERR_ALIGN;
+            if (!ld_ok(a.ldx, a.N, 4)) return DIT_ERR_INVALID_ARG;
+            return run<DIT_EPI_RESID>(a, dev_status, s);
+        case DIT_EPI_SWIGLU:
+            if (!a.b1 || !aligned16(a.b1) || !a.out || !aligned16(a.out)) return DIT_ERR_ALIGN;
+            if (!ld_ok(a.ldo, a.N, 2)) return DIT_ERR_INVALID_ARG;
+            return run<DIT_EPI_SWIGLU>(a, dev_status, s);
+        case DIT_EPI_DOWN:
+            if (a.acc_final) {
+                if (!a.x || !a.gate || !aligned16(a.x) || !aligned16(a.gate))
+                    return DIT_ERR_ALIGN;
+                if (!ld_ok(a.ldx, a.N, 4)) return DIT_ERR_INVALID_ARG;
+            }
+            if (a.acc_load || !a.acc_final) {
+                if (!a.acc || !aligned16(a.acc)) return DIT_ERR_ALIGN;
+                if (!ld_ok(a.ldacc, a.N, 4)) return DIT_ERR_INVALID_ARG;
+            }
+            return run<DIT_EPI_DOWN>(a, dev_status, s);
+        default:
+            return DIT_ERR_INVALID_ARG;
+    }
+}
+
+}  // namespace ds

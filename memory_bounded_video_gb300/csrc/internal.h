@@ -1,0 +1,45 @@
+// Host-side internals shared by the translation units of libditstream.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "ditstream.h"
+
+namespace ds {
+
+// Record a CUDA error for dit_last_cuda_error() and return DIT_ERR_CUDA.
+dit_status_t cuda_fail(cudaError_t e);
+// Check for a launch error right after a launch.
+dit_status_t check_launch();
+
+// Multiprocessor count of the current device (cached per device).
+int sm_count();
+
+// 2-D tensor map (row-major matrix: `inner` elements per row, `outer` rows,
+// `row_bytes` between rows) with a box of box_inner x box_outer elements and
+// 128-byte swizzle; out-of-range elements read as zero.
+bool make_tmap_2d(CUtensorMap *m, CUtensorMapDataType dt, const void *base,
+                  uint64_t inner, uint64_t outer, uint64_t row_bytes,
+                  uint32_t box_inner, uint32_t box_outer);
+
+dit_status_t launch_modln(const float *x, int64_t rows, int D, const float *shift,
+                          const float *scale, void *out, cudaStream_t s);
+
+dit_status_t launch_gemm(const dit_gemm_args_t &a, int *dev_status, cudaStream_t s);
+
+dit_status_t launch_attention(const void *q, int64_t Tq, int64_t ldq, const void *k,
+                              int64_t ldk, const void *vt, int64_t ldvt, int64_t T,
+                              int heads, int head_dim, void *o, int64_t ldo,
+                              int *dev_status, cudaStream_t s);
+
+dit_status_t launch_final(const float *x, int64_t T, int D, const void *wf,
+                          const float *wf_scale, const float *mod_f, float *out,
+                          cudaStream_t s);
+
+inline bool aligned16(const void *p) {
+    return (reinterpret_cast<uintptr_t>(p) & 15u) == 0;
+}
+
+}  // namespace ds

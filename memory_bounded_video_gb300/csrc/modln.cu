@@ -1,0 +1,107 @@
+// Norm + modulation + cast: one warp per token row.
+//   y = (x - mean) * rsqrt(var + 1e-6) * (1 + scale) + shift  -> bf16 (RNE)
+// Token-wise ("LayerStream: H3 Chunking", "How the slicing works"), HBM-bound:
+// 4*D bytes read and 2*D bytes written per row.  The row lives in registers
+// (D/128 float4 per lane, 128-bit coalesced loads), mean and biased variance
+// come from two warp-shuffle reductions in a fixed order, so a row's result
+// is the same whichever slab it is processed in.
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace ds {
+
+namespace {
+
+constexpr int kWarpsPerBlock = 8;
+
+template <int NV>
+__global__ void __launch_bounds__(32 * kWarpsPerBlock)
+    modln_cast_kernel(const float *__restrict__ x, int64_t rows, const float *__restrict__ shift,
+                      const float *__restrict__ scale, __nv_bfloat16 *__restrict__ out) {
+    constexpr int D = NV * 128;
+    const int lane = threadIdx.x & 31;
+    const int64_t warps = int64_t(gridDim.x) * kWarpsPerBlock;
+    for (int64_t r = int64_t(blockIdx.x) * kWarpsPerBlock + (threadIdx.x >> 5); r < rows;
+         r += warps) {
+        const float4 *xr = reinterpret_cast<const float4 *>(x + r * D);
+        float4 v[NV];
+#pragma unroll
+        for (int i = 0; i < NV; ++i) v[i] = __ldcs(xr + lane + 32 * i);
+        float s = 0.f;
+#pragma unroll
+        for (int i = 0; i < NV; ++i) s += (v[i].x + v[i].y) + (v[i].z + v[i].w);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+        const float mean = s * (1.0f / D);
+        float q = 0.f;
+#pragma unroll
+        for (int i = 0; i < NV; ++i) {
+            const float a = v[i].x - mean, b = v[i].y - mean, c = v[i].z - mean,
+                        d = v[i].w - mean;
+            q += (a * a + b * b) + (c * c + d * d);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) q += __shfl_xor_sync(0xffffffffu, q, o);
+        const float rstd = rsqrtf(q * (1.0f / D) + 1e-6f);
+        uint2 *orow = reinterpret_cast<uint2 *>(out + r * D);
+#pragma unroll
+        for (int i = 0; i < NV; ++i) {
+            const int c4 = lane + 32 * i;
+            const float4 sc = __ldg(reinterpret_cast<const float4 *>(scale) + c4);
+            const float4 sh = __ldg(reinterpret_cast<const float4 *>(shift) + c4);
+            const float y0 = __fmaf_rn((v[i].x - mean) * rstd, 1.0f + sc.x, sh.x);
+            const float y1 = __fmaf_rn((v[i].y - mean) * rstd, 1.0f + sc.y, sh.y);
+            const float y2 = __fmaf_rn((v[i].z - mean) * rstd, 1.0f + sc.z, sh.z);
+            const float y3 = __fmaf_rn((v[i].w - mean) * rstd, 1.0f + sc.w, sh.w);
+            uint2 pk;
+            pk.x = pack_bf16x2(y0, y1);
+            pk.y = pack_bf16x2(y2, y3);
+            orow[c4] = pk;
+        }
+    }
+}
+
+template <int NV>
+dit_status_t run(const float *x, int64_t rows, const float *shift, const float *scale,
+                 void *out, cudaStream_t s) {
+    const int64_t blocks_needed = (rows + kWarpsPerBlock - 1) / kWarpsPerBlock;
+    const int64_t cap = int64_t(sm_count()) * 8;
+    const int grid = int(blocks_needed < cap ? blocks_needed : cap);
+    modln_cast_kernel<NV><<<grid, 32 * kWarpsPerBlock, 0, s>>>(
+        x, rows, shift, scale, reinterpret_cast<__nv_bfloat16 *>(out));
+    return check_launch();
+}
+
+}  // namespace
+
+dit_status_t launch_modln(const float *x, int64_t rows, int D, const float *shift,
+                          const float *scale, void *out, cudaStream_t s) {
+    if (rows < 0 || D <= 0 || D % 128 || !x || !shift || !scale || !out)
+        return DIT_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(shift) || !aligned16(scale) || !aligned16(out))
+        return DIT_ERR_ALIGN;
+    if (rows == 0) return DIT_OK;
+    switch (D / 128) {
+#define DS_CASE(nv) \
+    case nv:        \
+        return run<nv>(x, rows, shift, scale, out, s);
+        DS_CASE(1)
+        DS_CASE(2)
+        DS_CASE(3)
+        DS_CASE(4)
+        DS_CASE(5)
+        DS_CASE(6)
+        DS_CASE(8)
+        DS_CASE(10)
+        DS_CASE(12)
+        DS_CASE(16)
+        DS_CASE(20)
+        DS_CASE(24)
+        DS_CASE(32)
+#undef DS_CASE
+        default:
+            return DIT_ERR_INVALID_ARG;
+    }
+}
+
+}  // namespace ds

@@ -1,0 +1,254 @@
+"""ctypes binding of libditstream (argument marshalling only).
+
+Every function here forwards to the C ABI declared in ``include/ditstream.h``
+with the same name (minus the ``dit_`` prefix); all compute runs in the CUDA
+kernels of the library.  Device buffers may be given as integers (device
+addresses) or as objects with ``data_ptr()`` (e.g. torch tensors); streams as
+integers (``cudaStream_t``) or objects with ``cuda_stream``.  A non-OK status
+raises :class:`DitError`.  There is no fallback: if the library is missing,
+:func:`load` raises.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "libditstream.so")
+
+OK = 0
+ERR_INVALID_ARG = -1
+ERR_CHUNK_ALIGN = -2
+ERR_ALIGN = -3
+ERR_NO_WORKSPACE = -4
+ERR_WORKSPACE_TOO_SMALL = -5
+ERR_CUDA = -6
+ERR_TIMEOUT = -7
+ERR_UNSUPPORTED_ARCH = -8
+
+W_BF16 = 0
+W_INT8 = 1
+
+EPI_STORE_BF16 = 0
+EPI_STORE_F32 = 1
+EPI_KV = 2
+EPI_RESID = 3
+EPI_SWIGLU = 4
+EPI_DOWN = 5
+
+# Exported symbols of the C ABI (checked by the CPU tests against the header).
+SYMBOLS = (
+    "dit_block_plan", "dit_block_plan_ex", "dit_block_plan_destroy",
+    "dit_block_plan_info", "dit_block_workspace_bytes",
+    "dit_block_bind_workspace", "dit_block_forward", "dit_block_sync_status",
+    "dit_final_forward", "dit_status_string", "dit_last_cuda_error",
+    "dit_abi_version", "dit_modln_cast", "dit_gemm", "dit_attention",
+)
+
+
+class DitError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        msg = _lib.dit_status_string(status).decode() if _lib else str(status)
+        if status == ERR_CUDA and _lib:
+            msg += ": " + _lib.dit_last_cuda_error().decode()
+        super().__init__(f"{where}: {msg} (status {status})")
+
+
+class BlockWeights(ctypes.Structure):
+    _fields_ = [("dtype", ctypes.c_int),
+                ("wqkv", ctypes.c_void_p), ("wo", ctypes.c_void_p),
+                ("wgate", ctypes.c_void_p), ("wup", ctypes.c_void_p),
+                ("wdown", ctypes.c_void_p),
+                ("wqkv_scale", ctypes.c_void_p), ("wo_scale", ctypes.c_void_p),
+                ("wgate_scale", ctypes.c_void_p), ("wup_scale", ctypes.c_void_p),
+                ("wdown_scale", ctypes.c_void_p)]
+
+
+class GemmArgs(ctypes.Structure):
+    _fields_ = [("mode", ctypes.c_int), ("M", ctypes.c_int64),
+                ("N", ctypes.c_int), ("K", ctypes.c_int),
+                ("a", ctypes.c_void_p), ("lda", ctypes.c_int64),
+                ("b0", ctypes.c_void_p), ("b1", ctypes.c_void_p),
+                ("ldb", ctypes.c_int64), ("b_dtype", ctypes.c_int),
+                ("b0_scale", ctypes.c_void_p), ("b1_scale", ctypes.c_void_p),
+                ("out", ctypes.c_void_p), ("ldo", ctypes.c_int64),
+                ("out2", ctypes.c_void_p), ("ldo2", ctypes.c_int64),
+                ("row_offset", ctypes.c_int64), ("split_n", ctypes.c_int),
+                ("x", ctypes.c_void_p), ("ldx", ctypes.c_int64),
+                ("gate", ctypes.c_void_p),
+                ("acc", ctypes.c_void_p), ("ldacc", ctypes.c_int64),
+                ("acc_load", ctypes.c_int), ("acc_final", ctypes.c_int)]
+
+
+_lib: Optional[ctypes.CDLL] = None
+
+
+def _declare(lib):
+    c_int, c_int64, c_size, vp = (ctypes.c_int, ctypes.c_int64, ctypes.c_size_t,
+                                  ctypes.c_void_p)
+    pp = ctypes.POINTER(ctypes.c_void_p)
+    sig = {
+        "dit_block_plan": (c_int, [c_int64, c_int, c_int, c_int, c_int, c_int, pp]),
+        "dit_block_plan_ex": (c_int, [c_int64, c_int, c_int, c_int, c_int, c_int,
+                                      c_int, pp]),
+        "dit_block_plan_destroy": (None, [vp]),
+        "dit_block_plan_info": (c_int, [vp] + [vp] * 7),
+        "dit_block_workspace_bytes": (c_size, [vp]),
+        "dit_block_bind_workspace": (c_int, [vp, vp, c_size]),
+        "dit_block_forward": (c_int, [vp, vp, ctypes.POINTER(BlockWeights), vp, vp]),
+        "dit_block_sync_status": (c_int, [vp, vp]),
+        "dit_final_forward": (c_int, [vp, vp, vp, vp, vp, vp, vp]),
+        "dit_status_string": (ctypes.c_char_p, [c_int]),
+        "dit_last_cuda_error": (ctypes.c_char_p, []),
+        "dit_abi_version": (c_int, []),
+        "dit_modln_cast": (c_int, [vp, c_int64, c_int, vp, vp, vp, vp]),
+        "dit_gemm": (c_int, [ctypes.POINTER(GemmArgs), vp, vp]),
+        "dit_attention": (c_int, [vp, c_int64, c_int64, vp, c_int64, vp, c_int64,
+                                  c_int64, c_int, c_int, vp, c_int64, vp, vp]),
+    }
+    for name, (res, args) in sig.items():
+        f = getattr(lib, name)
+        f.restype = res
+        f.argtypes = args
+
+
+def load(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Open the library (once).  Raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(path):
+            raise RuntimeError(
+                f"libditstream not built ({path} missing): run "
+                "`python -m memory_bounded_video_gb300.build`")
+        lib = ctypes.CDLL(path)
+        _declare(lib)
+        _lib = lib
+    return _lib
+
+
+def ptr(t) -> Optional[int]:
+    """Device address of a buffer given as int, None or tensor-like."""
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return int(t.data_ptr())
+
+
+def stream_handle(s) -> Optional[int]:
+    if s is None:
+        return None
+    if isinstance(s, int):
+        return s
+    return int(s.cuda_stream)
+
+
+def _check(status: int, where: str):
+    if status != OK:
+        raise DitError(status, where)
+
+
+def status_string(s: int) -> str:
+    return load().dit_status_string(s).decode()
+
+
+def abi_version() -> int:
+    return load().dit_abi_version()
+
+
+class BlockPlan:
+    """Owns a ``dit_plan_t``; see ``dit_block_plan_ex``."""
+
+    def __init__(self, T, D, heads, ffn, mlp_chunk_tokens, attn_chunk_tokens,
+                 ffn_slice=0):
+        lib = load()
+        h = ctypes.c_void_p()
+        _check(lib.dit_block_plan_ex(T, D, heads, ffn, mlp_chunk_tokens,
+                                     attn_chunk_tokens, ffn_slice,
+                                     ctypes.byref(h)), "dit_block_plan_ex")
+        self._h = h
+        self._ws = None
+
+    def __del__(self):
+        if getattr(self, "_h", None) and _lib is not None:
+            _lib.dit_block_plan_destroy(self._h)
+            self._h = None
+
+    @property
+    def handle(self):
+        return self._h
+
+    def info(self) -> dict:
+        T = ctypes.c_int64()
+        ints = [ctypes.c_int() for _ in range(6)]
+        _check(load().dit_block_plan_info(self._h, ctypes.byref(T),
+                                          *[ctypes.byref(i) for i in ints]),
+               "dit_block_plan_info")
+        keys = ("D", "heads", "ffn", "mlp_chunk", "attn_chunk", "ffn_slice")
+        return dict(T=T.value, **{k: v.value for k, v in zip(keys, ints)})
+
+    def workspace_bytes(self) -> int:
+        return int(load().dit_block_workspace_bytes(self._h))
+
+    def bind_workspace(self, buf, nbytes: Optional[int] = None):
+        if nbytes is None:
+            nbytes = buf.numel() * buf.element_size()
+        _check(load().dit_block_bind_workspace(self._h, ptr(buf), nbytes),
+               "dit_block_bind_workspace")
+        self._ws = buf  # keep the caller's buffer alive with the plan
+
+    def forward(self, x, weights: BlockWeights, modulation, stream=None):
+        _check(load().dit_block_forward(self._h, ptr(x), ctypes.byref(weights),
+                                        ptr(modulation), stream_handle(stream)),
+               "dit_block_forward")
+
+    def sync_status(self, stream=None) -> int:
+        return load().dit_block_sync_status(self._h, stream_handle(stream))
+
+    def final_forward(self, x, wf, wf_scale, mod_f, out, stream=None):
+        _check(load().dit_final_forward(self._h, ptr(x), ptr(wf), ptr(wf_scale),
+                                        ptr(mod_f), ptr(out),
+                                        stream_handle(stream)),
+               "dit_final_forward")
+
+
+def block_plan(T, D, heads, ffn, mlp_chunk_tokens, attn_chunk_tokens,
+               ffn_slice=0) -> BlockPlan:
+    return BlockPlan(T, D, heads, ffn, mlp_chunk_tokens, attn_chunk_tokens,
+                     ffn_slice)
+
+
+def block_weights(wqkv, wo, wgate, wup, wdown, scales=None) -> BlockWeights:
+    """Pack device weight buffers into the C struct (bf16, or int8 + scales)."""
+    w = BlockWeights()
+    w.dtype = W_INT8 if scales is not None else W_BF16
+    w.wqkv, w.wo, w.wgate, w.wup, w.wdown = (ptr(wqkv), ptr(wo), ptr(wgate),
+                                             ptr(wup), ptr(wdown))
+    if scales is not None:
+        w.wqkv_scale = ptr(scales["wqkv"])
+        w.wo_scale = ptr(scales["wo"])
+        w.wgate_scale = ptr(scales["wgate"])
+        w.wup_scale = ptr(scales["wup"])
+        w.wdown_scale = ptr(scales["wdown"])
+    return w
+
+
+def modln_cast(x, rows, D, shift, scale, out, stream=None):
+    _check(load().dit_modln_cast(ptr(x), rows, D, ptr(shift), ptr(scale),
+                                 ptr(out), stream_handle(stream)),
+           "dit_modln_cast")
+
+
+def gemm(args: GemmArgs, dev_status=None, stream=None):
+    _check(load().dit_gemm(ctypes.byref(args), ptr(dev_status),
+                           stream_handle(stream)), "dit_gemm")
+
+
+def attention(q, Tq, ldq, k, ldk, vt, ldvt, T, heads, head_dim, o, ldo,
+              dev_status=None, stream=None):
+    _check(load().dit_attention(ptr(q), Tq, ldq, ptr(k), ldk, ptr(vt), ldvt, T,
+                                heads, head_dim, ptr(o), ldo, ptr(dev_status),
+                                stream_handle(stream)), "dit_attention")

@@ -1,0 +1,93 @@
+"""Host-side driver of libditstream for PyTorch users.
+
+PyTorch supplies device memory and streams only: this module uploads
+weights, allocates the plan's workspace with ``torch.empty`` (so the caching
+allocator accounts for it) and calls the C ABI.  Every step of the block runs
+in the library's CUDA kernels; nothing here computes.
+"""
+
+from __future__ import annotations
+
+from dataclasses import dataclass
+from typing import List, Optional
+
+import torch
+
+from . import ditstream
+from .synth import DitInputs
+
+
+@dataclass
+class DeviceBlock:
+    tensors: dict            # device tensors (kept alive)
+    struct: ditstream.BlockWeights
+    mod: torch.Tensor        # [6, D] fp32 on device
+
+
+@dataclass
+class DeviceInputs:
+    x: torch.Tensor                        # [T, D] fp32 (pristine copy)
+    blocks: List[DeviceBlock]
+    mod_f: Optional[torch.Tensor] = None
+    wf: Optional[torch.Tensor] = None
+    wf_scale: Optional[torch.Tensor] = None
+
+
+def upload(inp: DitInputs, device="cuda") -> DeviceInputs:
+    """Copy seeded CPU inputs to the device (weights stay resident)."""
+    blocks = []
+    for bw, mod in zip(inp.blocks, inp.mods):
+        t = {k: v.to(device).contiguous() for k, v in bw.named().items()}
+        sc = None
+        if bw.scales is not None:
+            sc = {k: v.to(device).contiguous() for k, v in bw.scales.items()}
+            t.update({k + "_scale": v for k, v in sc.items()})
+        st = ditstream.block_weights(t["wqkv"], t["wo"], t["wgate"], t["wup"],
+                                     t["wdown"], scales=sc)
+        blocks.append(DeviceBlock(t, st, mod.to(device).contiguous()))
+    out = DeviceInputs(x=inp.x.to(device).contiguous(), blocks=blocks)
+    if inp.mod_f is not None:
+        out.mod_f = inp.mod_f.to(device).contiguous()
+        out.wf = inp.wf.to(device).contiguous()
+        if inp.wf_scale is not None:
+            out.wf_scale = inp.wf_scale.to(device).contiguous()
+    return out
+
+
+class DitStack:
+    """A stack of DiT blocks (one plan, one workspace) plus an optional
+    final layer.  ``forward`` updates ``x`` in place and returns the final
+    layer's output when there is one."""
+
+    def __init__(self, T, D, heads, F, mlp_chunk, attn_chunk, ffn_slice=0,
+                 device="cuda"):
+        self.plan = ditstream.block_plan(T, D, heads, F, mlp_chunk, attn_chunk,
+                                         ffn_slice)
+        self.T, self.D = T, D
+        self.workspace = torch.empty(self.plan.workspace_bytes(),
+                                     dtype=torch.uint8, device=device)
+        self.plan.bind_workspace(self.workspace)
+        self.device = device
+
+    def forward(self, x: torch.Tensor, dev: DeviceInputs, stream=None,
+                out: Optional[torch.Tensor] = None):
+        if stream is None:
+            stream = torch.cuda.current_stream(x.device)
+        for b in dev.blocks:
+            self.plan.forward(x, b.struct, b.mod, stream)
+        if dev.wf is not None:
+            if out is None:
+                out = torch.empty(self.T, 64, dtype=torch.float32,
+                                  device=x.device)
+            self.plan.final_forward(x, dev.wf, dev.wf_scale, dev.mod_f, out,
+                                    stream)
+            return out
+        return None
+
+    def check(self, stream=None):
+        """Synchronise and raise if a kernel recorded a device-side error."""
+        if stream is None:
+            stream = torch.cuda.current_stream()
+        s = self.plan.sync_status(stream)
+        if s != ditstream.OK:
+            raise ditstream.DitError(s, "dit_block_sync_status")

@@ -1,0 +1,176 @@
+"""CPU checks of the C ABI: the library loads, exports what the header
+declares, validates arguments and lays out its workspace as documented.
+No kernel is launched (no GPU needed)."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from memory_bounded_video_gb300 import build as dbuild
+from memory_bounded_video_gb300 import ditstream as ds
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "ditstream.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    dbuild.build()
+    return ds.load()
+
+
+def header_functions():
+    src = open(HEADER).read()
+    return sorted(set(re.findall(r"^DIT_API [^(]*?\b(dit_\w+)\(", src, re.M)))
+
+
+def header_defines():
+    src = open(HEADER).read()
+    return {k: int(v) for k, v in
+            re.findall(r"#define (DIT_\w+) \(?(-?\d+)\)?", src)}
+
+
+def test_every_declared_symbol_is_exported(lib):
+    declared = header_functions()
+    assert len(declared) >= 15
+    assert sorted(ds.SYMBOLS) == declared
+    for name in declared:
+        assert hasattr(lib, name), name
+
+
+def test_binding_constants_match_header():
+    d = header_defines()
+    pairs = dict(DIT_OK=ds.OK, DIT_ERR_INVALID_ARG=ds.ERR_INVALID_ARG,
+                 DIT_ERR_CHUNK_ALIGN=ds.ERR_CHUNK_ALIGN, DIT_ERR_ALIGN=ds.ERR_ALIGN,
+                 DIT_ERR_NO_WORKSPACE=ds.ERR_NO_WORKSPACE,
+                 DIT_ERR_WORKSPACE_TOO_SMALL=ds.ERR_WORKSPACE_TOO_SMALL,
+                 DIT_ERR_CUDA=ds.ERR_CUDA, DIT_ERR_TIMEOUT=ds.ERR_TIMEOUT,
+                 DIT_ERR_UNSUPPORTED_ARCH=ds.ERR_UNSUPPORTED_ARCH,
+                 DIT_W_BF16=ds.W_BF16, DIT_W_INT8=ds.W_INT8,
+                 DIT_EPI_STORE_BF16=ds.EPI_STORE_BF16,
+                 DIT_EPI_STORE_F32=ds.EPI_STORE_F32, DIT_EPI_KV=ds.EPI_KV,
+                 DIT_EPI_RESID=ds.EPI_RESID, DIT_EPI_SWIGLU=ds.EPI_SWIGLU,
+                 DIT_EPI_DOWN=ds.EPI_DOWN,
+                 DITSTREAM_ABI_VERSION=None)
+    for k, v in pairs.items():
+        if v is not None:
+            assert d[k] == v, k
+
+
+def test_struct_layouts_match_header():
+    # field order and count of the two POD structs
+    src = open(HEADER).read()
+    body = re.search(r"typedef struct \{([^}]*)\} dit_gemm_args_t;", src).group(1)
+    fields = re.findall(r"\b(\w+);", re.sub(r"/\*.*?\*/", "", body, flags=re.S))
+    assert fields == [f for f, _ in ds.GemmArgs._fields_]
+    body = re.search(r"typedef struct \{([^}]*)\} dit_block_weights_t;", src).group(1)
+    fields = re.findall(r"\b(\w+);", body)
+    assert fields == [f for f, _ in ds.BlockWeights._fields_]
+
+
+def test_status_strings(lib):
+    assert ds.abi_version() == 1
+    for s in (0, -1, -2, -3, -4, -5, -6, -7, -8):
+        assert ds.status_string(s) and ds.status_string(s) != "unknown status"
+    assert ds.status_string(-99) == "unknown status"
+
+
+@pytest.mark.parametrize("args,status", [
+    ((0, 256, 4, 704, 128, 128), ds.ERR_INVALID_ARG),       # T = 0
+    ((512, 250, 4, 704, 128, 128), ds.ERR_INVALID_ARG),     # D % 128
+    ((512, 256, 3, 704, 128, 128), ds.ERR_INVALID_ARG),     # D % heads
+    ((512, 256, 8, 704, 128, 128), ds.ERR_INVALID_ARG),     # d = 32
+    ((512, 256, 4, 700, 128, 128), ds.ERR_INVALID_ARG),     # ffn % 64
+    ((512, 256, 4, 704, 100, 128), ds.ERR_CHUNK_ALIGN),
+    ((512, 256, 4, 704, 128, 64), ds.ERR_CHUNK_ALIGN),
+    ((512, 256, 4, 704, -128, 128), ds.ERR_INVALID_ARG),
+])
+def test_plan_rejects_bad_arguments(lib, args, status):
+    h = ctypes.c_void_p()
+    assert lib.dit_block_plan(*args, ctypes.byref(h)) == status
+    assert not h.value
+
+
+def test_plan_ex_rejects_bad_ffn_slice(lib):
+    h = ctypes.c_void_p()
+    assert lib.dit_block_plan_ex(512, 256, 4, 704, 128, 128, 96,
+                                 ctypes.byref(h)) == ds.ERR_INVALID_ARG
+    assert lib.dit_block_plan_ex(512, 256, 4, 704, 128, 128, 768,
+                                 ctypes.byref(h)) == ds.ERR_INVALID_ARG
+
+
+def rup(v, a=1024):
+    return (v + a - 1) // a * a
+
+
+def expected_workspace(T, D, F, cm, ca, fs):
+    """The layout documented for dit_block_workspace_bytes, restated."""
+    cm = T if cm == 0 or cm >= T else cm
+    ca = T if ca == 0 or ca >= T else ca
+    fs = fs or F
+    k = 1024
+    vt = rup(k + 2 * T * D)
+    phase = rup(vt + 2 * D * rup(T, 128))
+    attn = rup(rup(phase + 2 * ca * D) + 2 * ca * D)
+    mlp = rup(rup(phase + 2 * cm * D) + 2 * cm * fs)
+    if fs < F:
+        mlp = rup(mlp + 4 * cm * D)
+    return max(attn, mlp)
+
+
+@pytest.mark.parametrize("cfg", [
+    (512, 256, 4, 704, 128, 128, 0),
+    (4096, 1024, 16, 2816, 0, 512, 0),
+    (16384, 3072, 24, 8192, 8192, 0, 0),
+    (65536, 3072, 24, 8192, 4096, 4096, 2048),
+    (1000, 1024, 8, 2816, 256, 384, 1024),
+])
+def test_workspace_layout_and_info(lib, cfg):
+    T, D, H, F, cm, ca, fs = cfg
+    p = ds.block_plan(T, D, H, F, cm, ca, fs)
+    assert p.workspace_bytes() == expected_workspace(T, D, F, cm, ca, fs)
+    info = p.info()
+    assert info["T"] == T and info["D"] == D and info["heads"] == H
+    assert info["mlp_chunk"] == (T if cm == 0 or cm >= T else cm)
+    assert info["attn_chunk"] == (T if ca == 0 or ca >= T else ca)
+    assert info["ffn_slice"] == (fs or F)
+
+
+def test_workspace_beyond_kv_floor_is_bounded_by_chunk():
+    # 4*T*D (K and V) grows with T; the rest depends on the chunks only.
+    D, F = 3072, 8192
+    rest = []
+    for T in (8192, 16384, 32768, 65536):
+        total = expected_workspace(T, D, F, 4096, 4096, 2048)
+        rest.append(total - 4 * T * D)
+    assert max(rest) - min(rest) <= 4 * 1024
+    assert ds.block_plan(65536, D, 24, F, 4096, 4096, 2048).workspace_bytes() \
+        - 4 * 65536 * D == rest[-1]
+
+
+def test_forward_without_workspace_fails_closed(lib):
+    p = ds.block_plan(512, 256, 4, 704, 128, 128)
+    w = ds.block_weights(16, 16, 16, 16, 16)
+    with pytest.raises(ds.DitError) as e:
+        p.forward(None, w, 16)
+    assert e.value.status == ds.ERR_INVALID_ARG  # null x
+    with pytest.raises(ds.DitError) as e:
+        p.forward(16, w, 16)
+    assert e.value.status == ds.ERR_NO_WORKSPACE
+
+
+def test_stage_entry_points_validate_before_launch(lib):
+    # misaligned or invalid arguments are rejected on the host
+    assert lib.dit_modln_cast(8, 4, 256, 16, 16, 16, None) == ds.ERR_ALIGN
+    assert lib.dit_modln_cast(16, 4, 200, 16, 16, 16, None) == ds.ERR_INVALID_ARG
+    g = ds.GemmArgs(mode=ds.EPI_STORE_BF16, M=128, N=100, K=64, a=16, lda=64,
+                    b0=16, ldb=64, out=16, ldo=128)
+    assert lib.dit_gemm(ctypes.byref(g), None, None) == ds.ERR_INVALID_ARG
+    g.N, g.mode = 128, 99
+    assert lib.dit_gemm(ctypes.byref(g), None, None) == ds.ERR_INVALID_ARG
+    assert lib.dit_attention(16, 128, 256, 16, 256, 16, 512, 512, 4, 32, 16,
+                             256, None, None) == ds.ERR_INVALID_ARG
+    assert lib.dit_attention(16, 128, 256, 16, 256, 16, 500, 512, 4, 64, 16,
+                             256, None, None) == ds.ERR_INVALID_ARG

@@ -1,0 +1,168 @@
+"""Whole-block parity of dit_block_forward against the float64 oracle, and
+bit-identity of the output across chunk settings (the exactness property of
+"LayerStream: H3 Chunking": chunked output equal to the unchunked output).
+
+Tolerance on the residual stream x_out: relative L2 <= 1e-2 and max-abs <=
+5e-2.  Because x ~ N(0, 1) dominates x_out, the branch x_out - x_in is
+checked as well (relative L2 <= 2e-2)."""
+
+import numpy as np
+import pytest
+import torch
+
+from memory_bounded_video_gb300 import build as dbuild
+from memory_bounded_video_gb300 import ditstream as ds
+from memory_bounded_video_gb300 import runner, synth
+from oracle import block as ob
+
+pytestmark = pytest.mark.gpu
+
+REL_L2 = 1e-2
+MAX_ABS = 5e-2
+BRANCH_REL_L2 = 2e-2
+
+
+@pytest.fixture(scope="module", autouse=True)
+def lib():
+    dbuild.build()
+    return ds.load()
+
+
+def weights64(bw, qk_mult=1.0):
+    w = ob.DitWeights(**{k: v.double().numpy() for k, v in bw.named().items()})
+    if qk_mult != 1.0:
+        D = w.D
+        w.wqkv = w.wqkv.copy()
+        w.wqkv[:2 * D] *= qk_mult
+    return w
+
+
+def sharpen(inp, mult):
+    """Multiply Wq and Wk by a power of two (exact in bf16) so the softmax is
+    peaked and the online rescaling is exercised."""
+    for bw in inp.blocks:
+        D = bw.wo.shape[0]
+        w = bw.wqkv.float()
+        w[:2 * D] *= mult
+        bw.wqkv = w.to(torch.bfloat16)
+    return inp
+
+
+def run_gpu(inp, cm, ca, fs=0):
+    T, D = inp.x.shape
+    H, F = inp.meta["heads"], inp.meta["F"]
+    dev = runner.upload(inp)
+    stack = runner.DitStack(T, D, H, F, cm, ca, fs)
+    x = dev.x.clone()
+    stack.forward(x, dev)
+    stack.check()
+    return x
+
+
+def compare(got, ref, x_in):
+    got, ref = np.asarray(got, np.float64), np.asarray(ref, np.float64)
+    rel = np.linalg.norm(got - ref) / np.linalg.norm(ref)
+    mx = np.abs(got - ref).max()
+    br = np.linalg.norm((got - x_in) - (ref - x_in)) / np.linalg.norm(ref - x_in)
+    return rel, mx, br
+
+
+@pytest.mark.parametrize("sharp", [1.0, 8.0])
+def test_block_T512_D256_full_oracle(sharp):
+    inp = synth.make_workload("dit_T512_D256", seed=0)
+    if sharp != 1.0:
+        sharpen(inp, sharp)
+    x = run_gpu(inp, 128, 128)
+    ref = ob.dit_block(inp.x.double().numpy(), weights64(inp.blocks[0]),
+                       inp.mods[0].double().numpy(), inp.meta["heads"])
+    rel, mx, br = compare(x.cpu().numpy(), ref, inp.x.double().numpy())
+    assert rel <= REL_L2 and mx <= MAX_ABS and br <= BRANCH_REL_L2, (rel, mx, br)
+
+
+def test_block_T4096_D1024_full_oracle():
+    inp = synth.make_workload("dit_T4096_D1024", seed=1)
+    x = run_gpu(inp, 512, 512)
+    ref = ob.dit_block(inp.x.double().numpy(), weights64(inp.blocks[0]),
+                       inp.mods[0].double().numpy(), inp.meta["heads"])
+    rel, mx, br = compare(x.cpu().numpy(), ref, inp.x.double().numpy())
+    assert rel <= REL_L2 and mx <= MAX_ABS and br <= BRANCH_REL_L2, (rel, mx, br)
+
+
+def test_block_bit_identical_across_chunks_T4096():
+    inp = synth.make_workload("dit_T4096_D1024", seed=2)
+    T, D = inp.x.shape
+    dev = runner.upload(inp)
+    outs = {}
+    for cm in (0, 512, 1024, 4096):
+        for ca in (0, 512, 1024, 4096):
+            stack = runner.DitStack(T, D, 16, 2816, cm, ca)
+            x = dev.x.clone()
+            stack.forward(x, dev)
+            stack.check()
+            outs[(cm, ca)] = x
+    base = outs[(0, 0)]
+    for key, x in outs.items():
+        assert torch.equal(x, base), key
+    # repeat run: deterministic
+    stack = runner.DitStack(T, D, 16, 2816, 512, 1024)
+    x = dev.x.clone()
+    stack.forward(x, dev)
+    stack.check()
+    assert torch.equal(x, base)
+
+
+def test_block_bit_identical_across_ffn_slices_and_ragged_chunks():
+    # T not a multiple of the chunks or of 128; FFN slices of 64, 256, 704
+    inp = synth.make_inputs(1000, 256, 4, 704, seed=3)
+    T, D = inp.x.shape
+    dev = runner.upload(inp)
+    outs = []
+    for cm, ca, fs in [(0, 0, 0), (128, 384, 64), (256, 128, 256), (384, 0, 704)]:
+        stack = runner.DitStack(T, D, 4, 704, cm, ca, fs)
+        x = dev.x.clone()
+        stack.forward(x, dev)
+        stack.check()
+        outs.append(x)
+    for x in outs[1:]:
+        assert torch.equal(x, outs[0])
+    ref = ob.dit_block(inp.x.double().numpy(), weights64(inp.blocks[0]),
+                       inp.mods[0].double().numpy(), 4)
+    rel, mx, br = compare(outs[0].cpu().numpy(), ref, inp.x.double().numpy())
+    assert rel <= REL_L2 and mx <= MAX_ABS and br <= BRANCH_REL_L2, (rel, mx, br)
+
+
+def test_zero_gates_leave_x_bitwise_unchanged():
+    inp = synth.make_workload("dit_T512_D256", seed=4)
+    inp.mods[0][2] = 0
+    inp.mods[0][5] = 0
+    x = run_gpu(inp, 128, 256)
+    assert torch.equal(x.cpu(), inp.x)
+
+
+def test_single_token():
+    inp = synth.make_inputs(1, 256, 4, 704, seed=5)
+    x = run_gpu(inp, 0, 0)
+    ref = ob.dit_block(inp.x.double().numpy(), weights64(inp.blocks[0]),
+                       inp.mods[0].double().numpy(), 4)
+    rel, mx, br = compare(x.cpu().numpy(), ref, inp.x.double().numpy())
+    assert rel <= REL_L2 and mx <= MAX_ABS, (rel, mx)
+
+
+def sampled_rows(T, n=512, seed=0):
+    rng = np.random.default_rng(seed)
+    rows = set(range(128)) | set(range(T - 128, T))
+    rows |= set(rng.choice(T, size=n, replace=False).tolist())
+    return np.array(sorted(rows))
+
+
+@pytest.mark.parametrize("ca", [0, 8192])
+def test_block_T16384_D3072_sampled_rows(ca):
+    inp = synth.make_workload("dit_T16384_D3072", seed=0)
+    T = inp.x.shape[0]
+    x = run_gpu(inp, 8192, ca)
+    rows = sampled_rows(T, 256)
+    ref, _ = ob.dit_block_rows(inp.x.double().numpy(), weights64(inp.blocks[0]),
+                               inp.mods[0].double().numpy(), 24, rows)
+    got = x.cpu().numpy()[rows]
+    rel, mx, br = compare(got, ref, inp.x.double().numpy()[rows])
+    assert rel <= REL_L2 and mx <= MAX_ABS and br <= BRANCH_REL_L2, (rel, mx, br)
