@@ -52,7 +52,8 @@ def test_modln_cast_matches_oracle(rows, D):
     shift = randn(g, D, std=0.1)
     scale = randn(g, D, std=0.1)
     out = torch.empty(rows, D, dtype=torch.bfloat16, device="cuda")
-    ds.modln_cast(x.cuda(), rows, D, shift.cuda(), scale.cuda(), out)
+    xd, shd, scd = x.cuda(), shift.cuda(), scale.cuda()
+    ds.modln_cast(xd, rows, D, shd, scd, out)
     torch.cuda.synchronize()
     ref = ob.ln_modulate(f64(x), f64(shift), f64(scale))
     got = f64(out)
@@ -76,14 +77,29 @@ def test_modln_cast_is_row_local():
 
 # ---------------------------------------------------------------- GEMM
 
+class Gemm:
+    """GemmArgs plus references to every device tensor it points at (the
+    tensors must outlive the launch)."""
+
+    def __init__(self, mode, a, b, **kw):
+        M, K = a.shape
+        N = b.shape[0]
+        self.keep = [a, b]
+        self.args = ds.GemmArgs(mode=mode, M=M, N=N, K=K, a=ds.ptr(a),
+                                lda=a.stride(0), b0=ds.ptr(b),
+                                ldb=b.stride(0), b_dtype=ds.W_BF16)
+        for k, v in kw.items():
+            if isinstance(v, torch.Tensor):
+                self.keep.append(v)
+                v = ds.ptr(v)
+            setattr(self.args, k, v)
+
+    def run(self, st=None):
+        ds.gemm(self.args, st)
+
+
 def gemm_args(mode, a, b, **kw):
-    M, K = a.shape
-    N = b.shape[0]
-    args = ds.GemmArgs(mode=mode, M=M, N=N, K=K, a=ds.ptr(a), lda=K, b0=ds.ptr(b),
-                       ldb=b.stride(0), b_dtype=ds.W_BF16)
-    for k, v in kw.items():
-        setattr(args, k, ds.ptr(v) if isinstance(v, torch.Tensor) else v)
-    return args
+    return Gemm(mode, a, b, **kw)
 
 
 def bf16_pair(g, M, N, K, std_a=1.0, std_b=0.05):
@@ -106,7 +122,7 @@ def test_gemm_store_f32(M, N, K):
     a, b = bf16_pair(g, M, N, K)
     out = torch.full((M, N), float("nan"), device="cuda")
     st = status_buf()
-    ds.gemm(gemm_args(ds.EPI_STORE_F32, a.cuda(), b.cuda(), out=out, ldo=N), st)
+    gemm_args(ds.EPI_STORE_F32, a.cuda(), b.cuda(), out=out, ldo=N).run(st)
     assert_status_ok(st)
     check_close(f64(out), f64(a) @ f64(b).T, K, "store_f32")
 
@@ -117,9 +133,9 @@ def test_gemm_store_bf16_and_row_locality():
     a, b = bf16_pair(g, M, N, K)
     ad, bd = a.cuda(), b.cuda()
     out = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
-    ds.gemm(gemm_args(ds.EPI_STORE_BF16, ad, bd, out=out, ldo=N))
+    gemm_args(ds.EPI_STORE_BF16, ad, bd, out=out, ldo=N).run()
     part = torch.empty(M - 300, N, dtype=torch.bfloat16, device="cuda")
-    ds.gemm(gemm_args(ds.EPI_STORE_BF16, ad[300:], bd, out=part, ldo=N))
+    gemm_args(ds.EPI_STORE_BF16, ad[300:], bd, out=part, ldo=N).run()
     torch.cuda.synchronize()
     ref = f64(a) @ f64(b).T
     err = np.abs(f64(out) - ref) / np.maximum(np.abs(ref), 1e-2)
@@ -133,8 +149,8 @@ def test_gemm_kv_epilogue_writes_k_and_transposed_v():
     a, b = bf16_pair(g, M, 2 * D, D)
     K = torch.zeros(T_pad, D, dtype=torch.bfloat16, device="cuda")
     Vt = torch.zeros(D, T_pad, dtype=torch.bfloat16, device="cuda")
-    ds.gemm(gemm_args(ds.EPI_KV, a.cuda(), b.cuda(), out=K, ldo=D, out2=Vt,
-                      ldo2=T_pad, row_offset=row_off, split_n=D))
+    gemm_args(ds.EPI_KV, a.cuda(), b.cuda(), out=K, ldo=D, out2=Vt,
+              ldo2=T_pad, row_offset=row_off, split_n=D).run()
     torch.cuda.synchronize()
     ref = f64(a) @ f64(b).T
     k_got = f64(K[row_off:row_off + M])
@@ -154,8 +170,8 @@ def test_gemm_resid_epilogue():
     x = randn(g, M, N)
     gate = torch.rand(N, generator=g)
     xd = x.cuda()
-    ds.gemm(gemm_args(ds.EPI_RESID, a.cuda(), b.cuda(), x=xd, ldx=N,
-                      gate=gate.cuda()))
+    gemm_args(ds.EPI_RESID, a.cuda(), b.cuda(), x=xd, ldx=N,
+              gate=gate.cuda()).run()
     torch.cuda.synchronize()
     ref = f64(x) + f64(gate) * (f64(a) @ f64(b).T)
     assert np.abs(f64(xd) - ref).max() < 1e-4
@@ -168,10 +184,8 @@ def test_gemm_swiglu_epilogue():
     wg = randn(g, N, K, std=0.1).to(torch.bfloat16)
     wu = randn(g, N, K, std=0.1).to(torch.bfloat16)
     out = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
-    args = gemm_args(ds.EPI_SWIGLU, a.cuda(), wg.cuda(), out=out, ldo=N)
-    wud = wu.cuda()
-    args.b1 = ds.ptr(wud)
-    ds.gemm(args)
+    gemm_args(ds.EPI_SWIGLU, a.cuda(), wg.cuda(), b1=wu.cuda(), out=out,
+              ldo=N).run()
     torch.cuda.synchronize()
     gv, uv = f64(a) @ f64(wg).T, f64(a) @ f64(wu).T
     ref = ob.silu(gv) * uv
@@ -188,16 +202,14 @@ def test_gemm_down_carry_is_bit_identical_to_unsliced(fs):
     x = randn(g, M, D)
     gate = torch.rand(D, generator=g).cuda()
     x_ref = x.cuda()
-    ds.gemm(gemm_args(ds.EPI_DOWN, h, wd, x=x_ref, ldx=D, gate=gate,
-                      acc_load=0, acc_final=1))
+    gemm_args(ds.EPI_DOWN, h, wd, x=x_ref, ldx=D, gate=gate, acc_load=0,
+              acc_final=1).run()
     x_sl = x.cuda()
     acc = torch.empty(M, D, device="cuda")
     for f in range(0, F, fs):
-        args = gemm_args(ds.EPI_DOWN, h[:, f:f + fs], wd[:, f:f + fs], x=x_sl,
-                         ldx=D, gate=gate, acc=acc, ldacc=D, acc_load=int(f > 0),
-                         acc_final=int(f + fs >= F))
-        args.lda, args.ldb = F, F
-        ds.gemm(args)
+        gemm_args(ds.EPI_DOWN, h[:, f:f + fs], wd[:, f:f + fs], x=x_sl,
+                  ldx=D, gate=gate, acc=acc, ldacc=D, acc_load=int(f > 0),
+                  acc_final=int(f + fs >= F)).run()
     torch.cuda.synchronize()
     ref = f64(x) + f64(gate) * (f64(h) @ f64(wd).T)
     assert np.abs(f64(x_ref) - ref).max() < 1e-4
@@ -214,7 +226,8 @@ def run_attention(q, k, v, heads, hd):
     vt[:, :T] = v.cuda().T
     o = torch.empty(Tq, D, dtype=torch.bfloat16, device="cuda")
     st = status_buf()
-    ds.attention(q.cuda(), Tq, D, k.cuda(), D, vt, ldvt, T, heads, hd, o, D, st)
+    qd, kd = q.cuda(), k.cuda()
+    ds.attention(qd, Tq, D, kd, D, vt, ldvt, T, heads, hd, o, D, st)
     assert_status_ok(st)
     return o
 
