@@ -1,0 +1,462 @@
+#!/usr/bin/env python
+"""Throughput of the bounded-activation DiT block forward on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                    [--impl ours|reference]
+
+A step is one pass of the whole hot path (every block of the workload, plus
+the final layer when it has one) over one batch of seeded synthetic tokens
+already resident in HBM.  The forward is in place on the residual stream, so
+step i+1 runs on step i's output (the work per step does not depend on the
+values).  W untimed warm-up steps, then exactly K steps between CUDA events
+on the launching stream, bracketed by a barrier and a device synchronize;
+the max over ranks is reported.  Inputs are larger than L2 (x alone is
+4*T*D bytes, K/V another 4*T*D), so L2 is not flushed between steps.
+
+One JSON line is printed by rank 0.  ``value`` is block-tokens per second
+(tokens x blocks per step / step time) summed over ranks.  With N > 1 every
+rank runs an independent replica (the path has no exchange step on one GPU;
+"scaling": "weak").
+
+``--impl reference`` times the float64 CPU oracle instead, on a bounded
+sample of the same workload (see ``cpu_sample``).
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+HEADLINE = "dit_T32768_D3072"
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0,
+                  "bf16_tflops_sustained": 1700.0}
+
+# kernel kind -> source file whose hash keys the ncu traffic figure
+KIND_SOURCE = {"attention": "attention.cu", "modln": "modln.cu",
+               "final": "final.cu", "gemm_kv": "gemm.cu", "gemm_q": "gemm.cu",
+               "gemm_o": "gemm.cu", "gemm_swiglu": "gemm.cu",
+               "gemm_down": "gemm.cu"}
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--workload", default=HEADLINE)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--cpu-rows", type=int, default=256,
+                    help="token rows in the oracle's timed sample")
+    return ap.parse_args(argv)
+
+
+# ------------------------------------------------------------------ helpers
+
+def load_peaks():
+    try:
+        with open(PEAKS_FILE) as f:
+            p = json.load(f)
+        return p, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def source_sha(name):
+    path = os.path.join(ROOT, "memory_bounded_video_gb300", "csrc", name)
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def traffic_for(kind, workload):
+    """DRAM bytes per launch from a committed ncu capture, if the kernel's
+    source is unchanged since (else None)."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            t = json.load(f)
+    except (OSError, ValueError):
+        return None
+    e = t.get(workload, {}).get(kind)
+    if not e or e.get("source_sha") != source_sha(KIND_SOURCE[kind]):
+        return None
+    return e.get("bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples every 200 ms while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,"
+              "clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_id=None):
+        self.proc = None
+        self.path = None
+        self.device_id = device_id
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}",
+               "--format=csv,noheader,nounits", "-lms", "200"]
+        if self.device_id:
+            cmd += ["-i", self.device_id]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=open(self.path, "w"),
+                                         stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.3)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    rows.append(dict(sm=float(parts[1]), sm_max=float(parts[2]),
+                                     power=float(parts[3]),
+                                     hw_slowdown=parts[5] == "Active",
+                                     hw_thermal=parts[6] == "Active",
+                                     sw_thermal=parts[7] == "Active",
+                                     sw_power_cap=parts[8] == "Active"))
+                except ValueError:
+                    continue
+        os.unlink(self.path)
+        if not rows:
+            return None
+        pmax = max(r["power"] for r in rows)
+        loaded = [r for r in rows if r["power"] >= 0.5 * pmax] or rows
+        reasons = sorted({k for r in loaded for k in
+                          ("hw_slowdown", "hw_thermal", "sw_thermal",
+                           "sw_power_cap") if r[k]})
+        names = {"hw_thermal": "hw_thermal_slowdown",
+                 "sw_thermal": "sw_thermal_slowdown"}
+        return {"sm_mhz": statistics.median(r["sm"] for r in loaded),
+                "sm_max_mhz": max(r["sm_max"] for r in rows),
+                "reasons": [names.get(k, k) for k in reasons],
+                "samples": len(rows), "power_w_max": pmax}
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+# ------------------------------------------------------------------ oracle (CPU) leg
+
+def cpu_sample(cfg, inp, rows_n, steps=1, warmup=0):
+    """Time the float64 oracle on a bounded sample of the workload.
+
+    Per block: K and V of all T tokens are computed first (untimed set-up, the
+    oracle's own projection); the timed sample is the K/V projection of
+    `rows_n` token rows plus every other stage of the block for those rows,
+    attending to all T keys, plus the final layer on those rows when the
+    workload has one.  Throughput = blocks x rows / time."""
+    import numpy as np
+    from oracle import block as ob
+
+    T, D, H = cfg["T"], cfg["D"], cfg["heads"]
+    rows = np.linspace(0, T - 1, rows_n).astype(np.int64)
+    x = inp.x.double().numpy()
+    blocks = []
+    for bw, mod in zip(inp.blocks, inp.mods):
+        if bw.int8:
+            w = ob.DitWeights(**{k: ob.dequant_int8(v.numpy(), bw.scales[k].numpy())
+                                 for k, v in bw.named().items()})
+        else:
+            w = ob.DitWeights(**{k: v.double().numpy() for k, v in bw.named().items()})
+        blocks.append((w, mod.double().numpy()))
+    # set-up: K/V of every token (block inputs taken as x for every block;
+    # the cost does not depend on the values)
+    kvs = []
+    for w, mod in blocks:
+        a = ob.ln_modulate(x, mod[0], mod[1])
+        _, wk, wv = w.q_k_v()
+        kvs.append((a @ wk.T, a @ wv.T))
+    wf = None
+    if inp.wf is not None:
+        wf = (ob.dequant_int8(inp.wf.numpy(), inp.wf_scale.numpy())
+              if inp.wf_scale is not None else inp.wf.double().numpy())
+        mod_f = inp.mod_f.double().numpy()
+
+    def one():
+        t0 = time.perf_counter()
+        for (w, mod), kv in zip(blocks, kvs):
+            a = ob.ln_modulate(x[rows], mod[0], mod[1])
+            _, wk, wv = w.q_k_v()
+            _ = (a @ wk.T, a @ wv.T)
+            ob.dit_block_rows(x, w, mod, H, rows, kv=kv)
+        if wf is not None:
+            ob.final_layer(x[rows], wf, mod_f)
+        return time.perf_counter() - t0
+
+    for _ in range(warmup):
+        one()
+    times = [one() for _ in range(steps)]
+    per_step = sum(times) / len(times)
+    value = len(blocks) * rows_n / per_step
+    sample = (f"{rows_n} of {T} token rows per block (their K/V projection, "
+              f"LN-mod, Q, attention against all {T} keys, O-proj, SwiGLU MLP"
+              + (", final layer" if wf is not None else "")
+              + f") x {len(blocks)} block(s), float64 numpy oracle; K/V of all "
+              "tokens precomputed untimed")
+    return value, per_step, sample, times
+
+
+# ------------------------------------------------------------------ GPU leg
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import torch.distributed as dist
+
+    from memory_bounded_video_gb300 import build as dbuild
+    from memory_bounded_video_gb300 import ditstream, runner, synth
+    from oracle import block as ob
+
+    cfg = dict(synth.WORKLOADS[args.workload])
+    T, D, H, F = cfg["T"], cfg["D"], cfg["heads"], cfg["F"]
+    dev_name = f"cuda:{local_rank}"
+    torch.cuda.set_device(local_rank)
+    dbuild.build()
+    ditstream.load()
+
+    inp = synth.make_workload(args.workload, seed=rank)
+    dev = runner.upload(inp, dev_name)
+    stack = runner.DitStack(T, D, H, F, cfg["mlp_chunk"], cfg["attn_chunk"],
+                            cfg["ffn_slice"], device=dev_name)
+    x = dev.x.clone()
+    stream = torch.cuda.current_stream()
+    mem0 = torch.cuda.memory_allocated()
+    torch.cuda.reset_peak_memory_stats()
+    for _ in range(args.warmup):
+        stack.forward(x, dev, stream)
+    stack.check(stream)
+    peak_fwd = torch.cuda.max_memory_allocated() - mem0
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    stack.plan.profile_enable(True)
+    stack.plan.profile_read()
+    try:
+        uuid = "GPU-" + str(torch.cuda.get_device_properties(local_rank).uuid)
+    except Exception:
+        uuid = None
+    clocks = ClockSampler(uuid)
+    clocks.start()
+    barrier()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        stack.forward(x, dev, stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    clk = clocks.stop()
+    ms = e0.elapsed_time(e1)
+    prof = stack.plan.profile_read()
+    stack.plan.profile_enable(False)
+    stack.check(stream)
+    if world > 1:
+        t = torch.tensor([ms], device=dev_name)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+
+    blocks = cfg["blocks"]
+    tokens_per_step = blocks * T
+    value = tokens_per_step * args.steps * world / (ms / 1e3)
+    ms_per_step = ms / args.steps
+    flops_step = blocks * ob.block_flops(T, D, F)
+    peaks, peak_src = load_peaks()
+    tflops = flops_step / (ms_per_step / 1e3) / 1e12
+
+    # per-kernel breakdown and the dominant kernel's roofline
+    kernels = {}
+    total_k = sum(v["ms"] for v in prof.values()) or 1.0
+    for k, v in prof.items():
+        if v["launches"]:
+            kernels[k] = dict(launches=v["launches"], ms=round(v["ms"], 4),
+                              share=round(v["ms"] / total_k, 4))
+    dom = max(prof, key=lambda k: prof[k]["ms"])
+    d = prof[dom]
+    if d["unit"] == "flops":
+        achieved = d["work"] / (d["ms"] / 1e3) / 1e12
+        peak = peaks["bf16_tflops_sustained"]
+        roof = dict(bound="tensor", achieved=round(achieved, 2), peak=peak,
+                    unit="TFLOP/s", frac=round(achieved / peak, 4))
+        peak_note = f"bf16_tflops_sustained of {peak_src}"
+    else:
+        achieved = d["work"] / (d["ms"] / 1e3) / 1e9
+        peak = peaks["hbm_gbs"]
+        roof = dict(bound="hbm", achieved=round(achieved, 1), peak=peak,
+                    unit="GB/s", frac=round(achieved / peak, 4))
+        peak_note = f"hbm_gbs of {peak_src}"
+    roof["kernel"] = dom
+    roof["launch_ms"] = round(d["ms"] / d["launches"], 4)
+    roof["work_per_launch"] = d["work"] / d["launches"]
+    roof["peak_source"] = peak_note
+    roof["traffic"] = traffic_for(dom, args.workload)
+
+    line = {
+        "metric": "DiT-block tokens/s @32k tokens, % BF16 tensor peak, "
+                  "peak activation GiB",
+        "value": round(value, 1),
+        "unit": "block-tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16 (fp32 accumulate, fp32 residual)",
+        "data": "synthetic (seeded N(0,1) tokens, N(0,0.02) weights)",
+        "config": {"workload": args.workload, "T": T, "D": D, "heads": H,
+                   "head_dim": D // H, "ffn": F, "blocks": blocks,
+                   "final_layer": cfg["final"], "int8_weights": cfg["int8"],
+                   "mlp_chunk_tokens": cfg["mlp_chunk"],
+                   "attn_chunk_tokens": cfg["attn_chunk"],
+                   "ffn_slice": cfg["ffn_slice"] or F,
+                   "l2": "not flushed: inputs larger than L2 "
+                         f"(x {4 * T * D / 2**20:.0f} MiB, K/V "
+                         f"{4 * T * D / 2**20:.0f} MiB per block)",
+                   "parallelism": f"replicas x{world}"},
+        "tflops": round(tflops, 2),
+        "tensor_peak_frac": round(tflops / peaks["bf16_tflops_sustained"], 4),
+        "tensor_peak_frac_burst": round(tflops / peaks["bf16_tflops"], 4),
+        "peak_activation_gib": round(stack.plan.workspace_bytes() / 2**30, 4),
+        "activation_beyond_kv_gib": round(
+            (stack.plan.workspace_bytes() - 4 * T * D) / 2**30, 4),
+        "measured_forward_alloc_gib": round(peak_fwd / 2**30, 4),
+        "roofline": roof,
+        "kernels": kernels,
+        "gpu_launches": int(sum(v["launches"] for v in prof.values())),
+        "clocks": clk,
+    }
+
+    # e2e through the public API with host buffers
+    if not args.no_e2e:
+        x_host = inp.x.pin_memory()
+        res_shape = (T, 64) if cfg["final"] else (T, D)
+        out_host = torch.empty(res_shape, dtype=torch.float32).pin_memory()
+        out_dev = torch.empty(res_shape, dtype=torch.float32, device=dev_name)
+        k_e2e = max(1, min(args.steps, 5))
+
+        def e2e_step():
+            x.copy_(x_host, non_blocking=True)
+            res = stack.forward(x, dev, stream, out=out_dev if cfg["final"] else None)
+            out_host.copy_(res if res is not None else x, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize()
+        barrier()
+        f0 = torch.cuda.Event(enable_timing=True)
+        f1 = torch.cuda.Event(enable_timing=True)
+        f0.record(stream)
+        for _ in range(k_e2e):
+            e2e_step()
+        f1.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+        ms_e2e = f0.elapsed_time(f1)
+        if world > 1:
+            t = torch.tensor([ms_e2e], device=dev_name)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            ms_e2e = float(t.item())
+        line["e2e"] = {"value": round(tokens_per_step * k_e2e * world / (ms_e2e / 1e3), 1),
+                       "unit": "block-tokens/s",
+                       "h2d_bytes_per_step": 4 * T * D,
+                       "d2h_bytes_per_step": 4 * res_shape[0] * res_shape[1],
+                       "steps": k_e2e}
+
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v, per, sample, _ = cpu_sample(cfg, inp, args.cpu_rows)
+        line["cpu_baseline"] = {"value": round(v, 2), "unit": "block-tokens/s",
+                                "cores": cpu_cores(), "kind": "oracle",
+                                "sample": sample,
+                                "seconds_per_sample": round(per, 3)}
+    return line
+
+
+def run_reference(args):
+    from memory_bounded_video_gb300 import synth
+
+    cfg = dict(synth.WORKLOADS[args.workload])
+    inp = synth.make_workload(args.workload, seed=0)
+    value, per_step, sample, times = cpu_sample(cfg, inp, args.cpu_rows,
+                                                steps=args.steps,
+                                                warmup=args.warmup)
+    T = cfg["T"]
+    return {
+        "impl": "reference",
+        "metric": "DiT-block tokens/s @32k tokens, % BF16 tensor peak, "
+                  "peak activation GiB",
+        "value": round(value, 3), "unit": "block-tokens/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(per_step * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic (seeded)",
+        "config": {"workload": args.workload, "T": T, "D": cfg["D"],
+                   "heads": cfg["heads"], "ffn": cfg["F"],
+                   "blocks": cfg["blocks"], "final_layer": cfg["final"],
+                   "int8_weights": cfg["int8"]},
+        "cpu_baseline": {"value": round(value, 3), "unit": "block-tokens/s",
+                         "cores": cpu_cores(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 3), "unit": "block-tokens/s",
+                "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return 0
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    line = run_ours(args, rank, world, local_rank)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -180,6 +180,32 @@ DIT_API dit_status_t dit_final_forward(const dit_plan_t *plan, const float *x,
                                const float *mod_f, float *out,
                                dit_stream_t stream);
 
+/* ----------------------------------------------------------------------
+ * Per-kernel timing.  When enabled, every kernel that dit_block_forward and
+ * dit_final_forward launch is bracketed by two CUDA events recorded on the
+ * launching stream.  dit_block_profile_read() waits for those events, adds
+ * up, per kernel kind, the elapsed milliseconds, the launch count and the
+ * algorithmic work (flops for the tensor-core kinds: 2*M*N*K per GEMM,
+ * 4*rows*T*D per attention launch; bytes for the memory-bound kinds:
+ * 6*rows*D per modln launch, 4*T*D + 4*64*D + 4*64*T per final-layer launch),
+ * writes them to the caller's arrays of DIT_NUM_KINDS entries (any may be
+ * NULL) and clears the record.  Events are created by the library and kept
+ * with the plan.
+ * ---------------------------------------------------------------------- */
+#define DIT_K_MODLN 0
+#define DIT_K_GEMM_KV 1
+#define DIT_K_GEMM_Q 2
+#define DIT_K_ATTENTION 3
+#define DIT_K_GEMM_O 4
+#define DIT_K_GEMM_SWIGLU 5
+#define DIT_K_GEMM_DOWN 6
+#define DIT_K_FINAL 7
+#define DIT_NUM_KINDS 8
+
+DIT_API dit_status_t dit_block_profile_enable(dit_plan_t *plan, int enable);
+DIT_API dit_status_t dit_block_profile_read(dit_plan_t *plan, double *ms,
+                                            int64_t *launches, double *work);
+
 DIT_API const char *dit_status_string(dit_status_t s);
 /* Text of the last CUDA error seen by this thread's calls ("" if none). */
 DIT_API const char *dit_last_cuda_error(void);

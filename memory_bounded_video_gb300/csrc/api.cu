@@ -20,6 +20,7 @@
 #include <cstdio>
 #include <cstring>
 #include <new>
+#include <vector>
 
 #include "internal.h"
 
@@ -32,6 +33,16 @@ struct dit_plan {
     size_t off_k, off_vt, off_a, off_q, off_b, off_h, off_acc, total;
     uint8_t *ws;
     size_t ws_bytes;
+    // per-kernel timing (dit_block_profile_*)
+    struct Rec {
+        int kind;
+        cudaEvent_t a, b;
+        double work;
+    };
+    bool prof = false;
+    std::vector<cudaEvent_t> pool;
+    size_t pool_used = 0;
+    std::vector<Rec> recs;
 };
 
 namespace ds {
@@ -109,6 +120,31 @@ bool make_tmap_2d(CUtensorMap *m, CUtensorMapDataType dt, const void *base, uint
                                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
+}
+
+// Launch `fn` (returning a dit_status_t) bracketed by profiling events when
+// the plan has profiling enabled.
+template <class Fn>
+dit_status_t timed(dit_plan *p, cudaStream_t st, int kind, double work, Fn &&fn) {
+    if (!p->prof) return fn();
+    cudaEvent_t ev[2];
+    for (int i = 0; i < 2; ++i) {
+        if (p->pool_used == p->pool.size()) {
+            cudaEvent_t e;
+            const cudaError_t err = cudaEventCreate(&e);
+            if (err != cudaSuccess) return cuda_fail(err);
+            p->pool.push_back(e);
+        }
+        ev[i] = p->pool[p->pool_used++];
+    }
+    cudaError_t err = cudaEventRecord(ev[0], st);
+    if (err != cudaSuccess) return cuda_fail(err);
+    const dit_status_t r = fn();
+    if (r != DIT_OK) return r;
+    err = cudaEventRecord(ev[1], st);
+    if (err != cudaSuccess) return cuda_fail(err);
+    p->recs.push_back({kind, ev[0], ev[1], work});
+    return DIT_OK;
 }
 
 }  // namespace ds
@@ -190,7 +226,44 @@ dit_status_t dit_block_plan(int64_t T, int D, int heads, int ffn, int mlp_chunk_
     return dit_block_plan_ex(T, D, heads, ffn, mlp_chunk_tokens, attn_chunk_tokens, 0, out);
 }
 
-void dit_block_plan_destroy(dit_plan_t *plan) { delete plan; }
+void dit_block_plan_destroy(dit_plan_t *plan) {
+    if (!plan) return;
+    for (cudaEvent_t e : plan->pool) cudaEventDestroy(e);
+    delete plan;
+}
+
+dit_status_t dit_block_profile_enable(dit_plan_t *p, int enable) {
+    if (!p) return DIT_ERR_INVALID_ARG;
+    p->prof = enable != 0;
+    return DIT_OK;
+}
+
+dit_status_t dit_block_profile_read(dit_plan_t *p, double *ms, int64_t *launches, double *work) {
+    if (!p) return DIT_ERR_INVALID_ARG;
+    double t[DIT_NUM_KINDS] = {0}, w[DIT_NUM_KINDS] = {0};
+    int64_t n[DIT_NUM_KINDS] = {0};
+    dit_status_t r = DIT_OK;
+    for (const auto &rec : p->recs) {
+        float e = 0.f;
+        cudaError_t err = cudaEventSynchronize(rec.b);
+        if (err == cudaSuccess) err = cudaEventElapsedTime(&e, rec.a, rec.b);
+        if (err != cudaSuccess) {
+            r = cuda_fail(err);
+            break;
+        }
+        t[rec.kind] += e;
+        w[rec.kind] += rec.work;
+        n[rec.kind] += 1;
+    }
+    p->recs.clear();
+    p->pool_used = 0;
+    for (int k = 0; k < DIT_NUM_KINDS; ++k) {
+        if (ms) ms[k] = t[k];
+        if (launches) launches[k] = n[k];
+        if (work) work[k] = w[k];
+    }
+    return r;
+}
 
 dit_status_t dit_block_plan_info(const dit_plan_t *p, int64_t *T, int *D, int *heads, int *ffn,
                                  int *mlp_chunk, int *attn_chunk, int *ffn_slice) {
@@ -224,8 +297,10 @@ dit_status_t dit_block_bind_workspace(dit_plan_t *p, void *dev_ptr, size_t bytes
     return DIT_OK;
 }
 
-dit_status_t dit_block_forward(const dit_plan_t *p, float *x, const dit_block_weights_t *w,
+dit_status_t dit_block_forward(const dit_plan_t *cp, float *x, const dit_block_weights_t *w,
                                const float *mod, dit_stream_t stream) {
+    // the plan is logically const; only its profiling record changes
+    dit_plan *p = const_cast<dit_plan *>(cp);
     if (!p || !x || !w || !mod) return DIT_ERR_INVALID_ARG;
     if (!p->ws) return DIT_ERR_NO_WORKSPACE;
     if (!w->wqkv || !w->wo || !w->wgate || !w->wup || !w->wdown) return DIT_ERR_INVALID_ARG;
@@ -254,7 +329,10 @@ dit_status_t dit_block_forward(const dit_plan_t *p, float *x, const dit_block_we
     // pass 1: K and V of every token
     for (int64_t s = 0; s < T; s += p->ca) {
         const int64_t rows = (T - s < p->ca) ? T - s : p->ca;
-        if ((r = launch_modln(x + s * Dl, rows, D, shift1, scale1, a, st)) != DIT_OK) return r;
+        if ((r = timed(p, st, DIT_K_MODLN, 6.0 * rows * D,
+                       [&] { return launch_modln(x + s * Dl, rows, D, shift1, scale1, a, st); })) !=
+            DIT_OK)
+            return r;
         dit_gemm_args_t g{};
         g.mode = DIT_EPI_KV;
         g.M = rows;
@@ -271,12 +349,17 @@ dit_status_t dit_block_forward(const dit_plan_t *p, float *x, const dit_block_we
         g.ldo2 = p->t_pad;
         g.row_offset = s;
         g.split_n = D;
-        if ((r = launch_gemm(g, status, st)) != DIT_OK) return r;
+        if ((r = timed(p, st, DIT_K_GEMM_KV, 2.0 * rows * 2 * D * D,
+                       [&] { return launch_gemm(g, status, st); })) != DIT_OK)
+            return r;
     }
     // pass 2: Q per slab, attention against all keys, O-projection into x
     for (int64_t s = 0; s < T; s += p->ca) {
         const int64_t rows = (T - s < p->ca) ? T - s : p->ca;
-        if ((r = launch_modln(x + s * Dl, rows, D, shift1, scale1, a, st)) != DIT_OK) return r;
+        if ((r = timed(p, st, DIT_K_MODLN, 6.0 * rows * D,
+                       [&] { return launch_modln(x + s * Dl, rows, D, shift1, scale1, a, st); })) !=
+            DIT_OK)
+            return r;
         dit_gemm_args_t g{};
         g.mode = DIT_EPI_STORE_BF16;
         g.M = rows;
@@ -289,10 +372,14 @@ dit_status_t dit_block_forward(const dit_plan_t *p, float *x, const dit_block_we
         g.b_dtype = DIT_W_BF16;
         g.out = Q;
         g.ldo = D;
-        if ((r = launch_gemm(g, status, st)) != DIT_OK) return r;
+        if ((r = timed(p, st, DIT_K_GEMM_Q, 2.0 * rows * D * D,
+                       [&] { return launch_gemm(g, status, st); })) != DIT_OK)
+            return r;
         // O_s overwrites a_s (dead once Q_s exists)
-        if ((r = launch_attention(Q, rows, D, K, D, Vt, p->t_pad, T, p->heads, p->head_dim, a,
-                                  D, status, st)) != DIT_OK)
+        if ((r = timed(p, st, DIT_K_ATTENTION, 4.0 * rows * double(T) * D, [&] {
+                 return launch_attention(Q, rows, D, K, D, Vt, p->t_pad, T, p->heads,
+                                         p->head_dim, a, D, status, st);
+             })) != DIT_OK)
             return r;
         dit_gemm_args_t o{};
         o.mode = DIT_EPI_RESID;
@@ -307,7 +394,9 @@ dit_status_t dit_block_forward(const dit_plan_t *p, float *x, const dit_block_we
         o.x = x + s * Dl;
         o.ldx = D;
         o.gate = gate1;
-        if ((r = launch_gemm(o, status, st)) != DIT_OK) return r;
+        if ((r = timed(p, st, DIT_K_GEMM_O, 2.0 * rows * D * D,
+                       [&] { return launch_gemm(o, status, st); })) != DIT_OK)
+            return r;
     }
     // MLP: token chunks x FFN feature slices
     const uint16_t *wg = static_cast<const uint16_t *>(w->wgate);
@@ -315,7 +404,10 @@ dit_status_t dit_block_forward(const dit_plan_t *p, float *x, const dit_block_we
     const uint16_t *wd = static_cast<const uint16_t *>(w->wdown);
     for (int64_t c = 0; c < T; c += p->cm) {
         const int64_t rows = (T - c < p->cm) ? T - c : p->cm;
-        if ((r = launch_modln(x + c * Dl, rows, D, shift2, scale2, b, st)) != DIT_OK) return r;
+        if ((r = timed(p, st, DIT_K_MODLN, 6.0 * rows * D,
+                       [&] { return launch_modln(x + c * Dl, rows, D, shift2, scale2, b, st); })) !=
+            DIT_OK)
+            return r;
         for (int f = 0; f < F; f += p->fs) {
             const int fw = (F - f < p->fs) ? F - f : p->fs;
             dit_gemm_args_t g{};
@@ -331,7 +423,9 @@ dit_status_t dit_block_forward(const dit_plan_t *p, float *x, const dit_block_we
             g.b_dtype = DIT_W_BF16;
             g.out = h;
             g.ldo = p->fs;
-            if ((r = launch_gemm(g, status, st)) != DIT_OK) return r;
+            if ((r = timed(p, st, DIT_K_GEMM_SWIGLU, 4.0 * rows * fw * D,
+                           [&] { return launch_gemm(g, status, st); })) != DIT_OK)
+                return r;
             dit_gemm_args_t d{};
             d.mode = DIT_EPI_DOWN;
             d.M = rows;
@@ -349,7 +443,9 @@ dit_status_t dit_block_forward(const dit_plan_t *p, float *x, const dit_block_we
             d.x = x + c * Dl;
             d.ldx = D;
             d.gate = gate2;
-            if ((r = launch_gemm(d, status, st)) != DIT_OK) return r;
+            if ((r = timed(p, st, DIT_K_GEMM_DOWN, 2.0 * rows * D * fw,
+                           [&] { return launch_gemm(d, status, st); })) != DIT_OK)
+                return r;
         }
     }
     return DIT_OK;
@@ -369,12 +465,16 @@ dit_status_t dit_block_sync_status(const dit_plan_t *p, dit_stream_t stream) {
     return v == 0 ? DIT_OK : (v == DIT_ERR_TIMEOUT ? DIT_ERR_TIMEOUT : DIT_ERR_CUDA);
 }
 
-dit_status_t dit_final_forward(const dit_plan_t *p, const float *x, const void *wf,
+dit_status_t dit_final_forward(const dit_plan_t *cp, const float *x, const void *wf,
                                const float *wf_scale, const float *mod_f, float *out,
                                dit_stream_t stream) {
+    dit_plan *p = const_cast<dit_plan *>(cp);
     if (!p) return DIT_ERR_INVALID_ARG;
-    return launch_final(x, p->T, p->D, wf, wf_scale, mod_f, out,
-                        static_cast<cudaStream_t>(stream));
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const double bytes = 4.0 * double(p->T) * p->D + 4.0 * 64 * p->D + 4.0 * 64 * double(p->T);
+    return timed(p, st, DIT_K_FINAL, bytes, [&] {
+        return launch_final(x, p->T, p->D, wf, wf_scale, mod_f, out, st);
+    });
 }
 
 dit_status_t dit_modln_cast(const float *x, int64_t rows, int D, const float *shift,

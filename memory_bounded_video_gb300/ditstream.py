@@ -45,7 +45,15 @@ SYMBOLS = (
     "dit_block_bind_workspace", "dit_block_forward", "dit_block_sync_status",
     "dit_final_forward", "dit_status_string", "dit_last_cuda_error",
     "dit_abi_version", "dit_modln_cast", "dit_gemm", "dit_attention",
+    "dit_block_profile_enable", "dit_block_profile_read",
 )
+
+# Kernel kinds of the per-kernel timing record (DIT_K_*).
+KINDS = ("modln", "gemm_kv", "gemm_q", "attention", "gemm_o", "gemm_swiglu",
+         "gemm_down", "final")
+# work unit of each kind: flops (tensor-core kinds) or bytes (memory-bound)
+KIND_UNITS = ("bytes", "flops", "flops", "flops", "flops", "flops", "flops",
+              "bytes")
 
 
 class DitError(RuntimeError):
@@ -108,6 +116,8 @@ def _declare(lib):
         "dit_gemm": (c_int, [ctypes.POINTER(GemmArgs), vp, vp]),
         "dit_attention": (c_int, [vp, c_int64, c_int64, vp, c_int64, vp, c_int64,
                                   c_int64, c_int, c_int, vp, c_int64, vp, vp]),
+        "dit_block_profile_enable": (c_int, [vp, c_int]),
+        "dit_block_profile_read": (c_int, [vp, vp, vp, vp]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -207,6 +217,21 @@ class BlockPlan:
 
     def sync_status(self, stream=None) -> int:
         return load().dit_block_sync_status(self._h, stream_handle(stream))
+
+    def profile_enable(self, on: bool = True):
+        _check(load().dit_block_profile_enable(self._h, int(bool(on))),
+               "dit_block_profile_enable")
+
+    def profile_read(self) -> dict:
+        """Per kernel kind: {"ms", "launches", "work"} since the last read."""
+        n = len(KINDS)
+        ms = (ctypes.c_double * n)()
+        cnt = (ctypes.c_int64 * n)()
+        work = (ctypes.c_double * n)()
+        _check(load().dit_block_profile_read(self._h, ms, cnt, work),
+               "dit_block_profile_read")
+        return {k: dict(ms=ms[i], launches=cnt[i], work=work[i],
+                        unit=KIND_UNITS[i]) for i, k in enumerate(KINDS)}
 
     def final_forward(self, x, wf, wf_scale, mod_f, out, stream=None):
         _check(load().dit_final_forward(self._h, ptr(x), ptr(wf), ptr(wf_scale),

@@ -52,7 +52,10 @@ def test_binding_constants_match_header():
                  DIT_EPI_STORE_BF16=ds.EPI_STORE_BF16,
                  DIT_EPI_STORE_F32=ds.EPI_STORE_F32, DIT_EPI_KV=ds.EPI_KV,
                  DIT_EPI_RESID=ds.EPI_RESID, DIT_EPI_SWIGLU=ds.EPI_SWIGLU,
-                 DIT_EPI_DOWN=ds.EPI_DOWN,
+                 DIT_EPI_DOWN=ds.EPI_DOWN, DIT_NUM_KINDS=len(ds.KINDS),
+                 DIT_K_MODLN=ds.KINDS.index("modln"),
+                 DIT_K_ATTENTION=ds.KINDS.index("attention"),
+                 DIT_K_FINAL=ds.KINDS.index("final"),
                  DITSTREAM_ABI_VERSION=None)
     for k, v in pairs.items():
         if v is not None:
