@@ -165,6 +165,34 @@ DIT_API dit_status_t dit_block_forward(const dit_plan_t *plan, float *x,
                                const dit_block_weights_t *w,
                                const float *modulation, dit_stream_t stream);
 
+/* Block forward that allocates nothing.  The method's pages have no
+ * counterpart to this entry point: it exists for callers that cannot
+ * allocate device memory (code that runs under an allocator owning every
+ * device byte, or where allocation is not allowed), so it needs no
+ * workspace bound to the plan.  Same computation, kernels and result bits as
+ * dit_block_forward; the scratch is a file-scope device array of 64 MiB
+ * (DIT_STATIC_SCRATCH_BYTES) that every device loading the library holds
+ * until the process exits.
+ *   - Plans whose dit_block_workspace_bytes exceeds that size are rejected
+ *     with DIT_ERR_WORKSPACE_TOO_SMALL before anything is launched.
+ *   - The first call on a device sets up the scratch address for that
+ *     device (with that device current); make that first call before any
+ *     stream capture.
+ *   - All calls share one scratch, which keeps the last call's contents:
+ *     calls whose work overlaps on the GPU (concurrent streams, several
+ *     host threads) race and give wrong results.  Serialise them.
+ *   - The scratch's status word is cleared at the start of each call; a
+ *     bounded device wait that runs out is recorded there but not reported
+ *     (dit_block_sync_status reads the plan's bound workspace only).
+ *   - Calls no cudaMalloc/cudaFree or any other allocating routine.
+ * Errors: as dit_block_forward, plus DIT_ERR_WORKSPACE_TOO_SMALL and
+ * DIT_ERR_UNSUPPORTED_ARCH. */
+#define DIT_STATIC_SCRATCH_BYTES (64u << 20)
+DIT_API dit_status_t dit_block_forward_static(const dit_plan_t *plan, float *x,
+                                              const dit_block_weights_t *w,
+                                              const float *modulation,
+                                              dit_stream_t stream);
+
 /* Synchronise `stream`, read and clear the plan's device status word.
  * Returns DIT_OK, DIT_ERR_TIMEOUT or DIT_ERR_CUDA. */
 DIT_API dit_status_t dit_block_sync_status(const dit_plan_t *plan, dit_stream_t stream);

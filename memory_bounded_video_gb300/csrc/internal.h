@@ -5,7 +5,31 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <vector>
+
 #include "ditstream.h"
+
+// A block plan: sizes, the workspace layout and the per-kernel timing record.
+struct dit_plan {
+    int64_t T;
+    int D, heads, head_dim, F;
+    int cm, ca, fs;  // effective mlp chunk, attention chunk, FFN slice
+    int64_t t_pad;   // row stride of V^T
+    // workspace layout (byte offsets)
+    size_t off_k, off_vt, off_a, off_q, off_b, off_h, off_acc, total;
+    uint8_t *ws;
+    size_t ws_bytes;
+    // per-kernel timing (dit_block_profile_*)
+    struct Rec {
+        int kind;
+        cudaEvent_t a, b;
+        double work;
+    };
+    bool prof = false;
+    std::vector<cudaEvent_t> pool;
+    size_t pool_used = 0;
+    std::vector<Rec> recs;
+};
 
 namespace ds {
 

@@ -46,7 +46,10 @@ SYMBOLS = (
     "dit_final_forward", "dit_status_string", "dit_last_cuda_error",
     "dit_abi_version", "dit_modln_cast", "dit_gemm", "dit_attention",
     "dit_block_profile_enable", "dit_block_profile_read",
+    "dit_block_forward_static",
 )
+
+STATIC_SCRATCH_BYTES = 64 << 20
 
 # Kernel kinds of the per-kernel timing record (DIT_K_*).
 KINDS = ("modln", "gemm_kv", "gemm_q", "attention", "gemm_o", "gemm_swiglu",
@@ -118,6 +121,8 @@ def _declare(lib):
                                   c_int64, c_int, c_int, vp, c_int64, vp, vp]),
         "dit_block_profile_enable": (c_int, [vp, c_int]),
         "dit_block_profile_read": (c_int, [vp, vp, vp, vp]),
+        "dit_block_forward_static": (c_int, [vp, vp, ctypes.POINTER(BlockWeights),
+                                             vp, vp]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -214,6 +219,15 @@ class BlockPlan:
         _check(load().dit_block_forward(self._h, ptr(x), ctypes.byref(weights),
                                         ptr(modulation), stream_handle(stream)),
                "dit_block_forward")
+
+    def forward_static(self, x, weights: BlockWeights, modulation, stream=None):
+        """dit_block_forward_static: the same forward with the library's
+        fixed device scratch instead of a bound workspace, for callers that
+        cannot allocate device memory."""
+        _check(load().dit_block_forward_static(self._h, ptr(x), ctypes.byref(weights),
+                                               ptr(modulation),
+                                               stream_handle(stream)),
+               "dit_block_forward_static")
 
     def sync_status(self, stream=None) -> int:
         return load().dit_block_sync_status(self._h, stream_handle(stream))
