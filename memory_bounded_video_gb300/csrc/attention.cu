@@ -2,21 +2,27 @@
 //
 // "LayerStream: H3 Chunking" ("How the slicing works"): every query needs
 // every key and value, so pass two attends each query slice to the K and V
-// kept for all tokens.  Per CTA: one head and 128 queries; the key loop runs
-// over all T keys in tiles of 128, always in ascending order, so a query's
-// output does not depend on the slab it belongs to.
+// kept for all tokens.  Per CTA: one head and two 128-query tiles (A, B);
+// the key loop runs over all T keys in tiles of 128, always in ascending
+// order, so a query's output does not depend on the slab it belongs to.
 //
-// Roles (192 threads, one CTA per SM):
-//   warp 0      TMA: the Q tile once, then K and V^T tiles into 2-stage rings
-//   warp 1      TMEM owner; one lane issues the tcgen05.mma:
-//                 S_j  = Q K_j^T  (M=128, N=128, K=d)   -> TMEM S[j%2]
-//                 PV_j = P_j V_j  (M=128, N=d,   K=128) -> TMEM PV[j%2]
-//   warps 2..5  softmax, one query row per thread: S_j from TMEM, running
-//               max and sum in fp32, P_j = exp2(S*log2e/sqrt(d) - m) as bf16
-//               into shared memory (128-byte-swizzled K-major, the A operand
-//               of the PV MMA), and O = alpha*O + PV_{j-1} in registers.
-// S and PV are double-buffered in TMEM so the tensor core computes S_{j+1}
-// and PV_j while the softmax threads work on S_j.
+// Roles (384 threads, one CTA per SM):
+//   warp 0        TMA: both Q tiles once, then K_j and V_j^T tiles through one
+//                 shared ring (K_0, V_0, K_1, V_1, ...)
+//   warp 1        TMEM owner; one lane issues the tcgen05.mma:
+//                   S_X  = Q_X K_j^T  (M=128, N=128, K=d)     -> TMEM S[X]
+//                   O_X += P_X V_j    (M=128, N=d,   K=128)   -> TMEM O[X]
+//                 in the order S_A S_B | PV_A S_A' PV_B S_B' | ... so the
+//                 tensor core works on one tile while the other's softmax runs
+//   warps 4..7    softmax of tile A, one query row per thread
+//   warps 8..11   softmax of tile B
+// Softmax per key tile: the row max from S (TMEM), P = exp2(S*log2e/sqrt(d)
+// - m) as bf16 into shared memory (128-byte-swizzled K-major: the A operand
+// of the PV MMA), the running sum l.  The reference max m is only moved when
+// the tile max exceeds it by more than 8 (log2 units); then the row of O is
+// rescaled in TMEM.  Otherwise P may reach 2^8, which bf16 and the fp32
+// accumulator represent without loss of range; O / l is unchanged in exact
+// arithmetic.
 //
 // V arrives transposed (V^T [H*d, T], written so by the K/V projection's
 // epilogue), which makes both MMAs K-major in both operands.
@@ -27,26 +33,24 @@ namespace ds {
 
 namespace {
 
-constexpr int kBQ = 128;    // queries per CTA
+constexpr int kBQ = 128;    // queries per tile
 constexpr int kBKV = 128;   // keys per tile
-constexpr int kThreads = 192;
+constexpr int kThreads = 384;
+constexpr float kRescaleLog2 = 8.0f;
 
 template <int HD>
 struct ACfg {
-    static constexpr int KS = 2;                         // K stages
-    static constexpr int VS = 2;                         // V stages
-    static constexpr int Q_BYTES = kBQ * HD * 2;
-    static constexpr int K_BYTES = kBKV * HD * 2;
-    static constexpr int V_BYTES = HD * kBKV * 2;
-    static constexpr int P_BYTES = kBQ * kBKV * 2;
+    static constexpr int RING = HD == 128 ? 3 : 4;       // K/V ring stages
+    static constexpr int Q_BYTES = kBQ * HD * 2;          // one Q tile
+    static constexpr int TILE_BYTES = kBKV * HD * 2;      // one K or V^T tile
+    static constexpr int P_BYTES = kBQ * kBKV * 2;        // one P tile
     static constexpr int OFF_Q = 0;
-    static constexpr int OFF_K = OFF_Q + Q_BYTES;
-    static constexpr int OFF_V = OFF_K + KS * K_BYTES;
-    static constexpr int OFF_P = OFF_V + VS * V_BYTES;
+    static constexpr int OFF_RING = OFF_Q + 2 * Q_BYTES;
+    static constexpr int OFF_P = OFF_RING + RING * TILE_BYTES;
     static constexpr int OFF_BAR = OFF_P + 2 * P_BYTES;
     static constexpr int SMEM_BYTES = OFF_BAR + 256 + 1024;
-    static constexpr int TMEM_COLS = 512;                 // S0 S1 PV0 PV1
-    static constexpr int COL_PV = 2 * kBKV;
+    static constexpr int TMEM_COLS = 512;
+    static constexpr int COL_O = 2 * kBKV;                // S_A S_B | O_A O_B
 };
 
 struct AttnParams {
@@ -64,6 +68,80 @@ DEV float ex2(float x) {
     return y;
 }
 
+// Row max of one S tile (128 fp32 columns from TMEM); keys >= nvalid masked.
+template <bool MASK>
+DEV float tile_max(uint32_t saddr, int nvalid) {
+    float m0 = -INFINITY, m1 = -INFINITY, m2 = -INFINITY, m3 = -INFINITY;
+#pragma unroll
+    for (int c0 = 0; c0 < kBKV; c0 += 32) {
+        uint32_t r[32];
+        tmem_ld32(saddr + c0, r);
+        tmem_ld_wait(r);
+#pragma unroll
+        for (int c = 0; c < 32; c += 4) {
+            float v0 = __uint_as_float(r[c]), v1 = __uint_as_float(r[c + 1]);
+            float v2 = __uint_as_float(r[c + 2]), v3 = __uint_as_float(r[c + 3]);
+            if (MASK) {
+                if (c0 + c >= nvalid) v0 = -INFINITY;
+                if (c0 + c + 1 >= nvalid) v1 = -INFINITY;
+                if (c0 + c + 2 >= nvalid) v2 = -INFINITY;
+                if (c0 + c + 3 >= nvalid) v3 = -INFINITY;
+            }
+            m0 = fmaxf(m0, v0);
+            m1 = fmaxf(m1, v1);
+            m2 = fmaxf(m2, v2);
+            m3 = fmaxf(m3, v3);
+        }
+    }
+    return fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
+}
+
+// P = exp2(S * sl2 - m) for one row: bf16 into the swizzled P tile, returns
+// the sum of the fp32 probabilities.
+template <bool MASK>
+DEV float tile_exp(uint32_t saddr, uint32_t prow, int row, float sl2, float m, int nvalid) {
+    float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+    const float neg_m = -m;
+#pragma unroll
+    for (int c0 = 0; c0 < kBKV; c0 += 32) {
+        uint32_t r[32];
+        tmem_ld32(saddr + c0, r);
+        tmem_ld_wait(r);
+        uint32_t pk[16];
+#pragma unroll
+        for (int c = 0; c < 32; c += 4) {
+            float p0 = ex2(__fmaf_rn(__uint_as_float(r[c]), sl2, neg_m));
+            float p1 = ex2(__fmaf_rn(__uint_as_float(r[c + 1]), sl2, neg_m));
+            float p2 = ex2(__fmaf_rn(__uint_as_float(r[c + 2]), sl2, neg_m));
+            float p3 = ex2(__fmaf_rn(__uint_as_float(r[c + 3]), sl2, neg_m));
+            if (MASK) {
+                if (c0 + c >= nvalid) p0 = 0.f;
+                if (c0 + c + 1 >= nvalid) p1 = 0.f;
+                if (c0 + c + 2 >= nvalid) p2 = 0.f;
+                if (c0 + c + 3 >= nvalid) p3 = 0.f;
+            }
+            s0 += p0;
+            s1 += p1;
+            s2 += p2;
+            s3 += p3;
+            pk[c >> 1] = pack_bf16x2(p0, p1);
+            pk[(c >> 1) + 1] = pack_bf16x2(p2, p3);
+        }
+        // 32 keys = 64 bytes = four 16-byte chunks of one 128-byte row
+        const uint32_t blk = prow + (c0 >> 6) * (kBQ * 128);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int chunk = ((c0 & 63) >> 3) + u;
+            const uint32_t addr = blk + uint32_t((chunk ^ (row & 7)) << 4);
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr),
+                         "r"(pk[4 * u]), "r"(pk[4 * u + 1]), "r"(pk[4 * u + 2]),
+                         "r"(pk[4 * u + 3])
+                         : "memory");
+        }
+    }
+    return (s0 + s1) + (s2 + s3);
+}
+
 template <int HD>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ,
@@ -74,35 +152,30 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t *sm = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + C::OFF_BAR);
-    // bars: q_full, k_full[KS], k_empty[KS], v_full[VS], v_empty[VS],
-    //       s_full[2], p_full[2], pv_full[2], drain
-    constexpr int B_Q = 0, B_KF = 1, B_KE = B_KF + C::KS, B_VF = B_KE + C::KS,
-                  B_VE = B_VF + C::VS, B_SF = B_VE + C::VS, B_PF = B_SF + 2, B_PV = B_PF + 2,
-                  B_DR = B_PV + 2, NBAR = B_DR + 1;
+    // bars: q_full, ring_full[RING], ring_empty[RING], s_full[2], p_full[2],
+    //       o_full, drain
+    constexpr int B_Q = 0, B_RF = 1, B_RE = B_RF + C::RING, B_SF = B_RE + C::RING,
+                  B_PF = B_SF + 2, B_O = B_PF + 2, B_DR = B_O + 1, NBAR = B_DR + 1;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + NBAR);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     const uint32_t bar0 = smem_u32(bars);
     auto bar = [&](int i) { return bar0 + 8u * i; };
 
     const int warp = warp_id(), lane = lane_id();
-    const int qt = blockIdx.x, head = blockIdx.y;
+    const int qpair = blockIdx.x, head = blockIdx.y;
     const int n_kv = p.n_kv;
 
     if (threadIdx.x == 0) {
         mbar_init(bar(B_Q), 1);
-        for (int s = 0; s < C::KS; ++s) {
-            mbar_init(bar(B_KF + s), 1);
-            mbar_init(bar(B_KE + s), 1);
+        for (int s = 0; s < C::RING; ++s) {
+            mbar_init(bar(B_RF + s), 1);
+            mbar_init(bar(B_RE + s), 1);
         }
-        for (int s = 0; s < C::VS; ++s) {
-            mbar_init(bar(B_VF + s), 1);
-            mbar_init(bar(B_VE + s), 1);
+        for (int x = 0; x < 2; ++x) {
+            mbar_init(bar(B_SF + x), 1);
+            mbar_init(bar(B_PF + x), 128);
         }
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(bar(B_SF + b), 1);
-            mbar_init(bar(B_PF + b), 128);
-            mbar_init(bar(B_PV + b), 1);
-        }
+        mbar_init(bar(B_O), 1);
         mbar_init(bar(B_DR), 1);
         *abort_flag = 0;
         fence_barrier_init();
@@ -122,56 +195,47 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = *tmem_slot;
     const WaitCtx wc{abort_flag, p.status};
     const uint32_t sQ = smem_u32(sm + C::OFF_Q);
-    const uint32_t sK = smem_u32(sm + C::OFF_K);
-    const uint32_t sV = smem_u32(sm + C::OFF_V);
+    const uint32_t sRing = smem_u32(sm + C::OFF_RING);
     const uint32_t sP = smem_u32(sm + C::OFF_P);
 
     if (warp == 0) {
         if (lane == 0) {
             // ------------------------------------------------ TMA producer
-            bool ok = true;
-            int k_issued = 0, v_issued = 0;
-            mbar_arrive_expect_tx(bar(B_Q), C::Q_BYTES);
+            mbar_arrive_expect_tx(bar(B_Q), 2 * C::Q_BYTES);
 #pragma unroll
-            for (int b = 0; b < HD / 64; ++b)
-                tma_load_2d(sQ + b * (kBQ * 128), &tmQ, bar(B_Q), head * HD + 64 * b, qt * kBQ);
-            auto load_k = [&](int j) -> bool {
-                const int s = j % C::KS;
-                if (!mbar_wait(bar(B_KE + s), uint32_t((j / C::KS) & 1) ^ 1u, wc)) return false;
-                mbar_arrive_expect_tx(bar(B_KF + s), C::K_BYTES);
-                const uint32_t dst = sK + s * C::K_BYTES;
+            for (int x = 0; x < 2; ++x)
 #pragma unroll
                 for (int b = 0; b < HD / 64; ++b)
-                    tma_load_2d(dst + b * (kBKV * 128), &tmK, bar(B_KF + s), head * HD + 64 * b,
-                                j * kBKV);
-                ++k_issued;
-                return true;
-            };
-            auto load_v = [&](int j) -> bool {
-                const int s = j % C::VS;
-                if (!mbar_wait(bar(B_VE + s), uint32_t((j / C::VS) & 1) ^ 1u, wc)) return false;
-                mbar_arrive_expect_tx(bar(B_VF + s), C::V_BYTES);
-                const uint32_t dst = sV + s * C::V_BYTES;
-#pragma unroll
-                for (int b = 0; b < kBKV / 64; ++b)
-                    tma_load_2d(dst + b * (HD * 128), &tmV, bar(B_VF + s), j * kBKV + 64 * b,
-                                head * HD);
-                ++v_issued;
-                return true;
-            };
-            ok = load_k(0);
-            if (ok && n_kv > 1) ok = load_k(1);
+                    tma_load_2d(sQ + x * C::Q_BYTES + b * (kBQ * 128), &tmQ, bar(B_Q),
+                                head * HD + 64 * b, (2 * qpair + x) * kBQ);
+            int seq = 0;
+            bool ok = true;
             for (int j = 0; ok && j < n_kv; ++j) {
-                ok = load_v(j);
-                if (ok && j + 2 < n_kv) ok = load_k(j + 2);
+                for (int kind = 0; ok && kind < 2; ++kind, ++seq) {
+                    const int s = seq % C::RING;
+                    if (!mbar_wait(bar(B_RE + s), uint32_t((seq / C::RING) & 1) ^ 1u, wc)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(bar(B_RF + s), C::TILE_BYTES);
+                    const uint32_t dst = sRing + s * C::TILE_BYTES;
+                    if (kind == 0) {
+#pragma unroll
+                        for (int b = 0; b < HD / 64; ++b)
+                            tma_load_2d(dst + b * (kBKV * 128), &tmK, bar(B_RF + s),
+                                        head * HD + 64 * b, j * kBKV);
+                    } else {
+#pragma unroll
+                        for (int b = 0; b < kBKV / 64; ++b)
+                            tma_load_2d(dst + b * (HD * 128), &tmV, bar(B_RF + s),
+                                        j * kBKV + 64 * b, head * HD);
+                    }
+                }
             }
             if (!ok) {  // let the copies in flight land before the CTA exits
                 mbar_wait_quiet(bar(B_Q), 0, kWaitLimitNs);
-                for (int j = k_issued > C::KS ? k_issued - C::KS : 0; j < k_issued; ++j)
-                    mbar_wait_quiet(bar(B_KF + j % C::KS), uint32_t((j / C::KS) & 1),
-                                    kWaitLimitNs);
-                for (int j = v_issued > C::VS ? v_issued - C::VS : 0; j < v_issued; ++j)
-                    mbar_wait_quiet(bar(B_VF + j % C::VS), uint32_t((j / C::VS) & 1),
+                for (int i = seq > C::RING ? seq - C::RING : 0; i < seq; ++i)
+                    mbar_wait_quiet(bar(B_RF + i % C::RING), uint32_t((i / C::RING) & 1),
                                     kWaitLimitNs);
             }
         }
@@ -180,162 +244,160 @@ __global__ void __launch_bounds__(kThreads, 1)
             // ------------------------------------------------ MMA issuer
             constexpr uint32_t ID_S = idesc_bf16_f32(kBQ, kBKV);
             constexpr uint32_t ID_PV = idesc_bf16_f32(kBQ, HD);
-            bool ok = mbar_wait(bar(B_Q), 0, wc);
-            auto issue_s = [&](int j) -> bool {
-                const int s = j % C::KS;
-                if (!mbar_wait(bar(B_KF + s), uint32_t((j / C::KS) & 1), wc)) return false;
-                tc_fence_after();
-                const uint32_t kbase = sK + s * C::K_BYTES;
-                const uint32_t d = tmem + uint32_t((j & 1) * kBKV);
+            auto ring_wait = [&](int seq) {
+                return mbar_wait(bar(B_RF + seq % C::RING), uint32_t((seq / C::RING) & 1), wc);
+            };
+            auto issue_s = [&](int x, int seq) {
+                const uint32_t kb = sRing + (seq % C::RING) * C::TILE_BYTES;
+                const uint32_t qb = sQ + x * C::Q_BYTES;
+                const uint32_t d = tmem + uint32_t(x * kBKV);
 #pragma unroll
                 for (int kk = 0; kk < HD / 16; ++kk) {
                     const uint32_t off = (kk >> 2) * (kBQ * 128) + (kk & 3) * 32;
-                    const uint32_t offk = (kk >> 2) * (kBKV * 128) + (kk & 3) * 32;
-                    mma_bf16_ss(d, desc_sw128(sQ + off), desc_sw128(kbase + offk), ID_S,
-                                kk > 0);
+                    mma_bf16_ss(d, desc_sw128(qb + off), desc_sw128(kb + off), ID_S, kk > 0);
                 }
-                mma_commit(bar(B_KE + s));
-                mma_commit(bar(B_SF + (j & 1)));
-                return true;
+                mma_commit(bar(B_SF + x));
             };
-            if (ok) ok = issue_s(0);
-            if (ok && n_kv > 1) ok = issue_s(1);
-            for (int j = 0; ok && j < n_kv; ++j) {
-                if (!mbar_wait(bar(B_PF + (j & 1)), uint32_t((j >> 1) & 1), wc)) {
-                    ok = false;
-                    break;
-                }
-                const int s = j % C::VS;
-                if (!mbar_wait(bar(B_VF + s), uint32_t((j / C::VS) & 1), wc)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                const uint32_t pbase = sP + (j & 1) * C::P_BYTES;
-                const uint32_t vbase = sV + s * C::V_BYTES;
-                const uint32_t d = tmem + uint32_t(C::COL_PV + (j & 1) * HD);
+            auto issue_pv = [&](int x, int seq, int j) {
+                const uint32_t vb = sRing + (seq % C::RING) * C::TILE_BYTES;
+                const uint32_t pb = sP + x * C::P_BYTES;
+                const uint32_t d = tmem + uint32_t(C::COL_O + x * HD);
 #pragma unroll
                 for (int kk = 0; kk < kBKV / 16; ++kk) {
                     const uint32_t offp = (kk >> 2) * (kBQ * 128) + (kk & 3) * 32;
                     const uint32_t offv = (kk >> 2) * (HD * 128) + (kk & 3) * 32;
-                    mma_bf16_ss(d, desc_sw128(pbase + offp), desc_sw128(vbase + offv), ID_PV,
-                                kk > 0);
+                    mma_bf16_ss(d, desc_sw128(pb + offp), desc_sw128(vb + offv), ID_PV,
+                                (j > 0 || kk > 0) ? 1u : 0u);
                 }
-                mma_commit(bar(B_VE + s));
-                mma_commit(bar(B_PV + (j & 1)));
-                if (j + 2 < n_kv) ok = issue_s(j + 2);
+            };
+            bool ok = mbar_wait(bar(B_Q), 0, wc) && ring_wait(0);
+            if (ok) {
+                tc_fence_after();
+                issue_s(0, 0);
+                issue_s(1, 0);
+                mma_commit(bar(B_RE + 0));
             }
-            if (!ok) {
+            for (int j = 0; ok && j < n_kv; ++j) {
+                const int seq_v = 2 * j + 1, seq_k = 2 * j + 2;
+                const bool more = j + 1 < n_kv;
+                if (!ring_wait(seq_v) || !mbar_wait(bar(B_PF + 0), uint32_t(j & 1), wc)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                issue_pv(0, seq_v, j);
+                if (more) {
+                    if (!ring_wait(seq_k)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    issue_s(0, seq_k);
+                }
+                if (!mbar_wait(bar(B_PF + 1), uint32_t(j & 1), wc)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                issue_pv(1, seq_v, j);
+                mma_commit(bar(B_RE + seq_v % C::RING));
+                if (more) {
+                    issue_s(1, seq_k);
+                    mma_commit(bar(B_RE + seq_k % C::RING));
+                }
+            }
+            if (ok) {
+                mma_commit(bar(B_O));
+            } else {
                 mma_commit(bar(B_DR));
                 mbar_wait_quiet(bar(B_DR), 0, kWaitLimitNs);
             }
         }
-    } else {
+    } else if (warp >= 4) {
         // ---------------------------------------------------- softmax
-        const int qd = warp & 3;
-        const int row = qd * 32 + lane;  // query row within the tile
+        const int x = (warp - 4) >> 2;          // tile A or B
+        const int qd = warp & 3;                // TMEM lane quadrant
+        const int row = qd * 32 + lane;         // query row within the tile
         const uint32_t lane_base = tmem + (uint32_t(qd * 32) << 16);
+        const uint32_t saddr = lane_base + uint32_t(x * kBKV);
+        const uint32_t oaddr = lane_base + uint32_t(C::COL_O + x * HD);
+        const uint32_t prow = sP + x * C::P_BYTES + row * 128;
         const float sl2 = p.scale_log2;
-        float o[HD];
-#pragma unroll
-        for (int c = 0; c < HD; ++c) o[c] = 0.f;
-        float m = -INFINITY, l = 0.f, alpha_prev = 1.f;
         const int last_valid = int(p.T - int64_t(n_kv - 1) * kBKV);  // keys in last tile
+        float m = -INFINITY, l = 0.f;
         bool ok = true;
-        auto consume_pv = [&](int jj, float alpha) -> bool {
-            bool w = mbar_wait(bar(B_PV + (jj & 1)), uint32_t((jj >> 1) & 1), wc);
-            w = __all_sync(0xffffffffu, w);
-            if (!w) return false;
-            tc_fence_after();
-            const uint32_t pvaddr = lane_base + uint32_t(C::COL_PV + (jj & 1) * HD);
-#pragma unroll
-            for (int c0 = 0; c0 < HD; c0 += 32) {
-                uint32_t r[32];
-                tmem_ld32(pvaddr + c0, r);
-                tmem_ld_wait(r);
-#pragma unroll
-                for (int c = 0; c < 32; ++c)
-                    o[c0 + c] = __fmaf_rn(o[c0 + c], alpha, __uint_as_float(r[c]));
-            }
-            return true;
-        };
         for (int j = 0; j < n_kv; ++j) {
-            bool w = mbar_wait(bar(B_SF + (j & 1)), uint32_t((j >> 1) & 1), wc);
+            bool w = mbar_wait(bar(B_SF + x), uint32_t(j & 1), wc);
             w = __all_sync(0xffffffffu, w);
             if (!w) {
                 ok = false;
                 break;
             }
             tc_fence_after();
-            const uint32_t saddr = lane_base + uint32_t((j & 1) * kBKV);
-            const int nvalid = (j == n_kv - 1) ? last_valid : kBKV;
-            // pass 1: row max of this tile
-            float mx = -INFINITY;
+            const bool masked = (j == n_kv - 1) && last_valid < kBKV;
+            const float mx =
+                (masked ? tile_max<true>(saddr, last_valid) : tile_max<false>(saddr, kBKV)) *
+                sl2;
+            if (j == 0) {
+                m = mx;
+            } else if (__any_sync(0xffffffffu, mx > m + kRescaleLog2)) {
+                // Move the reference max of the rows that need it: O_row *=
+                // 2^(m - m_new), l likewise.  The branch is warp-uniform (the
+                // TMEM accesses are warp-collective); the other rows keep m
+                // and are multiplied by exactly 1, so each row's result
+                // depends on that row alone.
+                const float m_new = (mx > m + kRescaleLog2) ? mx : m;
+                const float alpha = ex2(m - m_new);
 #pragma unroll
-            for (int c0 = 0; c0 < kBKV; c0 += 32) {
-                uint32_t r[32];
-                tmem_ld32(saddr + c0, r);
-                tmem_ld_wait(r);
+                for (int c0 = 0; c0 < HD; c0 += 32) {
+                    uint32_t r[32];
+                    tmem_ld32(oaddr + c0, r);
+                    tmem_ld_wait(r);
 #pragma unroll
-                for (int c = 0; c < 32; ++c)
-                    if (c0 + c < nvalid) mx = fmaxf(mx, __uint_as_float(r[c]));
-            }
-            const float m_new = fmaxf(m, mx * sl2);
-            const float alpha = ex2(m - m_new);  // 0 on the first tile
-            // pass 2: probabilities, their sum, bf16 P row into shared memory
-            float sum = 0.f;
-            const uint32_t prow = sP + (j & 1) * C::P_BYTES + row * 128;
-#pragma unroll
-            for (int c0 = 0; c0 < kBKV; c0 += 32) {
-                uint32_t r[32];
-                tmem_ld32(saddr + c0, r);
-                tmem_ld_wait(r);
-                uint32_t pk[16];
-#pragma unroll
-                for (int c = 0; c < 32; c += 2) {
-                    float p0 = ex2(__fmaf_rn(__uint_as_float(r[c]), sl2, -m_new));
-                    float p1 = ex2(__fmaf_rn(__uint_as_float(r[c + 1]), sl2, -m_new));
-                    if (c0 + c >= nvalid) p0 = 0.f;
-                    if (c0 + c + 1 >= nvalid) p1 = 0.f;
-                    sum += p0 + p1;
-                    pk[c >> 1] = pack_bf16x2(p0, p1);
+                    for (int c = 0; c < 32; ++c)
+                        r[c] = __float_as_uint(__uint_as_float(r[c]) * alpha);
+                    tmem_st32_sync(oaddr + c0, r);
                 }
-                // 32 keys = 64 bytes = four 16-byte chunks of one 128-byte row
-                const uint32_t blk = prow + (c0 >> 6) * (kBQ * 128);
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const int chunk = ((c0 & 63) >> 3) + u;
-                    const uint32_t addr = blk + uint32_t(((chunk ^ (row & 7)) << 4));
-                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr),
-                                 "r"(pk[4 * u]), "r"(pk[4 * u + 1]), "r"(pk[4 * u + 2]),
-                                 "r"(pk[4 * u + 3])
-                                 : "memory");
-                }
+                l *= alpha;
+                m = m_new;
             }
-            l = __fmaf_rn(l, alpha, sum);
-            m = m_new;
+            const float sum = masked ? tile_exp<true>(saddr, prow, row, sl2, m, last_valid)
+                                     : tile_exp<false>(saddr, prow, row, sl2, m, kBKV);
+            l += sum;
             fence_proxy_async_smem();  // P is read by the tensor core (async proxy)
-            tc_fence_before();         // S_j reads finish before S_{j+2} overwrites
-            mbar_arrive(bar(B_PF + (j & 1)));
-            if (j > 0 && !consume_pv(j - 1, alpha_prev)) {
-                ok = false;
-                break;
-            }
-            alpha_prev = alpha;
+            tc_fence_before();         // S/O accesses finish before the next MMAs
+            mbar_arrive(bar(B_PF + x));
         }
-        if (ok && n_kv > 0) ok = consume_pv(n_kv - 1, alpha_prev);
-        const int64_t qrow = int64_t(qt) * kBQ + row;
-        if (ok && qrow < p.Tq) {
+        if (ok) {
+            bool w = mbar_wait(bar(B_O), 0, wc);
+            ok = __all_sync(0xffffffffu, w);
+        }
+        const int64_t qrow = (2 * int64_t(qpair) + x) * kBQ + row;
+        if (ok) {
+            tc_fence_after();
             const float inv = 1.0f / l;
             uint4 *dst = reinterpret_cast<uint4 *>(p.o + qrow * p.ldo + int64_t(head) * HD);
 #pragma unroll
-            for (int c = 0; c < HD; c += 8) {
-                uint4 v;
-                v.x = pack_bf16x2(o[c] * inv, o[c + 1] * inv);
-                v.y = pack_bf16x2(o[c + 2] * inv, o[c + 3] * inv);
-                v.z = pack_bf16x2(o[c + 4] * inv, o[c + 5] * inv);
-                v.w = pack_bf16x2(o[c + 6] * inv, o[c + 7] * inv);
-                dst[c >> 3] = v;
+            for (int c0 = 0; c0 < HD; c0 += 32) {
+                uint32_t r[32];
+                __syncwarp();
+                tmem_ld32(oaddr + c0, r);
+                tmem_ld_wait(r);
+                if (qrow < p.Tq) {
+#pragma unroll
+                    for (int c = 0; c < 32; c += 8) {
+                        uint4 v;
+                        v.x = pack_bf16x2(__uint_as_float(r[c]) * inv,
+                                          __uint_as_float(r[c + 1]) * inv);
+                        v.y = pack_bf16x2(__uint_as_float(r[c + 2]) * inv,
+                                          __uint_as_float(r[c + 3]) * inv);
+                        v.z = pack_bf16x2(__uint_as_float(r[c + 4]) * inv,
+                                          __uint_as_float(r[c + 5]) * inv);
+                        v.w = pack_bf16x2(__uint_as_float(r[c + 6]) * inv,
+                                          __uint_as_float(r[c + 7]) * inv);
+                        dst[(c0 + c) >> 3] = v;
+                    }
+                }
             }
         }
     }
@@ -375,7 +437,8 @@ dit_status_t run(const void *q, int64_t Tq, int64_t ldq, const void *k, int64_t 
         if (e != cudaSuccess) return cuda_fail(e);
         attr_done = true;
     }
-    const dim3 grid(unsigned((Tq + kBQ - 1) / kBQ), unsigned(heads));
+    const int64_t qtiles = (Tq + kBQ - 1) / kBQ;
+    const dim3 grid(unsigned((qtiles + 1) / 2), unsigned(heads));
     attn_fwd_kernel<HD><<<grid, kThreads, C::SMEM_BYTES, s>>>(tQ, tK, tV, p);
     return check_launch();
 }
@@ -393,7 +456,7 @@ dit_status_t launch_attention(const void *q, int64_t Tq, int64_t ldq, const void
     const int64_t D = int64_t(heads) * head_dim;
     if (ldq < D || ldk < D || ldo < D || ldvt < T) return DIT_ERR_INVALID_ARG;
     if (ldq % 8 || ldk % 8 || ldo % 8 || ldvt % 8) return DIT_ERR_INVALID_ARG;
-    if (Tq > (int64_t(1) << 31) - kBQ || T > (int64_t(1) << 31) - kBKV || heads > 65535)
+    if (Tq > (int64_t(1) << 31) - 2 * kBQ || T > (int64_t(1) << 31) - kBKV || heads > 65535)
         return DIT_ERR_INVALID_ARG;
     if (Tq == 0) return DIT_OK;
     if (head_dim == 64)
