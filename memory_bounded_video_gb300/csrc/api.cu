@@ -87,7 +87,8 @@ int sm_count() {
 }
 
 bool make_tmap_2d(CUtensorMap *m, CUtensorMapDataType dt, const void *base, uint64_t inner,
-                  uint64_t outer, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer) {
+                  uint64_t outer, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer,
+                  CUtensorMapSwizzle swizzle) {
     if (!load_encode()) return false;
     if (inner == 0 || outer == 0 || row_bytes % 16 || !aligned16(base)) return false;
     const cuuint64_t dims[2] = {inner, outer};
@@ -95,7 +96,7 @@ bool make_tmap_2d(CUtensorMap *m, CUtensorMapDataType dt, const void *base, uint
     const cuuint32_t box[2] = {box_inner, box_outer};
     const cuuint32_t estr[2] = {1, 1};
     const CUresult r = g_encode(m, dt, 2, const_cast<void *>(base), dims, strides, box, estr,
-                                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
                                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
@@ -286,7 +287,19 @@ dit_status_t dit_block_forward(const dit_plan_t *cp, float *x, const dit_block_w
     if (!aligned16(x) || !aligned16(mod) || !aligned16(w->wqkv) || !aligned16(w->wo) ||
         !aligned16(w->wgate) || !aligned16(w->wup) || !aligned16(w->wdown))
         return DIT_ERR_ALIGN;
-    if (w->dtype != DIT_W_BF16) return DIT_ERR_INVALID_ARG;
+    if (w->dtype != DIT_W_BF16 && w->dtype != DIT_W_INT8) return DIT_ERR_INVALID_ARG;
+    const bool i8 = w->dtype == DIT_W_INT8;
+    if (i8) {
+        if (!w->wqkv_scale || !w->wo_scale || !w->wgate_scale || !w->wup_scale ||
+            !w->wdown_scale)
+            return DIT_ERR_INVALID_ARG;
+        if (!aligned16(w->wqkv_scale) || !aligned16(w->wo_scale) ||
+            !aligned16(w->wgate_scale) || !aligned16(w->wup_scale) ||
+            !aligned16(w->wdown_scale))
+            return DIT_ERR_ALIGN;
+    }
+    const int bdt = w->dtype;
+    const int64_t el = i8 ? 1 : 2;  // bytes per weight element
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const int64_t T = p->T;
@@ -302,7 +315,7 @@ dit_status_t dit_block_forward(const dit_plan_t *cp, float *x, const dit_block_w
     float *acc = reinterpret_cast<float *>(p->ws + p->off_acc);
     const float *shift1 = mod, *scale1 = mod + Dl, *gate1 = mod + 2 * Dl;
     const float *shift2 = mod + 3 * Dl, *scale2 = mod + 4 * Dl, *gate2 = mod + 5 * Dl;
-    const uint16_t *wqkv = static_cast<const uint16_t *>(w->wqkv);
+    const uint8_t *wqkv = static_cast<const uint8_t *>(w->wqkv);
     dit_status_t r;
 
     // pass 1: K and V of every token
@@ -319,9 +332,10 @@ dit_status_t dit_block_forward(const dit_plan_t *cp, float *x, const dit_block_w
         g.K = D;
         g.a = a;
         g.lda = D;
-        g.b0 = wqkv + Dl * Dl;  // rows D..3D-1: Wk then Wv
+        g.b0 = wqkv + Dl * Dl * el;  // rows D..3D-1: Wk then Wv
         g.ldb = D;
-        g.b_dtype = DIT_W_BF16;
+        g.b_dtype = bdt;
+        g.b0_scale = i8 ? w->wqkv_scale + Dl : nullptr;
         g.out = K;
         g.ldo = D;
         g.out2 = Vt;
@@ -348,7 +362,8 @@ dit_status_t dit_block_forward(const dit_plan_t *cp, float *x, const dit_block_w
         g.lda = D;
         g.b0 = wqkv;
         g.ldb = D;
-        g.b_dtype = DIT_W_BF16;
+        g.b_dtype = bdt;
+        g.b0_scale = i8 ? w->wqkv_scale : nullptr;
         g.out = Q;
         g.ldo = D;
         if ((r = timed(p, st, DIT_K_GEMM_Q, 2.0 * rows * D * D,
@@ -369,7 +384,8 @@ dit_status_t dit_block_forward(const dit_plan_t *cp, float *x, const dit_block_w
         o.lda = D;
         o.b0 = w->wo;
         o.ldb = D;
-        o.b_dtype = DIT_W_BF16;
+        o.b_dtype = bdt;
+        o.b0_scale = i8 ? w->wo_scale : nullptr;
         o.x = x + s * Dl;
         o.ldx = D;
         o.gate = gate1;
@@ -378,9 +394,9 @@ dit_status_t dit_block_forward(const dit_plan_t *cp, float *x, const dit_block_w
             return r;
     }
     // MLP: token chunks x FFN feature slices
-    const uint16_t *wg = static_cast<const uint16_t *>(w->wgate);
-    const uint16_t *wu = static_cast<const uint16_t *>(w->wup);
-    const uint16_t *wd = static_cast<const uint16_t *>(w->wdown);
+    const uint8_t *wg = static_cast<const uint8_t *>(w->wgate);
+    const uint8_t *wu = static_cast<const uint8_t *>(w->wup);
+    const uint8_t *wd = static_cast<const uint8_t *>(w->wdown);
     for (int64_t c = 0; c < T; c += p->cm) {
         const int64_t rows = (T - c < p->cm) ? T - c : p->cm;
         if ((r = timed(p, st, DIT_K_MODLN, 6.0 * rows * D,
@@ -396,10 +412,12 @@ dit_status_t dit_block_forward(const dit_plan_t *cp, float *x, const dit_block_w
             g.K = D;
             g.a = b;
             g.lda = D;
-            g.b0 = wg + int64_t(f) * Dl;
-            g.b1 = wu + int64_t(f) * Dl;
+            g.b0 = wg + int64_t(f) * Dl * el;
+            g.b1 = wu + int64_t(f) * Dl * el;
             g.ldb = D;
-            g.b_dtype = DIT_W_BF16;
+            g.b_dtype = bdt;
+            g.b0_scale = i8 ? w->wgate_scale + f : nullptr;
+            g.b1_scale = i8 ? w->wup_scale + f : nullptr;
             g.out = h;
             g.ldo = p->fs;
             if ((r = timed(p, st, DIT_K_GEMM_SWIGLU, 4.0 * rows * fw * D,
@@ -412,9 +430,10 @@ dit_status_t dit_block_forward(const dit_plan_t *cp, float *x, const dit_block_w
             d.K = fw;
             d.a = h;
             d.lda = p->fs;
-            d.b0 = wd + f;  // columns f .. f+fw-1 of Wdown [D, F]
+            d.b0 = wd + int64_t(f) * el;  // columns f .. f+fw-1 of Wdown [D, F]
             d.ldb = F;
-            d.b_dtype = DIT_W_BF16;
+            d.b_dtype = bdt;
+            d.b0_scale = i8 ? w->wdown_scale : nullptr;
             d.acc = acc;
             d.ldacc = D;
             d.acc_load = f > 0;

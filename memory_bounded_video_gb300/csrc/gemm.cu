@@ -1,15 +1,20 @@
 // Tensor-core GEMM for sm_103a:  acc[M, N] = A[M, K] * B[N, K]^T
-// (bf16 operands, fp32 accumulation in tensor memory) with the block's fused
-// epilogues: K/V store, Q store, gated fp32 residual add, SwiGLU, and the
-// down projection's accumulate-across-FFN-slices.
+// (bf16 A, bf16 or int8 B, fp32 accumulation in tensor memory) with the
+// block's fused epilogues: K/V store, Q store, gated fp32 residual add,
+// SwiGLU, and the down projection's accumulate-across-FFN-slices.
 //
 // Structure (one CTA per SM, persistent over 128 x BN output tiles):
-//   warp 0      TMA producer: A and B k-blocks (64 wide, 128-byte swizzle)
-//               into a 4-stage shared-memory ring
+//   warp 0      TMA producer: A and B k-blocks (64 wide) into a shared-memory
+//               ring (bf16 tiles in the 128-byte swizzle the MMA reads)
 //   warp 1      allocates TMEM; one lane issues tcgen05.mma (M=128, N=BN,
 //               K=16) into one of two TMEM accumulators
 //   warps 2..5  epilogue: tcgen05.ld of the accumulator (one token row per
 //               thread), the fused math, stores to global
+//   warps 6..9  (int8 B only) dequantise: each int8 B tile staged by TMA is
+//               converted to bf16 (exact: |q| <= 127) into the swizzled layout
+//               of the MMA operand; the per-row scale multiplies the fp32
+//               accumulator in the epilogue (W = s_row * q, "MiniMax-H3-Comfy-
+//               NPU" section 2.2)
 // The accumulator is double-buffered, so the epilogue of tile i overlaps the
 // main loop of tile i+1.
 //
@@ -25,8 +30,6 @@ namespace {
 
 constexpr int kBM = 128;
 constexpr int kBK = 64;
-constexpr int kStages = 4;
-constexpr int kThreads = 192;
 
 struct GemmParams {
     int64_t M;
@@ -44,21 +47,28 @@ struct GemmParams {
     float *acc;
     int64_t ldacc;
     int acc_load, acc_final;
+    const float *s0, *s1;  // int8 per-row scales of B0 / B1
     int *status;
 };
 
-template <int MODE>
+template <int MODE, bool I8>
 struct Cfg {
     static constexpr int NB = (MODE == DIT_EPI_SWIGLU) ? 2 : 1;  // B operands
     static constexpr int BN = (MODE == DIT_EPI_SWIGLU) ? 128 : 256;
+    static constexpr int STAGES = I8 ? 3 : 4;
+    static constexpr int THREADS = I8 ? 320 : 192;
     static constexpr int A_BYTES = kBM * kBK * 2;
-    static constexpr int B_BYTES = BN * kBK * 2;
-    static constexpr int STAGE_BYTES = A_BYTES + NB * B_BYTES;
+    static constexpr int B_BYTES = BN * kBK * 2;         // one bf16 B tile
+    static constexpr int BQ_BYTES = I8 ? NB * BN * kBK : 0;  // int8 staging
+    static constexpr int OFF_B = A_BYTES;                 // bf16 B tile(s)
+    static constexpr int OFF_BQ = A_BYTES + NB * B_BYTES;
+    static constexpr int STAGE_BYTES = OFF_BQ + BQ_BYTES;
+    static constexpr int TMA_BYTES = A_BYTES + (I8 ? BQ_BYTES : NB * B_BYTES);
     static constexpr int ACC_COLS = NB * BN;  // fp32 TMEM columns per accumulator
     static constexpr int TMEM_COLS = 2 * ACC_COLS;
     static constexpr int OUT_COLS = BN;       // output columns per tile
     static constexpr int BAR_BYTES = 256;
-    static constexpr int SMEM_BYTES = kStages * STAGE_BYTES + BAR_BYTES + 1024;
+    static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + BAR_BYTES + 1024;
 };
 
 DEV void store_bf16x32(__nv_bfloat16 *dst, const float (&f)[32]) {
@@ -90,11 +100,44 @@ DEV void gated_residual32(float *x, const float *gate, const float (&f)[32]) {
     }
 }
 
+// f[0..31] *= s[0..31] (per-output-row int8 weight scales).
+DEV void scale32(float (&f)[32], const float *s) {
+    const float4 *sv = reinterpret_cast<const float4 *>(s);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const float4 v = __ldg(sv + i);
+        f[4 * i + 0] *= v.x;
+        f[4 * i + 1] *= v.y;
+        f[4 * i + 2] *= v.z;
+        f[4 * i + 3] *= v.w;
+    }
+}
+
 DEV float silu(float z) { return z / (1.0f + __expf(-z)); }
 
-template <int MODE>
+// Eight int8 (two words) -> eight bf16 (four words of bf16x2), exact.
+// q + 128 (the byte XOR 0x80) placed in the low mantissa bits of 2^23 gives
+// the float 2^23 + 128 + q exactly; subtracting 2^23 + 128 leaves q.
+DEV uint4 int8x8_to_bf16x8(uint2 w) {
+    const uint32_t lo = w.x ^ 0x80808080u, hi = w.y ^ 0x80808080u;
+    const float bias = 8388736.0f;  // 2^23 + 128
+    float f[8];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        f[k] = __uint_as_float(__byte_perm(lo, 0x4B000000u, 0x7540u + k)) - bias;
+        f[4 + k] = __uint_as_float(__byte_perm(hi, 0x4B000000u, 0x7540u + k)) - bias;
+    }
+    uint4 r;
+    r.x = pack_bf16x2(f[0], f[1]);
+    r.y = pack_bf16x2(f[2], f[3]);
+    r.z = pack_bf16x2(f[4], f[5]);
+    r.w = pack_bf16x2(f[6], f[7]);
+    return r;
+}
+
+template <int MODE, bool I8>
 DEV void epilogue_tile(const GemmParams &p, uint32_t taddr, int64_t m, int nb) {
-    using C = Cfg<MODE>;
+    using C = Cfg<MODE, I8>;
     const bool row_ok = m < p.M;
 #pragma unroll 1
     for (int c0 = 0; c0 < C::OUT_COLS; c0 += 32) {
@@ -112,6 +155,9 @@ DEV void epilogue_tile(const GemmParams &p, uint32_t taddr, int64_t m, int nb) {
         float f[32];
 #pragma unroll
         for (int j = 0; j < 32; ++j) f[j] = __uint_as_float(r[j]);
+        // The DOWN carry stays unscaled (the row scale is the same for every
+        // FFN slice and is applied once, with the residual add).
+        if (I8 && !(MODE == DIT_EPI_DOWN && !p.acc_final)) scale32(f, p.s0 + n);
         if constexpr (MODE == DIT_EPI_STORE_BF16) {
             store_bf16x32(reinterpret_cast<__nv_bfloat16 *>(p.out) + m * p.ldo + n, f);
         } else if constexpr (MODE == DIT_EPI_STORE_F32) {
@@ -133,9 +179,13 @@ DEV void epilogue_tile(const GemmParams &p, uint32_t taddr, int64_t m, int nb) {
         } else if constexpr (MODE == DIT_EPI_RESID) {
             gated_residual32(p.x + m * p.ldx + n, p.gate + n, f);
         } else if constexpr (MODE == DIT_EPI_SWIGLU) {
+            float g[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) g[j] = __uint_as_float(u[j]);
+            if (I8) scale32(g, p.s1 + n);
             float h[32];
 #pragma unroll
-            for (int j = 0; j < 32; ++j) h[j] = silu(f[j]) * __uint_as_float(u[j]);
+            for (int j = 0; j < 32; ++j) h[j] = silu(f[j]) * g[j];
             store_bf16x32(reinterpret_cast<__nv_bfloat16 *>(p.out) + m * p.ldo + n, h);
         } else if constexpr (MODE == DIT_EPI_DOWN) {
             if (p.acc_final) {
@@ -152,8 +202,9 @@ DEV void epilogue_tile(const GemmParams &p, uint32_t taddr, int64_t m, int nb) {
 
 // DOWN with acc_load: write the carried fp32 accumulator of tile t into the
 // TMEM buffer before the tile's MMAs start (they then accumulate onto it).
+template <bool I8>
 DEV void preload_tile(const GemmParams &p, uint32_t taddr, int64_t m, int nb) {
-    using C = Cfg<DIT_EPI_DOWN>;
+    using C = Cfg<DIT_EPI_DOWN, I8>;
     const bool row_ok = m < p.M;
 #pragma unroll 1
     for (int c0 = 0; c0 < C::OUT_COLS; c0 += 32) {
@@ -178,33 +229,36 @@ DEV void preload_tile(const GemmParams &p, uint32_t taddr, int64_t m, int nb) {
     }
 }
 
-template <int MODE>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int MODE, bool I8>
+__global__ void __launch_bounds__(Cfg<MODE, I8>::THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                    const __grid_constant__ CUtensorMap tmB0,
                    const __grid_constant__ CUtensorMap tmB1, const GemmParams p) {
-    using C = Cfg<MODE>;
+    using C = Cfg<MODE, I8>;
+    constexpr int S = C::STAGES;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *tiles = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t *bars = reinterpret_cast<uint64_t *>(tiles + kStages * C::STAGE_BYTES);
-    // bars: full[kStages], empty[kStages], tfull[2], tempty[2], drain
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * kStages + 5);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(tiles + S * C::STAGE_BYTES);
+    // bars: full[S], empty[S], conv[S], tfull[2], tempty[2], drain
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 3 * S + 5);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     const int warp = warp_id();
     const int lane = lane_id();
     const uint32_t bar0 = smem_u32(bars);
     auto full_bar = [&](int s) { return bar0 + 8u * s; };
-    auto empty_bar = [&](int s) { return bar0 + 8u * (kStages + s); };
-    auto tfull_bar = [&](int b) { return bar0 + 8u * (2 * kStages + b); };
-    auto tempty_bar = [&](int b) { return bar0 + 8u * (2 * kStages + 2 + b); };
-    const uint32_t drain_bar = bar0 + 8u * (2 * kStages + 4);
+    auto empty_bar = [&](int s) { return bar0 + 8u * (S + s); };
+    auto conv_bar = [&](int s) { return bar0 + 8u * (2 * S + s); };
+    auto tfull_bar = [&](int b) { return bar0 + 8u * (3 * S + b); };
+    auto tempty_bar = [&](int b) { return bar0 + 8u * (3 * S + 2 + b); };
+    const uint32_t drain_bar = bar0 + 8u * (3 * S + 4);
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) {
+        for (int s = 0; s < S; ++s) {
             mbar_init(full_bar(s), 1);
             mbar_init(empty_bar(s), 1);
+            mbar_init(conv_bar(s), 128);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(tfull_bar(b), 1);
@@ -246,24 +300,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                     }
                     const uint32_t sA = smem_u32(tiles + stage * C::STAGE_BYTES);
-                    mbar_arrive_expect_tx(full_bar(stage), C::STAGE_BYTES);
+                    const uint32_t sB = sA + (I8 ? C::OFF_BQ : C::OFF_B);
+                    const uint32_t b_step = I8 ? C::BN * kBK : C::B_BYTES;
+                    mbar_arrive_expect_tx(full_bar(stage), C::TMA_BYTES);
                     tma_load_2d(sA, &tmA, full_bar(stage), kb * kBK, mb * kBM);
-                    tma_load_2d(sA + C::A_BYTES, &tmB0, full_bar(stage), kb * kBK, nb * C::BN);
+                    tma_load_2d(sB, &tmB0, full_bar(stage), kb * kBK, nb * C::BN);
                     if (C::NB == 2)
-                        tma_load_2d(sA + C::A_BYTES + C::B_BYTES, &tmB1, full_bar(stage),
-                                    kb * kBK, nb * C::BN);
+                        tma_load_2d(sB + b_step, &tmB1, full_bar(stage), kb * kBK, nb * C::BN);
                     ++issued;
-                    if (++stage == kStages) {
+                    if (++stage == S) {
                         stage = 0;
                         ph ^= 1u;
                     }
                 }
             }
             if (!ok) {  // let the copies already in flight land before exit
-                const int64_t first = issued > kStages ? issued - kStages : 0;
+                const int64_t first = issued > S ? issued - S : 0;
                 for (int64_t i = first; i < issued; ++i)
-                    mbar_wait_quiet(full_bar(int(i % kStages)), uint32_t((i / kStages) & 1),
-                                    kWaitLimitNs);
+                    mbar_wait_quiet(full_bar(int(i % S)), uint32_t((i / S) & 1), kWaitLimitNs);
             }
         }
     } else if (warp == 1) {
@@ -283,24 +337,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
                 const uint32_t d = tmem + uint32_t(buf * C::ACC_COLS);
                 for (int kb = 0; kb < p.num_k; ++kb) {
-                    if (!mbar_wait(full_bar(stage), ph, wc)) {
+                    if (!mbar_wait(full_bar(stage), ph, wc) ||
+                        (I8 && !mbar_wait(conv_bar(stage), ph, wc))) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
                     const uint32_t sA = smem_u32(tiles + stage * C::STAGE_BYTES);
+                    const uint32_t sB = sA + C::OFF_B;
 #pragma unroll
                     for (int k = 0; k < kBK / 16; ++k) {
                         const uint64_t ad = desc_sw128(sA + 32u * k);
                         const uint32_t accum = (kb | k) != 0 || preload;
-                        mma_bf16_ss(d, ad, desc_sw128(sA + C::A_BYTES + 32u * k), IDESC, accum);
+                        mma_bf16_ss(d, ad, desc_sw128(sB + 32u * k), IDESC, accum);
                         if (C::NB == 2)
-                            mma_bf16_ss(d + C::BN, ad,
-                                        desc_sw128(sA + C::A_BYTES + C::B_BYTES + 32u * k),
+                            mma_bf16_ss(d + C::BN, ad, desc_sw128(sB + C::B_BYTES + 32u * k),
                                         IDESC, accum);
                     }
                     mma_commit(empty_bar(stage));
-                    if (++stage == kStages) {
+                    if (++stage == S) {
                         stage = 0;
                         ph ^= 1u;
                     }
@@ -317,7 +372,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_wait_quiet(drain_bar, 0, kWaitLimitNs);
             }
         }
-    } else {
+    } else if (warp < 6) {
         // -------------------------------------------------- epilogue
         const int q = warp & 3;  // TMEM lane quadrant this warp may access
         const uint32_t lane_base = tmem + (uint32_t(q * 32) << 16);
@@ -325,7 +380,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t bph = 0;
         int t = blockIdx.x;
         if (preload && t < num_tiles) {
-            preload_tile(p, lane_base, int64_t(t / p.num_n) * kBM + q * 32 + lane, t % p.num_n);
+            preload_tile<I8>(p, lane_base, int64_t(t / p.num_n) * kBM + q * 32 + lane,
+                             t % p.num_n);
             tc_fence_before();
             mbar_arrive(tempty_bar(0));
         }
@@ -333,8 +389,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (preload) {
                 const int tn = t + gridDim.x;
                 if (tn < num_tiles) {
-                    preload_tile(p, lane_base + uint32_t((buf ^ 1) * C::ACC_COLS),
-                                 int64_t(tn / p.num_n) * kBM + q * 32 + lane, tn % p.num_n);
+                    preload_tile<I8>(p, lane_base + uint32_t((buf ^ 1) * C::ACC_COLS),
+                                     int64_t(tn / p.num_n) * kBM + q * 32 + lane,
+                                     tn % p.num_n);
                     tc_fence_before();
                     mbar_arrive(tempty_bar(buf ^ 1));
                 }
@@ -344,8 +401,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!ok) break;
             tc_fence_after();
             const int mb = t / p.num_n, nb = t % p.num_n;
-            epilogue_tile<MODE>(p, lane_base + uint32_t(buf * C::ACC_COLS),
-                                int64_t(mb) * kBM + q * 32 + lane, nb);
+            epilogue_tile<MODE, I8>(p, lane_base + uint32_t(buf * C::ACC_COLS),
+                                    int64_t(mb) * kBM + q * 32 + lane, nb);
             if (!preload) {
                 tc_fence_before();
                 mbar_arrive(tempty_bar(buf));
@@ -354,6 +411,45 @@ __global__ void __launch_bounds__(kThreads, 1)
                 buf = 0;
                 bph ^= 1u;
             }
+        }
+    } else if (I8) {
+        // -------------------------------------------------- int8 -> bf16
+        // Staged int8 rows (64 bytes each, NB*BN rows) become 128-byte bf16
+        // rows; 16-byte chunk c of row r lands at chunk c ^ (r % 8) of the
+        // row (the 128-byte swizzle), rows in 8-row groups of 1024 bytes.
+        const int tid = threadIdx.x - 192;
+        int stage = 0;
+        uint32_t ph = 0;
+        for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
+            bool ok = true;
+            for (int kb = 0; kb < p.num_k; ++kb) {
+                bool w = mbar_wait(full_bar(stage), ph, wc);
+                w = __all_sync(0xffffffffu, w);
+                if (!w) {
+                    ok = false;
+                    break;
+                }
+                const uint8_t *sb = tiles + stage * C::STAGE_BYTES;
+                const uint32_t dst0 = smem_u32(sb + C::OFF_B);
+#pragma unroll 4
+                for (int i = tid; i < C::NB * C::BN * 8; i += 128) {
+                    const int r = i >> 3, c = i & 7;
+                    const uint2 w8 =
+                        *reinterpret_cast<const uint2 *>(sb + C::OFF_BQ + r * kBK + c * 8);
+                    const uint4 v = int8x8_to_bf16x8(w8);
+                    const uint32_t addr = dst0 + uint32_t(r * 128 + ((c ^ (r & 7)) << 4));
+                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr),
+                                 "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                                 : "memory");
+                }
+                fence_proxy_async_smem();  // the tensor core reads what we wrote
+                mbar_arrive(conv_bar(stage));
+                if (++stage == S) {
+                    stage = 0;
+                    ph ^= 1u;
+                }
+            }
+            if (!ok) break;
         }
     }
 
@@ -365,20 +461,30 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-template <int MODE>
+int &attr_flag(int mode, bool i8) {
+    static int done[8][2][64] = {};  // per mode, B type, device
+    int dev = 0;
+    cudaGetDevice(&dev);
+    return done[mode][i8 ? 1 : 0][dev & 63];
+}
+
+template <int MODE, bool I8>
 dit_status_t run(const dit_gemm_args_t &a, int *dev_status, cudaStream_t s) {
-    using C = Cfg<MODE>;
-    const CUtensorMapDataType bf16 = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    using C = Cfg<MODE, I8>;
     CUtensorMap tA, tB0, tB1;
-    if (!make_tmap_2d(&tA, bf16, a.a, uint64_t(a.K), uint64_t(a.M), uint64_t(a.lda) * 2, kBK,
-                      kBM))
+    if (!make_tmap_2d(&tA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.a, uint64_t(a.K), uint64_t(a.M),
+                      uint64_t(a.lda) * 2, kBK, kBM))
         return DIT_ERR_INVALID_ARG;
-    if (!make_tmap_2d(&tB0, bf16, a.b0, uint64_t(a.K), uint64_t(a.N), uint64_t(a.ldb) * 2, kBK,
-                      C::BN))
+    const CUtensorMapDataType bdt =
+        I8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    const uint64_t bel = I8 ? 1 : 2;
+    const CUtensorMapSwizzle bsw = I8 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B;
+    if (!make_tmap_2d(&tB0, bdt, a.b0, uint64_t(a.K), uint64_t(a.N), uint64_t(a.ldb) * bel, kBK,
+                      C::BN, bsw))
         return DIT_ERR_INVALID_ARG;
     tB1 = tB0;
-    if (C::NB == 2 && !make_tmap_2d(&tB1, bf16, a.b1, uint64_t(a.K), uint64_t(a.N),
-                                    uint64_t(a.ldb) * 2, kBK, C::BN))
+    if (C::NB == 2 && !make_tmap_2d(&tB1, bdt, a.b1, uint64_t(a.K), uint64_t(a.N),
+                                    uint64_t(a.ldb) * bel, kBK, C::BN, bsw))
         return DIT_ERR_INVALID_ARG;
 
     GemmParams p{};
@@ -401,20 +507,28 @@ dit_status_t run(const dit_gemm_args_t &a, int *dev_status, cudaStream_t s) {
     p.ldacc = a.ldacc;
     p.acc_load = a.acc_load;
     p.acc_final = a.acc_final;
+    p.s0 = a.b0_scale;
+    p.s1 = a.b1_scale;
     p.status = dev_status;
 
-    static bool attr_done = false;  // per instantiation
-    if (!attr_done) {
-        cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<MODE>,
+    int &done = attr_flag(MODE, I8);
+    if (!done) {
+        cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<MODE, I8>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              C::SMEM_BYTES);
         if (e != cudaSuccess) return cuda_fail(e);
-        attr_done = true;
+        done = 1;
     }
     const int tiles = p.num_m * p.num_n;
     const int grid = tiles < sm_count() ? tiles : sm_count();
-    gemm_tc_kernel<MODE><<<grid, kThreads, C::SMEM_BYTES, s>>>(tA, tB0, tB1, p);
+    gemm_tc_kernel<MODE, I8><<<grid, C::THREADS, C::SMEM_BYTES, s>>>(tA, tB0, tB1, p);
     return check_launch();
+}
+
+template <int MODE>
+dit_status_t run_b(const dit_gemm_args_t &a, int *dev_status, cudaStream_t s) {
+    return a.b_dtype == DIT_W_INT8 ? run<MODE, true>(a, dev_status, s)
+                                   : run<MODE, false>(a, dev_status, s);
 }
 
 bool ld_ok(int64_t ld, int64_t min_ld, int elem_bytes) {
@@ -426,35 +540,41 @@ bool ld_ok(int64_t ld, int64_t min_ld, int elem_bytes) {
 dit_status_t launch_gemm(const dit_gemm_args_t &a, int *dev_status, cudaStream_t s) {
     if (a.M < 0 || a.N <= 0 || a.K <= 0 || a.N % 32 || a.K % kBK) return DIT_ERR_INVALID_ARG;
     if (a.M > (int64_t(1) << 31) - kBM) return DIT_ERR_INVALID_ARG;
-    if (a.b_dtype != DIT_W_BF16) return DIT_ERR_INVALID_ARG;
+    if (a.b_dtype != DIT_W_BF16 && a.b_dtype != DIT_W_INT8) return DIT_ERR_INVALID_ARG;
+    const bool i8 = a.b_dtype == DIT_W_INT8;
     if (!a.a || !a.b0) return DIT_ERR_INVALID_ARG;
     if (!aligned16(a.a) || !aligned16(a.b0)) return DIT_ERR_ALIGN;
-    if (!ld_ok(a.lda, a.K, 2) || !ld_ok(a.ldb, a.K, 2)) return DIT_ERR_INVALID_ARG;
+    if (!ld_ok(a.lda, a.K, 2) || !ld_ok(a.ldb, a.K, i8 ? 1 : 2)) return DIT_ERR_INVALID_ARG;
+    if (i8) {
+        if (!a.b0_scale || !aligned16(a.b0_scale)) return DIT_ERR_ALIGN;
+        if (a.mode == DIT_EPI_SWIGLU && (!a.b1_scale || !aligned16(a.b1_scale)))
+            return DIT_ERR_ALIGN;
+    }
     if (a.M == 0) return DIT_OK;
     switch (a.mode) {
         case DIT_EPI_STORE_BF16:
             if (!a.out || !aligned16(a.out)) return DIT_ERR_ALIGN;
             if (!ld_ok(a.ldo, a.N, 2)) return DIT_ERR_INVALID_ARG;
-            return run<DIT_EPI_STORE_BF16>(a, dev_status, s);
+            return run_b<DIT_EPI_STORE_BF16>(a, dev_status, s);
         case DIT_EPI_STORE_F32:
             if (!a.out || !aligned16(a.out)) return DIT_ERR_ALIGN;
             if (!ld_ok(a.ldo, a.N, 4)) return DIT_ERR_INVALID_ARG;
-            return run<DIT_EPI_STORE_F32>(a, dev_status, s);
+            return run_b<DIT_EPI_STORE_F32>(a, dev_status, s);
         case DIT_EPI_KV:
             if (!a.out || !a.out2 || !aligned16(a.out)) return DIT_ERR_ALIGN;
             if (a.split_n < 0 || a.split_n % 32 || a.split_n > a.N || a.row_offset < 0)
                 return DIT_ERR_INVALID_ARG;
             if (!ld_ok(a.ldo, a.split_n, 2) || a.ldo2 < a.row_offset + a.M)
                 return DIT_ERR_INVALID_ARG;
-            return run<DIT_EPI_KV>(a, dev_status, s);
+            return run_b<DIT_EPI_KV>(a, dev_status, s);
         case DIT_EPI_RESID:
             if (!a.x || !a.gate || !aligned16(a.x) || !aligned16(a.gate)) return DIT_ERR_ALIGN;
             if (!ld_ok(a.ldx, a.N, 4)) return DIT_ERR_INVALID_ARG;
-            return run<DIT_EPI_RESID>(a, dev_status, s);
+            return run_b<DIT_EPI_RESID>(a, dev_status, s);
         case DIT_EPI_SWIGLU:
             if (!a.b1 || !aligned16(a.b1) || !a.out || !aligned16(a.out)) return DIT_ERR_ALIGN;
             if (!ld_ok(a.ldo, a.N, 2)) return DIT_ERR_INVALID_ARG;
-            return run<DIT_EPI_SWIGLU>(a, dev_status, s);
+            return run_b<DIT_EPI_SWIGLU>(a, dev_status, s);
         case DIT_EPI_DOWN:
             if (a.acc_final) {
                 if (!a.x || !a.gate || !aligned16(a.x) || !aligned16(a.gate))
@@ -465,7 +585,7 @@ dit_status_t launch_gemm(const dit_gemm_args_t &a, int *dev_status, cudaStream_t
                 if (!a.acc || !aligned16(a.acc)) return DIT_ERR_ALIGN;
                 if (!ld_ok(a.ldacc, a.N, 4)) return DIT_ERR_INVALID_ARG;
             }
-            return run<DIT_EPI_DOWN>(a, dev_status, s);
+            return run_b<DIT_EPI_DOWN>(a, dev_status, s);
         default:
             return DIT_ERR_INVALID_ARG;
     }

@@ -43,10 +43,12 @@ int sm_count();
 
 // 2-D tensor map (row-major matrix: `inner` elements per row, `outer` rows,
 // `row_bytes` between rows) with a box of box_inner x box_outer elements and
-// 128-byte swizzle; out-of-range elements read as zero.
+// the given shared-memory swizzle (128-byte by default); out-of-range
+// elements read as zero.
 bool make_tmap_2d(CUtensorMap *m, CUtensorMapDataType dt, const void *base,
                   uint64_t inner, uint64_t outer, uint64_t row_bytes,
-                  uint32_t box_inner, uint32_t box_outer);
+                  uint32_t box_inner, uint32_t box_outer,
+                  CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B);
 
 dit_status_t launch_modln(const float *x, int64_t rows, int D, const float *shift,
                           const float *scale, void *out, cudaStream_t s);

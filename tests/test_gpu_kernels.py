@@ -273,3 +273,84 @@ def test_attention_equal_values_return_that_row():
     # sum of bf16-rounded probabilities is within 2^-8 of one
     np.testing.assert_allclose(f64(o), np.tile(f64(row), (150, 1)), rtol=1e-2,
                                atol=1e-2)
+
+
+# ---------------------------------------------------------------- int8 weights
+
+def int8_weight(g, N, K, jitter=True):
+    q = torch.randint(-127, 128, (N, K), generator=g, dtype=torch.int16).to(torch.int8)
+    s = torch.full((N,), 0.02 / 127)
+    if jitter:
+        s = s * (0.5 + torch.rand(N, generator=g))
+    return q, s
+
+
+def deq(q, s):
+    return ob.dequant_int8(q.numpy(), s.numpy())
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 32, 64), (300, 288, 320), (1000, 512, 1024)])
+def test_gemm_int8_store_f32(M, N, K):
+    g = gen(100 + M)
+    a = randn(g, M, K).to(torch.bfloat16)
+    q, s = int8_weight(g, N, K)
+    out = torch.full((M, N), float("nan"), device="cuda")
+    st = status_buf()
+    gemm_args(ds.EPI_STORE_F32, a.cuda(), q.cuda(), out=out, ldo=N,
+              b_dtype=ds.W_INT8, b0_scale=s.cuda()).run(st)
+    assert_status_ok(st)
+    check_close(f64(out), f64(a) @ deq(q, s).T, K, "int8 store_f32")
+
+
+def test_gemm_int8_swiglu_and_kv():
+    g = gen(101)
+    M, N, K = 300, 704, 256
+    a = randn(g, M, K).to(torch.bfloat16)
+    qg, sg = int8_weight(g, N, K)
+    qu, su = int8_weight(g, N, K)
+    out = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+    gemm_args(ds.EPI_SWIGLU, a.cuda(), qg.cuda(), b1=qu.cuda(), out=out, ldo=N,
+              b_dtype=ds.W_INT8, b0_scale=sg.cuda(), b1_scale=su.cuda()).run()
+    torch.cuda.synchronize()
+    ref = ob.silu(f64(a) @ deq(qg, sg).T) * (f64(a) @ deq(qu, su).T)
+    err = np.abs(f64(out) - ref) / np.maximum(np.abs(ref), 1e-2)
+    assert err.max() <= 2.0 ** -7
+    # K/V store with int8 weights
+    D, row_off, T_pad = 256, 64, 512
+    qkv, skv = int8_weight(g, 2 * D, D)
+    a2 = randn(g, 200, D).to(torch.bfloat16)
+    Kb = torch.zeros(T_pad, D, dtype=torch.bfloat16, device="cuda")
+    Vt = torch.zeros(D, T_pad, dtype=torch.bfloat16, device="cuda")
+    gemm_args(ds.EPI_KV, a2.cuda(), qkv.cuda(), out=Kb, ldo=D, out2=Vt, ldo2=T_pad,
+              row_offset=row_off, split_n=D, b_dtype=ds.W_INT8,
+              b0_scale=skv.cuda()).run()
+    torch.cuda.synchronize()
+    ref = f64(a2) @ deq(qkv, skv).T
+    for got, r in ((f64(Kb[row_off:row_off + 200]), ref[:, :D]),
+                   (f64(Vt[:, row_off:row_off + 200]).T, ref[:, D:])):
+        e = np.abs(got - r) / np.maximum(np.abs(r), 1e-2)
+        assert e.max() <= 2.0 ** -8 + 1e-3
+
+
+@pytest.mark.parametrize("fs", [64, 256])
+def test_gemm_int8_down_carry_bit_identical(fs):
+    g = gen(102 + fs)
+    M, D, F = 300, 512, 512
+    h = randn(g, M, F).to(torch.bfloat16).cuda()
+    q, s = int8_weight(g, D, F)
+    qd, sd = q.cuda(), s.cuda()
+    x = randn(g, M, D)
+    gate = torch.rand(D, generator=g).cuda()
+    x_ref = x.cuda()
+    gemm_args(ds.EPI_DOWN, h, qd, x=x_ref, ldx=D, gate=gate, acc_load=0,
+              acc_final=1, b_dtype=ds.W_INT8, b0_scale=sd).run()
+    x_sl = x.cuda()
+    acc = torch.empty(M, D, device="cuda")
+    for f in range(0, F, fs):
+        gemm_args(ds.EPI_DOWN, h[:, f:f + fs], qd[:, f:f + fs], x=x_sl, ldx=D,
+                  gate=gate, acc=acc, ldacc=D, acc_load=int(f > 0),
+                  acc_final=int(f + fs >= F), b_dtype=ds.W_INT8, b0_scale=sd).run()
+    torch.cuda.synchronize()
+    ref = f64(x) + f64(gate) * (f64(h) @ deq(q, s).T)
+    assert np.abs(f64(x_ref) - ref).max() < 1e-4
+    assert torch.equal(x_ref, x_sl)
