@@ -55,20 +55,24 @@ template <int MODE, bool I8>
 struct Cfg {
     static constexpr int NB = (MODE == DIT_EPI_SWIGLU) ? 2 : 1;  // B operands
     static constexpr int BN = (MODE == DIT_EPI_SWIGLU) ? 128 : 256;
-    static constexpr int STAGES = I8 ? 3 : 4;
     static constexpr int THREADS = I8 ? 320 : 192;
     static constexpr int A_BYTES = kBM * kBK * 2;
     static constexpr int B_BYTES = BN * kBK * 2;         // one bf16 B tile
-    static constexpr int BQ_BYTES = I8 ? NB * BN * kBK : 0;  // int8 staging
-    static constexpr int OFF_B = A_BYTES;                 // bf16 B tile(s)
-    static constexpr int OFF_BQ = A_BYTES + NB * B_BYTES;
-    static constexpr int STAGE_BYTES = OFF_BQ + BQ_BYTES;
-    static constexpr int TMA_BYTES = A_BYTES + (I8 ? BQ_BYTES : NB * B_BYTES);
+    static constexpr int BQ_BYTES = NB * BN * kBK;       // int8 B staging
+    // TMA ring: bf16: A + B (4 stages); int8: A + int8 B (4 stages).
+    static constexpr int STAGES = 4;
+    static constexpr int STAGE_BYTES = A_BYTES + (I8 ? BQ_BYTES : NB * B_BYTES);
+    static constexpr int TMA_BYTES = STAGE_BYTES;
+    // int8 only: ring of converted bf16 B tiles read by the MMA (3 stages),
+    // decoupled from the TMA ring so TMA latency and conversion overlap.
+    static constexpr int CSTAGES = I8 ? 3 : 0;
+    static constexpr int C_BYTES = NB * B_BYTES;
+    static constexpr int OFF_C = STAGES * STAGE_BYTES;
     static constexpr int ACC_COLS = NB * BN;  // fp32 TMEM columns per accumulator
     static constexpr int TMEM_COLS = 2 * ACC_COLS;
     static constexpr int OUT_COLS = BN;       // output columns per tile
     static constexpr int BAR_BYTES = 256;
-    static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + BAR_BYTES + 1024;
+    static constexpr int SMEM_BYTES = OFF_C + CSTAGES * C_BYTES + BAR_BYTES + 1024;
 };
 
 DEV void store_bf16x32(__nv_bfloat16 *dst, const float (&f)[32]) {
@@ -115,24 +119,35 @@ DEV void scale32(float (&f)[32], const float *s) {
 
 DEV float silu(float z) { return z / (1.0f + __expf(-z)); }
 
-// Eight int8 (two words) -> eight bf16 (four words of bf16x2), exact.
-// q + 128 (the byte XOR 0x80) placed in the low mantissa bits of 2^23 gives
-// the float 2^23 + 128 + q exactly; subtracting 2^23 + 128 leaves q.
-DEV uint4 int8x8_to_bf16x8(uint2 w) {
-    const uint32_t lo = w.x ^ 0x80808080u, hi = w.y ^ 0x80808080u;
-    const float bias = 8388736.0f;  // 2^23 + 128
-    float f[8];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-        f[k] = __uint_as_float(__byte_perm(lo, 0x4B000000u, 0x7540u + k)) - bias;
-        f[4 + k] = __uint_as_float(__byte_perm(hi, 0x4B000000u, 0x7540u + k)) - bias;
-    }
-    uint4 r;
-    r.x = pack_bf16x2(f[0], f[1]);
-    r.y = pack_bf16x2(f[2], f[3]);
-    r.z = pack_bf16x2(f[4], f[5]);
-    r.w = pack_bf16x2(f[6], f[7]);
+// Two floats (as raw bits) -> one bf16x2 word by taking their high halves.
+// Exact for the values produced below: small integers whose low 16 mantissa
+// bits are zero.
+DEV uint32_t hi_halves(uint32_t f_lo, uint32_t f_hi) { return __byte_perm(f_lo, f_hi, 0x7632u); }
+
+// Four int8 (one word, already XORed with 0x80808080 so each byte is
+// u = q + 128) -> four bf16 (two bf16x2 words), exact.  u placed in the low
+// mantissa bits of 2^23 is the float 2^23 + u; one packed subtraction of
+// 2^23 + 128 leaves q, which has at most 8 significant bits, so its bf16
+// value is the high half of its fp32 bits.
+DEV uint2 int8x4_to_bf16x4(uint32_t u) {
+    const uint64_t bias2 = 0xCB000080CB000080ull;  // (-(2^23 + 128)) x 2
+    uint64_t a = (uint64_t(__byte_perm(u, 0x4B000000u, 0x7541u)) << 32) |
+                 __byte_perm(u, 0x4B000000u, 0x7540u);
+    uint64_t b = (uint64_t(__byte_perm(u, 0x4B000000u, 0x7543u)) << 32) |
+                 __byte_perm(u, 0x4B000000u, 0x7542u);
+    asm("add.rn.f32x2 %0, %0, %1;" : "+l"(a) : "l"(bias2));
+    asm("add.rn.f32x2 %0, %0, %1;" : "+l"(b) : "l"(bias2));
+    uint2 r;
+    r.x = hi_halves(uint32_t(a), uint32_t(a >> 32));
+    r.y = hi_halves(uint32_t(b), uint32_t(b >> 32));
     return r;
+}
+
+// Eight int8 (two words) -> eight bf16 (four bf16x2 words), exact.
+DEV uint4 int8x8_to_bf16x8(uint2 w) {
+    const uint2 lo = int8x4_to_bf16x4(w.x ^ 0x80808080u);
+    const uint2 hi = int8x4_to_bf16x4(w.y ^ 0x80808080u);
+    return make_uint4(lo.x, lo.y, hi.x, hi.y);
 }
 
 template <int MODE, bool I8>
@@ -236,12 +251,13 @@ __global__ void __launch_bounds__(Cfg<MODE, I8>::THREADS, 1)
                    const __grid_constant__ CUtensorMap tmB1, const GemmParams p) {
     using C = Cfg<MODE, I8>;
     constexpr int S = C::STAGES;
+    constexpr int CS = C::CSTAGES;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *tiles = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t *bars = reinterpret_cast<uint64_t *>(tiles + S * C::STAGE_BYTES);
-    // bars: full[S], empty[S], conv[S], tfull[2], tempty[2], drain
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 3 * S + 5);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(tiles + C::OFF_C + CS * C::C_BYTES);
+    // bars: full[S], empty[S], cfull[4], cempty[4], tfull[2], tempty[2], drain
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * S + 8 + 5);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     const int warp = warp_id();
@@ -249,16 +265,20 @@ __global__ void __launch_bounds__(Cfg<MODE, I8>::THREADS, 1)
     const uint32_t bar0 = smem_u32(bars);
     auto full_bar = [&](int s) { return bar0 + 8u * s; };
     auto empty_bar = [&](int s) { return bar0 + 8u * (S + s); };
-    auto conv_bar = [&](int s) { return bar0 + 8u * (2 * S + s); };
-    auto tfull_bar = [&](int b) { return bar0 + 8u * (3 * S + b); };
-    auto tempty_bar = [&](int b) { return bar0 + 8u * (3 * S + 2 + b); };
-    const uint32_t drain_bar = bar0 + 8u * (3 * S + 4);
+    auto cfull_bar = [&](int s) { return bar0 + 8u * (2 * S + s); };
+    auto cempty_bar = [&](int s) { return bar0 + 8u * (2 * S + 4 + s); };
+    auto tfull_bar = [&](int b) { return bar0 + 8u * (2 * S + 8 + b); };
+    auto tempty_bar = [&](int b) { return bar0 + 8u * (2 * S + 10 + b); };
+    const uint32_t drain_bar = bar0 + 8u * (2 * S + 12);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
             mbar_init(full_bar(s), 1);
             mbar_init(empty_bar(s), 1);
-            mbar_init(conv_bar(s), 128);
+        }
+        for (int s = 0; s < CS; ++s) {
+            mbar_init(cfull_bar(s), 128);
+            mbar_init(cempty_bar(s), 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(tfull_bar(b), 1);
@@ -300,7 +320,7 @@ __global__ void __launch_bounds__(Cfg<MODE, I8>::THREADS, 1)
                         break;
                     }
                     const uint32_t sA = smem_u32(tiles + stage * C::STAGE_BYTES);
-                    const uint32_t sB = sA + (I8 ? C::OFF_BQ : C::OFF_B);
+                    const uint32_t sB = sA + C::A_BYTES;
                     const uint32_t b_step = I8 ? C::BN * kBK : C::B_BYTES;
                     mbar_arrive_expect_tx(full_bar(stage), C::TMA_BYTES);
                     tma_load_2d(sA, &tmA, full_bar(stage), kb * kBK, mb * kBM);
@@ -324,8 +344,8 @@ __global__ void __launch_bounds__(Cfg<MODE, I8>::THREADS, 1)
         if (lane == 0) {
             // ---------------------------------------------- MMA issuer
             constexpr uint32_t IDESC = idesc_bf16_f32(kBM, C::BN);
-            int stage = 0;
-            uint32_t ph = 0;
+            int stage = 0, cstage = 0;
+            uint32_t ph = 0, cph = 0;
             int buf = 0;
             uint32_t bph = 0;
             bool ok = true;
@@ -338,13 +358,14 @@ __global__ void __launch_bounds__(Cfg<MODE, I8>::THREADS, 1)
                 const uint32_t d = tmem + uint32_t(buf * C::ACC_COLS);
                 for (int kb = 0; kb < p.num_k; ++kb) {
                     if (!mbar_wait(full_bar(stage), ph, wc) ||
-                        (I8 && !mbar_wait(conv_bar(stage), ph, wc))) {
+                        (I8 && !mbar_wait(cfull_bar(cstage), cph, wc))) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
                     const uint32_t sA = smem_u32(tiles + stage * C::STAGE_BYTES);
-                    const uint32_t sB = sA + C::OFF_B;
+                    const uint32_t sB = I8 ? smem_u32(tiles + C::OFF_C + cstage * C::C_BYTES)
+                                           : sA + C::A_BYTES;
 #pragma unroll
                     for (int k = 0; k < kBK / 16; ++k) {
                         const uint64_t ad = desc_sw128(sA + 32u * k);
@@ -358,6 +379,13 @@ __global__ void __launch_bounds__(Cfg<MODE, I8>::THREADS, 1)
                     if (++stage == S) {
                         stage = 0;
                         ph ^= 1u;
+                    }
+                    if (I8) {
+                        mma_commit(cempty_bar(cstage));
+                        if (++cstage == CS) {
+                            cstage = 0;
+                            cph ^= 1u;
+                        }
                     }
                 }
                 if (!ok) break;
@@ -415,41 +443,56 @@ __global__ void __launch_bounds__(Cfg<MODE, I8>::THREADS, 1)
     } else if (I8) {
         // -------------------------------------------------- int8 -> bf16
         // Staged int8 rows (64 bytes each, NB*BN rows) become 128-byte bf16
-        // rows; 16-byte chunk c of row r lands at chunk c ^ (r % 8) of the
-        // row (the 128-byte swizzle), rows in 8-row groups of 1024 bytes.
+        // rows of a converted-B stage; 16-byte chunk c of row r lands at
+        // chunk c ^ (r % 8) of the row (the 128-byte swizzle), rows in 8-row
+        // groups of 1024 bytes.
         const int tid = threadIdx.x - 192;
-        int stage = 0;
-        uint32_t ph = 0;
-        for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
-            bool ok = true;
+        int stage = 0, cstage = 0;
+        uint32_t ph = 0, cph = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
             for (int kb = 0; kb < p.num_k; ++kb) {
-                bool w = mbar_wait(full_bar(stage), ph, wc);
+                bool w = mbar_wait(full_bar(stage), ph, wc) &&
+                         mbar_wait(cempty_bar(cstage), cph ^ 1u, wc);
                 w = __all_sync(0xffffffffu, w);
                 if (!w) {
                     ok = false;
                     break;
                 }
-                const uint8_t *sb = tiles + stage * C::STAGE_BYTES;
-                const uint32_t dst0 = smem_u32(sb + C::OFF_B);
-#pragma unroll 4
-                for (int i = tid; i < C::NB * C::BN * 8; i += 128) {
-                    const int r = i >> 3, c = i & 7;
-                    const uint2 w8 =
-                        *reinterpret_cast<const uint2 *>(sb + C::OFF_BQ + r * kBK + c * 8);
-                    const uint4 v = int8x8_to_bf16x8(w8);
-                    const uint32_t addr = dst0 + uint32_t(r * 128 + ((c ^ (r & 7)) << 4));
-                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr),
-                                 "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
-                                 : "memory");
+                const uint8_t *sq = tiles + stage * C::STAGE_BYTES + C::A_BYTES;
+                uint8_t *dst0 = tiles + C::OFF_C + cstage * C::C_BYTES;
+                // Each thread owns pieces tid + 128 i (8 int8 each); loads are
+                // batched ahead of the conversions so their latency overlaps.
+                constexpr int kPieces = C::NB * C::BN * 8 / 128;
+                constexpr int kBatch = 8;
+#pragma unroll
+                for (int i0 = 0; i0 < kPieces; i0 += kBatch) {
+                    uint2 w8[kBatch];
+#pragma unroll
+                    for (int i = 0; i < kBatch; ++i) {
+                        const int piece = tid + 128 * (i0 + i);
+                        w8[i] = *reinterpret_cast<const uint2 *>(sq + (piece >> 3) * kBK +
+                                                                 (piece & 7) * 8);
+                    }
+#pragma unroll
+                    for (int i = 0; i < kBatch; ++i) {
+                        const int piece = tid + 128 * (i0 + i);
+                        const int r = piece >> 3, c = piece & 7;
+                        *reinterpret_cast<uint4 *>(dst0 + r * 128 + ((c ^ (r & 7)) << 4)) =
+                            int8x8_to_bf16x8(w8[i]);
+                    }
                 }
                 fence_proxy_async_smem();  // the tensor core reads what we wrote
-                mbar_arrive(conv_bar(stage));
+                mbar_arrive(cfull_bar(cstage));
                 if (++stage == S) {
                     stage = 0;
                     ph ^= 1u;
                 }
+                if (++cstage == CS) {
+                    cstage = 0;
+                    cph ^= 1u;
+                }
             }
-            if (!ok) break;
         }
     }
 
