@@ -55,7 +55,8 @@ template <int MODE, bool I8>
 struct Cfg {
     static constexpr int NB = (MODE == DIT_EPI_SWIGLU) ? 2 : 1;  // B operands
     static constexpr int BN = (MODE == DIT_EPI_SWIGLU) ? 128 : 256;
-    static constexpr int THREADS = I8 ? 320 : 192;
+    static constexpr int CONV_WARPS = 4;                   // int8 only
+    static constexpr int THREADS = I8 ? 192 + 32 * CONV_WARPS : 192;
     static constexpr int A_BYTES = kBM * kBK * 2;
     static constexpr int B_BYTES = BN * kBK * 2;         // one bf16 B tile
     static constexpr int BQ_BYTES = NB * BN * kBK;       // int8 B staging
@@ -277,7 +278,7 @@ __global__ void __launch_bounds__(Cfg<MODE, I8>::THREADS, 1)
             mbar_init(empty_bar(s), 1);
         }
         for (int s = 0; s < CS; ++s) {
-            mbar_init(cfull_bar(s), 128);
+            mbar_init(cfull_bar(s), 32 * C::CONV_WARPS);
             mbar_init(cempty_bar(s), 1);
         }
         for (int b = 0; b < 2; ++b) {
@@ -461,26 +462,25 @@ __global__ void __launch_bounds__(Cfg<MODE, I8>::THREADS, 1)
                 }
                 const uint8_t *sq = tiles + stage * C::STAGE_BYTES + C::A_BYTES;
                 uint8_t *dst0 = tiles + C::OFF_C + cstage * C::C_BYTES;
-                // Each thread owns pieces tid + 128 i (8 int8 each); loads are
-                // batched ahead of the conversions so their latency overlaps.
-                constexpr int kPieces = C::NB * C::BN * 8 / 128;
-                constexpr int kBatch = 8;
+                // Thread tid owns pieces tid + kConv * i (8 int8 each): row
+                // r = tid / 8 + (kConv / 8) i, chunk c = tid % 8, and r % 8 is
+                // the same for all of them.  Loads are batched ahead of the
+                // conversions so their latency overlaps.
+                constexpr int kConv = 32 * C::CONV_WARPS;
+                constexpr int kPieces = C::NB * C::BN * 8 / kConv;
+                constexpr int kBatch = kPieces < 8 ? kPieces : 8;
+                const uint8_t *src = sq + (tid >> 3) * kBK + (tid & 7) * 8;
+                uint8_t *dst = dst0 + (tid >> 3) * 128 + (((tid & 7) ^ ((tid >> 3) & 7)) << 4);
 #pragma unroll
                 for (int i0 = 0; i0 < kPieces; i0 += kBatch) {
                     uint2 w8[kBatch];
 #pragma unroll
-                    for (int i = 0; i < kBatch; ++i) {
-                        const int piece = tid + 128 * (i0 + i);
-                        w8[i] = *reinterpret_cast<const uint2 *>(sq + (piece >> 3) * kBK +
-                                                                 (piece & 7) * 8);
-                    }
+                    for (int i = 0; i < kBatch; ++i)
+                        w8[i] = *reinterpret_cast<const uint2 *>(src + (i0 + i) * (kConv / 8) * kBK);
 #pragma unroll
-                    for (int i = 0; i < kBatch; ++i) {
-                        const int piece = tid + 128 * (i0 + i);
-                        const int r = piece >> 3, c = piece & 7;
-                        *reinterpret_cast<uint4 *>(dst0 + r * 128 + ((c ^ (r & 7)) << 4)) =
+                    for (int i = 0; i < kBatch; ++i)
+                        *reinterpret_cast<uint4 *>(dst + (i0 + i) * (kConv / 8) * 128) =
                             int8x8_to_bf16x8(w8[i]);
-                    }
                 }
                 fence_proxy_async_smem();  // the tensor core reads what we wrote
                 mbar_arrive(cfull_bar(cstage));
