@@ -12,13 +12,15 @@
 //   warp 1        TMEM owner; one lane issues the tcgen05.mma:
 //                   S_X  = Q_X K_j^T  (M=128, N=128, K=d)     -> TMEM S[X]
 //                   O_X += P_X V_j    (M=128, N=d,   K=128)   -> TMEM O[X]
+//                 (P_X from TMEM, aliasing S_X; V_j from shared memory)
 //                 in the order S_A S_B | PV_A S_A' PV_B S_B' | ... so the
 //                 tensor core works on one tile while the other's softmax runs
 //   warps 4..7    softmax of tile A, one query row per thread
 //   warps 8..11   softmax of tile B
 // Softmax per key tile: the row max from S (TMEM), P = exp2(S*log2e/sqrt(d)
-// - m) as bf16 into shared memory (128-byte-swizzled K-major: the A operand
-// of the PV MMA), the running sum l.  The reference max m is only moved when
+// - m) as bf16 written back into the first 64 columns of the same TMEM
+// region (P is the A operand of the PV MMA, read straight from tensor
+// memory, so P never touches shared memory), the running sum l.  The reference max m is only moved when
 // the tile max exceeds it by more than 8 (log2 units); then the row of O is
 // rescaled in TMEM.  Otherwise P may reach 2^8, which bf16 and the fp32
 // accumulator represent without loss of range; O / l is unchanged in exact
@@ -40,14 +42,12 @@ constexpr float kRescaleLog2 = 8.0f;
 
 template <int HD>
 struct ACfg {
-    static constexpr int RING = HD == 128 ? 3 : 4;       // K/V ring stages
+    static constexpr int RING = HD == 128 ? 5 : 8;       // K/V ring stages
     static constexpr int Q_BYTES = kBQ * HD * 2;          // one Q tile
     static constexpr int TILE_BYTES = kBKV * HD * 2;      // one K or V^T tile
-    static constexpr int P_BYTES = kBQ * kBKV * 2;        // one P tile
     static constexpr int OFF_Q = 0;
     static constexpr int OFF_RING = OFF_Q + 2 * Q_BYTES;
-    static constexpr int OFF_P = OFF_RING + RING * TILE_BYTES;
-    static constexpr int OFF_BAR = OFF_P + 2 * P_BYTES;
+    static constexpr int OFF_BAR = OFF_RING + RING * TILE_BYTES;
     static constexpr int SMEM_BYTES = OFF_BAR + 256 + 1024;
     static constexpr int TMEM_COLS = 512;
     static constexpr int COL_O = 2 * kBKV;                // S_A S_B | O_A O_B
@@ -96,10 +96,12 @@ DEV float tile_max(uint32_t saddr, int nvalid) {
     return fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
 }
 
-// P = exp2(S * sl2 - m) for one row: bf16 into the swizzled P tile, returns
-// the sum of the fp32 probabilities.
+// P = exp2(S * sl2 - m) for one row, as bf16 written over the consumed S
+// columns (keys 2i, 2i+1 -> column i), returns the sum of the fp32
+// probabilities.  Chunk c (keys 32c..32c+31) is read before its P (columns
+// 16c..16c+15) is written, so the write never clobbers unread S.
 template <bool MASK>
-DEV float tile_exp(uint32_t saddr, uint32_t prow, int row, float sl2, float m, int nvalid) {
+DEV float tile_exp(uint32_t saddr, float sl2, float m, int nvalid) {
     float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
     const float neg_m = -m;
 #pragma unroll
@@ -127,17 +129,7 @@ DEV float tile_exp(uint32_t saddr, uint32_t prow, int row, float sl2, float m, i
             pk[c >> 1] = pack_bf16x2(p0, p1);
             pk[(c >> 1) + 1] = pack_bf16x2(p2, p3);
         }
-        // 32 keys = 64 bytes = four 16-byte chunks of one 128-byte row
-        const uint32_t blk = prow + (c0 >> 6) * (kBQ * 128);
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const int chunk = ((c0 & 63) >> 3) + u;
-            const uint32_t addr = blk + uint32_t((chunk ^ (row & 7)) << 4);
-            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr),
-                         "r"(pk[4 * u]), "r"(pk[4 * u + 1]), "r"(pk[4 * u + 2]),
-                         "r"(pk[4 * u + 3])
-                         : "memory");
-        }
+        tmem_st16(saddr + (c0 >> 1), pk);
     }
     return (s0 + s1) + (s2 + s3);
 }
@@ -196,7 +188,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const WaitCtx wc{abort_flag, p.status};
     const uint32_t sQ = smem_u32(sm + C::OFF_Q);
     const uint32_t sRing = smem_u32(sm + C::OFF_RING);
-    const uint32_t sP = smem_u32(sm + C::OFF_P);
 
     if (warp == 0) {
         if (lane == 0) {
@@ -260,13 +251,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             };
             auto issue_pv = [&](int x, int seq, int j) {
                 const uint32_t vb = sRing + (seq % C::RING) * C::TILE_BYTES;
-                const uint32_t pb = sP + x * C::P_BYTES;
+                const uint32_t pt = tmem + uint32_t(x * kBKV);  // P_X: lanes 0..127
                 const uint32_t d = tmem + uint32_t(C::COL_O + x * HD);
 #pragma unroll
                 for (int kk = 0; kk < kBKV / 16; ++kk) {
-                    const uint32_t offp = (kk >> 2) * (kBQ * 128) + (kk & 3) * 32;
                     const uint32_t offv = (kk >> 2) * (HD * 128) + (kk & 3) * 32;
-                    mma_bf16_ss(d, desc_sw128(pb + offp), desc_sw128(vb + offv), ID_PV,
+                    mma_bf16_ts(d, pt + uint32_t(8 * kk), desc_sw128(vb + offv), ID_PV,
                                 (j > 0 || kk > 0) ? 1u : 0u);
                 }
             };
@@ -321,7 +311,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t lane_base = tmem + (uint32_t(qd * 32) << 16);
         const uint32_t saddr = lane_base + uint32_t(x * kBKV);
         const uint32_t oaddr = lane_base + uint32_t(C::COL_O + x * HD);
-        const uint32_t prow = sP + x * C::P_BYTES + row * 128;
         const float sl2 = p.scale_log2;
         const int last_valid = int(p.T - int64_t(n_kv - 1) * kBKV);  // keys in last tile
         float m = -INFINITY, l = 0.f;
@@ -361,11 +350,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 l *= alpha;
                 m = m_new;
             }
-            const float sum = masked ? tile_exp<true>(saddr, prow, row, sl2, m, last_valid)
-                                     : tile_exp<false>(saddr, prow, row, sl2, m, kBKV);
+            const float sum = masked ? tile_exp<true>(saddr, sl2, m, last_valid)
+                                     : tile_exp<false>(saddr, sl2, m, kBKV);
             l += sum;
-            fence_proxy_async_smem();  // P is read by the tensor core (async proxy)
-            tc_fence_before();         // S/O accesses finish before the next MMAs
+            tmem_st_wait();    // P is in tensor memory before the PV MMA reads it
+            tc_fence_before(); // S/O/P accesses finish before the next MMAs
             mbar_arrive(bar(B_PF + x));
         }
         if (ok) {
