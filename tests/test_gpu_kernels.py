@@ -354,3 +354,22 @@ def test_gemm_int8_down_carry_bit_identical(fs):
     ref = f64(x) + f64(gate) * (f64(h) @ deq(q, s).T)
     assert np.abs(f64(x_ref) - ref).max() < 1e-4
     assert torch.equal(x_ref, x_sl)
+
+
+def test_attention_probabilities_elementwise():
+    # With V = I (T = d keys) the output row is the probability row itself,
+    # so every exponential is checked element by element: bf16 rounding of P
+    # and of the output (up to 2^-8 relative each) bound the relative error;
+    # an error of 1% in the exponential for any subset of keys exceeds it.
+    g = gen(23)
+    hd, T, Tq = 128, 128, 256
+    q = (randn(g, Tq, hd) * 2).to(torch.bfloat16)
+    k = (randn(g, T, hd) * 2).to(torch.bfloat16)
+    v = torch.eye(T, hd).to(torch.bfloat16)
+    o = run_attention(q, k, v, 1, hd)
+    ref = ob.mha_attention(f64(q), f64(k), f64(v), 1)
+    got = f64(o)
+    big = ref > 1e-3
+    rel = np.abs(got - ref)[big] / ref[big]
+    assert rel.max() < 2 * 2.0 ** -8 + 1e-4, rel.max()
+    np.testing.assert_allclose(got.sum(axis=1), 1.0, atol=2e-2)
