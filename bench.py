@@ -37,7 +37,7 @@ import time
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-HEADLINE = "dit_T32768_D3072"
+HEADLINE = "dit4_int8_final_T32768_D3072"
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0,
@@ -194,13 +194,16 @@ def cpu_sample(cfg, inp, rows_n, steps=1, warmup=0):
         else:
             w = ob.DitWeights(**{k: v.double().numpy() for k, v in bw.named().items()})
         blocks.append((w, mod.double().numpy()))
-    # set-up: K/V of every token (block inputs taken as x for every block;
-    # the cost does not depend on the values)
-    kvs = []
-    for w, mod in blocks:
-        a = ob.ln_modulate(x, mod[0], mod[1])
-        _, wk, wv = w.q_k_v()
-        kvs.append((a @ wk.T, a @ wv.T))
+    # set-up: K/V of every token for the first block, by the oracle's own
+    # projection; every block's sampled rows attend to that key/value set
+    # (the oracle's cost does not depend on the values, and this keeps the
+    # untimed set-up to one full projection)
+    w0, mod0 = blocks[0]
+    a = ob.ln_modulate(x, mod0[0], mod0[1])
+    _, wk, wv = w0.q_k_v()
+    kv = (a @ wk.T, a @ wv.T)
+    del a
+    kvs = [kv] * len(blocks)
     wf = None
     if inp.wf is not None:
         wf = (ob.dequant_int8(inp.wf.numpy(), inp.wf_scale.numpy())
@@ -227,7 +230,8 @@ def cpu_sample(cfg, inp, rows_n, steps=1, warmup=0):
               f"LN-mod, Q, attention against all {T} keys, O-proj, SwiGLU MLP"
               + (", final layer" if wf is not None else "")
               + f") x {len(blocks)} block(s), float64 numpy oracle; K/V of all "
-              "tokens precomputed untimed")
+              "tokens precomputed untimed (first block's, reused as every "
+              "block's key/value set)")
     return value, per_step, sample, times
 
 
