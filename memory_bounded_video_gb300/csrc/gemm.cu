@@ -344,7 +344,10 @@ __global__ void __launch_bounds__(Cfg<MODE, I8>::THREADS, 1)
     } else if (warp == 1) {
         if (lane == 0) {
             // ---------------------------------------------- MMA issuer
-            constexpr uint32_t IDESC = idesc_bf16_f32(kBM, C::BN);
+            // The NB B tiles are contiguous in shared memory (rows of B1 follow
+            // those of B0), so one MMA with N = NB * BN covers both; its
+            // accumulator columns BN.. are the B1 results.
+            constexpr uint32_t IDESC = idesc_bf16_f32(kBM, C::NB * C::BN);
             int stage = 0, cstage = 0;
             uint32_t ph = 0, cph = 0;
             int buf = 0;
@@ -369,12 +372,9 @@ __global__ void __launch_bounds__(Cfg<MODE, I8>::THREADS, 1)
                                            : sA + C::A_BYTES;
 #pragma unroll
                     for (int k = 0; k < kBK / 16; ++k) {
-                        const uint64_t ad = desc_sw128(sA + 32u * k);
                         const uint32_t accum = (kb | k) != 0 || preload;
-                        mma_bf16_ss(d, ad, desc_sw128(sB + 32u * k), IDESC, accum);
-                        if (C::NB == 2)
-                            mma_bf16_ss(d + C::BN, ad, desc_sw128(sB + C::B_BYTES + 32u * k),
-                                        IDESC, accum);
+                        mma_bf16_ss(d, desc_sw128(sA + 32u * k), desc_sw128(sB + 32u * k),
+                                    IDESC, accum);
                     }
                     mma_commit(empty_bar(stage));
                     if (++stage == S) {
