@@ -295,7 +295,15 @@ typedef struct {
     int64_t ldacc;
     int acc_load;
     int acc_final;
+    int flags;              /* 0, or DIT_GEMM_FLAG_* test hooks */
 } dit_gemm_args_t;
+
+/* Test hook for failure detection: CTA 0's producer arms its first
+ * shared-memory stage but withholds the copy, so the MMA's bounded wait runs
+ * out.  The kernel then records DIT_ERR_TIMEOUT in *dev_status, lets its
+ * in-flight copies and MMAs land, frees its tensor memory and returns
+ * (after about two wait limits, ~4 s); the CUDA context stays usable. */
+#define DIT_GEMM_FLAG_INJECT_STALL 1
 
 DIT_API dit_status_t dit_gemm(const dit_gemm_args_t *args, int *dev_status,
                       dit_stream_t stream);

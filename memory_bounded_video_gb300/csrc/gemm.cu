@@ -48,6 +48,7 @@ struct GemmParams {
     int64_t ldacc;
     int acc_load, acc_final;
     const float *s0, *s1;  // int8 per-row scales of B0 / B1
+    int inject_stall;      // DIT_GEMM_FLAG_INJECT_STALL test hook
     int *status;
 };
 
@@ -324,10 +325,16 @@ __global__ void __launch_bounds__(Cfg<MODE, I8>::THREADS, 1)
                     const uint32_t sB = sA + C::A_BYTES;
                     const uint32_t b_step = I8 ? C::BN * kBK : C::B_BYTES;
                     mbar_arrive_expect_tx(full_bar(stage), C::TMA_BYTES);
-                    tma_load_2d(sA, &tmA, full_bar(stage), kb * kBK, mb * kBM);
-                    tma_load_2d(sB, &tmB0, full_bar(stage), kb * kBK, nb * C::BN);
-                    if (C::NB == 2)
-                        tma_load_2d(sB + b_step, &tmB1, full_bar(stage), kb * kBK, nb * C::BN);
+                    // test hook: CTA 0 withholds its first copy (the stage's
+                    // transaction count then never completes)
+                    const bool withhold = p.inject_stall && blockIdx.x == 0 && issued == 0;
+                    if (!withhold) {
+                        tma_load_2d(sA, &tmA, full_bar(stage), kb * kBK, mb * kBM);
+                        tma_load_2d(sB, &tmB0, full_bar(stage), kb * kBK, nb * C::BN);
+                        if (C::NB == 2)
+                            tma_load_2d(sB + b_step, &tmB1, full_bar(stage), kb * kBK,
+                                        nb * C::BN);
+                    }
                     ++issued;
                     if (++stage == S) {
                         stage = 0;
@@ -552,6 +559,7 @@ dit_status_t run(const dit_gemm_args_t &a, int *dev_status, cudaStream_t s) {
     p.acc_final = a.acc_final;
     p.s0 = a.b0_scale;
     p.s1 = a.b1_scale;
+    p.inject_stall = (a.flags & DIT_GEMM_FLAG_INJECT_STALL) != 0;
     p.status = dev_status;
 
     int &done = attr_flag(MODE, I8);
@@ -584,6 +592,7 @@ dit_status_t launch_gemm(const dit_gemm_args_t &a, int *dev_status, cudaStream_t
     if (a.M < 0 || a.N <= 0 || a.K <= 0 || a.N % 32 || a.K % kBK) return DIT_ERR_INVALID_ARG;
     if (a.M > (int64_t(1) << 31) - kBM) return DIT_ERR_INVALID_ARG;
     if (a.b_dtype != DIT_W_BF16 && a.b_dtype != DIT_W_INT8) return DIT_ERR_INVALID_ARG;
+    if (a.flags & ~DIT_GEMM_FLAG_INJECT_STALL) return DIT_ERR_INVALID_ARG;
     const bool i8 = a.b_dtype == DIT_W_INT8;
     if (!a.a || !a.b0) return DIT_ERR_INVALID_ARG;
     if (!aligned16(a.a) || !aligned16(a.b0)) return DIT_ERR_ALIGN;

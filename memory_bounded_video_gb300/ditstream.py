@@ -38,6 +38,8 @@ EPI_RESID = 3
 EPI_SWIGLU = 4
 EPI_DOWN = 5
 
+GEMM_FLAG_INJECT_STALL = 1
+
 # Exported symbols of the C ABI (checked by the CPU tests against the header).
 SYMBOLS = (
     "dit_block_plan", "dit_block_plan_ex", "dit_block_plan_destroy",
@@ -91,7 +93,8 @@ class GemmArgs(ctypes.Structure):
                 ("x", ctypes.c_void_p), ("ldx", ctypes.c_int64),
                 ("gate", ctypes.c_void_p),
                 ("acc", ctypes.c_void_p), ("ldacc", ctypes.c_int64),
-                ("acc_load", ctypes.c_int), ("acc_final", ctypes.c_int)]
+                ("acc_load", ctypes.c_int), ("acc_final", ctypes.c_int),
+                ("flags", ctypes.c_int)]
 
 
 _lib: Optional[ctypes.CDLL] = None
