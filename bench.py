@@ -163,6 +163,25 @@ class ClockSampler:
                 "samples": len(rows), "power_w_max": pmax}
 
 
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    """Max of a per-rank time over all ranks (identity on one rank).  Runs
+    on whatever process group is initialised (NCCL on GPUs, gloo in the CPU
+    tests)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_throughput(units_per_rank: float, world: int, ms_max: float) -> float:
+    """Whole-job throughput of `world` independent replicas: the units all
+    ranks processed over the slowest rank's time."""
+    return units_per_rank * world / (ms_max / 1e3)
+
+
 def cpu_cores():
     try:
         return len(os.sched_getaffinity(0))
@@ -292,14 +311,11 @@ def run_ours(args, rank, world, local_rank):
     prof = stack.plan.profile_read()
     stack.plan.profile_enable(False)
     stack.check(stream)
-    if world > 1:
-        t = torch.tensor([ms], device=dev_name)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, world, dev_name)
 
     blocks = cfg["blocks"]
     tokens_per_step = blocks * T
-    value = tokens_per_step * args.steps * world / (ms / 1e3)
+    value = replica_throughput(tokens_per_step * args.steps, world, ms)
     ms_per_step = ms / args.steps
     flops_step = blocks * ob.block_flops(T, D, F)
     peaks, peak_src = load_peaks()
@@ -389,12 +405,9 @@ def run_ours(args, rank, world, local_rank):
         f1.record(stream)
         torch.cuda.synchronize()
         barrier()
-        ms_e2e = f0.elapsed_time(f1)
-        if world > 1:
-            t = torch.tensor([ms_e2e], device=dev_name)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            ms_e2e = float(t.item())
-        line["e2e"] = {"value": round(tokens_per_step * k_e2e * world / (ms_e2e / 1e3), 1),
+        ms_e2e = max_over_ranks(f0.elapsed_time(f1), world, dev_name)
+        line["e2e"] = {"value": round(replica_throughput(tokens_per_step * k_e2e, world,
+                                                         ms_e2e), 1),
                        "unit": "block-tokens/s",
                        "h2d_bytes_per_step": 4 * T * D,
                        "d2h_bytes_per_step": 4 * res_shape[0] * res_shape[1],

@@ -132,6 +132,20 @@ DIT_API dit_status_t dit_block_plan_ex(int64_t T, int D, int heads, int ffn,
                                int mlp_chunk_tokens, int attn_chunk_tokens,
                                int ffn_slice, dit_plan_t **out);
 
+/* Plan with automatic chunk sizes: the largest chunks whose workspace fits
+ * budget_bytes ("LayerStream: H3 Chunking", "The two numbers you set": use
+ * the largest chunk that fits; "Proposal: Generic memory-aware streaming
+ * execution ...", "Automatic chunk sizing").  The attention slab is chosen
+ * first (largest multiple of 128 tokens, or all T, that fits); then the MLP
+ * token chunk, largest first, with the FFN unsliced unless a slice width of
+ * ffn/2, ffn/4, ... (at least 1024 features) lets a token chunk at least 25%
+ * larger fit (a slice's fp32 carry costs 4*C_m*D bytes).
+ * Any choice gives bit-identical results.  Errors: as dit_block_plan, and
+ * DIT_ERR_WORKSPACE_TOO_SMALL when even 128-token chunks do not fit (K and V
+ * of all T tokens alone take 4*T*D bytes). */
+DIT_API dit_status_t dit_block_plan_auto(int64_t T, int D, int heads, int ffn,
+                                         size_t budget_bytes, dit_plan_t **out);
+
 DIT_API void dit_block_plan_destroy(dit_plan_t *plan);
 
 /* Effective sizes of a plan after clamping: fills any non-NULL pointer. */

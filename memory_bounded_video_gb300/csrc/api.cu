@@ -17,6 +17,7 @@
 //                                  x_c += gate2 * acc                  (DOWN)
 // Pass 2 reads x_s before writing it, and K/V come from pass 1, so every
 // query attends to the pre-attention keys and values of all tokens.
+#include <cstdint>
 #include <cstdio>
 #include <cstring>
 #include <new>
@@ -199,6 +200,63 @@ dit_status_t dit_block_plan_ex(int64_t T, int D, int heads, int ffn, int mlp_chu
     p->ws_bytes = 0;
     *out = p;
     return DIT_OK;
+}
+
+dit_status_t dit_block_plan_auto(int64_t T, int D, int heads, int ffn, size_t budget_bytes,
+                                 dit_plan_t **out) {
+    // "LayerStream: H3 Chunking" ("The two numbers you set"): use the largest
+    // chunk that fits; "Proposal: ... streaming execution" ("Automatic chunk
+    // sizing"): choose the largest chunks that fit a memory envelope.  The
+    // attention slab is the largest multiple of 128 (or all T tokens) whose
+    // plan fits; the MLP takes the largest token chunk, with the FFN unsliced
+    // if that fits and sliced (halving down to 512 features) only when it is
+    // needed to fit that chunk.  Every choice gives the same result bits.
+    if (!out) return DIT_ERR_INVALID_ARG;
+    *out = nullptr;
+    dit_plan_t *probe = nullptr;
+    dit_status_t r = dit_block_plan_ex(T, D, heads, ffn, 128, 128, 0, &probe);
+    if (r != DIT_OK) return r;
+    dit_block_plan_destroy(probe);
+    auto total = [&](int cm, int ca, int fs) -> size_t {
+        dit_plan_t *q = nullptr;
+        if (dit_block_plan_ex(T, D, heads, ffn, cm, ca, fs, &q) != DIT_OK) return SIZE_MAX;
+        const size_t b = q->total;
+        dit_block_plan_destroy(q);
+        return b;
+    };
+    // candidate chunk sizes, largest first: all T tokens, then multiples of 128
+    const int64_t top = (T + 127) / 128 * 128;
+    auto chunk_of = [&](int64_t c) -> int { return c >= T ? 0 : int(c); };
+    int ca = -1;
+    for (int64_t c = top; c >= 128 && ca < 0; c -= 128)
+        if (total(128, chunk_of(c), 0) <= budget_bytes) ca = chunk_of(c);
+    if (ca < 0) return DIT_ERR_WORKSPACE_TOO_SMALL;
+    // For each FFN slice width (unsliced, then halvings down to 1024) the
+    // largest MLP token chunk that fits; slicing is taken only when it buys a
+    // token chunk at least 25% larger than a wider slice does (its fp32
+    // carry adds 4*C_m*D bytes of workspace and HBM traffic per slice).
+    int cm = -1, fs = 0;
+    int64_t best_tokens = 0;
+    for (int f = ffn; f >= 64; f = (f / 2) / 64 * 64) {
+        if (f != ffn && f < 1024) break;
+        const int fs_try = f == ffn ? 0 : f;
+        int cm_f = -1;
+        int64_t tokens = 0;
+        for (int64_t c = top; c >= 128; c -= 128)
+            if (total(chunk_of(c), ca, fs_try) <= budget_bytes) {
+                cm_f = chunk_of(c);
+                tokens = c < T ? c : T;
+                break;
+            }
+        if (cm_f < 0) continue;
+        if (cm < 0 || tokens * 4 >= best_tokens * 5) {
+            cm = cm_f;
+            fs = fs_try;
+            best_tokens = tokens;
+        }
+    }
+    if (cm < 0) return DIT_ERR_WORKSPACE_TOO_SMALL;
+    return dit_block_plan_ex(T, D, heads, ffn, cm, ca, fs, out);
 }
 
 dit_status_t dit_block_plan(int64_t T, int D, int heads, int ffn, int mlp_chunk_tokens,

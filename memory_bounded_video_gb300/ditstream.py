@@ -48,7 +48,7 @@ SYMBOLS = (
     "dit_final_forward", "dit_status_string", "dit_last_cuda_error",
     "dit_abi_version", "dit_modln_cast", "dit_gemm", "dit_attention",
     "dit_block_profile_enable", "dit_block_profile_read",
-    "dit_block_forward_static",
+    "dit_block_forward_static", "dit_block_plan_auto",
 )
 
 STATIC_SCRATCH_BYTES = 64 << 20
@@ -126,6 +126,7 @@ def _declare(lib):
         "dit_block_profile_read": (c_int, [vp, vp, vp, vp]),
         "dit_block_forward_static": (c_int, [vp, vp, ctypes.POINTER(BlockWeights),
                                              vp, vp]),
+        "dit_block_plan_auto": (c_int, [c_int64, c_int, c_int, c_int, c_size, pp]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -178,15 +179,21 @@ def abi_version() -> int:
 
 
 class BlockPlan:
-    """Owns a ``dit_plan_t``; see ``dit_block_plan_ex``."""
+    """Owns a ``dit_plan_t``; see ``dit_block_plan_ex``.  With
+    ``budget_bytes`` set the chunk sizes are chosen by
+    ``dit_block_plan_auto`` instead."""
 
-    def __init__(self, T, D, heads, ffn, mlp_chunk_tokens, attn_chunk_tokens,
-                 ffn_slice=0):
+    def __init__(self, T, D, heads, ffn, mlp_chunk_tokens=0, attn_chunk_tokens=0,
+                 ffn_slice=0, budget_bytes=None):
         lib = load()
         h = ctypes.c_void_p()
-        _check(lib.dit_block_plan_ex(T, D, heads, ffn, mlp_chunk_tokens,
-                                     attn_chunk_tokens, ffn_slice,
-                                     ctypes.byref(h)), "dit_block_plan_ex")
+        if budget_bytes is not None:
+            _check(lib.dit_block_plan_auto(T, D, heads, ffn, int(budget_bytes),
+                                           ctypes.byref(h)), "dit_block_plan_auto")
+        else:
+            _check(lib.dit_block_plan_ex(T, D, heads, ffn, mlp_chunk_tokens,
+                                         attn_chunk_tokens, ffn_slice,
+                                         ctypes.byref(h)), "dit_block_plan_ex")
         self._h = h
         self._ws = None
 
@@ -261,6 +268,11 @@ def block_plan(T, D, heads, ffn, mlp_chunk_tokens, attn_chunk_tokens,
                ffn_slice=0) -> BlockPlan:
     return BlockPlan(T, D, heads, ffn, mlp_chunk_tokens, attn_chunk_tokens,
                      ffn_slice)
+
+
+def block_plan_auto(T, D, heads, ffn, budget_bytes) -> BlockPlan:
+    """The largest chunks whose workspace fits ``budget_bytes``."""
+    return BlockPlan(T, D, heads, ffn, budget_bytes=budget_bytes)
 
 
 def block_weights(wqkv, wo, wgate, wup, wdown, scales=None) -> BlockWeights:

@@ -177,3 +177,51 @@ def test_stage_entry_points_validate_before_launch(lib):
                              256, None, None) == ds.ERR_INVALID_ARG
     assert lib.dit_attention(16, 128, 256, 16, 256, 16, 500, 512, 4, 64, 16,
                              256, None, None) == ds.ERR_INVALID_ARG
+
+
+def test_plan_auto_picks_largest_chunks_that_fit(lib):
+    T, D, H, F = 65536, 3072, 24, 8192
+    floor = 4 * T * D
+    # unlimited budget: one slab of all tokens, unsliced FFN
+    p = ds.block_plan_auto(T, D, H, F, 1 << 40)
+    info = p.info()
+    assert info["attn_chunk"] == T and info["mlp_chunk"] == T
+    assert info["ffn_slice"] == F
+    prev = None
+    for extra_mib in (40, 88, 200, 500, 1500):
+        budget = floor + 2 * 1024 * 1024 + extra_mib * 2**20
+        p = ds.block_plan_auto(T, D, H, F, budget)
+        info = p.info()
+        assert p.workspace_bytes() <= budget
+        # the chosen chunks are maximal: the next larger attention chunk
+        # would not fit
+        ca = info["attn_chunk"]
+        if ca < T:
+            bigger = ds.block_plan(T, D, H, F, 128, ca + 128)
+            assert bigger.workspace_bytes() > budget
+        if prev is not None:
+            assert info["attn_chunk"] >= prev["attn_chunk"]
+            assert info["mlp_chunk"] >= prev["mlp_chunk"]
+        prev = info
+
+
+def test_plan_auto_rejects_budgets_below_the_kv_floor(lib):
+    T, D = 8192, 1024
+    h = ctypes.c_void_p()
+    st = lib.dit_block_plan_auto(T, D, 16, 2816, 4 * T * D, ctypes.byref(h))
+    assert st == ds.ERR_WORKSPACE_TOO_SMALL and not h.value
+    st = lib.dit_block_plan_auto(T, 1000, 16, 2816, 1 << 40, ctypes.byref(h))
+    assert st == ds.ERR_INVALID_ARG
+
+
+def test_plan_auto_slices_the_ffn_only_when_needed(lib):
+    T, D, H, F = 16384, 3072, 24, 8192
+    # enough for 4096-token attention slabs but not for a 4096-token MLP
+    # chunk with the full FFN intermediate
+    attn_4096 = ds.block_plan(T, D, H, F, 128, 4096).workspace_bytes()
+    p = ds.block_plan_auto(T, D, H, F, attn_4096)
+    info = p.info()
+    assert p.workspace_bytes() <= attn_4096
+    if info["ffn_slice"] < F:
+        unsliced = ds.block_plan(T, D, H, F, info["mlp_chunk"], info["attn_chunk"])
+        assert unsliced.workspace_bytes() > attn_4096

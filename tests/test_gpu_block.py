@@ -166,3 +166,22 @@ def test_block_T16384_D3072_sampled_rows(ca):
     got = x.cpu().numpy()[rows]
     rel, mx, br = compare(got, ref, inp.x.double().numpy()[rows])
     assert rel <= REL_L2 and mx <= MAX_ABS and br <= BRANCH_REL_L2, (rel, mx, br)
+
+
+def test_auto_planned_chunks_give_the_same_bits():
+    inp = synth.make_workload("dit_T4096_D1024", seed=6)
+    T, D = inp.x.shape
+    dev = runner.upload(inp)
+    ref_stack = runner.DitStack(T, D, 16, 2816, 0, 0)
+    x_ref = dev.x.clone()
+    ref_stack.forward(x_ref, dev)
+    ref_stack.check()
+    plan = ds.block_plan_auto(T, D, 16, 2816, 24 * 2**20)
+    info = plan.info()
+    assert info["mlp_chunk"] < T and plan.workspace_bytes() <= 24 * 2**20
+    ws = torch.empty(plan.workspace_bytes(), dtype=torch.uint8, device="cuda")
+    plan.bind_workspace(ws)
+    x = dev.x.clone()
+    plan.forward(x, dev.blocks[0].struct, dev.blocks[0].mod)
+    assert plan.sync_status() == ds.OK
+    assert torch.equal(x, x_ref)
