@@ -46,4 +46,7 @@ from .block import (  # noqa: F401
     final_layer,
     dequant_int8,
     block_flops,
+    rms_norm,
+    rope_rotate,
+    qk_transform,
 )

@@ -162,16 +162,73 @@ def swiglu_mlp(b, w: DitWeights) -> np.ndarray:
     return h @ w.wdown.T
 
 
+def rms_norm(x, gamma, eps: float = LN_EPS) -> np.ndarray:
+    """RMSNorm over the last axis: x / sqrt(mean(x^2) + eps) * gamma."""
+    x = _f64(x)
+    return x / np.sqrt((x * x).mean(axis=-1, keepdims=True) + eps) * _f64(gamma)
+
+
+def rope_rotate(x, cos, sin) -> np.ndarray:
+    """Rotate channel pairs (2i, 2i+1) of x [T, d] by the angles whose cosine
+    and sine are cos, sin [T, d/2]: (x0, x1) -> (x0 c - x1 s, x0 s + x1 c)."""
+    x = _f64(x)
+    c, s = _f64(cos), _f64(sin)
+    x0, x1 = x[:, 0::2], x[:, 1::2]
+    out = np.empty_like(x)
+    out[:, 0::2] = x0 * c - x1 * s
+    out[:, 1::2] = x0 * s + x1 * c
+    return out
+
+
+def qk_transform(t, heads: int, gamma, cos, sin, eps: float = LN_EPS) -> np.ndarray:
+    """Per-head RMSNorm (weights gamma [d], or none) then rotary embedding
+    (tables cos/sin [T, d/2], or none) of a Q or K matrix [T, H*d].
+
+    "Proposal: Generic memory-aware streaming execution for transformer
+    models", attention streaming plan: the model's Q normalisation and
+    positional transform are applied to each streamed Q region (and to K).
+    The pages name the steps only; per-head RMSNorm with a learned weight and
+    the rotation of interleaved pairs by caller-given angles are the
+    readings taken."""
+    t = _f64(t)
+    T, D = t.shape
+    d = D // heads
+    out = np.empty_like(t)
+    for h in range(heads):
+        u = t[:, h * d:(h + 1) * d]
+        if gamma is not None:
+            u = rms_norm(u, gamma, eps)
+        if cos is not None:
+            u = rope_rotate(u, cos, sin)
+        out[:, h * d:(h + 1) * d] = u
+    return out
+
+
+def _qk_one(t, heads, qk, which, rows=None):
+    """The Q (which = "q") or K ("k") transform of ``qk`` applied to t, whose
+    rows are the tokens ``rows`` (all tokens from 0 when None)."""
+    if qk is None:
+        return t
+    cos, sin = qk.get("cos"), qk.get("sin")
+    if cos is not None and rows is not None:
+        cos, sin = _f64(cos)[rows], _f64(sin)[rows]
+    return qk_transform(t, heads, qk.get(which + "_norm"), cos, sin,
+                        qk.get("eps", LN_EPS))
+
+
 def dit_block(x, w: DitWeights, mod, heads: int, eps: float = LN_EPS,
-              taps: bool = False):
+              taps: bool = False, qk=None):
     """Unchunked forward of one block; returns x2 (and the stage taps).
 
-    ``mod`` is [6, D]: shift1, scale1, gate1, shift2, scale2, gate2."""
+    ``mod`` is [6, D]: shift1, scale1, gate1, shift2, scale2, gate2.
+    ``qk`` (optional): dict with q_norm, k_norm ([d] or None), cos, sin
+    ([T, d/2] or None) and eps — the Q/K transform before attention."""
     x = _f64(x)
     mod = _f64(mod)
     wq, wk, wv = w.q_k_v()
     a = ln_modulate(x, mod[0], mod[1], eps)
     q, k, v = a @ wq.T, a @ wk.T, a @ wv.T
+    q, k = _qk_one(q, heads, qk, "q"), _qk_one(k, heads, qk, "k")
     o = mha_attention(q, k, v, heads)
     x1 = x + mod[2] * (o @ w.wo.T)
     b = ln_modulate(x1, mod[3], mod[4], eps)
@@ -184,7 +241,7 @@ def dit_block(x, w: DitWeights, mod, heads: int, eps: float = LN_EPS,
 
 
 def dit_block_chunked(x, w: DitWeights, mod, heads: int, attn_chunk: int,
-                      mlp_chunk: int, ffn_slice: int, eps: float = LN_EPS):
+                      mlp_chunk: int, ffn_slice: int, eps: float = LN_EPS, qk=None):
     """The pages' bounded schedule, written out on token slices (self-check).
 
     "LayerStream: H3 Chunking", "How the slicing works": pass one keeps
@@ -206,11 +263,12 @@ def dit_block_chunked(x, w: DitWeights, mod, heads: int, attn_chunk: int,
     V = np.empty((T, D))
     for s in range(0, T, ca):                       # pass one: K/V only
         a = ln_modulate(x[s:s + ca], mod[0], mod[1], eps)
-        K[s:s + ca] = a @ wk.T
+        K[s:s + ca] = _qk_one(a @ wk.T, heads, qk, "k", np.arange(s, min(s + ca, T)))
         V[s:s + ca] = a @ wv.T
     for s in range(0, T, ca):                       # pass two: Q slab
         a = ln_modulate(x[s:s + ca], mod[0], mod[1], eps)
-        o = mha_attention(a @ wq.T, K, V, heads)
+        q = _qk_one(a @ wq.T, heads, qk, "q", np.arange(s, min(s + ca, T)))
+        o = mha_attention(q, K, V, heads)
         x[s:s + ca] += mod[2] * (o @ w.wo.T)
     for c in range(0, T, cm):                       # MLP token chunks
         b = ln_modulate(x[c:c + cm], mod[3], mod[4], eps)
@@ -223,7 +281,7 @@ def dit_block_chunked(x, w: DitWeights, mod, heads: int, attn_chunk: int,
 
 
 def dit_block_rows(x, w: DitWeights, mod, heads: int, rows,
-                   eps: float = LN_EPS, kv=None):
+                   eps: float = LN_EPS, kv=None, qk=None):
     """The block's output on selected token rows only.
 
     Every stage but attention is token-wise, so the output rows ``rows``
@@ -235,11 +293,11 @@ def dit_block_rows(x, w: DitWeights, mod, heads: int, rows,
     wq, wk, wv = w.q_k_v()
     if kv is None:
         a_all = ln_modulate(x, mod[0], mod[1], eps)
-        kv = (a_all @ wk.T, a_all @ wv.T)
+        kv = (_qk_one(a_all @ wk.T, heads, qk, "k"), a_all @ wv.T)
     K, V = kv
     xr = x[rows]
     a = ln_modulate(xr, mod[0], mod[1], eps)
-    q = a @ wq.T
+    q = _qk_one(a @ wq.T, heads, qk, "q", rows)
     o = mha_attention(q, K, V, heads)
     x1 = xr + mod[2] * (o @ w.wo.T)
     b = ln_modulate(x1, mod[3], mod[4], eps)
