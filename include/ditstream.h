@@ -52,7 +52,7 @@
 extern "C" {
 #endif
 
-#define DITSTREAM_ABI_VERSION 1
+#define DITSTREAM_ABI_VERSION 2
 
 #if defined(__GNUC__)
 #define DIT_API __attribute__((visibility("default")))
@@ -179,6 +179,42 @@ DIT_API dit_status_t dit_block_forward(const dit_plan_t *plan, float *x,
                                const dit_block_weights_t *w,
                                const float *modulation, dit_stream_t stream);
 
+/* Optional per-head transform of Q and K, applied in the fp32 epilogues of
+ * the Q and K projections before their bf16 store.  For one token at
+ * sequence position p and one head h, with u its head_dim values of Q (or K):
+ *   u <- u / sqrt(mean(u^2) + eps) * norm          when norm != NULL
+ *   (u[2i], u[2i+1]) <- (u[2i] c - u[2i+1] s, u[2i] s + u[2i+1] c),
+ *       c = rope_cos[p, i], s = rope_sin[p, i]     when rope_cos != NULL
+ * norm is q_norm for Q and k_norm for K: device fp32 [head_dim], the same for
+ * every head.  rope_cos, rope_sin: device fp32 [T, head_dim / 2] row-major,
+ * 16-byte aligned, both NULL or both set; one row of angles per token, shared
+ * by all heads and by Q and K (a 3-D video rotary embedding is one such
+ * table, laid out by the caller).  eps > 0.
+ * "Proposal: Generic memory-aware streaming execution for transformer
+ * models", attention section: the model's Q normalisation and positional
+ * transform are applied to each bounded Q region before its attention; the
+ * block description lists optional Q/K normalisation and a RoPE step.  The
+ * page names the steps only: the RMSNorm with a learned weight and the
+ * rotation of interleaved pairs are this library's reading. */
+typedef struct {
+    const float *q_norm;    /* [head_dim] or NULL */
+    const float *k_norm;    /* [head_dim] or NULL */
+    const float *rope_cos;  /* [T, head_dim / 2] or NULL */
+    const float *rope_sin;  /* [T, head_dim / 2] or NULL */
+    float eps;
+} dit_qk_t;
+
+/* dit_block_forward with the Q/K transform `qk` (NULL: none, identical to
+ * dit_block_forward).  The transform is row-local and uses each token's
+ * position in the whole sequence, so the output stays bit-identical across
+ * chunk settings.  Errors: as dit_block_forward; DIT_ERR_INVALID_ARG when
+ * only one of rope_cos / rope_sin is set or eps <= 0, DIT_ERR_ALIGN for a
+ * table or weight not 16-byte aligned. */
+DIT_API dit_status_t dit_block_forward_qk(const dit_plan_t *plan, float *x,
+                                          const dit_block_weights_t *w,
+                                          const float *modulation,
+                                          const dit_qk_t *qk, dit_stream_t stream);
+
 /* Block forward that allocates nothing.  The method's pages have no
  * counterpart to this entry point: it exists for callers that cannot
  * allocate device memory (code that runs under an allocator owning every
@@ -300,7 +336,7 @@ typedef struct {
     int64_t ldo;
     void *out2;             /* KV: V^T */
     int64_t ldo2;
-    int64_t row_offset;     /* KV: token index of A's row 0 */
+    int64_t row_offset;     /* KV: token index of A's row 0; rotary position of row 0 */
     int split_n;            /* KV: first V column */
     float *x;               /* RESID, DOWN */
     int64_t ldx;
@@ -310,6 +346,16 @@ typedef struct {
     int acc_load;
     int acc_final;
     int flags;              /* 0, or DIT_GEMM_FLAG_* test hooks */
+    /* Q/K transform (see dit_qk_t) on STORE_BF16 output and on the K columns
+     * (n < split_n) of KV output; off when qk_norm and rope_cos are NULL.
+     * Heads are head_dim (64 or 128) consecutive columns; the rotary position
+     * of row m is row_offset + m (in STORE_BF16 mode row_offset moves the
+     * position only, not the output row). */
+    const float *qk_norm;   /* [head_dim] or NULL */
+    const float *rope_cos;  /* [positions, head_dim / 2] or NULL */
+    const float *rope_sin;
+    int head_dim;
+    float qk_eps;
 } dit_gemm_args_t;
 
 /* Test hook for failure detection: CTA 0's producer arms its first

@@ -337,9 +337,30 @@ dit_status_t dit_block_bind_workspace(dit_plan_t *p, void *dev_ptr, size_t bytes
 
 dit_status_t dit_block_forward(const dit_plan_t *cp, float *x, const dit_block_weights_t *w,
                                const float *mod, dit_stream_t stream) {
+    return dit_block_forward_qk(cp, x, w, mod, nullptr, stream);
+}
+
+dit_status_t dit_block_forward_qk(const dit_plan_t *cp, float *x, const dit_block_weights_t *w,
+                                  const float *mod, const dit_qk_t *qk, dit_stream_t stream) {
     // the plan is logically const; only its profiling record changes
     dit_plan *p = const_cast<dit_plan *>(cp);
     if (!p || !x || !w || !mod) return DIT_ERR_INVALID_ARG;
+    if (qk) {
+        if (!qk->rope_cos != !qk->rope_sin) return DIT_ERR_INVALID_ARG;
+        if ((qk->q_norm || qk->k_norm) && !(qk->eps > 0.0f)) return DIT_ERR_INVALID_ARG;
+        if (!aligned16(qk->q_norm) || !aligned16(qk->k_norm) || !aligned16(qk->rope_cos) ||
+            !aligned16(qk->rope_sin))
+            return DIT_ERR_ALIGN;
+    }
+    // the GEMM's Q/K transform fields for Q (which = 0) or K (which = 1)
+    auto set_qk = [&](dit_gemm_args_t &g, int which) {
+        if (!qk) return;
+        g.qk_norm = which ? qk->k_norm : qk->q_norm;
+        g.rope_cos = qk->rope_cos;
+        g.rope_sin = qk->rope_sin;
+        g.head_dim = p->head_dim;
+        g.qk_eps = qk->eps;
+    };
     if (!p->ws) return DIT_ERR_NO_WORKSPACE;
     if (!w->wqkv || !w->wo || !w->wgate || !w->wup || !w->wdown) return DIT_ERR_INVALID_ARG;
     if (!aligned16(x) || !aligned16(mod) || !aligned16(w->wqkv) || !aligned16(w->wo) ||
@@ -400,6 +421,7 @@ dit_status_t dit_block_forward(const dit_plan_t *cp, float *x, const dit_block_w
         g.ldo2 = p->t_pad;
         g.row_offset = s;
         g.split_n = D;
+        set_qk(g, 1);
         if ((r = timed(p, st, DIT_K_GEMM_KV, 2.0 * rows * 2 * D * D,
                        [&] { return launch_gemm(g, status, st); })) != DIT_OK)
             return r;
@@ -424,6 +446,8 @@ dit_status_t dit_block_forward(const dit_plan_t *cp, float *x, const dit_block_w
         g.b0_scale = i8 ? w->wqkv_scale : nullptr;
         g.out = Q;
         g.ldo = D;
+        g.row_offset = s;  // rotary position of the slab's first token
+        set_qk(g, 0);
         if ((r = timed(p, st, DIT_K_GEMM_Q, 2.0 * rows * D * D,
                        [&] { return launch_gemm(g, status, st); })) != DIT_OK)
             return r;

@@ -1,6 +1,7 @@
 // Tensor-core GEMM for sm_103a:  acc[M, N] = A[M, K] * B[N, K]^T
 // (bf16 A, bf16 or int8 B, fp32 accumulation in tensor memory) with the
-// block's fused epilogues: K/V store, Q store, gated fp32 residual add,
+// block's fused epilogues: K/V store, Q store (both optionally with the
+// per-head Q/K RMSNorm and rotary embedding), gated fp32 residual add,
 // SwiGLU, and the down projection's accumulate-across-FFN-slices.
 //
 // Structure (one CTA per SM, persistent over 128 x BN output tiles):
@@ -50,6 +51,12 @@ struct GemmParams {
     const float *s0, *s1;  // int8 per-row scales of B0 / B1
     int inject_stall;      // DIT_GEMM_FLAG_INJECT_STALL test hook
     int *status;
+    // Q/K transform (STORE_BF16, and K columns of KV); qk == 0: off
+    int qk;
+    const float *qk_norm;  // [head_dim] or null
+    const float *rope_cos, *rope_sin;  // [positions, head_dim / 2] or null
+    int head_dim;
+    float qk_eps;
 };
 
 template <int MODE, bool I8>
@@ -152,9 +159,114 @@ DEV uint4 int8x8_to_bf16x8(uint2 w) {
     return make_uint4(lo.x, lo.y, hi.x, hi.y);
 }
 
+// One 32-column chunk of the accumulator row as fp32, with the int8 row
+// scales applied.
+template <bool I8>
+DEV void load_chunk(const GemmParams &p, uint32_t taddr, int n, float (&f)[32]) {
+    uint32_t r[32];
+    tmem_ld32(taddr, r);
+    tmem_ld_wait(r);
+#pragma unroll
+    for (int j = 0; j < 32; ++j) f[j] = __uint_as_float(r[j]);
+    if (I8) scale32(f, p.s0 + n);
+}
+
+// Q/K epilogue with the per-head transform: for each head of d columns in
+// the tile, the sum of squares over its accumulator columns (first pass over
+// TMEM), then the RMSNorm scale and weight, the rotation of pairs (2i, 2i+1)
+// by the angles of the row's position, and the bf16 store (second pass).
+// "Proposal: Generic memory-aware streaming execution for transformer
+// models", attention section (Q normalisation and positional transform on
+// each bounded Q region).  V columns of KV pass through as in the plain
+// epilogue.
+template <int MODE, bool I8>
+DEV void epilogue_qk_tile(const GemmParams &p, uint32_t taddr, int64_t m, int nb) {
+    using C = Cfg<MODE, I8>;
+    const bool row_ok = m < p.M;
+    const int d = p.head_dim;
+    const int64_t pos = p.row_offset + m;
+    __nv_bfloat16 *orow = reinterpret_cast<__nv_bfloat16 *>(p.out) +
+                          (MODE == DIT_EPI_KV ? pos : m) * p.ldo;
+#pragma unroll 1
+    for (int h0 = 0; h0 < C::OUT_COLS; h0 += d) {
+        const int nh = nb * C::BN + h0;  // first column of the head (warp-uniform)
+        if (nh >= p.N) break;
+        if (MODE == DIT_EPI_KV && nh >= p.split_n) {
+#pragma unroll 1
+            for (int c0 = 0; c0 < d; c0 += 32) {
+                __syncwarp();
+                float f[32];
+                load_chunk<I8>(p, taddr + h0 + c0, nh + c0, f);
+                if (!row_ok) continue;
+                __nv_bfloat16 *vt = reinterpret_cast<__nv_bfloat16 *>(p.out2) +
+                                    int64_t(nh + c0 - p.split_n) * p.ldo2 + pos;
+#pragma unroll
+                for (int j = 0; j < 32; ++j) vt[int64_t(j) * p.ldo2] = __float2bfloat16_rn(f[j]);
+            }
+            continue;
+        }
+        float inv_rms = 1.0f;
+        if (p.qk_norm) {
+            float ss = 0.0f;
+#pragma unroll 1
+            for (int c0 = 0; c0 < d; c0 += 32) {
+                __syncwarp();
+                float f[32];
+                load_chunk<I8>(p, taddr + h0 + c0, nh + c0, f);
+#pragma unroll
+                for (int j = 0; j < 32; ++j) ss = __fmaf_rn(f[j], f[j], ss);
+            }
+            // d is a power of two: the mean is exact
+            inv_rms = rsqrtf(ss * (1.0f / float(d)) + p.qk_eps);
+        }
+#pragma unroll 1
+        for (int c0 = 0; c0 < d; c0 += 32) {
+            __syncwarp();
+            float f[32];
+            load_chunk<I8>(p, taddr + h0 + c0, nh + c0, f);
+            if (!row_ok) continue;
+            if (p.qk_norm) {
+                const float4 *g = reinterpret_cast<const float4 *>(p.qk_norm + c0);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const float4 w = __ldg(g + i);
+                    f[4 * i + 0] = f[4 * i + 0] * inv_rms * w.x;
+                    f[4 * i + 1] = f[4 * i + 1] * inv_rms * w.y;
+                    f[4 * i + 2] = f[4 * i + 2] * inv_rms * w.z;
+                    f[4 * i + 3] = f[4 * i + 3] * inv_rms * w.w;
+                }
+            }
+            if (p.rope_cos) {
+                const int64_t off = pos * (d / 2) + c0 / 2;
+                const float4 *cv = reinterpret_cast<const float4 *>(p.rope_cos + off);
+                const float4 *sv = reinterpret_cast<const float4 *>(p.rope_sin + off);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const float4 c4 = __ldg(cv + i), s4 = __ldg(sv + i);
+                    const float cs[4] = {c4.x, c4.y, c4.z, c4.w};
+                    const float sn[4] = {s4.x, s4.y, s4.z, s4.w};
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const float a = f[8 * i + 2 * k], b = f[8 * i + 2 * k + 1];
+                        f[8 * i + 2 * k] = a * cs[k] - b * sn[k];
+                        f[8 * i + 2 * k + 1] = a * sn[k] + b * cs[k];
+                    }
+                }
+            }
+            store_bf16x32(orow + nh + c0, f);
+        }
+    }
+}
+
 template <int MODE, bool I8>
 DEV void epilogue_tile(const GemmParams &p, uint32_t taddr, int64_t m, int nb) {
     using C = Cfg<MODE, I8>;
+    if constexpr (MODE == DIT_EPI_STORE_BF16 || MODE == DIT_EPI_KV) {
+        if (p.qk) {
+            epilogue_qk_tile<MODE, I8>(p, taddr, m, nb);
+            return;
+        }
+    }
     const bool row_ok = m < p.M;
 #pragma unroll 1
     for (int c0 = 0; c0 < C::OUT_COLS; c0 += 32) {
@@ -561,6 +673,12 @@ dit_status_t run(const dit_gemm_args_t &a, int *dev_status, cudaStream_t s) {
     p.s1 = a.b1_scale;
     p.inject_stall = (a.flags & DIT_GEMM_FLAG_INJECT_STALL) != 0;
     p.status = dev_status;
+    p.qk = (a.qk_norm || a.rope_cos) ? 1 : 0;
+    p.qk_norm = a.qk_norm;
+    p.rope_cos = a.rope_cos;
+    p.rope_sin = a.rope_sin;
+    p.head_dim = a.head_dim;
+    p.qk_eps = a.qk_eps;
 
     int &done = attr_flag(MODE, I8);
     if (!done) {
@@ -600,6 +718,16 @@ dit_status_t launch_gemm(const dit_gemm_args_t &a, int *dev_status, cudaStream_t
     if (i8) {
         if (!a.b0_scale || !aligned16(a.b0_scale)) return DIT_ERR_ALIGN;
         if (a.mode == DIT_EPI_SWIGLU && (!a.b1_scale || !aligned16(a.b1_scale)))
+            return DIT_ERR_ALIGN;
+    }
+    if (a.qk_norm || a.rope_cos || a.rope_sin) {
+        if (a.mode != DIT_EPI_STORE_BF16 && a.mode != DIT_EPI_KV) return DIT_ERR_INVALID_ARG;
+        if (a.head_dim != 64 && a.head_dim != 128) return DIT_ERR_INVALID_ARG;
+        if (a.N % a.head_dim || (a.mode == DIT_EPI_KV && a.split_n % a.head_dim))
+            return DIT_ERR_INVALID_ARG;
+        if (!a.rope_cos != !a.rope_sin || a.row_offset < 0) return DIT_ERR_INVALID_ARG;
+        if (a.qk_norm && !(a.qk_eps > 0.0f)) return DIT_ERR_INVALID_ARG;
+        if (!aligned16(a.qk_norm) || !aligned16(a.rope_cos) || !aligned16(a.rope_sin))
             return DIT_ERR_ALIGN;
     }
     if (a.M == 0) return DIT_OK;

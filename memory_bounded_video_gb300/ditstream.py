@@ -48,7 +48,7 @@ SYMBOLS = (
     "dit_final_forward", "dit_status_string", "dit_last_cuda_error",
     "dit_abi_version", "dit_modln_cast", "dit_gemm", "dit_attention",
     "dit_block_profile_enable", "dit_block_profile_read",
-    "dit_block_forward_static", "dit_block_plan_auto",
+    "dit_block_forward_static", "dit_block_plan_auto", "dit_block_forward_qk",
 )
 
 STATIC_SCRATCH_BYTES = 64 << 20
@@ -94,7 +94,17 @@ class GemmArgs(ctypes.Structure):
                 ("gate", ctypes.c_void_p),
                 ("acc", ctypes.c_void_p), ("ldacc", ctypes.c_int64),
                 ("acc_load", ctypes.c_int), ("acc_final", ctypes.c_int),
-                ("flags", ctypes.c_int)]
+                ("flags", ctypes.c_int),
+                ("qk_norm", ctypes.c_void_p), ("rope_cos", ctypes.c_void_p),
+                ("rope_sin", ctypes.c_void_p), ("head_dim", ctypes.c_int),
+                ("qk_eps", ctypes.c_float)]
+
+
+class QkArgs(ctypes.Structure):
+    """dit_qk_t: per-head Q/K RMSNorm weights and rotary angle tables."""
+    _fields_ = [("q_norm", ctypes.c_void_p), ("k_norm", ctypes.c_void_p),
+                ("rope_cos", ctypes.c_void_p), ("rope_sin", ctypes.c_void_p),
+                ("eps", ctypes.c_float)]
 
 
 _lib: Optional[ctypes.CDLL] = None
@@ -127,6 +137,8 @@ def _declare(lib):
         "dit_block_forward_static": (c_int, [vp, vp, ctypes.POINTER(BlockWeights),
                                              vp, vp]),
         "dit_block_plan_auto": (c_int, [c_int64, c_int, c_int, c_int, c_size, pp]),
+        "dit_block_forward_qk": (c_int, [vp, vp, ctypes.POINTER(BlockWeights), vp,
+                                         ctypes.POINTER(QkArgs), vp]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -225,10 +237,17 @@ class BlockPlan:
                "dit_block_bind_workspace")
         self._ws = buf  # keep the caller's buffer alive with the plan
 
-    def forward(self, x, weights: BlockWeights, modulation, stream=None):
-        _check(load().dit_block_forward(self._h, ptr(x), ctypes.byref(weights),
-                                        ptr(modulation), stream_handle(stream)),
-               "dit_block_forward")
+    def forward(self, x, weights: BlockWeights, modulation, stream=None,
+                qk: Optional["QkArgs"] = None):
+        if qk is None:
+            _check(load().dit_block_forward(self._h, ptr(x), ctypes.byref(weights),
+                                            ptr(modulation), stream_handle(stream)),
+                   "dit_block_forward")
+        else:
+            _check(load().dit_block_forward_qk(self._h, ptr(x), ctypes.byref(weights),
+                                               ptr(modulation), ctypes.byref(qk),
+                                               stream_handle(stream)),
+                   "dit_block_forward_qk")
 
     def forward_static(self, x, weights: BlockWeights, modulation, stream=None):
         """dit_block_forward_static: the same forward with the library's
@@ -288,6 +307,16 @@ def block_weights(wqkv, wo, wgate, wup, wdown, scales=None) -> BlockWeights:
         w.wup_scale = ptr(scales["wup"])
         w.wdown_scale = ptr(scales["wdown"])
     return w
+
+
+def qk_args(q_norm=None, k_norm=None, rope_cos=None, rope_sin=None,
+            eps=1e-6) -> QkArgs:
+    """Pack device buffers of the Q/K transform into a ``dit_qk_t``."""
+    a = QkArgs()
+    a.q_norm, a.k_norm = ptr(q_norm), ptr(k_norm)
+    a.rope_cos, a.rope_sin = ptr(rope_cos), ptr(rope_sin)
+    a.eps = eps
+    return a
 
 
 def modln_cast(x, rows, D, shift, scale, out, stream=None):

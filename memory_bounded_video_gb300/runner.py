@@ -54,6 +54,21 @@ def upload(inp: DitInputs, device="cuda") -> DeviceInputs:
     return out
 
 
+@dataclass
+class DeviceQk:
+    tensors: dict            # device tensors (kept alive)
+    struct: ditstream.QkArgs
+
+
+def upload_qk(qk: dict, device="cuda") -> DeviceQk:
+    """Copy Q/K transform inputs (``synth.make_qk``) to the device."""
+    t = {k: (v.to(device).contiguous() if isinstance(v, torch.Tensor) else None)
+         for k, v in qk.items() if k != "eps"}
+    st = ditstream.qk_args(t["q_norm"], t["k_norm"], t["cos"], t["sin"],
+                           qk.get("eps", 1e-6))
+    return DeviceQk(t, st)
+
+
 class DitStack:
     """A stack of DiT blocks (one plan, one workspace) plus an optional
     final layer.  ``forward`` updates ``x`` in place and returns the final
@@ -70,11 +85,13 @@ class DitStack:
         self.device = device
 
     def forward(self, x: torch.Tensor, dev: DeviceInputs, stream=None,
-                out: Optional[torch.Tensor] = None):
+                out: Optional[torch.Tensor] = None,
+                qk: Optional[DeviceQk] = None):
         if stream is None:
             stream = torch.cuda.current_stream(x.device)
         for b in dev.blocks:
-            self.plan.forward(x, b.struct, b.mod, stream)
+            self.plan.forward(x, b.struct, b.mod, stream,
+                              qk=None if qk is None else qk.struct)
         if dev.wf is not None:
             if out is None:
                 out = torch.empty(self.T, 64, dtype=torch.float32,

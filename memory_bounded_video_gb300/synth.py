@@ -17,7 +17,9 @@ in for them):
   (0.02/127, optionally times U(0.5, 1.5) so row/column mix-ups show);
 * ``modulation`` [6, D] fp32 : shift/scale rows N(0, 0.1), gate rows U(0, 1);
 * final layer                : ``mod_f`` [2, D] N(0, 0.1); ``W_f`` [64, D]
-  N(0, 0.02) fp32 (or int8 like the block weights).
+  N(0, 0.02) fp32 (or int8 like the block weights);
+* optional Q/K transform      : RMSNorm weights [d] N(1, 0.1); rotary angle
+  tables [T, d/2] fp32 (see ``make_qk``).
 """
 
 from __future__ import annotations
@@ -163,3 +165,46 @@ def make_workload(name: str, seed=0, T: Optional[int] = None,
     return make_inputs(c["T"], c["D"], c["heads"], c["F"], seed=seed,
                        blocks=c["blocks"], int8=c["int8"], final=c["final"],
                        jitter=jitter)
+
+
+def axial_angles(T, head_dim, grid_hw=(32, 32), base=10000.0) -> torch.Tensor:
+    """Rotary angles [T, head_dim/2] of a video laid out frame by frame, each
+    frame ``grid_hw`` patches row-major: the pairs are split between the
+    frame, row and column index (the last two get (d/2)//3 pairs each, the
+    frame the rest) and pair j of an axis with n pairs turns at
+    base^(-j/n) radians per step.  An input table, like the weights: the
+    block applies whatever angles it is given."""
+    h, w = grid_hw
+    t = torch.arange(T, dtype=torch.float64)
+    pos = (torch.div(t, h * w, rounding_mode="floor"),
+           torch.remainder(torch.div(t, w, rounding_mode="floor"), h),
+           torch.remainder(t, w))
+    half = head_dim // 2
+    n_hw = half // 3
+    cols = []
+    for p_axis, n in zip(pos, (half - 2 * n_hw, n_hw, n_hw)):
+        inv = base ** (-torch.arange(n, dtype=torch.float64) / n)
+        cols.append(p_axis[:, None] * inv[None, :])
+    return torch.cat(cols, dim=1)
+
+
+def make_qk(T, head_dim, seed=0, angles="axial", norm=True) -> dict:
+    """Q/K transform inputs: fp32 ``q_norm``/``k_norm`` [head_dim] (or None)
+    and ``cos``/``sin`` [T, head_dim/2] (or None) of ``angles`` = "axial"
+    (``axial_angles``), "random" (U(0, 2 pi) per entry) or None."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(seed)
+    out = dict(q_norm=None, k_norm=None, cos=None, sin=None, eps=1e-6)
+    if norm:
+        out["q_norm"] = 1.0 + _normal(g, (head_dim,), 0.1)
+        out["k_norm"] = 1.0 + _normal(g, (head_dim,), 0.1)
+    if angles is not None:
+        if angles == "axial":
+            th = axial_angles(T, head_dim)
+        elif angles == "random":
+            th = torch.rand(T, head_dim // 2, generator=g, dtype=torch.float64) * 6.283185307179586
+        else:
+            raise ValueError(angles)
+        out["cos"] = torch.cos(th).float()
+        out["sin"] = torch.sin(th).float()
+    return out

@@ -71,10 +71,13 @@ def test_struct_layouts_match_header():
     body = re.search(r"typedef struct \{([^}]*)\} dit_block_weights_t;", src).group(1)
     fields = re.findall(r"\b(\w+);", body)
     assert fields == [f for f, _ in ds.BlockWeights._fields_]
+    body = re.search(r"typedef struct \{([^}]*)\} dit_qk_t;", src).group(1)
+    fields = re.findall(r"\b(\w+);", re.sub(r"/\*.*?\*/", "", body, flags=re.S))
+    assert fields == [f for f, _ in ds.QkArgs._fields_]
 
 
 def test_status_strings(lib):
-    assert ds.abi_version() == 1
+    assert ds.abi_version() == 2
     for s in (0, -1, -2, -3, -4, -5, -6, -7, -8):
         assert ds.status_string(s) and ds.status_string(s) != "unknown status"
     assert ds.status_string(-99) == "unknown status"
@@ -177,6 +180,41 @@ def test_stage_entry_points_validate_before_launch(lib):
                              256, None, None) == ds.ERR_INVALID_ARG
     assert lib.dit_attention(16, 128, 256, 16, 256, 16, 500, 512, 4, 64, 16,
                              256, None, None) == ds.ERR_INVALID_ARG
+
+
+def test_qk_transform_arguments_validated_before_launch(lib):
+    # every call below is rejected on the host: nothing is launched
+    base = dict(mode=ds.EPI_STORE_BF16, M=128, N=256, K=64, a=16, lda=64, b0=16,
+                ldb=64, out=16, ldo=256, head_dim=128, qk_eps=1e-6)
+    cases = [
+        (dict(mode=ds.EPI_RESID, x=16, ldx=256, gate=16, qk_norm=16), ds.ERR_INVALID_ARG),
+        (dict(qk_norm=16, head_dim=96), ds.ERR_INVALID_ARG),
+        (dict(qk_norm=16, N=192, ldo=192), ds.ERR_INVALID_ARG),  # N % d
+        (dict(rope_cos=16), ds.ERR_INVALID_ARG),                  # sin missing
+        (dict(rope_sin=16), ds.ERR_INVALID_ARG),
+        (dict(qk_norm=16, qk_eps=0.0), ds.ERR_INVALID_ARG),
+        (dict(qk_norm=16, row_offset=-1), ds.ERR_INVALID_ARG),
+        (dict(qk_norm=8), ds.ERR_ALIGN),
+        (dict(rope_cos=16, rope_sin=24), ds.ERR_ALIGN),
+        (dict(mode=ds.EPI_KV, out2=16, ldo2=4096, split_n=192, N=384, ldo=192,
+              rope_cos=16, rope_sin=16), ds.ERR_INVALID_ARG),      # split_n % d
+    ]
+    for kw, want in cases:
+        g = ds.GemmArgs(**{**base, **kw})
+        assert lib.dit_gemm(ctypes.byref(g), None, None) == want, kw
+
+
+def test_forward_qk_validates_before_launch(lib):
+    # no workspace is bound, so even a valid call stops before any launch
+    p = ds.block_plan(512, 256, 4, 704, 128, 128)
+    w = ds.block_weights(16, 16, 16, 16, 16)
+    for qk, want in [(ds.qk_args(rope_cos=16), ds.ERR_INVALID_ARG),
+                     (ds.qk_args(q_norm=16, eps=0.0), ds.ERR_INVALID_ARG),
+                     (ds.qk_args(k_norm=8), ds.ERR_ALIGN),
+                     (ds.qk_args(q_norm=16), ds.ERR_NO_WORKSPACE)]:
+        with pytest.raises(ds.DitError) as e:
+            p.forward(16, w, 16, qk=qk)
+        assert e.value.status == want
 
 
 def test_plan_auto_picks_largest_chunks_that_fit(lib):
