@@ -57,6 +57,9 @@ def parse_args(argv=None):
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--workload", default=HEADLINE)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--qk", choices=("none", "axial"), default="none",
+                    help="add the per-head Q/K RMSNorm + rotary embedding "
+                         "(axial video angles) to every block")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-rows", type=int, default=256,
@@ -191,7 +194,7 @@ def cpu_cores():
 
 # ------------------------------------------------------------------ oracle (CPU) leg
 
-def cpu_sample(cfg, inp, rows_n, steps=1, warmup=0):
+def cpu_sample(cfg, inp, rows_n, steps=1, warmup=0, qk=None):
     """Time the float64 oracle on a bounded sample of the workload.
 
     Per block: K and V of all T tokens are computed first (untimed set-up, the
@@ -220,7 +223,13 @@ def cpu_sample(cfg, inp, rows_n, steps=1, warmup=0):
     w0, mod0 = blocks[0]
     a = ob.ln_modulate(x, mod0[0], mod0[1])
     _, wk, wv = w0.q_k_v()
-    kv = (a @ wk.T, a @ wv.T)
+    qk64 = None
+    if qk is not None:
+        qk64 = {k: (v.double().numpy() if hasattr(v, "double") else v)
+                for k, v in qk.items()}
+    kv = (ob.qk_transform(a @ wk.T, H, None if qk64 is None else qk64["k_norm"],
+                          None if qk64 is None else qk64["cos"],
+                          None if qk64 is None else qk64["sin"]), a @ wv.T)
     del a
     kvs = [kv] * len(blocks)
     wf = None
@@ -235,7 +244,7 @@ def cpu_sample(cfg, inp, rows_n, steps=1, warmup=0):
             a = ob.ln_modulate(x[rows], mod[0], mod[1])
             _, wk, wv = w.q_k_v()
             _ = (a @ wk.T, a @ wv.T)
-            ob.dit_block_rows(x, w, mod, H, rows, kv=kv)
+            ob.dit_block_rows(x, w, mod, H, rows, kv=kv, qk=qk64)
         if wf is not None:
             ob.final_layer(x[rows], wf, mod_f)
         return time.perf_counter() - t0
@@ -248,6 +257,7 @@ def cpu_sample(cfg, inp, rows_n, steps=1, warmup=0):
     sample = (f"{rows_n} of {T} token rows per block (their K/V projection, "
               f"LN-mod, Q, attention against all {T} keys, O-proj, SwiGLU MLP"
               + (", final layer" if wf is not None else "")
+              + (", Q/K RMSNorm + rotary" if qk64 is not None else "")
               + f") x {len(blocks)} block(s), float64 numpy oracle; K/V of all "
               "tokens precomputed untimed (first block's, reused as every "
               "block's key/value set)")
@@ -275,12 +285,16 @@ def run_ours(args, rank, world, local_rank):
     dev = runner.upload(inp, dev_name)
     stack = runner.DitStack(T, D, H, F, cfg["mlp_chunk"], cfg["attn_chunk"],
                             cfg["ffn_slice"], device=dev_name)
+    qk = dqk = None
+    if args.qk != "none":
+        qk = synth.make_qk(T, D // H, seed=rank, angles=args.qk)
+        dqk = runner.upload_qk(qk, dev_name)
     x = dev.x.clone()
     stream = torch.cuda.current_stream()
     mem0 = torch.cuda.memory_allocated()
     torch.cuda.reset_peak_memory_stats()
     for _ in range(args.warmup):
-        stack.forward(x, dev, stream)
+        stack.forward(x, dev, stream, qk=dqk)
     stack.check(stream)
     peak_fwd = torch.cuda.max_memory_allocated() - mem0
 
@@ -302,7 +316,7 @@ def run_ours(args, rank, world, local_rank):
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for _ in range(args.steps):
-        stack.forward(x, dev, stream)
+        stack.forward(x, dev, stream, qk=dqk)
     e1.record(stream)
     torch.cuda.synchronize()
     barrier()
@@ -367,6 +381,8 @@ def run_ours(args, rank, world, local_rank):
                    "l2": "not flushed: inputs larger than L2 "
                          f"(x {4 * T * D / 2**20:.0f} MiB, K/V "
                          f"{4 * T * D / 2**20:.0f} MiB per block)",
+                   "qk_transform": (None if qk is None else
+                                    f"q/k rmsnorm + {args.qk} rotary"),
                    "parallelism": f"replicas x{world}"},
         "tflops": round(tflops, 2),
         "tensor_peak_frac": round(tflops / peaks["bf16_tflops_sustained"], 4),
@@ -391,7 +407,8 @@ def run_ours(args, rank, world, local_rank):
 
         def e2e_step():
             x.copy_(x_host, non_blocking=True)
-            res = stack.forward(x, dev, stream, out=out_dev if cfg["final"] else None)
+            res = stack.forward(x, dev, stream, out=out_dev if cfg["final"] else None,
+                                qk=dqk)
             out_host.copy_(res if res is not None else x, non_blocking=True)
 
         e2e_step()
@@ -414,7 +431,7 @@ def run_ours(args, rank, world, local_rank):
                        "steps": k_e2e}
 
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        v, per, sample, _ = cpu_sample(cfg, inp, args.cpu_rows)
+        v, per, sample, _ = cpu_sample(cfg, inp, args.cpu_rows, qk=qk)
         line["cpu_baseline"] = {"value": round(v, 2), "unit": "block-tokens/s",
                                 "cores": cpu_cores(), "kind": "oracle",
                                 "sample": sample,
@@ -427,9 +444,12 @@ def run_reference(args):
 
     cfg = dict(synth.WORKLOADS[args.workload])
     inp = synth.make_workload(args.workload, seed=0)
+    qk = None
+    if args.qk != "none":
+        qk = synth.make_qk(cfg["T"], cfg["D"] // cfg["heads"], seed=0, angles=args.qk)
     value, per_step, sample, times = cpu_sample(cfg, inp, args.cpu_rows,
                                                 steps=args.steps,
-                                                warmup=args.warmup)
+                                                warmup=args.warmup, qk=qk)
     T = cfg["T"]
     return {
         "impl": "reference",
@@ -443,7 +463,9 @@ def run_reference(args):
         "config": {"workload": args.workload, "T": T, "D": cfg["D"],
                    "heads": cfg["heads"], "ffn": cfg["F"],
                    "blocks": cfg["blocks"], "final_layer": cfg["final"],
-                   "int8_weights": cfg["int8"]},
+                   "int8_weights": cfg["int8"],
+                   "qk_transform": (None if qk is None else
+                                    f"q/k rmsnorm + {args.qk} rotary")},
         "cpu_baseline": {"value": round(value, 3), "unit": "block-tokens/s",
                          "cores": cpu_cores(), "kind": "oracle",
                          "sample": sample},

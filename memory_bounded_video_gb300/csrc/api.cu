@@ -209,7 +209,7 @@ dit_status_t dit_block_plan_auto(int64_t T, int D, int heads, int ffn, size_t bu
     // sizing"): choose the largest chunks that fit a memory envelope.  The
     // attention slab is the largest multiple of 128 (or all T tokens) whose
     // plan fits; the MLP takes the largest token chunk, with the FFN unsliced
-    // if that fits and sliced (halving down to 512 features) only when it is
+    // if that fits and sliced (halving down to 1024 features) only when it is
     // needed to fit that chunk.  Every choice gives the same result bits.
     if (!out) return DIT_ERR_INVALID_ARG;
     *out = nullptr;
