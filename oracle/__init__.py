@@ -48,5 +48,7 @@ from .block import (  # noqa: F401
     block_flops,
     rms_norm,
     rope_rotate,
+    lora_delta,
+    merge_lora,
     qk_transform,
 )

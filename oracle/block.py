@@ -36,7 +36,13 @@ Readings where the pages are silent (the same list is kept in the design doc):
   per channel, ``x += gate * branch``.
 * SwiGLU is ``silu(gate_proj) * up_proj`` with separate W_gate / W_up;
   ``silu(z) = z / (1 + exp(-z))``.
-* No biases anywhere; no Q/K normalisation or rotary embedding.
+* No biases anywhere.  Q/K normalisation and rotary embedding are optional
+  (``qk``); see ``qk_transform``.
+* Activation-space LoRA is optional (``lora``): each adapted linear gives
+  ``t W^T + alpha (t A^T) B^T`` ("ComfyUI-StaticPipeline", section
+  "Activation-space LoRA (bypass mode)": y = W x + alpha B (A x), weights
+  left packed).  The fused Q/K/V projection has one adapter whose B rows
+  follow Wqkv's (Q, K, V); the down projection's A is [r, F].
 * Weights are row-major [out, in] (the ``nn.Linear.weight`` convention);
   head h owns hidden columns h*d .. (h+1)*d-1 of Q, K, V and O.
 * INT8 weights are ``W = s_row * q`` with one float scale per output row
@@ -216,32 +222,74 @@ def _qk_one(t, heads, qk, which, rows=None):
                         qk.get("eps", LN_EPS))
 
 
+def lora_delta(t, adapter, rows=None):
+    """``alpha * (t A^T) B[rows]^T`` for an adapter (A [r, in], B [out, r],
+    alpha), or 0 when there is none.
+
+    "ComfyUI-StaticPipeline", section "Activation-space LoRA (bypass mode)":
+    the adapter is applied to the activations, y = W x + alpha B (A x),
+    instead of being merged into the (packed) weights."""
+    if adapter is None:
+        return 0.0
+    A, B, alpha = adapter
+    B = _f64(B)
+    if rows is not None:
+        B = B[rows]
+    return alpha * ((_f64(t) @ _f64(A).T) @ B.T)
+
+
+def merge_lora(w: DitWeights, lora) -> DitWeights:
+    """The weights with every adapter merged in, W + alpha B A (the form the
+    bypass avoids; used to pin ``lora_delta`` by linearity)."""
+    out = DitWeights(*(getattr(w, k).copy() for k in
+                       ("wqkv", "wo", "wgate", "wup", "wdown")))
+    for name, attr in (("qkv", "wqkv"), ("o", "wo"), ("gate", "wgate"),
+                       ("up", "wup"), ("down", "wdown")):
+        ad = _ad(lora, name)
+        if ad is not None:
+            A, B, alpha = ad
+            setattr(out, attr, getattr(out, attr) + alpha * (_f64(B) @ _f64(A)))
+    return out
+
+
+def _ad(lora, name):
+    return None if lora is None else lora.get(name)
+
+
 def dit_block(x, w: DitWeights, mod, heads: int, eps: float = LN_EPS,
-              taps: bool = False, qk=None):
+              taps: bool = False, qk=None, lora=None):
     """Unchunked forward of one block; returns x2 (and the stage taps).
 
     ``mod`` is [6, D]: shift1, scale1, gate1, shift2, scale2, gate2.
     ``qk`` (optional): dict with q_norm, k_norm ([d] or None), cos, sin
-    ([T, d/2] or None) and eps — the Q/K transform before attention."""
+    ([T, d/2] or None) and eps — the Q/K transform before attention.
+    ``lora`` (optional): dict name -> (A, B, alpha) for the linears "qkv",
+    "o", "gate", "up", "down" — see ``lora_delta``."""
     x = _f64(x)
     mod = _f64(mod)
+    D = w.D
     wq, wk, wv = w.q_k_v()
     a = ln_modulate(x, mod[0], mod[1], eps)
-    q, k, v = a @ wq.T, a @ wk.T, a @ wv.T
+    ad = _ad(lora, "qkv")
+    q = a @ wq.T + lora_delta(a, ad, slice(0, D))
+    k = a @ wk.T + lora_delta(a, ad, slice(D, 2 * D))
+    v = a @ wv.T + lora_delta(a, ad, slice(2 * D, 3 * D))
     q, k = _qk_one(q, heads, qk, "q"), _qk_one(k, heads, qk, "k")
     o = mha_attention(q, k, v, heads)
-    x1 = x + mod[2] * (o @ w.wo.T)
+    x1 = x + mod[2] * (o @ w.wo.T + lora_delta(o, _ad(lora, "o")))
     b = ln_modulate(x1, mod[3], mod[4], eps)
-    g, u = b @ w.wgate.T, b @ w.wup.T
+    g = b @ w.wgate.T + lora_delta(b, _ad(lora, "gate"))
+    u = b @ w.wup.T + lora_delta(b, _ad(lora, "up"))
     h = silu(g) * u
-    x2 = x1 + mod[5] * (h @ w.wdown.T)
+    x2 = x1 + mod[5] * (h @ w.wdown.T + lora_delta(h, _ad(lora, "down")))
     if not taps:
         return x2
     return x2, dict(a=a, q=q, k=k, v=v, o=o, x1=x1, b=b, h=h, x2=x2)
 
 
 def dit_block_chunked(x, w: DitWeights, mod, heads: int, attn_chunk: int,
-                      mlp_chunk: int, ffn_slice: int, eps: float = LN_EPS, qk=None):
+                      mlp_chunk: int, ffn_slice: int, eps: float = LN_EPS, qk=None,
+                      lora=None):
     """The pages' bounded schedule, written out on token slices (self-check).
 
     "LayerStream: H3 Chunking", "How the slicing works": pass one keeps
@@ -261,27 +309,39 @@ def dit_block_chunked(x, w: DitWeights, mod, heads: int, attn_chunk: int,
     wq, wk, wv = w.q_k_v()
     K = np.empty((T, D))
     V = np.empty((T, D))
+    aq = _ad(lora, "qkv")
     for s in range(0, T, ca):                       # pass one: K/V only
         a = ln_modulate(x[s:s + ca], mod[0], mod[1], eps)
-        K[s:s + ca] = _qk_one(a @ wk.T, heads, qk, "k", np.arange(s, min(s + ca, T)))
-        V[s:s + ca] = a @ wv.T
+        k = a @ wk.T + lora_delta(a, aq, slice(D, 2 * D))
+        K[s:s + ca] = _qk_one(k, heads, qk, "k", np.arange(s, min(s + ca, T)))
+        V[s:s + ca] = a @ wv.T + lora_delta(a, aq, slice(2 * D, 3 * D))
     for s in range(0, T, ca):                       # pass two: Q slab
         a = ln_modulate(x[s:s + ca], mod[0], mod[1], eps)
-        q = _qk_one(a @ wq.T, heads, qk, "q", np.arange(s, min(s + ca, T)))
+        q = a @ wq.T + lora_delta(a, aq, slice(0, D))
+        q = _qk_one(q, heads, qk, "q", np.arange(s, min(s + ca, T)))
         o = mha_attention(q, K, V, heads)
-        x[s:s + ca] += mod[2] * (o @ w.wo.T)
+        x[s:s + ca] += mod[2] * (o @ w.wo.T + lora_delta(o, _ad(lora, "o")))
+    ag, au, adn = _ad(lora, "gate"), _ad(lora, "up"), _ad(lora, "down")
     for c in range(0, T, cm):                       # MLP token chunks
         b = ln_modulate(x[c:c + cm], mod[3], mod[4], eps)
         acc = np.zeros((b.shape[0], D))
+        ud = 0.0                                    # down adapter: h A_d^T
         for f in range(0, F, fs):                   # FFN feature slices
-            hf = silu(b @ w.wgate[f:f + fs].T) * (b @ w.wup[f:f + fs].T)
-            acc += hf @ w.wdown[:, f:f + fs].T
+            fr = slice(f, f + fs)
+            g = b @ w.wgate[fr].T + lora_delta(b, ag, fr)
+            u = b @ w.wup[fr].T + lora_delta(b, au, fr)
+            hf = silu(g) * u
+            acc += hf @ w.wdown[:, fr].T
+            if adn is not None:
+                ud = ud + hf @ _f64(adn[0])[:, fr].T
+        if adn is not None:
+            acc += adn[2] * (ud @ _f64(adn[1]).T)
         x[c:c + cm] += mod[5] * acc
     return x
 
 
 def dit_block_rows(x, w: DitWeights, mod, heads: int, rows,
-                   eps: float = LN_EPS, kv=None, qk=None):
+                   eps: float = LN_EPS, kv=None, qk=None, lora=None):
     """The block's output on selected token rows only.
 
     Every stage but attention is token-wise, so the output rows ``rows``
@@ -291,18 +351,23 @@ def dit_block_rows(x, w: DitWeights, mod, heads: int, rows,
     mod = _f64(mod)
     rows = np.asarray(rows, dtype=np.int64)
     wq, wk, wv = w.q_k_v()
+    D = w.D
+    aq = _ad(lora, "qkv")
     if kv is None:
         a_all = ln_modulate(x, mod[0], mod[1], eps)
-        kv = (_qk_one(a_all @ wk.T, heads, qk, "k"), a_all @ wv.T)
+        k = a_all @ wk.T + lora_delta(a_all, aq, slice(D, 2 * D))
+        kv = (_qk_one(k, heads, qk, "k"),
+              a_all @ wv.T + lora_delta(a_all, aq, slice(2 * D, 3 * D)))
     K, V = kv
     xr = x[rows]
     a = ln_modulate(xr, mod[0], mod[1], eps)
-    q = _qk_one(a @ wq.T, heads, qk, "q", rows)
+    q = _qk_one(a @ wq.T + lora_delta(a, aq, slice(0, D)), heads, qk, "q", rows)
     o = mha_attention(q, K, V, heads)
-    x1 = xr + mod[2] * (o @ w.wo.T)
+    x1 = xr + mod[2] * (o @ w.wo.T + lora_delta(o, _ad(lora, "o")))
     b = ln_modulate(x1, mod[3], mod[4], eps)
-    h = silu(b @ w.wgate.T) * (b @ w.wup.T)
-    x2 = x1 + mod[5] * (h @ w.wdown.T)
+    h = silu(b @ w.wgate.T + lora_delta(b, _ad(lora, "gate"))) * \
+        (b @ w.wup.T + lora_delta(b, _ad(lora, "up")))
+    x2 = x1 + mod[5] * (h @ w.wdown.T + lora_delta(h, _ad(lora, "down")))
     return x2, dict(q=q, o=o, x1=x1, b=b, h=h, k=K, v=V)
 
 
