@@ -52,7 +52,7 @@
 extern "C" {
 #endif
 
-#define DITSTREAM_ABI_VERSION 2
+#define DITSTREAM_ABI_VERSION 3
 
 #if defined(__GNUC__)
 #define DIT_API __attribute__((visibility("default")))
@@ -157,7 +157,8 @@ DIT_API dit_status_t dit_block_plan_info(const dit_plan_t *plan, int64_t *T, int
  *   256 (status words) + K [T, D] bf16 + V^T [D, roundup(T, 128)] bf16
  *   + max(attention phase 4 * C_a * D,
  *         MLP phase 2 * C_m * D + 2 * C_m * F_s + (F_s < F ? 4 * C_m * D : 0))
- * each region rounded up to 1 KiB.  K/V for all tokens is the floor that
+ * each region rounded up to 1 KiB, plus the LoRA regions when the plan has a
+ * LoRA rank (dit_block_plan_set_lora_rank).  K/V for all tokens is the floor that
  * grows with T ("Where people get burned": K and V of the whole sequence
  * stay resident); everything else is bounded by the chunk sizes. */
 DIT_API size_t dit_block_workspace_bytes(const dit_plan_t *plan);
@@ -214,6 +215,62 @@ DIT_API dit_status_t dit_block_forward_qk(const dit_plan_t *plan, float *x,
                                           const dit_block_weights_t *w,
                                           const float *modulation,
                                           const dit_qk_t *qk, dit_stream_t stream);
+
+/* Activation-space LoRA ("ComfyUI-StaticPipeline", section "Activation-space
+ * LoRA (bypass mode)"): an adapted linear computes y = W x + alpha B (A x)
+ * with W left as it is (bf16 or packed int8).  Here the delta joins W's
+ * product inside the same tensor-core accumulation: u = x A^T (bf16, one
+ * small GEMM per token chunk), then ceil(rank / 64) extra K-steps of
+ * u B'^T after W's, so every fused epilogue (SwiGLU, gated residual, the
+ * down projection's carry) sees W x + delta before its nonlinearity.
+ * B' = alpha * B (divided by W's int8 row scale, which the epilogue applies)
+ * is made once per adapter by dit_lora_prepare.
+ *   a: device bf16 [rank, in] row-major (in = D, or ffn for "down");
+ *   b: device bf16 [out, rank] row-major, the output of dit_lora_prepare;
+ *   rank: multiple of 32, at most the plan's LoRA rank; a == NULL or
+ *   b == NULL: no adapter on that linear.
+ * The fused Q/K/V projection has one adapter whose B rows follow Wqkv's
+ * (out = 3D: rows of Q, then K, then V). */
+typedef struct {
+    const void *a;
+    const void *b;
+    int rank;
+} dit_lora_t;
+
+typedef struct {
+    dit_lora_t qkv, o, gate, up, down;
+} dit_block_lora_t;
+
+#define DIT_LORA_MAX_RANK 256
+
+/* b_out[n, j] = bf16_rne(alpha * b[n, j] / row_scale[n]) for n < rows,
+ * j < rank (row_scale == NULL: no division).  b, b_out: device bf16, row
+ * strides ld_b, ld_out elements (>= rank, multiples of 8); row_scale: the
+ * int8 scales of the adapted weight's rows (the same rows as b's), or NULL
+ * for bf16 weights.  Asynchronous on `stream`.
+ * Errors: DIT_ERR_INVALID_ARG, DIT_ERR_ALIGN, DIT_ERR_CUDA. */
+DIT_API dit_status_t dit_lora_prepare(const void *b, int64_t rows, int rank, int64_t ld_b,
+                                      float alpha, const float *row_scale, void *b_out,
+                                      int64_t ld_out, dit_stream_t stream);
+
+/* Reserve workspace for adapters of rank <= max_rank (a multiple of 32, at
+ * most DIT_LORA_MAX_RANK; 0 = none, the default).  Must be called before a
+ * workspace is bound (else DIT_ERR_INVALID_ARG).  The workspace grows by
+ * 4*C_a*R (u of the Q/K/V and O adapters) plus 6*C_m*R, and 4*C_m*R more when
+ * the FFN is sliced (u of gate, up, down and the down adapter's fp32 carry). */
+DIT_API dit_status_t dit_block_plan_set_lora_rank(dit_plan_t *plan, int max_rank);
+
+/* dit_block_forward with the optional Q/K transform (`qk`, see dit_qk_t)
+ * and activation-space LoRA adapters (`lora`); either may be NULL.  The
+ * output stays bit-identical across chunk settings and FFN slice widths.
+ * Errors: as dit_block_forward_qk; DIT_ERR_INVALID_ARG when an adapter's
+ * rank is not a multiple of 32 or exceeds the plan's LoRA rank,
+ * DIT_ERR_ALIGN for an adapter matrix not 16-byte aligned. */
+DIT_API dit_status_t dit_block_forward_ex(const dit_plan_t *plan, float *x,
+                                          const dit_block_weights_t *w,
+                                          const float *modulation, const dit_qk_t *qk,
+                                          const dit_block_lora_t *lora,
+                                          dit_stream_t stream);
 
 /* Block forward that allocates nothing.  The method's pages have no
  * counterpart to this entry point: it exists for callers that cannot
@@ -278,7 +335,8 @@ DIT_API dit_status_t dit_final_forward(const dit_plan_t *plan, const float *x,
 #define DIT_K_GEMM_SWIGLU 5
 #define DIT_K_GEMM_DOWN 6
 #define DIT_K_FINAL 7
-#define DIT_NUM_KINDS 8
+#define DIT_K_LORA_U 8      /* LoRA u = x A^T GEMMs (dit_block_forward_ex) */
+#define DIT_NUM_KINDS 9
 
 DIT_API dit_status_t dit_block_profile_enable(dit_plan_t *plan, int enable);
 DIT_API dit_status_t dit_block_profile_read(dit_plan_t *plan, double *ms,
@@ -306,7 +364,8 @@ DIT_API dit_status_t dit_modln_cast(const float *x, int64_t rows, int D,
 
 /* Epilogues of the tensor-core GEMM  acc[M, N] = A[M, K] B[N, K]^T
  * (A bf16, B bf16 or int8 with per-row fp32 scale applied to acc). */
-#define DIT_EPI_STORE_BF16 0  /* out bf16 [M, N], row stride ldo             */
+#define DIT_EPI_STORE_BF16 0  /* out bf16 [M, N], row stride ldo; if acc_load
+                                 the fp32 accumulator starts from acc[m, n]  */
 #define DIT_EPI_STORE_F32 1   /* out fp32 [M, N], row stride ldo             */
 #define DIT_EPI_KV 2          /* n < split_n: out (K) bf16 [row_offset+m, n],
                                  stride ldo; n >= split_n: out2 (V^T) bf16
@@ -356,6 +415,22 @@ typedef struct {
     const float *rope_sin;
     int head_dim;
     float qk_eps;
+    /* LoRA K-steps (see dit_lora_t): after the K-steps of A B^T the
+     * accumulator takes ceil(rank / 64) more of U L^T, U = lora_u bf16
+     * [M, rank] (row stride lora_ldu), L = lora_l bf16 [N, rank] (row stride
+     * lora_ldl), rank % 8 == 0, <= DIT_LORA_MAX_RANK.  Half 0 (lora_*0)
+     * feeds every output column (SWIGLU: the gate's), half 1 only the up
+     * accumulator of SWIGLU.  lora_l0 == NULL and lora_l1 == NULL: off. */
+    const void *lora_u0;
+    int64_t lora_ldu0;
+    const void *lora_l0;
+    int64_t lora_ldl0;
+    int lora_rank0;
+    const void *lora_u1;
+    int64_t lora_ldu1;
+    const void *lora_l1;
+    int64_t lora_ldl1;
+    int lora_rank1;
 } dit_gemm_args_t;
 
 /* Test hook for failure detection: CTA 0's producer arms its first

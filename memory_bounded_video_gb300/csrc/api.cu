@@ -153,6 +153,50 @@ const char *dit_status_string(dit_status_t s) {
     }
 }
 
+namespace {
+
+// Workspace layout of a plan (byte offsets, 1 KiB-aligned regions).
+void layout(dit_plan *p) {
+    const size_t A = 1024;
+    const size_t Dz = size_t(p->D);
+    const size_t R = size_t(p->lora_r);
+    p->off_k = A;  // [0, 256): device status words
+    p->off_vt = round_up(p->off_k + 2 * size_t(p->T) * Dz, A);
+    const size_t phase = round_up(p->off_vt + 2 * Dz * size_t(p->t_pad), A);
+    // attention phase: a_s / O_s share one region (a_s is dead once Q_s exists)
+    p->off_a = phase;
+    p->off_q = round_up(p->off_a + 2 * size_t(p->ca) * Dz, A);
+    size_t attn_end = round_up(p->off_q + 2 * size_t(p->ca) * Dz, A);
+    p->off_uq = attn_end;
+    p->off_uo = round_up(p->off_uq + 2 * size_t(p->ca) * R, A);
+    if (R) attn_end = round_up(p->off_uo + 2 * size_t(p->ca) * R, A);
+    // MLP phase (aliases the attention phase: the two never overlap in time)
+    p->off_b = phase;
+    p->off_h = round_up(p->off_b + 2 * size_t(p->cm) * Dz, A);
+    p->off_acc = round_up(p->off_h + 2 * size_t(p->cm) * size_t(p->fs), A);
+    size_t mlp_end = p->off_acc;
+    if (p->fs < p->F) mlp_end = round_up(p->off_acc + 4 * size_t(p->cm) * Dz, A);
+    p->off_ug = mlp_end;
+    p->off_uu = round_up(p->off_ug + 2 * size_t(p->cm) * R, A);
+    p->off_ud = round_up(p->off_uu + 2 * size_t(p->cm) * R, A);
+    p->off_udc = round_up(p->off_ud + 2 * size_t(p->cm) * R, A);
+    if (R) {
+        mlp_end = p->off_udc;
+        if (p->fs < p->F) mlp_end = round_up(p->off_udc + 4 * size_t(p->cm) * R, A);
+    }
+    p->total = attn_end > mlp_end ? attn_end : mlp_end;
+}
+
+}  // namespace
+
+dit_status_t dit_block_plan_set_lora_rank(dit_plan_t *p, int max_rank) {
+    if (!p || p->ws) return DIT_ERR_INVALID_ARG;
+    if (max_rank < 0 || max_rank > DIT_LORA_MAX_RANK || max_rank % 32) return DIT_ERR_INVALID_ARG;
+    p->lora_r = max_rank;
+    layout(p);
+    return DIT_OK;
+}
+
 dit_status_t dit_block_plan_ex(int64_t T, int D, int heads, int ffn, int mlp_chunk_tokens,
                                int attn_chunk_tokens, int ffn_slice, dit_plan_t **out) {
     if (!out) return DIT_ERR_INVALID_ARG;
@@ -180,22 +224,7 @@ dit_status_t dit_block_plan_ex(int64_t T, int D, int heads, int ffn, int mlp_chu
     p->ca = clamp(attn_chunk_tokens);
     p->fs = ffn_slice == 0 ? ffn : ffn_slice;
     p->t_pad = int64_t(round_up(size_t(T), 128));
-    const size_t A = 1024;
-    const size_t Dz = size_t(D);
-    p->off_k = A;  // [0, 256): device status words
-    p->off_vt = round_up(p->off_k + 2 * size_t(T) * Dz, A);
-    const size_t phase = round_up(p->off_vt + 2 * Dz * size_t(p->t_pad), A);
-    // attention phase: a_s / O_s share one region (a_s is dead once Q_s exists)
-    p->off_a = phase;
-    p->off_q = round_up(p->off_a + 2 * size_t(p->ca) * Dz, A);
-    const size_t attn_end = round_up(p->off_q + 2 * size_t(p->ca) * Dz, A);
-    // MLP phase (aliases the attention phase: the two never overlap in time)
-    p->off_b = phase;
-    p->off_h = round_up(p->off_b + 2 * size_t(p->cm) * Dz, A);
-    p->off_acc = round_up(p->off_h + 2 * size_t(p->cm) * size_t(p->fs), A);
-    size_t mlp_end = p->off_acc;
-    if (p->fs < p->F) mlp_end = round_up(p->off_acc + 4 * size_t(p->cm) * Dz, A);
-    p->total = attn_end > mlp_end ? attn_end : mlp_end;
+    layout(p);
     p->ws = nullptr;
     p->ws_bytes = 0;
     *out = p;
@@ -342,6 +371,12 @@ dit_status_t dit_block_forward(const dit_plan_t *cp, float *x, const dit_block_w
 
 dit_status_t dit_block_forward_qk(const dit_plan_t *cp, float *x, const dit_block_weights_t *w,
                                   const float *mod, const dit_qk_t *qk, dit_stream_t stream) {
+    return dit_block_forward_ex(cp, x, w, mod, qk, nullptr, stream);
+}
+
+dit_status_t dit_block_forward_ex(const dit_plan_t *cp, float *x, const dit_block_weights_t *w,
+                                  const float *mod, const dit_qk_t *qk,
+                                  const dit_block_lora_t *lora, dit_stream_t stream) {
     // the plan is logically const; only its profiling record changes
     dit_plan *p = const_cast<dit_plan *>(cp);
     if (!p || !x || !w || !mod) return DIT_ERR_INVALID_ARG;
@@ -352,15 +387,15 @@ dit_status_t dit_block_forward_qk(const dit_plan_t *cp, float *x, const dit_bloc
             !aligned16(qk->rope_sin))
             return DIT_ERR_ALIGN;
     }
-    // the GEMM's Q/K transform fields for Q (which = 0) or K (which = 1)
-    auto set_qk = [&](dit_gemm_args_t &g, int which) {
-        if (!qk) return;
-        g.qk_norm = which ? qk->k_norm : qk->q_norm;
-        g.rope_cos = qk->rope_cos;
-        g.rope_sin = qk->rope_sin;
-        g.head_dim = p->head_dim;
-        g.qk_eps = qk->eps;
-    };
+    // an adapter is present when both of its matrices are given
+    auto on = [&](const dit_lora_t &l) { return lora && l.a && l.b; };
+    if (lora) {
+        for (const dit_lora_t *l : {&lora->qkv, &lora->o, &lora->gate, &lora->up, &lora->down}) {
+            if (!on(*l)) continue;
+            if (l->rank <= 0 || l->rank % 32 || l->rank > p->lora_r) return DIT_ERR_INVALID_ARG;
+            if (!aligned16(l->a) || !aligned16(l->b)) return DIT_ERR_ALIGN;
+        }
+    }
     if (!p->ws) return DIT_ERR_NO_WORKSPACE;
     if (!w->wqkv || !w->wo || !w->wgate || !w->wup || !w->wdown) return DIT_ERR_INVALID_ARG;
     if (!aligned16(x) || !aligned16(mod) || !aligned16(w->wqkv) || !aligned16(w->wo) ||
@@ -392,10 +427,83 @@ dit_status_t dit_block_forward_qk(const dit_plan_t *cp, float *x, const dit_bloc
     void *b = p->ws + p->off_b;
     void *h = p->ws + p->off_h;
     float *acc = reinterpret_cast<float *>(p->ws + p->off_acc);
+    void *u_q = p->ws + p->off_uq;
+    void *u_o = p->ws + p->off_uo;
+    void *u_g = p->ws + p->off_ug;
+    void *u_u = p->ws + p->off_uu;
+    void *u_d = p->ws + p->off_ud;
+    float *u_dc = reinterpret_cast<float *>(p->ws + p->off_udc);
     const float *shift1 = mod, *scale1 = mod + Dl, *gate1 = mod + 2 * Dl;
     const float *shift2 = mod + 3 * Dl, *scale2 = mod + 4 * Dl, *gate2 = mod + 5 * Dl;
     const uint8_t *wqkv = static_cast<const uint8_t *>(w->wqkv);
     dit_status_t r;
+
+    // the GEMM's Q/K transform fields for Q (which = 0) or K (which = 1)
+    auto set_qk = [&](dit_gemm_args_t &g, int which) {
+        if (!qk) return;
+        g.qk_norm = which ? qk->k_norm : qk->q_norm;
+        g.rope_cos = qk->rope_cos;
+        g.rope_sin = qk->rope_sin;
+        g.head_dim = p->head_dim;
+        g.qk_eps = qk->eps;
+    };
+    // LoRA: u = t A^T (bf16 [rows, rank]); A's columns col0.. of row stride lda_a
+    auto lora_u = [&](const void *t, int64_t ldt, int64_t rows, int K_, const dit_lora_t &l,
+                      int64_t col0, int64_t lda_a, void *u, float *carry, int load,
+                      int final_) -> dit_status_t {
+        dit_gemm_args_t g{};
+        g.M = rows;
+        g.N = l.rank;
+        g.K = K_;
+        g.a = t;
+        g.lda = ldt;
+        g.b0 = static_cast<const uint8_t *>(l.a) + col0 * 2;
+        g.ldb = lda_a;
+        g.b_dtype = DIT_W_BF16;
+        if (final_) {  // bf16 u, from the fp32 carry when there is one
+            g.mode = DIT_EPI_STORE_BF16;
+            g.out = u;
+            g.ldo = l.rank;
+            g.acc_load = load;
+            g.acc = carry;
+            g.ldacc = l.rank;
+        } else {  // fp32 carry of a K-sliced u (the down adapter over FFN slices)
+            g.mode = DIT_EPI_DOWN;
+            g.acc = carry;
+            g.ldacc = l.rank;
+            g.acc_load = load;
+            g.acc_final = 0;
+        }
+        return timed(p, st, DIT_K_LORA_U, 2.0 * rows * l.rank * K_,
+                     [&] { return launch_gemm(g, status, st); });
+    };
+    // LoRA K-steps of a GEMM: u [rows, rank] and rows row0.. of the prepared B
+    auto attach = [&](dit_gemm_args_t &g, int half, const void *u, const dit_lora_t &l,
+                      int64_t row0) {
+        const void *lb = static_cast<const uint8_t *>(l.b) + row0 * l.rank * 2;
+        if (half == 0) {
+            g.lora_u0 = u;
+            g.lora_ldu0 = l.rank;
+            g.lora_l0 = lb;
+            g.lora_ldl0 = l.rank;
+            g.lora_rank0 = l.rank;
+        } else {
+            g.lora_u1 = u;
+            g.lora_ldu1 = l.rank;
+            g.lora_l1 = lb;
+            g.lora_ldl1 = l.rank;
+            g.lora_rank1 = l.rank;
+        }
+    };
+    const dit_lora_t none{};
+    const dit_lora_t &l_qkv = lora ? lora->qkv : none;
+    const dit_lora_t &l_o = lora ? lora->o : none;
+    const dit_lora_t &l_g = lora ? lora->gate : none;
+    const dit_lora_t &l_u = lora ? lora->up : none;
+    const dit_lora_t &l_d = lora ? lora->down : none;
+    auto lflops = [&](const dit_lora_t &l, int64_t rows, int n_out) {
+        return on(l) ? 2.0 * rows * n_out * l.rank : 0.0;
+    };
 
     // pass 1: K and V of every token
     for (int64_t s = 0; s < T; s += p->ca) {
@@ -403,6 +511,8 @@ dit_status_t dit_block_forward_qk(const dit_plan_t *cp, float *x, const dit_bloc
         if ((r = timed(p, st, DIT_K_MODLN, 6.0 * rows * D,
                        [&] { return launch_modln(x + s * Dl, rows, D, shift1, scale1, a, st); })) !=
             DIT_OK)
+            return r;
+        if (on(l_qkv) && (r = lora_u(a, D, rows, D, l_qkv, 0, D, u_q, nullptr, 0, 1)) != DIT_OK)
             return r;
         dit_gemm_args_t g{};
         g.mode = DIT_EPI_KV;
@@ -422,7 +532,8 @@ dit_status_t dit_block_forward_qk(const dit_plan_t *cp, float *x, const dit_bloc
         g.row_offset = s;
         g.split_n = D;
         set_qk(g, 1);
-        if ((r = timed(p, st, DIT_K_GEMM_KV, 2.0 * rows * 2 * D * D,
+        if (on(l_qkv)) attach(g, 0, u_q, l_qkv, Dl);
+        if ((r = timed(p, st, DIT_K_GEMM_KV, 2.0 * rows * 2 * D * D + lflops(l_qkv, rows, 2 * D),
                        [&] { return launch_gemm(g, status, st); })) != DIT_OK)
             return r;
     }
@@ -432,6 +543,8 @@ dit_status_t dit_block_forward_qk(const dit_plan_t *cp, float *x, const dit_bloc
         if ((r = timed(p, st, DIT_K_MODLN, 6.0 * rows * D,
                        [&] { return launch_modln(x + s * Dl, rows, D, shift1, scale1, a, st); })) !=
             DIT_OK)
+            return r;
+        if (on(l_qkv) && (r = lora_u(a, D, rows, D, l_qkv, 0, D, u_q, nullptr, 0, 1)) != DIT_OK)
             return r;
         dit_gemm_args_t g{};
         g.mode = DIT_EPI_STORE_BF16;
@@ -448,7 +561,8 @@ dit_status_t dit_block_forward_qk(const dit_plan_t *cp, float *x, const dit_bloc
         g.ldo = D;
         g.row_offset = s;  // rotary position of the slab's first token
         set_qk(g, 0);
-        if ((r = timed(p, st, DIT_K_GEMM_Q, 2.0 * rows * D * D,
+        if (on(l_qkv)) attach(g, 0, u_q, l_qkv, 0);
+        if ((r = timed(p, st, DIT_K_GEMM_Q, 2.0 * rows * D * D + lflops(l_qkv, rows, D),
                        [&] { return launch_gemm(g, status, st); })) != DIT_OK)
             return r;
         // O_s overwrites a_s (dead once Q_s exists)
@@ -456,6 +570,8 @@ dit_status_t dit_block_forward_qk(const dit_plan_t *cp, float *x, const dit_bloc
                  return launch_attention(Q, rows, D, K, D, Vt, p->t_pad, T, p->heads,
                                          p->head_dim, a, D, status, st);
              })) != DIT_OK)
+            return r;
+        if (on(l_o) && (r = lora_u(a, D, rows, D, l_o, 0, D, u_o, nullptr, 0, 1)) != DIT_OK)
             return r;
         dit_gemm_args_t o{};
         o.mode = DIT_EPI_RESID;
@@ -471,7 +587,8 @@ dit_status_t dit_block_forward_qk(const dit_plan_t *cp, float *x, const dit_bloc
         o.x = x + s * Dl;
         o.ldx = D;
         o.gate = gate1;
-        if ((r = timed(p, st, DIT_K_GEMM_O, 2.0 * rows * D * D,
+        if (on(l_o)) attach(o, 0, u_o, l_o, 0);
+        if ((r = timed(p, st, DIT_K_GEMM_O, 2.0 * rows * D * D + lflops(l_o, rows, D),
                        [&] { return launch_gemm(o, status, st); })) != DIT_OK)
             return r;
     }
@@ -485,8 +602,13 @@ dit_status_t dit_block_forward_qk(const dit_plan_t *cp, float *x, const dit_bloc
                        [&] { return launch_modln(x + c * Dl, rows, D, shift2, scale2, b, st); })) !=
             DIT_OK)
             return r;
+        if (on(l_g) && (r = lora_u(b, D, rows, D, l_g, 0, D, u_g, nullptr, 0, 1)) != DIT_OK)
+            return r;
+        if (on(l_u) && (r = lora_u(b, D, rows, D, l_u, 0, D, u_u, nullptr, 0, 1)) != DIT_OK)
+            return r;
         for (int f = 0; f < F; f += p->fs) {
             const int fw = (F - f < p->fs) ? F - f : p->fs;
+            const bool last = f + fw >= F;
             dit_gemm_args_t g{};
             g.mode = DIT_EPI_SWIGLU;
             g.M = rows;
@@ -502,8 +624,16 @@ dit_status_t dit_block_forward_qk(const dit_plan_t *cp, float *x, const dit_bloc
             g.b1_scale = i8 ? w->wup_scale + f : nullptr;
             g.out = h;
             g.ldo = p->fs;
-            if ((r = timed(p, st, DIT_K_GEMM_SWIGLU, 4.0 * rows * fw * D,
+            if (on(l_g)) attach(g, 0, u_g, l_g, f);
+            if (on(l_u)) attach(g, 1, u_u, l_u, f);
+            if ((r = timed(p, st, DIT_K_GEMM_SWIGLU,
+                           4.0 * rows * fw * D + lflops(l_g, rows, fw) + lflops(l_u, rows, fw),
                            [&] { return launch_gemm(g, status, st); })) != DIT_OK)
+                return r;
+            // the down adapter's u = h A_d^T accumulates over the FFN slices
+            // (fp32 carry; bf16 after the last), in the unsliced K order
+            if (on(l_d) &&
+                (r = lora_u(h, p->fs, rows, fw, l_d, f, F, u_d, u_dc, f > 0, last)) != DIT_OK)
                 return r;
             dit_gemm_args_t d{};
             d.mode = DIT_EPI_DOWN;
@@ -519,11 +649,13 @@ dit_status_t dit_block_forward_qk(const dit_plan_t *cp, float *x, const dit_bloc
             d.acc = acc;
             d.ldacc = D;
             d.acc_load = f > 0;
-            d.acc_final = f + fw >= F;
+            d.acc_final = last;
             d.x = x + c * Dl;
             d.ldx = D;
             d.gate = gate2;
-            if ((r = timed(p, st, DIT_K_GEMM_DOWN, 2.0 * rows * D * fw,
+            if (last && on(l_d)) attach(d, 0, u_d, l_d, 0);
+            if ((r = timed(p, st, DIT_K_GEMM_DOWN,
+                           2.0 * rows * D * fw + (last ? lflops(l_d, rows, D) : 0.0),
                            [&] { return launch_gemm(d, status, st); })) != DIT_OK)
                 return r;
         }

@@ -19,6 +19,16 @@
 // The accumulator is double-buffered, so the epilogue of tile i overlaps the
 // main loop of tile i+1.
 //
+// Activation-space LoRA ("ComfyUI-StaticPipeline", "Activation-space LoRA
+// (bypass mode)": y = W x + alpha B (A x)) continues the same accumulation:
+// after W's K-steps, each 64-wide K-step of U L^T (U = x A^T, L = alpha B)
+// takes two ring stages, one per half of the accumulator's columns (an M=128,
+// N=128 MMA each: the two 128-row halves of the output tile, or for SwiGLU
+// the gate and the up accumulator with their own U and L).  A LoRA stage
+// holds a bf16 U tile where A's tile goes and a bf16 L tile at the start of
+// the B area; with int8 weights the MMA reads it there directly and the
+// converter warps skip the stage.
+//
 // Per-row exactness: every output element is the same fp32 accumulation over
 // K in the same order (k-blocks of 64, MMAs of 16), whatever M, the tile
 // schedule or the grid — so results do not depend on how tokens are chunked.
@@ -57,7 +67,13 @@ struct GemmParams {
     const float *rope_cos, *rope_sin;  // [positions, head_dim / 2] or null
     int head_dim;
     float qk_eps;
+    // LoRA: K-steps of U L^T after the main ones (two half stages each)
+    int num_lk;
+    int lora_on0, lora_on1;
 };
+
+constexpr int kLoraRows = 128;                    // rows of a half's L tile
+constexpr int kLoraStageBytes = (kBM + kLoraRows) * kBK * 2;
 
 template <int MODE, bool I8>
 struct Cfg {
@@ -83,6 +99,23 @@ struct Cfg {
     static constexpr int BAR_BYTES = 256;
     static constexpr int SMEM_BYTES = OFF_C + CSTAGES * C_BYTES + BAR_BYTES + 1024;
 };
+
+// LoRA half h of output tile nb: whether it has work, and the first row of
+// its L tile (the tile's rows h*128.. for one B operand; SwiGLU: the tile's
+// rows of the gate (h = 0) or up (h = 1) adapter).
+template <int MODE, bool I8>
+DEV bool lora_half_on(const GemmParams &p, int h, int nb) {
+    using C = Cfg<MODE, I8>;
+    if (h == 0) return p.lora_on0 != 0;
+    if (C::NB == 2) return p.lora_on1 != 0;
+    return p.lora_on1 != 0 && nb * C::BN + kLoraRows < p.N;
+}
+
+template <int MODE, bool I8>
+DEV int lora_row(int h, int nb) {
+    using C = Cfg<MODE, I8>;
+    return C::NB == 2 ? nb * C::BN : nb * C::BN + h * kLoraRows;
+}
 
 DEV void store_bf16x32(__nv_bfloat16 *dst, const float (&f)[32]) {
     uint4 *d = reinterpret_cast<uint4 *>(dst);
@@ -362,7 +395,11 @@ template <int MODE, bool I8>
 __global__ void __launch_bounds__(Cfg<MODE, I8>::THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                    const __grid_constant__ CUtensorMap tmB0,
-                   const __grid_constant__ CUtensorMap tmB1, const GemmParams p) {
+                   const __grid_constant__ CUtensorMap tmB1,
+                   const __grid_constant__ CUtensorMap tmU0,
+                   const __grid_constant__ CUtensorMap tmL0,
+                   const __grid_constant__ CUtensorMap tmU1,
+                   const __grid_constant__ CUtensorMap tmL1, const GemmParams p) {
     using C = Cfg<MODE, I8>;
     constexpr int S = C::STAGES;
     constexpr int CS = C::CSTAGES;
@@ -406,6 +443,12 @@ __global__ void __launch_bounds__(Cfg<MODE, I8>::THREADS, 1)
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB0);
         if (C::NB == 2) tma_prefetch_desc(&tmB1);
+        if (p.num_lk) {
+            tma_prefetch_desc(&tmU0);
+            tma_prefetch_desc(&tmL0);
+            tma_prefetch_desc(&tmU1);
+            tma_prefetch_desc(&tmL1);
+        }
     }
     if (warp == 1) {
         tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
@@ -417,7 +460,7 @@ __global__ void __launch_bounds__(Cfg<MODE, I8>::THREADS, 1)
     const uint32_t tmem = *tmem_slot;
     const WaitCtx wc{abort_flag, p.status};
     const int num_tiles = p.num_m * p.num_n;
-    const bool preload = (MODE == DIT_EPI_DOWN) && p.acc_load;
+    const bool preload = (MODE == DIT_EPI_DOWN || MODE == DIT_EPI_STORE_BF16) && p.acc_load;
 
     if (warp == 0) {
         if (lane == 0) {
@@ -453,6 +496,30 @@ __global__ void __launch_bounds__(Cfg<MODE, I8>::THREADS, 1)
                         ph ^= 1u;
                     }
                 }
+                // LoRA K-steps: U and L tiles, one half stage per accumulator half
+                for (int lk = 0; lk < p.num_lk && ok; ++lk) {
+                    for (int h = 0; h < 2; ++h) {
+                        if (!mbar_wait(empty_bar(stage), ph ^ 1u, wc)) {
+                            ok = false;
+                            break;
+                        }
+                        const uint32_t sA = smem_u32(tiles + stage * C::STAGE_BYTES);
+                        if (lora_half_on<MODE, I8>(p, h, nb)) {
+                            mbar_arrive_expect_tx(full_bar(stage), kLoraStageBytes);
+                            tma_load_2d(sA, h ? &tmU1 : &tmU0, full_bar(stage), lk * kBK,
+                                        mb * kBM);
+                            tma_load_2d(sA + C::A_BYTES, h ? &tmL1 : &tmL0, full_bar(stage),
+                                        lk * kBK, lora_row<MODE, I8>(h, nb));
+                        } else {
+                            mbar_arrive(full_bar(stage));  // nothing to load
+                        }
+                        ++issued;
+                        if (++stage == S) {
+                            stage = 0;
+                            ph ^= 1u;
+                        }
+                    }
+                }
             }
             if (!ok) {  // let the copies already in flight land before exit
                 const int64_t first = issued > S ? issued - S : 0;
@@ -467,6 +534,7 @@ __global__ void __launch_bounds__(Cfg<MODE, I8>::THREADS, 1)
             // those of B0), so one MMA with N = NB * BN covers both; its
             // accumulator columns BN.. are the B1 results.
             constexpr uint32_t IDESC = idesc_bf16_f32(kBM, C::NB * C::BN);
+            constexpr uint32_t IDESC_L = idesc_bf16_f32(kBM, kLoraRows);
             int stage = 0, cstage = 0;
             uint32_t ph = 0, cph = 0;
             int buf = 0;
@@ -505,6 +573,30 @@ __global__ void __launch_bounds__(Cfg<MODE, I8>::THREADS, 1)
                         if (++cstage == CS) {
                             cstage = 0;
                             cph ^= 1u;
+                        }
+                    }
+                }
+                if (!ok) break;
+                const int nb = t % p.num_n;
+                for (int lk = 0; lk < p.num_lk && ok; ++lk) {
+                    for (int h = 0; h < 2; ++h) {
+                        if (!mbar_wait(full_bar(stage), ph, wc)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        if (lora_half_on<MODE, I8>(p, h, nb)) {
+                            const uint32_t sU = smem_u32(tiles + stage * C::STAGE_BYTES);
+                            const uint32_t sL = sU + C::A_BYTES;
+#pragma unroll
+                            for (int k = 0; k < kBK / 16; ++k)
+                                mma_bf16_ss(d + uint32_t(h * kLoraRows), desc_sw128(sU + 32u * k),
+                                            desc_sw128(sL + 32u * k), IDESC_L, 1u);
+                        }
+                        mma_commit(empty_bar(stage));
+                        if (++stage == S) {
+                            stage = 0;
+                            ph ^= 1u;
                         }
                     }
                 }
@@ -612,6 +704,13 @@ __global__ void __launch_bounds__(Cfg<MODE, I8>::THREADS, 1)
                     cph ^= 1u;
                 }
             }
+            // the tile's LoRA stages hold bf16 tiles the MMA reads directly
+            for (int i = 0; ok && i < 2 * p.num_lk; ++i) {
+                if (++stage == S) {
+                    stage = 0;
+                    ph ^= 1u;
+                }
+            }
         }
     }
 
@@ -649,6 +748,34 @@ dit_status_t run(const dit_gemm_args_t &a, int *dev_status, cudaStream_t s) {
                                     uint64_t(a.ldb) * bel, kBK, C::BN, bsw))
         return DIT_ERR_INVALID_ARG;
 
+    // LoRA operand maps (unused ones alias A's map)
+    CUtensorMap tU0 = tA, tL0 = tA, tU1 = tA, tL1 = tA;
+    int rmax = 0;
+    if (a.lora_l0) {
+        if (!make_tmap_2d(&tU0, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.lora_u0,
+                          uint64_t(a.lora_rank0), uint64_t(a.M), uint64_t(a.lora_ldu0) * 2, kBK,
+                          kBM) ||
+            !make_tmap_2d(&tL0, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.lora_l0,
+                          uint64_t(a.lora_rank0), uint64_t(a.N), uint64_t(a.lora_ldl0) * 2, kBK,
+                          kLoraRows))
+            return DIT_ERR_INVALID_ARG;
+        rmax = a.lora_rank0;
+    }
+    if (C::NB == 2 && a.lora_l1) {
+        if (!make_tmap_2d(&tU1, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.lora_u1,
+                          uint64_t(a.lora_rank1), uint64_t(a.M), uint64_t(a.lora_ldu1) * 2, kBK,
+                          kBM) ||
+            !make_tmap_2d(&tL1, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.lora_l1,
+                          uint64_t(a.lora_rank1), uint64_t(a.N), uint64_t(a.lora_ldl1) * 2, kBK,
+                          kLoraRows))
+            return DIT_ERR_INVALID_ARG;
+        if (a.lora_rank1 > rmax) rmax = a.lora_rank1;
+    }
+    if (C::NB == 1) {  // one adapter: its two halves cover the tile's rows
+        tU1 = tU0;
+        tL1 = tL0;
+    }
+
     GemmParams p{};
     p.M = a.M;
     p.N = a.N;
@@ -679,6 +806,9 @@ dit_status_t run(const dit_gemm_args_t &a, int *dev_status, cudaStream_t s) {
     p.rope_sin = a.rope_sin;
     p.head_dim = a.head_dim;
     p.qk_eps = a.qk_eps;
+    p.num_lk = (rmax + kBK - 1) / kBK;
+    p.lora_on0 = a.lora_l0 != nullptr;
+    p.lora_on1 = C::NB == 2 ? a.lora_l1 != nullptr : a.lora_l0 != nullptr;
 
     int &done = attr_flag(MODE, I8);
     if (!done) {
@@ -690,7 +820,8 @@ dit_status_t run(const dit_gemm_args_t &a, int *dev_status, cudaStream_t s) {
     }
     const int tiles = p.num_m * p.num_n;
     const int grid = tiles < sm_count() ? tiles : sm_count();
-    gemm_tc_kernel<MODE, I8><<<grid, C::THREADS, C::SMEM_BYTES, s>>>(tA, tB0, tB1, p);
+    gemm_tc_kernel<MODE, I8><<<grid, C::THREADS, C::SMEM_BYTES, s>>>(tA, tB0, tB1, tU0, tL0,
+                                                                     tU1, tL1, p);
     return check_launch();
 }
 
@@ -730,11 +861,29 @@ dit_status_t launch_gemm(const dit_gemm_args_t &a, int *dev_status, cudaStream_t
         if (!aligned16(a.qk_norm) || !aligned16(a.rope_cos) || !aligned16(a.rope_sin))
             return DIT_ERR_ALIGN;
     }
+    if (a.lora_l0 || a.lora_l1 || a.lora_u0 || a.lora_u1) {
+        if ((a.lora_l1 || a.lora_u1) && a.mode != DIT_EPI_SWIGLU) return DIT_ERR_INVALID_ARG;
+        auto half_ok = [](const void *u, int64_t ldu, const void *l, int64_t ldl, int r) {
+            if (!u && !l) return DIT_OK;
+            if (!u || !l || r <= 0 || r > DIT_LORA_MAX_RANK || r % 8) return DIT_ERR_INVALID_ARG;
+            if (!ld_ok(ldu, r, 2) || !ld_ok(ldl, r, 2)) return DIT_ERR_INVALID_ARG;
+            if (!aligned16(u) || !aligned16(l)) return DIT_ERR_ALIGN;
+            return DIT_OK;
+        };
+        dit_status_t e = half_ok(a.lora_u0, a.lora_ldu0, a.lora_l0, a.lora_ldl0, a.lora_rank0);
+        if (e == DIT_OK)
+            e = half_ok(a.lora_u1, a.lora_ldu1, a.lora_l1, a.lora_ldl1, a.lora_rank1);
+        if (e != DIT_OK) return e;
+    }
     if (a.M == 0) return DIT_OK;
     switch (a.mode) {
         case DIT_EPI_STORE_BF16:
             if (!a.out || !aligned16(a.out)) return DIT_ERR_ALIGN;
             if (!ld_ok(a.ldo, a.N, 2)) return DIT_ERR_INVALID_ARG;
+            if (a.acc_load) {
+                if (!a.acc || !aligned16(a.acc)) return DIT_ERR_ALIGN;
+                if (!ld_ok(a.ldacc, a.N, 4)) return DIT_ERR_INVALID_ARG;
+            }
             return run_b<DIT_EPI_STORE_BF16>(a, dev_status, s);
         case DIT_EPI_STORE_F32:
             if (!a.out || !aligned16(a.out)) return DIT_ERR_ALIGN;

@@ -15,8 +15,11 @@ struct dit_plan {
     int D, heads, head_dim, F;
     int cm, ca, fs;  // effective mlp chunk, attention chunk, FFN slice
     int64_t t_pad;   // row stride of V^T
+    int lora_r = 0;  // LoRA rank the workspace holds (0: none)
     // workspace layout (byte offsets)
     size_t off_k, off_vt, off_a, off_q, off_b, off_h, off_acc, total;
+    size_t off_uq, off_uo;                   // LoRA u of Q/K/V and O (attention phase)
+    size_t off_ug, off_uu, off_ud, off_udc;  // LoRA u of gate, up, down; down's carry
     uint8_t *ws;
     size_t ws_bytes;
     // per-kernel timing (dit_block_profile_*)

@@ -49,16 +49,17 @@ SYMBOLS = (
     "dit_abi_version", "dit_modln_cast", "dit_gemm", "dit_attention",
     "dit_block_profile_enable", "dit_block_profile_read",
     "dit_block_forward_static", "dit_block_plan_auto", "dit_block_forward_qk",
+    "dit_block_forward_ex", "dit_block_plan_set_lora_rank", "dit_lora_prepare",
 )
 
 STATIC_SCRATCH_BYTES = 64 << 20
 
 # Kernel kinds of the per-kernel timing record (DIT_K_*).
 KINDS = ("modln", "gemm_kv", "gemm_q", "attention", "gemm_o", "gemm_swiglu",
-         "gemm_down", "final")
+         "gemm_down", "final", "lora_u")
 # work unit of each kind: flops (tensor-core kinds) or bytes (memory-bound)
 KIND_UNITS = ("bytes", "flops", "flops", "flops", "flops", "flops", "flops",
-              "bytes")
+              "bytes", "flops")
 
 
 class DitError(RuntimeError):
@@ -97,7 +98,24 @@ class GemmArgs(ctypes.Structure):
                 ("flags", ctypes.c_int),
                 ("qk_norm", ctypes.c_void_p), ("rope_cos", ctypes.c_void_p),
                 ("rope_sin", ctypes.c_void_p), ("head_dim", ctypes.c_int),
-                ("qk_eps", ctypes.c_float)]
+                ("qk_eps", ctypes.c_float),
+                ("lora_u0", ctypes.c_void_p), ("lora_ldu0", ctypes.c_int64),
+                ("lora_l0", ctypes.c_void_p), ("lora_ldl0", ctypes.c_int64),
+                ("lora_rank0", ctypes.c_int),
+                ("lora_u1", ctypes.c_void_p), ("lora_ldu1", ctypes.c_int64),
+                ("lora_l1", ctypes.c_void_p), ("lora_ldl1", ctypes.c_int64),
+                ("lora_rank1", ctypes.c_int)]
+
+
+class LoraArgs(ctypes.Structure):
+    """dit_lora_t: one adapter (A [rank, in], prepared B [out, rank])."""
+    _fields_ = [("a", ctypes.c_void_p), ("b", ctypes.c_void_p), ("rank", ctypes.c_int)]
+
+
+class BlockLora(ctypes.Structure):
+    """dit_block_lora_t: the adapters of one block (absent ones zero)."""
+    _fields_ = [("qkv", LoraArgs), ("o", LoraArgs), ("gate", LoraArgs),
+                ("up", LoraArgs), ("down", LoraArgs)]
 
 
 class QkArgs(ctypes.Structure):
@@ -139,6 +157,12 @@ def _declare(lib):
         "dit_block_plan_auto": (c_int, [c_int64, c_int, c_int, c_int, c_size, pp]),
         "dit_block_forward_qk": (c_int, [vp, vp, ctypes.POINTER(BlockWeights), vp,
                                          ctypes.POINTER(QkArgs), vp]),
+        "dit_block_forward_ex": (c_int, [vp, vp, ctypes.POINTER(BlockWeights), vp,
+                                         ctypes.POINTER(QkArgs), ctypes.POINTER(BlockLora),
+                                         vp]),
+        "dit_block_plan_set_lora_rank": (c_int, [vp, c_int]),
+        "dit_lora_prepare": (c_int, [vp, c_int64, c_int, c_int64, ctypes.c_float, vp, vp,
+                                     c_int64, vp]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -238,8 +262,13 @@ class BlockPlan:
         self._ws = buf  # keep the caller's buffer alive with the plan
 
     def forward(self, x, weights: BlockWeights, modulation, stream=None,
-                qk: Optional["QkArgs"] = None):
-        if qk is None:
+                qk: Optional["QkArgs"] = None, lora: Optional["BlockLora"] = None):
+        if lora is not None:
+            _check(load().dit_block_forward_ex(
+                self._h, ptr(x), ctypes.byref(weights), ptr(modulation),
+                None if qk is None else ctypes.byref(qk), ctypes.byref(lora),
+                stream_handle(stream)), "dit_block_forward_ex")
+        elif qk is None:
             _check(load().dit_block_forward(self._h, ptr(x), ctypes.byref(weights),
                                             ptr(modulation), stream_handle(stream)),
                    "dit_block_forward")
@@ -248,6 +277,11 @@ class BlockPlan:
                                                ptr(modulation), ctypes.byref(qk),
                                                stream_handle(stream)),
                    "dit_block_forward_qk")
+
+    def set_lora_rank(self, max_rank: int):
+        """Reserve workspace for adapters of rank <= max_rank (before binding)."""
+        _check(load().dit_block_plan_set_lora_rank(self._h, max_rank),
+               "dit_block_plan_set_lora_rank")
 
     def forward_static(self, x, weights: BlockWeights, modulation, stream=None):
         """dit_block_forward_static: the same forward with the library's
@@ -317,6 +351,21 @@ def qk_args(q_norm=None, k_norm=None, rope_cos=None, rope_sin=None,
     a.rope_cos, a.rope_sin = ptr(rope_cos), ptr(rope_sin)
     a.eps = eps
     return a
+
+
+def lora_prepare(b, rows, rank, ld_b, alpha, row_scale, b_out, ld_out, stream=None):
+    """dit_lora_prepare: b_out = bf16(alpha * b / row_scale) (row_scale may be None)."""
+    _check(load().dit_lora_prepare(ptr(b), rows, rank, ld_b, alpha, ptr(row_scale),
+                                   ptr(b_out), ld_out, stream_handle(stream)),
+           "dit_lora_prepare")
+
+
+def block_lora(**adapters) -> BlockLora:
+    """Pack adapters given as name=(a, b_prepared, rank) into a ``BlockLora``."""
+    bl = BlockLora()
+    for name, (a, b, rank) in adapters.items():
+        setattr(bl, name, LoraArgs(ptr(a), ptr(b), rank))
+    return bl
 
 
 def modln_cast(x, rows, D, shift, scale, out, stream=None):

@@ -69,15 +69,43 @@ def upload_qk(qk: dict, device="cuda") -> DeviceQk:
     return DeviceQk(t, st)
 
 
+@dataclass
+class DeviceLora:
+    tensors: dict            # device tensors (kept alive)
+    struct: ditstream.BlockLora
+
+
+_LORA_WEIGHT = dict(qkv="wqkv", o="wo", gate="wgate", up="wup", down="wdown")
+
+
+def upload_lora(lora: dict, block: DeviceBlock, stream=None) -> DeviceLora:
+    """Place adapters (``synth.make_lora``) on the device for one block:
+    A as given, B prepared by ``dit_lora_prepare`` (alpha folded in and, for
+    int8 weights, divided by the adapted weight's row scales)."""
+    keep, packed = {}, {}
+    for name, (A, B, alpha) in lora.items():
+        a = A.to("cuda").contiguous()
+        b = B.to("cuda").contiguous()
+        rows, rank = b.shape
+        bp = torch.empty_like(b)
+        scale = block.tensors.get(_LORA_WEIGHT[name] + "_scale")
+        ditstream.lora_prepare(b, rows, rank, rank, alpha, scale, bp, rank, stream)
+        keep[name] = (a, b, bp)
+        packed[name] = (a, bp, rank)
+    return DeviceLora(keep, ditstream.block_lora(**packed))
+
+
 class DitStack:
     """A stack of DiT blocks (one plan, one workspace) plus an optional
     final layer.  ``forward`` updates ``x`` in place and returns the final
     layer's output when there is one."""
 
     def __init__(self, T, D, heads, F, mlp_chunk, attn_chunk, ffn_slice=0,
-                 device="cuda"):
+                 device="cuda", lora_rank=0):
         self.plan = ditstream.block_plan(T, D, heads, F, mlp_chunk, attn_chunk,
                                          ffn_slice)
+        if lora_rank:
+            self.plan.set_lora_rank(lora_rank)
         self.T, self.D = T, D
         self.workspace = torch.empty(self.plan.workspace_bytes(),
                                      dtype=torch.uint8, device=device)
@@ -86,12 +114,16 @@ class DitStack:
 
     def forward(self, x: torch.Tensor, dev: DeviceInputs, stream=None,
                 out: Optional[torch.Tensor] = None,
-                qk: Optional[DeviceQk] = None):
+                qk: Optional[DeviceQk] = None,
+                lora: Optional[List[DeviceLora]] = None):
+        """``lora``: one DeviceLora (or None) per block."""
         if stream is None:
             stream = torch.cuda.current_stream(x.device)
-        for b in dev.blocks:
+        for i, b in enumerate(dev.blocks):
+            ad = None if lora is None else lora[i]
             self.plan.forward(x, b.struct, b.mod, stream,
-                              qk=None if qk is None else qk.struct)
+                              qk=None if qk is None else qk.struct,
+                              lora=None if ad is None else ad.struct)
         if dev.wf is not None:
             if out is None:
                 out = torch.empty(self.T, 64, dtype=torch.float32,

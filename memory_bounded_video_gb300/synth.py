@@ -19,7 +19,9 @@ in for them):
 * final layer                : ``mod_f`` [2, D] N(0, 0.1); ``W_f`` [64, D]
   N(0, 0.02) fp32 (or int8 like the block weights);
 * optional Q/K transform      : RMSNorm weights [d] N(1, 0.1); rotary angle
-  tables [T, d/2] fp32 (see ``make_qk``).
+  tables [T, d/2] fp32 (see ``make_qk``);
+* optional LoRA adapters      : A [r, in], B [out, r] ~ N(0, 0.02) rounded to
+  bf16, alpha given (see ``make_lora``).
 """
 
 from __future__ import annotations
@@ -207,4 +209,22 @@ def make_qk(T, head_dim, seed=0, angles="axial", norm=True) -> dict:
             raise ValueError(angles)
         out["cos"] = torch.cos(th).float()
         out["sin"] = torch.sin(th).float()
+    return out
+
+
+LORA_SHAPES = ("qkv", "o", "gate", "up", "down")
+
+
+def make_lora(D, F, rank, seed=0, names=LORA_SHAPES, std=0.02, alpha=1.0) -> dict:
+    """Adapters name -> (A bf16 [rank, in], B bf16 [out, rank], alpha) for
+    the linears ``names`` of a block (in/out: qkv D/3D, o D/D, gate and up
+    D/F, down F/D)."""
+    dims = dict(qkv=(D, 3 * D), o=(D, D), gate=(D, F), up=(D, F), down=(F, D))
+    g = torch.Generator(device="cpu")
+    g.manual_seed(seed)
+    out = {}
+    for n in names:
+        i, o = dims[n]
+        out[n] = (_normal(g, (rank, i), std).to(torch.bfloat16),
+                  _normal(g, (o, rank), std).to(torch.bfloat16), float(alpha))
     return out

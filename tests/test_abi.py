@@ -56,6 +56,8 @@ def test_binding_constants_match_header():
                  DIT_K_MODLN=ds.KINDS.index("modln"),
                  DIT_K_ATTENTION=ds.KINDS.index("attention"),
                  DIT_K_FINAL=ds.KINDS.index("final"),
+                 DIT_K_LORA_U=ds.KINDS.index("lora_u"),
+                 DIT_LORA_MAX_RANK=256,
                  DITSTREAM_ABI_VERSION=None)
     for k, v in pairs.items():
         if v is not None:
@@ -71,13 +73,18 @@ def test_struct_layouts_match_header():
     body = re.search(r"typedef struct \{([^}]*)\} dit_block_weights_t;", src).group(1)
     fields = re.findall(r"\b(\w+);", body)
     assert fields == [f for f, _ in ds.BlockWeights._fields_]
+    body = re.search(r"typedef struct \{([^}]*)\} dit_lora_t;", src).group(1)
+    assert re.findall(r"\b(\w+);", body) == [f for f, _ in ds.LoraArgs._fields_]
+    body = re.search(r"typedef struct \{([^}]*)\} dit_block_lora_t;", src).group(1)
+    names = re.search(r"dit_lora_t ([\w, ]+);", body).group(1).replace(" ", "").split(",")
+    assert names == [f for f, _ in ds.BlockLora._fields_]
     body = re.search(r"typedef struct \{([^}]*)\} dit_qk_t;", src).group(1)
     fields = re.findall(r"\b(\w+);", re.sub(r"/\*.*?\*/", "", body, flags=re.S))
     assert fields == [f for f, _ in ds.QkArgs._fields_]
 
 
 def test_status_strings(lib):
-    assert ds.abi_version() == 2
+    assert ds.abi_version() == 3
     for s in (0, -1, -2, -3, -4, -5, -6, -7, -8):
         assert ds.status_string(s) and ds.status_string(s) != "unknown status"
     assert ds.status_string(-99) == "unknown status"
@@ -111,8 +118,9 @@ def rup(v, a=1024):
     return (v + a - 1) // a * a
 
 
-def expected_workspace(T, D, F, cm, ca, fs):
-    """The layout documented for dit_block_workspace_bytes, restated."""
+def expected_workspace(T, D, F, cm, ca, fs, R=0):
+    """The layout documented for dit_block_workspace_bytes (and, with a
+    LoRA rank R, dit_block_plan_set_lora_rank), restated."""
     cm = T if cm == 0 or cm >= T else cm
     ca = T if ca == 0 or ca >= T else ca
     fs = fs or F
@@ -123,6 +131,11 @@ def expected_workspace(T, D, F, cm, ca, fs):
     mlp = rup(rup(phase + 2 * cm * D) + 2 * cm * fs)
     if fs < F:
         mlp = rup(mlp + 4 * cm * D)
+    if R:
+        attn = rup(rup(attn + 2 * ca * R) + 2 * ca * R)    # u of Q/K/V and O
+        mlp = rup(rup(rup(mlp + 2 * cm * R) + 2 * cm * R) + 2 * cm * R)  # gate, up, down
+        if fs < F:
+            mlp = rup(mlp + 4 * cm * R)                     # down's fp32 carry
     return max(attn, mlp)
 
 
@@ -142,6 +155,69 @@ def test_workspace_layout_and_info(lib, cfg):
     assert info["mlp_chunk"] == (T if cm == 0 or cm >= T else cm)
     assert info["attn_chunk"] == (T if ca == 0 or ca >= T else ca)
     assert info["ffn_slice"] == (fs or F)
+
+
+@pytest.mark.parametrize("cfg", [
+    (512, 256, 4, 704, 128, 128, 0, 32),
+    (1000, 1024, 8, 2816, 256, 384, 1024, 64),
+    (32768, 3072, 24, 8192, 8192, 8192, 0, 256),
+])
+def test_workspace_with_lora_rank(lib, cfg):
+    T, D, H, F, cm, ca, fs, R = cfg
+    p = ds.block_plan(T, D, H, F, cm, ca, fs)
+    p.set_lora_rank(R)
+    assert p.workspace_bytes() == expected_workspace(T, D, F, cm, ca, fs, R)
+    p.set_lora_rank(0)
+    assert p.workspace_bytes() == expected_workspace(T, D, F, cm, ca, fs)
+
+
+def test_lora_rank_rules(lib):
+    p = ds.block_plan(512, 256, 4, 704, 128, 128)
+    for bad in (-32, 16, 48, 288):
+        with pytest.raises(ds.DitError) as e:
+            p.set_lora_rank(bad)
+        assert e.value.status == ds.ERR_INVALID_ARG
+    assert lib.dit_block_plan_set_lora_rank(None, 32) == ds.ERR_INVALID_ARG
+
+
+def test_lora_arguments_validated_before_launch(lib):
+    base = dict(mode=ds.EPI_STORE_F32, M=128, N=256, K=64, a=16, lda=64, b0=16,
+                ldb=64, out=16, ldo=256)
+    lo = dict(lora_u0=16, lora_ldu0=64, lora_l0=16, lora_ldl0=64, lora_rank0=64)
+    cases = [
+        (dict(lora_u0=16), ds.ERR_INVALID_ARG),                       # l missing
+        (dict(lora_l0=16, lora_rank0=64, lora_ldl0=64), ds.ERR_INVALID_ARG),
+        ({**lo, "lora_rank0": 12}, ds.ERR_INVALID_ARG),               # rank % 8
+        ({**lo, "lora_rank0": 264, "lora_ldu0": 264, "lora_ldl0": 264}, ds.ERR_INVALID_ARG),
+        ({**lo, "lora_ldu0": 32}, ds.ERR_INVALID_ARG),                 # ldu < rank
+        ({**lo, "lora_ldl0": 68}, ds.ERR_INVALID_ARG),                 # stride % 16 B
+        ({**lo, "lora_u0": 24}, ds.ERR_ALIGN),
+        ({**lo, "lora_l1": 16, "lora_u1": 16, "lora_rank1": 64, "lora_ldu1": 64,
+          "lora_ldl1": 64}, ds.ERR_INVALID_ARG),                      # half 1: SWIGLU only
+        (dict(mode=ds.EPI_STORE_BF16, ldo=256, out=16, acc_load=1), ds.ERR_ALIGN),  # no acc
+    ]
+    for kw, want in cases:
+        g = ds.GemmArgs(**{**base, **kw})
+        assert lib.dit_gemm(ctypes.byref(g), None, None) == want, kw
+    # dit_lora_prepare
+    assert lib.dit_lora_prepare(16, 100, 0, 64, 1.0, None, 16, 64, None) == ds.ERR_INVALID_ARG
+    assert lib.dit_lora_prepare(16, 100, 64, 60, 1.0, None, 16, 64, None) == ds.ERR_INVALID_ARG
+    assert lib.dit_lora_prepare(24, 100, 64, 64, 1.0, None, 16, 64, None) == ds.ERR_ALIGN
+
+
+def test_forward_ex_validates_adapters_before_launch(lib):
+    # no workspace is bound, so even a valid call stops before any launch
+    p = ds.block_plan(512, 256, 4, 704, 128, 128)
+    p.set_lora_rank(64)
+    w = ds.block_weights(16, 16, 16, 16, 16)
+    for kw, want in [(dict(o=(16, 16, 48)), ds.ERR_INVALID_ARG),     # rank % 32
+                     (dict(up=(16, 16, 128)), ds.ERR_INVALID_ARG),   # above the plan's
+                     (dict(down=(8, 16, 32)), ds.ERR_ALIGN),
+                     (dict(qkv=(16, 16, 64), gate=(16, 16, 32)), ds.ERR_NO_WORKSPACE),
+                     (dict(qkv=(16, None, 64)), ds.ERR_NO_WORKSPACE)]:  # absent adapter
+        with pytest.raises(ds.DitError) as e:
+            p.forward(16, w, 16, lora=ds.block_lora(**kw))
+        assert e.value.status == want, kw
 
 
 def test_workspace_beyond_kv_floor_is_bounded_by_chunk():
