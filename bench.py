@@ -57,6 +57,12 @@ def parse_args(argv=None):
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--workload", default=HEADLINE)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--weight-scratch", choices=("on", "off"), default="on",
+                    help="int8 blocks: expand each phase's weights to bf16 in a "
+                         "scratch ahead of the GEMMs (exact; same result bits)")
+    ap.add_argument("--lora", type=int, default=0,
+                    help="rank of activation-space LoRA adapters on all five "
+                         "linears of every block (0: none)")
     ap.add_argument("--qk", choices=("none", "axial"), default="none",
                     help="add the per-head Q/K RMSNorm + rotary embedding "
                          "(axial video angles) to every block")
@@ -194,7 +200,7 @@ def cpu_cores():
 
 # ------------------------------------------------------------------ oracle (CPU) leg
 
-def cpu_sample(cfg, inp, rows_n, steps=1, warmup=0, qk=None):
+def cpu_sample(cfg, inp, rows_n, steps=1, warmup=0, qk=None, loras=None):
     """Time the float64 oracle on a bounded sample of the workload.
 
     Per block: K and V of all T tokens are computed first (untimed set-up, the
@@ -216,6 +222,10 @@ def cpu_sample(cfg, inp, rows_n, steps=1, warmup=0, qk=None):
         else:
             w = ob.DitWeights(**{k: v.double().numpy() for k, v in bw.named().items()})
         blocks.append((w, mod.double().numpy()))
+    l64 = [None] * len(blocks)
+    if loras is not None:
+        l64 = [{k: (A.double().numpy(), B.double().numpy(), al)
+                for k, (A, B, al) in lo.items()} for lo in loras]
     # set-up: K/V of every token for the first block, by the oracle's own
     # projection; every block's sampled rows attend to that key/value set
     # (the oracle's cost does not depend on the values, and this keeps the
@@ -227,9 +237,14 @@ def cpu_sample(cfg, inp, rows_n, steps=1, warmup=0, qk=None):
     if qk is not None:
         qk64 = {k: (v.double().numpy() if hasattr(v, "double") else v)
                 for k, v in qk.items()}
-    kv = (ob.qk_transform(a @ wk.T, H, None if qk64 is None else qk64["k_norm"],
+    Dm = cfg["D"]
+    kproj = a @ wk.T + ob.lora_delta(a, None if l64[0] is None else l64[0]["qkv"],
+                                     slice(Dm, 2 * Dm))
+    vproj = a @ wv.T + ob.lora_delta(a, None if l64[0] is None else l64[0]["qkv"],
+                                     slice(2 * Dm, 3 * Dm))
+    kv = (ob.qk_transform(kproj, H, None if qk64 is None else qk64["k_norm"],
                           None if qk64 is None else qk64["cos"],
-                          None if qk64 is None else qk64["sin"]), a @ wv.T)
+                          None if qk64 is None else qk64["sin"]), vproj)
     del a
     kvs = [kv] * len(blocks)
     wf = None
@@ -240,11 +255,13 @@ def cpu_sample(cfg, inp, rows_n, steps=1, warmup=0, qk=None):
 
     def one():
         t0 = time.perf_counter()
-        for (w, mod), kv in zip(blocks, kvs):
+        for (w, mod), kv, lo in zip(blocks, kvs, l64):
             a = ob.ln_modulate(x[rows], mod[0], mod[1])
             _, wk, wv = w.q_k_v()
-            _ = (a @ wk.T, a @ wv.T)
-            ob.dit_block_rows(x, w, mod, H, rows, kv=kv, qk=qk64)
+            ad = None if lo is None else lo["qkv"]
+            _ = (a @ wk.T + ob.lora_delta(a, ad, slice(Dm, 2 * Dm)),
+                 a @ wv.T + ob.lora_delta(a, ad, slice(2 * Dm, 3 * Dm)))
+            ob.dit_block_rows(x, w, mod, H, rows, kv=kv, qk=qk64, lora=lo)
         if wf is not None:
             ob.final_layer(x[rows], wf, mod_f)
         return time.perf_counter() - t0
@@ -258,6 +275,7 @@ def cpu_sample(cfg, inp, rows_n, steps=1, warmup=0, qk=None):
               f"LN-mod, Q, attention against all {T} keys, O-proj, SwiGLU MLP"
               + (", final layer" if wf is not None else "")
               + (", Q/K RMSNorm + rotary" if qk64 is not None else "")
+              + (", LoRA adapters" if loras is not None else "")
               + f") x {len(blocks)} block(s), float64 numpy oracle; K/V of all "
               "tokens precomputed untimed (first block's, reused as every "
               "block's key/value set)")
@@ -283,8 +301,15 @@ def run_ours(args, rank, world, local_rank):
 
     inp = synth.make_workload(args.workload, seed=rank)
     dev = runner.upload(inp, dev_name)
+    scratch = cfg["int8"] and args.weight_scratch == "on"
     stack = runner.DitStack(T, D, H, F, cfg["mlp_chunk"], cfg["attn_chunk"],
-                            cfg["ffn_slice"], device=dev_name)
+                            cfg["ffn_slice"], device=dev_name, lora_rank=args.lora,
+                            weight_scratch=scratch)
+    loras = dls = None
+    if args.lora:
+        loras = [synth.make_lora(D, F, args.lora, seed=100 * rank + i)
+                 for i in range(cfg["blocks"])]
+        dls = [runner.upload_lora(lo, b) for lo, b in zip(loras, dev.blocks)]
     qk = dqk = None
     if args.qk != "none":
         qk = synth.make_qk(T, D // H, seed=rank, angles=args.qk)
@@ -294,7 +319,7 @@ def run_ours(args, rank, world, local_rank):
     mem0 = torch.cuda.memory_allocated()
     torch.cuda.reset_peak_memory_stats()
     for _ in range(args.warmup):
-        stack.forward(x, dev, stream, qk=dqk)
+        stack.forward(x, dev, stream, qk=dqk, lora=dls)
     stack.check(stream)
     peak_fwd = torch.cuda.max_memory_allocated() - mem0
 
@@ -316,7 +341,7 @@ def run_ours(args, rank, world, local_rank):
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for _ in range(args.steps):
-        stack.forward(x, dev, stream, qk=dqk)
+        stack.forward(x, dev, stream, qk=dqk, lora=dls)
     e1.record(stream)
     torch.cuda.synchronize()
     barrier()
@@ -332,6 +357,8 @@ def run_ours(args, rank, world, local_rank):
     value = replica_throughput(tokens_per_step * args.steps, world, ms)
     ms_per_step = ms / args.steps
     flops_step = blocks * ob.block_flops(T, D, F)
+    if args.lora:  # u = x A^T and the u B^T K-steps of the five adapted linears
+        flops_step += blocks * T * 2 * args.lora * (9 * D + 3 * F)
     peaks, peak_src = load_peaks()
     tflops = flops_step / (ms_per_step / 1e3) / 1e12
 
@@ -383,6 +410,9 @@ def run_ours(args, rank, world, local_rank):
                          f"{4 * T * D / 2**20:.0f} MiB per block)",
                    "qk_transform": (None if qk is None else
                                     f"q/k rmsnorm + {args.qk} rotary"),
+                   "lora_rank": args.lora or None,
+                   "int8_weight_scratch_gib": (round(stack.plan.weight_scratch_bytes()
+                                                     / 2**30, 4) if scratch else None),
                    "parallelism": f"replicas x{world}"},
         "tflops": round(tflops, 2),
         "tensor_peak_frac": round(tflops / peaks["bf16_tflops_sustained"], 4),
@@ -408,7 +438,7 @@ def run_ours(args, rank, world, local_rank):
         def e2e_step():
             x.copy_(x_host, non_blocking=True)
             res = stack.forward(x, dev, stream, out=out_dev if cfg["final"] else None,
-                                qk=dqk)
+                                qk=dqk, lora=dls)
             out_host.copy_(res if res is not None else x, non_blocking=True)
 
         e2e_step()
@@ -431,7 +461,7 @@ def run_ours(args, rank, world, local_rank):
                        "steps": k_e2e}
 
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        v, per, sample, _ = cpu_sample(cfg, inp, args.cpu_rows, qk=qk)
+        v, per, sample, _ = cpu_sample(cfg, inp, args.cpu_rows, qk=qk, loras=loras)
         line["cpu_baseline"] = {"value": round(v, 2), "unit": "block-tokens/s",
                                 "cores": cpu_cores(), "kind": "oracle",
                                 "sample": sample,
@@ -447,9 +477,13 @@ def run_reference(args):
     qk = None
     if args.qk != "none":
         qk = synth.make_qk(cfg["T"], cfg["D"] // cfg["heads"], seed=0, angles=args.qk)
+    loras = None
+    if args.lora:
+        loras = [synth.make_lora(cfg["D"], cfg["F"], args.lora, seed=i)
+                 for i in range(cfg["blocks"])]
     value, per_step, sample, times = cpu_sample(cfg, inp, args.cpu_rows,
                                                 steps=args.steps,
-                                                warmup=args.warmup, qk=qk)
+                                                warmup=args.warmup, qk=qk, loras=loras)
     T = cfg["T"]
     return {
         "impl": "reference",
@@ -465,7 +499,8 @@ def run_reference(args):
                    "blocks": cfg["blocks"], "final_layer": cfg["final"],
                    "int8_weights": cfg["int8"],
                    "qk_transform": (None if qk is None else
-                                    f"q/k rmsnorm + {args.qk} rotary")},
+                                    f"q/k rmsnorm + {args.qk} rotary"),
+                   "lora_rank": args.lora or None},
         "cpu_baseline": {"value": round(value, 3), "unit": "block-tokens/s",
                          "cores": cpu_cores(), "kind": "oracle",
                          "sample": sample},

@@ -52,7 +52,7 @@
 extern "C" {
 #endif
 
-#define DITSTREAM_ABI_VERSION 3
+#define DITSTREAM_ABI_VERSION 4
 
 #if defined(__GNUC__)
 #define DIT_API __attribute__((visibility("default")))
@@ -170,6 +170,24 @@ DIT_API size_t dit_block_workspace_bytes(const dit_plan_t *plan);
  * DIT_ERR_WORKSPACE_TOO_SMALL, DIT_ERR_UNSUPPORTED_ARCH, DIT_ERR_CUDA. */
 DIT_API dit_status_t dit_block_bind_workspace(dit_plan_t *plan, void *dev_ptr,
                                       size_t bytes);
+
+/* Optional weight scratch for int8 blocks.  An int8 weight value q
+ * (|q| <= 127) is exact in bf16, so with a scratch bound the forward expands
+ * each phase's int8 weights into it (Wqkv and Wo before pass one; Wgate,
+ * Wup and Wdown after pass two) and runs the bf16 tensor-core main loop,
+ * applying the same per-row scale to the fp32 accumulator as the int8 path
+ * ("MiniMax-H3-Comfy-NPU" section 2.2: W = s_row * q).  The MMAs see the
+ * same operands in the same order, so the output bits are the same as
+ * without the scratch; the GEMMs skip the in-kernel shared-memory conversion,
+ * for 2 * max(4 D^2, 3 D F) bytes of weight scratch (independent of T and of
+ * the chunks; the resident weights stay int8).  bf16 weights ignore it.
+ * dit_block_weight_scratch_bytes: the size needed.
+ * dit_block_bind_weight_scratch: bind caller-owned device memory (>= that
+ * size, 256-byte aligned); dev_ptr = NULL unbinds.  Errors:
+ * DIT_ERR_INVALID_ARG, DIT_ERR_ALIGN, DIT_ERR_WORKSPACE_TOO_SMALL. */
+DIT_API size_t dit_block_weight_scratch_bytes(const dit_plan_t *plan);
+DIT_API dit_status_t dit_block_bind_weight_scratch(dit_plan_t *plan, void *dev_ptr,
+                                                   size_t bytes);
 
 /* One block forward, in place on x [T, D] fp32 (device, caller-owned,
  * 16-byte aligned).  modulation: device float [6, D].  Asynchronous on
@@ -336,7 +354,8 @@ DIT_API dit_status_t dit_final_forward(const dit_plan_t *plan, const float *x,
 #define DIT_K_GEMM_DOWN 6
 #define DIT_K_FINAL 7
 #define DIT_K_LORA_U 8      /* LoRA u = x A^T GEMMs (dit_block_forward_ex) */
-#define DIT_NUM_KINDS 9
+#define DIT_K_EXPAND 9      /* int8 -> bf16 weight expansion (weight scratch) */
+#define DIT_NUM_KINDS 10
 
 DIT_API dit_status_t dit_block_profile_enable(dit_plan_t *plan, int enable);
 DIT_API dit_status_t dit_block_profile_read(dit_plan_t *plan, double *ms,
@@ -389,7 +408,8 @@ typedef struct {
     const void *b1;         /* second B (SWIGLU only) */
     int64_t ldb;
     int b_dtype;            /* DIT_W_BF16 or DIT_W_INT8 */
-    const float *b0_scale;  /* per-row scales [N] (int8 only) */
+    const float *b0_scale;  /* per-row scales [N]: int8 B, or bf16 B holding
+                               int8 values (dit_int8_to_bf16); else NULL */
     const float *b1_scale;
     void *out;              /* STORE_*, KV (K), SWIGLU */
     int64_t ldo;
@@ -442,6 +462,11 @@ typedef struct {
 
 DIT_API dit_status_t dit_gemm(const dit_gemm_args_t *args, int *dev_status,
                       dit_stream_t stream);
+
+/* out[i] = bf16(q[i]) for n int8 values q (exact: |q| <= 127 needs 8 bits).
+ * n % 16 == 0; q, out 16-byte aligned.  The weight scratch's expansion. */
+DIT_API dit_status_t dit_int8_to_bf16(const void *q, int64_t n, void *out,
+                                      dit_stream_t stream);
 
 /* Non-causal multi-head attention of Tq queries against T keys:
  *   o[i, h*d:(h+1)*d] = softmax(q_h[i] . k_h^T / sqrt(d)) v_h

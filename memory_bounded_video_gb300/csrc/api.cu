@@ -189,6 +189,27 @@ void layout(dit_plan *p) {
 
 }  // namespace
 
+size_t dit_block_weight_scratch_bytes(const dit_plan_t *p) {
+    if (!p) return 0;
+    const size_t D = size_t(p->D), F = size_t(p->F);
+    const size_t attn = 4 * D * D, mlp = 3 * D * F;
+    return 2 * (attn > mlp ? attn : mlp);
+}
+
+dit_status_t dit_block_bind_weight_scratch(dit_plan_t *p, void *dev_ptr, size_t bytes) {
+    if (!p) return DIT_ERR_INVALID_ARG;
+    if (!dev_ptr) {
+        p->wscratch = nullptr;
+        p->wscratch_bytes = 0;
+        return DIT_OK;
+    }
+    if (reinterpret_cast<uintptr_t>(dev_ptr) % 256) return DIT_ERR_ALIGN;
+    if (bytes < dit_block_weight_scratch_bytes(p)) return DIT_ERR_WORKSPACE_TOO_SMALL;
+    p->wscratch = static_cast<uint8_t *>(dev_ptr);
+    p->wscratch_bytes = bytes;
+    return DIT_OK;
+}
+
 dit_status_t dit_block_plan_set_lora_rank(dit_plan_t *p, int max_rank) {
     if (!p || p->ws) return DIT_ERR_INVALID_ARG;
     if (max_rank < 0 || max_rank > DIT_LORA_MAX_RANK || max_rank % 32) return DIT_ERR_INVALID_ARG;
@@ -412,8 +433,10 @@ dit_status_t dit_block_forward_ex(const dit_plan_t *cp, float *x, const dit_bloc
             !aligned16(w->wdown_scale))
             return DIT_ERR_ALIGN;
     }
-    const int bdt = w->dtype;
-    const int64_t el = i8 ? 1 : 2;  // bytes per weight element
+    // int8 weights expanded into the weight scratch run as bf16 with scales
+    const bool expand = i8 && p->wscratch;
+    const int bdt = expand ? DIT_W_BF16 : w->dtype;
+    const int64_t el = (i8 && !expand) ? 1 : 2;  // bytes per weight element
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const int64_t T = p->T;
@@ -436,7 +459,19 @@ dit_status_t dit_block_forward_ex(const dit_plan_t *cp, float *x, const dit_bloc
     const float *shift1 = mod, *scale1 = mod + Dl, *gate1 = mod + 2 * Dl;
     const float *shift2 = mod + 3 * Dl, *scale2 = mod + 4 * Dl, *gate2 = mod + 5 * Dl;
     const uint8_t *wqkv = static_cast<const uint8_t *>(w->wqkv);
+    const void *wo_m = w->wo;
     dit_status_t r;
+    auto expand_into = [&](const void *q, int64_t n, uint8_t *dst) -> dit_status_t {
+        return timed(p, st, DIT_K_EXPAND, 3.0 * n,
+                     [&] { return launch_expand_int8(q, n, dst, st); });
+    };
+    if (expand) {  // attention-phase weights: Wqkv [3D, D], Wo [D, D]
+        if ((r = expand_into(w->wqkv, 3 * Dl * Dl, p->wscratch)) != DIT_OK ||
+            (r = expand_into(w->wo, Dl * Dl, p->wscratch + 6 * Dl * Dl)) != DIT_OK)
+            return r;
+        wqkv = p->wscratch;
+        wo_m = p->wscratch + 6 * Dl * Dl;
+    }
 
     // the GEMM's Q/K transform fields for Q (which = 0) or K (which = 1)
     auto set_qk = [&](dit_gemm_args_t &g, int which) {
@@ -580,7 +615,7 @@ dit_status_t dit_block_forward_ex(const dit_plan_t *cp, float *x, const dit_bloc
         o.K = D;
         o.a = a;
         o.lda = D;
-        o.b0 = w->wo;
+        o.b0 = wo_m;
         o.ldb = D;
         o.b_dtype = bdt;
         o.b0_scale = i8 ? w->wo_scale : nullptr;
@@ -596,6 +631,17 @@ dit_status_t dit_block_forward_ex(const dit_plan_t *cp, float *x, const dit_bloc
     const uint8_t *wg = static_cast<const uint8_t *>(w->wgate);
     const uint8_t *wu = static_cast<const uint8_t *>(w->wup);
     const uint8_t *wd = static_cast<const uint8_t *>(w->wdown);
+    if (expand) {  // MLP-phase weights over the attention ones (stream order)
+        const int64_t nf = int64_t(F) * Dl;
+        uint8_t *sg = p->wscratch, *su = sg + 2 * nf, *sd = su + 2 * nf;
+        if ((r = expand_into(w->wgate, nf, sg)) != DIT_OK ||
+            (r = expand_into(w->wup, nf, su)) != DIT_OK ||
+            (r = expand_into(w->wdown, nf, sd)) != DIT_OK)
+            return r;
+        wg = sg;
+        wu = su;
+        wd = sd;
+    }
     for (int64_t c = 0; c < T; c += p->cm) {
         const int64_t rows = (T - c < p->cm) ? T - c : p->cm;
         if ((r = timed(p, st, DIT_K_MODLN, 6.0 * rows * D,

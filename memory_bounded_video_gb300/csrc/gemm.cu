@@ -59,6 +59,7 @@ struct GemmParams {
     int64_t ldacc;
     int acc_load, acc_final;
     const float *s0, *s1;  // int8 per-row scales of B0 / B1
+    int bscale;            // bf16 B holding int8 values: apply s0 / s1 too
     int inject_stall;      // DIT_GEMM_FLAG_INJECT_STALL test hook
     int *status;
     // Q/K transform (STORE_BF16, and K columns of KV); qk == 0: off
@@ -201,7 +202,7 @@ DEV void load_chunk(const GemmParams &p, uint32_t taddr, int n, float (&f)[32]) 
     tmem_ld_wait(r);
 #pragma unroll
     for (int j = 0; j < 32; ++j) f[j] = __uint_as_float(r[j]);
-    if (I8) scale32(f, p.s0 + n);
+    if (I8 || p.bscale) scale32(f, p.s0 + n);
 }
 
 // Q/K epilogue with the per-head transform: for each head of d columns in
@@ -319,7 +320,7 @@ DEV void epilogue_tile(const GemmParams &p, uint32_t taddr, int64_t m, int nb) {
         for (int j = 0; j < 32; ++j) f[j] = __uint_as_float(r[j]);
         // The DOWN carry stays unscaled (the row scale is the same for every
         // FFN slice and is applied once, with the residual add).
-        if (I8 && !(MODE == DIT_EPI_DOWN && !p.acc_final)) scale32(f, p.s0 + n);
+        if ((I8 || p.bscale) && !(MODE == DIT_EPI_DOWN && !p.acc_final)) scale32(f, p.s0 + n);
         if constexpr (MODE == DIT_EPI_STORE_BF16) {
             store_bf16x32(reinterpret_cast<__nv_bfloat16 *>(p.out) + m * p.ldo + n, f);
         } else if constexpr (MODE == DIT_EPI_STORE_F32) {
@@ -344,7 +345,7 @@ DEV void epilogue_tile(const GemmParams &p, uint32_t taddr, int64_t m, int nb) {
             float g[32];
 #pragma unroll
             for (int j = 0; j < 32; ++j) g[j] = __uint_as_float(u[j]);
-            if (I8) scale32(g, p.s1 + n);
+            if (I8 || p.bscale) scale32(g, p.s1 + n);
             float h[32];
 #pragma unroll
             for (int j = 0; j < 32; ++j) h[j] = silu(f[j]) * g[j];
@@ -798,6 +799,7 @@ dit_status_t run(const dit_gemm_args_t &a, int *dev_status, cudaStream_t s) {
     p.acc_final = a.acc_final;
     p.s0 = a.b0_scale;
     p.s1 = a.b1_scale;
+    p.bscale = (!I8 && a.b0_scale) ? 1 : 0;
     p.inject_stall = (a.flags & DIT_GEMM_FLAG_INJECT_STALL) != 0;
     p.status = dev_status;
     p.qk = (a.qk_norm || a.rope_cos) ? 1 : 0;
@@ -846,7 +848,7 @@ dit_status_t launch_gemm(const dit_gemm_args_t &a, int *dev_status, cudaStream_t
     if (!a.a || !a.b0) return DIT_ERR_INVALID_ARG;
     if (!aligned16(a.a) || !aligned16(a.b0)) return DIT_ERR_ALIGN;
     if (!ld_ok(a.lda, a.K, 2) || !ld_ok(a.ldb, a.K, i8 ? 1 : 2)) return DIT_ERR_INVALID_ARG;
-    if (i8) {
+    if (i8 || a.b0_scale) {  // bf16 B may carry row scales too (expanded int8)
         if (!a.b0_scale || !aligned16(a.b0_scale)) return DIT_ERR_ALIGN;
         if (a.mode == DIT_EPI_SWIGLU && (!a.b1_scale || !aligned16(a.b1_scale)))
             return DIT_ERR_ALIGN;

@@ -22,6 +22,9 @@ struct dit_plan {
     size_t off_ug, off_uu, off_ud, off_udc;  // LoRA u of gate, up, down; down's carry
     uint8_t *ws;
     size_t ws_bytes;
+    // optional bf16 scratch for int8 weights expanded ahead of their GEMMs
+    uint8_t *wscratch = nullptr;
+    size_t wscratch_bytes = 0;
     // per-kernel timing (dit_block_profile_*)
     struct Rec {
         int kind;
@@ -66,6 +69,9 @@ dit_status_t launch_attention(const void *q, int64_t Tq, int64_t ldq, const void
 dit_status_t launch_final(const float *x, int64_t T, int D, const void *wf,
                           const float *wf_scale, const float *mod_f, float *out,
                           cudaStream_t s);
+
+// bf16 copy of n int8 values (exact); n % 16 == 0, both 16-byte aligned.
+dit_status_t launch_expand_int8(const void *q, int64_t n, void *out, cudaStream_t s);
 
 inline bool aligned16(const void *p) {
     return (reinterpret_cast<uintptr_t>(p) & 15u) == 0;

@@ -50,16 +50,17 @@ SYMBOLS = (
     "dit_block_profile_enable", "dit_block_profile_read",
     "dit_block_forward_static", "dit_block_plan_auto", "dit_block_forward_qk",
     "dit_block_forward_ex", "dit_block_plan_set_lora_rank", "dit_lora_prepare",
+    "dit_block_weight_scratch_bytes", "dit_block_bind_weight_scratch", "dit_int8_to_bf16",
 )
 
 STATIC_SCRATCH_BYTES = 64 << 20
 
 # Kernel kinds of the per-kernel timing record (DIT_K_*).
 KINDS = ("modln", "gemm_kv", "gemm_q", "attention", "gemm_o", "gemm_swiglu",
-         "gemm_down", "final", "lora_u")
+         "gemm_down", "final", "lora_u", "expand")
 # work unit of each kind: flops (tensor-core kinds) or bytes (memory-bound)
 KIND_UNITS = ("bytes", "flops", "flops", "flops", "flops", "flops", "flops",
-              "bytes", "flops")
+              "bytes", "flops", "bytes")
 
 
 class DitError(RuntimeError):
@@ -161,6 +162,9 @@ def _declare(lib):
                                          ctypes.POINTER(QkArgs), ctypes.POINTER(BlockLora),
                                          vp]),
         "dit_block_plan_set_lora_rank": (c_int, [vp, c_int]),
+        "dit_block_weight_scratch_bytes": (c_size, [vp]),
+        "dit_block_bind_weight_scratch": (c_int, [vp, vp, c_size]),
+        "dit_int8_to_bf16": (c_int, [vp, c_int64, vp, vp]),
         "dit_lora_prepare": (c_int, [vp, c_int64, c_int, c_int64, ctypes.c_float, vp, vp,
                                      c_int64, vp]),
     }
@@ -278,6 +282,21 @@ class BlockPlan:
                                                stream_handle(stream)),
                    "dit_block_forward_qk")
 
+    def weight_scratch_bytes(self) -> int:
+        return int(load().dit_block_weight_scratch_bytes(self._h))
+
+    def bind_weight_scratch(self, buf, nbytes: Optional[int] = None):
+        """Bind (or, with None, unbind) the int8 weight-expansion scratch."""
+        if buf is None:
+            _check(load().dit_block_bind_weight_scratch(self._h, None, 0),
+                   "dit_block_bind_weight_scratch")
+        else:
+            if nbytes is None:
+                nbytes = buf.numel() * buf.element_size()
+            _check(load().dit_block_bind_weight_scratch(self._h, ptr(buf), nbytes),
+                   "dit_block_bind_weight_scratch")
+        self._wscratch = buf
+
     def set_lora_rank(self, max_rank: int):
         """Reserve workspace for adapters of rank <= max_rank (before binding)."""
         _check(load().dit_block_plan_set_lora_rank(self._h, max_rank),
@@ -366,6 +385,11 @@ def block_lora(**adapters) -> BlockLora:
     for name, (a, b, rank) in adapters.items():
         setattr(bl, name, LoraArgs(ptr(a), ptr(b), rank))
     return bl
+
+
+def int8_to_bf16(q, n, out, stream=None):
+    _check(load().dit_int8_to_bf16(ptr(q), n, ptr(out), stream_handle(stream)),
+           "dit_int8_to_bf16")
 
 
 def modln_cast(x, rows, D, shift, scale, out, stream=None):

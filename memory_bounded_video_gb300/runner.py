@@ -101,11 +101,16 @@ class DitStack:
     layer's output when there is one."""
 
     def __init__(self, T, D, heads, F, mlp_chunk, attn_chunk, ffn_slice=0,
-                 device="cuda", lora_rank=0):
+                 device="cuda", lora_rank=0, weight_scratch=False):
         self.plan = ditstream.block_plan(T, D, heads, F, mlp_chunk, attn_chunk,
                                          ffn_slice)
         if lora_rank:
             self.plan.set_lora_rank(lora_rank)
+        self.weight_scratch = None
+        if weight_scratch:  # int8 weights expanded to bf16 ahead of the GEMMs
+            self.weight_scratch = torch.empty(self.plan.weight_scratch_bytes(),
+                                              dtype=torch.uint8, device=device)
+            self.plan.bind_weight_scratch(self.weight_scratch)
         self.T, self.D = T, D
         self.workspace = torch.empty(self.plan.workspace_bytes(),
                                      dtype=torch.uint8, device=device)

@@ -29,7 +29,7 @@ def header_functions():
 def header_defines():
     src = open(HEADER).read()
     return {k: int(v) for k, v in
-            re.findall(r"#define (DIT_\w+) \(?(-?\d+)\)?", src)}
+            re.findall(r"#define (DIT\w+) \(?(-?\d+)\)?", src)}
 
 
 def test_every_declared_symbol_is_exported(lib):
@@ -57,6 +57,7 @@ def test_binding_constants_match_header():
                  DIT_K_ATTENTION=ds.KINDS.index("attention"),
                  DIT_K_FINAL=ds.KINDS.index("final"),
                  DIT_K_LORA_U=ds.KINDS.index("lora_u"),
+                 DIT_K_EXPAND=ds.KINDS.index("expand"),
                  DIT_LORA_MAX_RANK=256,
                  DITSTREAM_ABI_VERSION=None)
     for k, v in pairs.items():
@@ -84,7 +85,7 @@ def test_struct_layouts_match_header():
 
 
 def test_status_strings(lib):
-    assert ds.abi_version() == 3
+    assert ds.abi_version() == header_defines()["DITSTREAM_ABI_VERSION"]
     for s in (0, -1, -2, -3, -4, -5, -6, -7, -8):
         assert ds.status_string(s) and ds.status_string(s) != "unknown status"
     assert ds.status_string(-99) == "unknown status"
@@ -218,6 +219,20 @@ def test_forward_ex_validates_adapters_before_launch(lib):
         with pytest.raises(ds.DitError) as e:
             p.forward(16, w, 16, lora=ds.block_lora(**kw))
         assert e.value.status == want, kw
+
+
+@pytest.mark.parametrize("D,F", [(256, 704), (3072, 8192), (1024, 1024)])
+def test_weight_scratch_size_and_binding(lib, D, F):
+    p = ds.block_plan(512, D, D // 64, F, 128, 128)
+    need = 2 * max(4 * D * D, 3 * D * F)
+    assert p.weight_scratch_bytes() == need
+    assert lib.dit_block_bind_weight_scratch(p.handle, 256 + 16, need) == ds.ERR_ALIGN
+    assert lib.dit_block_bind_weight_scratch(p.handle, 256, need - 1) == \
+        ds.ERR_WORKSPACE_TOO_SMALL
+    assert lib.dit_block_bind_weight_scratch(p.handle, 256, need) == ds.OK
+    assert lib.dit_block_bind_weight_scratch(p.handle, None, 0) == ds.OK  # unbind
+    assert lib.dit_int8_to_bf16(16, 24, 16, None) == ds.ERR_INVALID_ARG   # n % 16
+    assert lib.dit_int8_to_bf16(8, 32, 16, None) == ds.ERR_ALIGN
 
 
 def test_workspace_beyond_kv_floor_is_bounded_by_chunk():

@@ -161,3 +161,53 @@ def test_headline_stack_T32768_full_size():
     for x, out in results[1:]:
         assert torch.equal(x, results[0][0])
         assert torch.equal(out, results[0][1])
+
+
+# ---------------------------------------------------------------- weight scratch
+
+def test_int8_to_bf16_is_exact():
+    q = torch.arange(-128, 128, dtype=torch.int16).to(torch.int8).repeat(64)
+    out = torch.empty(q.numel(), dtype=torch.bfloat16, device="cuda")
+    ds.int8_to_bf16(q.cuda(), q.numel(), out)
+    torch.cuda.synchronize()
+    assert torch.equal(out.cpu().float(), q.float())
+
+
+def run_scratch(inp, cm, ca, fs, scratch, lora=None, rank=0, qk=None):
+    T, D = inp.x.shape
+    dev = runner.upload(inp)
+    stack = runner.DitStack(T, D, inp.meta["heads"], inp.meta["F"], cm, ca, fs,
+                            lora_rank=rank, weight_scratch=scratch)
+    dl = None if lora is None else [runner.upload_lora(lo, b)
+                                    for lo, b in zip(lora, dev.blocks)]
+    x = dev.x.clone()
+    out = stack.forward(x, dev, lora=dl, qk=None if qk is None else runner.upload_qk(qk))
+    stack.check()
+    return x, out
+
+
+@pytest.mark.parametrize("cm,ca,fs", [(0, 0, 0), (128, 256, 64), (384, 128, 0)])
+def test_weight_scratch_gives_the_same_bits(cm, ca, fs):
+    # int8 weights expanded to bf16 ahead of the GEMMs: same MMA operands,
+    # order and epilogue scale as the in-kernel conversion
+    inp = synth.make_inputs(1000, 256, 4, 704, seed=31, int8=True, jitter=True, blocks=2,
+                            final=True)
+    x0, o0 = run_scratch(inp, cm, ca, fs, False)
+    x1, o1 = run_scratch(inp, cm, ca, fs, True)
+    assert torch.equal(x0, x1) and torch.equal(o0, o1)
+
+
+def test_weight_scratch_with_lora_and_qk_gives_the_same_bits():
+    inp = synth.make_inputs(768, 1024, 8, 1024, seed=32, int8=True, jitter=True)
+    lora = [synth.make_lora(1024, 1024, 64, seed=3)]
+    qk = synth.make_qk(768, 128, seed=4, angles="axial")
+    x0, _ = run_scratch(inp, 256, 256, 512, False, lora, 64, qk)
+    x1, _ = run_scratch(inp, 256, 256, 512, True, lora, 64, qk)
+    assert torch.equal(x0, x1)
+
+
+def test_weight_scratch_full_size_block_T4096_D3072():
+    inp = synth.make_inputs(4096, 3072, 24, 8192, seed=33, int8=True, jitter=True)
+    x0, _ = run_scratch(inp, 2048, 2048, 0, False)
+    x1, _ = run_scratch(inp, 2048, 2048, 0, True)
+    assert torch.equal(x0, x1)
