@@ -68,6 +68,7 @@ struct GemmParams {
     const float *rope_cos, *rope_sin;  // [positions, head_dim / 2] or null
     int head_dim;
     float qk_eps;
+    int group_n;  // tile order: groups of group_n N-blocks, M-blocks within
     // LoRA: K-steps of U L^T after the main ones (two half stages each)
     int num_lk;
     int lora_on0, lora_on1;
@@ -100,6 +101,20 @@ struct Cfg {
     static constexpr int BAR_BYTES = 256;
     static constexpr int SMEM_BYTES = OFF_C + CSTAGES * C_BYTES + BAR_BYTES + 1024;
 };
+
+// Output tile of persistent work index t.  Tiles go in groups of group_n
+// N-blocks; within a group M-block by M-block, N fastest.  The CTAs in flight
+// then share the group's B tiles (kept to a size that stays in L2) and each
+// A row block; a group of all N-blocks is plain M-major order.
+DEV void tile_of(const GemmParams &p, int t, int &mb, int &nb) {
+    const int per_group = p.group_n * p.num_m;
+    const int g = t / per_group;
+    const int r = t - g * per_group;
+    const int n0 = g * p.group_n;
+    const int gw = min(p.group_n, p.num_n - n0);
+    mb = r / gw;
+    nb = n0 + (r - (r / gw) * gw);
+}
 
 // LoRA half h of output tile nb: whether it has work, and the first row of
 // its L tile (the tile's rows h*128.. for one B operand; SwiGLU: the tile's
@@ -471,7 +486,8 @@ __global__ void __launch_bounds__(Cfg<MODE, I8>::THREADS, 1)
             int64_t issued = 0;
             bool ok = true;
             for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
-                const int mb = t / p.num_n, nb = t % p.num_n;
+                int mb, nb;
+                tile_of(p, t, mb, nb);
                 for (int kb = 0; kb < p.num_k; ++kb) {
                     if (!mbar_wait(empty_bar(stage), ph ^ 1u, wc)) {
                         ok = false;
@@ -578,7 +594,8 @@ __global__ void __launch_bounds__(Cfg<MODE, I8>::THREADS, 1)
                     }
                 }
                 if (!ok) break;
-                const int nb = t % p.num_n;
+                int mb, nb;
+                tile_of(p, t, mb, nb);
                 for (int lk = 0; lk < p.num_lk && ok; ++lk) {
                     for (int h = 0; h < 2; ++h) {
                         if (!mbar_wait(full_bar(stage), ph, wc)) {
@@ -621,8 +638,9 @@ __global__ void __launch_bounds__(Cfg<MODE, I8>::THREADS, 1)
         uint32_t bph = 0;
         int t = blockIdx.x;
         if (preload && t < num_tiles) {
-            preload_tile<I8>(p, lane_base, int64_t(t / p.num_n) * kBM + q * 32 + lane,
-                             t % p.num_n);
+            int mb0, nb0;
+            tile_of(p, t, mb0, nb0);
+            preload_tile<I8>(p, lane_base, int64_t(mb0) * kBM + q * 32 + lane, nb0);
             tc_fence_before();
             mbar_arrive(tempty_bar(0));
         }
@@ -630,9 +648,10 @@ __global__ void __launch_bounds__(Cfg<MODE, I8>::THREADS, 1)
             if (preload) {
                 const int tn = t + gridDim.x;
                 if (tn < num_tiles) {
+                    int mbn, nbn;
+                    tile_of(p, tn, mbn, nbn);
                     preload_tile<I8>(p, lane_base + uint32_t((buf ^ 1) * C::ACC_COLS),
-                                     int64_t(tn / p.num_n) * kBM + q * 32 + lane,
-                                     tn % p.num_n);
+                                     int64_t(mbn) * kBM + q * 32 + lane, nbn);
                     tc_fence_before();
                     mbar_arrive(tempty_bar(buf ^ 1));
                 }
@@ -641,7 +660,8 @@ __global__ void __launch_bounds__(Cfg<MODE, I8>::THREADS, 1)
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
             tc_fence_after();
-            const int mb = t / p.num_n, nb = t % p.num_n;
+            int mb, nb;
+            tile_of(p, t, mb, nb);
             epilogue_tile<MODE, I8>(p, lane_base + uint32_t(buf * C::ACC_COLS),
                                     int64_t(mb) * kBM + q * 32 + lane, nb);
             if (!preload) {
@@ -784,6 +804,12 @@ dit_status_t run(const dit_gemm_args_t &a, int *dev_status, cudaStream_t s) {
     p.num_m = int((a.M + kBM - 1) / kBM);
     p.num_n = (a.N + C::BN - 1) / C::BN;
     p.num_k = a.K / kBK;
+    {  // N-blocks per tile group: the group's B tiles within ~48 MB of L2
+        const int64_t b_block = int64_t(C::NB) * C::BN * a.K * (I8 ? 1 : 2);
+        int64_t gn = (int64_t(48) << 20) / b_block;
+        if (gn < 1) gn = 1;
+        p.group_n = gn < p.num_n ? int(gn) : p.num_n;
+    }
     p.out = a.out;
     p.ldo = a.ldo;
     p.out2 = a.out2;

@@ -6,6 +6,11 @@
         --T 8192 --heads 4 --head-dim 128 --reps 3
     python -m memory_bounded_video_gb300.profile_case modln --M 8192 --D 3072
     python -m memory_bounded_video_gb300.profile_case final --M 8192 --D 3072
+    python -m memory_bounded_video_gb300.profile_case expand --M 8192 --D 3072
+
+``gemm --scaled`` runs the bf16 main loop on int8 values with per-row scales
+(the weight-scratch path); ``expand`` the int8 -> bf16 expansion of an
+[M, D] int8 matrix.
 
 Every launch goes through the C ABI; the inputs are random device tensors of
 the requested shapes (sized to exceed L2 where the case allows), the outputs
@@ -36,6 +41,13 @@ def gemm_case(a):
                            dtype=torch.int8)
         B1 = torch.randint(-127, 128, (N, K), device="cuda", generator=g,
                            dtype=torch.int8)
+        s0 = torch.full((N,), 0.02 / 127, device="cuda")
+        s1 = s0.clone()
+    elif a.scaled:
+        B0 = torch.randint(-127, 128, (N, K), device="cuda", generator=g,
+                           dtype=torch.int8).to(torch.bfloat16)
+        B1 = torch.randint(-127, 128, (N, K), device="cuda", generator=g,
+                           dtype=torch.int8).to(torch.bfloat16)
         s0 = torch.full((N,), 0.02 / 127, device="cuda")
         s1 = s0.clone()
     else:
@@ -92,11 +104,19 @@ def final_case(a):
     return (lambda: plan.final_forward(x, wf, None, mod_f, out)), 4 * a.M * a.D, keep
 
 
+def expand_case(a):
+    q = torch.randint(-127, 128, (a.M, a.D), device="cuda", dtype=torch.int8)
+    out = torch.empty(a.M, a.D, device="cuda", dtype=torch.bfloat16)
+    keep = (q, out)
+    return (lambda: ds.int8_to_bf16(q, a.M * a.D, out)), 3 * a.M * a.D, keep
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
-    ap.add_argument("kernel", choices=("gemm", "attention", "modln", "final"))
+    ap.add_argument("kernel", choices=("gemm", "attention", "modln", "final", "expand"))
     ap.add_argument("--mode", default="store_bf16", choices=sorted(MODES))
     ap.add_argument("--int8", action="store_true")
+    ap.add_argument("--scaled", action="store_true")
     ap.add_argument("--M", type=int, default=2048)
     ap.add_argument("--N", type=int, default=3072)
     ap.add_argument("--K", type=int, default=3072)
@@ -110,7 +130,8 @@ def main(argv=None):
     dbuild.build()
     ds.load()
     fn, work, keep = {"gemm": gemm_case, "attention": attention_case,
-                      "modln": modln_case, "final": final_case}[a.kernel](a)
+                      "modln": modln_case, "final": final_case,
+                      "expand": expand_case}[a.kernel](a)
     fn()
     torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
@@ -121,7 +142,7 @@ def main(argv=None):
     e1.record()
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / a.reps
-    unit = "GB/s" if a.kernel in ("modln", "final") else "TFLOP/s"
+    unit = "GB/s" if a.kernel in ("modln", "final", "expand") else "TFLOP/s"
     rate = work / (ms / 1e3) / (1e9 if unit == "GB/s" else 1e12)
     print(f"{a.kernel}: {ms:.4f} ms per launch, {rate:.1f} {unit}")
     del keep
