@@ -52,7 +52,7 @@
 extern "C" {
 #endif
 
-#define DITSTREAM_ABI_VERSION 4
+#define DITSTREAM_ABI_VERSION 5
 
 #if defined(__GNUC__)
 #define DIT_API __attribute__((visibility("default")))
@@ -170,6 +170,39 @@ DIT_API size_t dit_block_workspace_bytes(const dit_plan_t *plan);
  * DIT_ERR_WORKSPACE_TOO_SMALL, DIT_ERR_UNSUPPORTED_ARCH, DIT_ERR_CUDA. */
 DIT_API dit_status_t dit_block_bind_workspace(dit_plan_t *plan, void *dev_ptr,
                                       size_t bytes);
+
+/* K/V offload below the K/V floor.  "LayerStream: H3 Chunking" ("Where
+ * people get burned"): K and V of the whole sequence stay resident, a floor
+ * that chunking cannot go under; only K/V offload can.  With
+ * key_block_tokens > 0 (a multiple of 128) K [T, D] and V^T [D, T_pad] of
+ * all tokens live in caller-owned pinned host memory instead of the device
+ * workspace:
+ *   - pass one's K/V projection writes them there directly (the buffer is
+ *     mapped into the device's address space);
+ *   - pass two streams them back, per query slab, in blocks of
+ *     key_block_tokens keys through a two-slot device ring (copies on the
+ *     plan's own copy stream, one block ahead of the attention), and the
+ *     attention carries its running max, sum and fp32 output from block to
+ *     block in the workspace.
+ * Key tiles are visited in the same order with the same arithmetic, so the
+ * output bits equal the resident schedule's.  The workspace then holds the
+ * ring (2 x 4 * key_block_tokens * D bytes) and the carried state
+ * (4 * C_a * D + 8 * C_a * heads bytes) instead of 4 * T * D, so it no longer
+ * grows with T.
+ * dit_block_plan_set_kv_offload: before a workspace is bound (else
+ * DIT_ERR_INVALID_ARG); 0 turns it off (the default).
+ * dit_block_kv_host_bytes: bytes of the host buffer (2 T D + 2 D T_pad).
+ * dit_block_bind_kv_host: bind the host buffer (allocated with
+ * cudaHostAlloc or registered with cudaHostRegister, so that the device can
+ * address it; 16-byte aligned, >= dit_block_kv_host_bytes) and create the
+ * plan's copy stream and events on the current device (released by
+ * dit_block_plan_destroy).  Errors: DIT_ERR_INVALID_ARG,
+ * DIT_ERR_ALIGN, DIT_ERR_WORKSPACE_TOO_SMALL, DIT_ERR_CUDA (the buffer is not
+ * mapped for the device).  A forward of an offloading plan without a bound
+ * host buffer returns DIT_ERR_NO_WORKSPACE. */
+DIT_API dit_status_t dit_block_plan_set_kv_offload(dit_plan_t *plan, int key_block_tokens);
+DIT_API size_t dit_block_kv_host_bytes(const dit_plan_t *plan);
+DIT_API dit_status_t dit_block_bind_kv_host(dit_plan_t *plan, void *host_ptr, size_t bytes);
 
 /* Optional weight scratch for int8 blocks.  An int8 weight value q
  * (|q| <= 127) is exact in bf16, so with a scratch bound the forward expands
@@ -462,6 +495,23 @@ typedef struct {
 
 DIT_API dit_status_t dit_gemm(const dit_gemm_args_t *args, int *dev_status,
                       dit_stream_t stream);
+
+/* dit_attention over one block of a longer key sequence (keys k0 .. k0 +
+ * T_block - 1 of it, k and vt pointing at that block), carrying the softmax
+ * state between the blocks, which must be passed in ascending key order:
+ * o_state fp32 [Tq, H*d] (row stride ld_state, a multiple of 4), m_state and
+ * l_state fp32 [Tq, H] hold the running max, sum and unnormalised output.
+ * first != 0: the state is started here; last != 0: the output is
+ * normalised into o (bf16), else the state is written back.  Every block but
+ * the last holds a multiple of 128 keys.  The result equals one dit_attention
+ * call over all the keys bit for bit. */
+DIT_API dit_status_t dit_attention_part(const void *q, int64_t Tq, int64_t ldq,
+                                        const void *k, int64_t ldk, const void *vt,
+                                        int64_t ldvt, int64_t T_block, int heads,
+                                        int head_dim, void *o, int64_t ldo, float *o_state,
+                                        float *m_state, float *l_state, int64_t ld_state,
+                                        int first, int last, int *dev_status,
+                                        dit_stream_t stream);
 
 /* out[i] = bf16(q[i]) for n int8 values q (exact: |q| <= 127 needs 8 bits).
  * n % 16 == 0; q, out 16-byte aligned.  The weight scratch's expansion. */

@@ -160,9 +160,17 @@ void layout(dit_plan *p) {
     const size_t A = 1024;
     const size_t Dz = size_t(p->D);
     const size_t R = size_t(p->lora_r);
-    p->off_k = A;  // [0, 256): device status words
-    p->off_vt = round_up(p->off_k + 2 * size_t(p->T) * Dz, A);
-    const size_t phase = round_up(p->off_vt + 2 * Dz * size_t(p->t_pad), A);
+    size_t phase;
+    if (p->kvb) {  // K/V in host memory: a two-slot ring of key blocks
+        p->off_k = p->off_vt = 0;
+        p->off_ring = A;  // [0, 256): device status words
+        p->ring_slot = round_up(4 * size_t(p->kvb) * Dz, A);
+        phase = p->off_ring + 2 * p->ring_slot;
+    } else {
+        p->off_k = A;  // [0, 256): device status words
+        p->off_vt = round_up(p->off_k + 2 * size_t(p->T) * Dz, A);
+        phase = round_up(p->off_vt + 2 * Dz * size_t(p->t_pad), A);
+    }
     // attention phase: a_s / O_s share one region (a_s is dead once Q_s exists)
     p->off_a = phase;
     p->off_q = round_up(p->off_a + 2 * size_t(p->ca) * Dz, A);
@@ -170,6 +178,12 @@ void layout(dit_plan *p) {
     p->off_uq = attn_end;
     p->off_uo = round_up(p->off_uq + 2 * size_t(p->ca) * R, A);
     if (R) attn_end = round_up(p->off_uo + 2 * size_t(p->ca) * R, A);
+    if (p->kvb) {  // carried attention state: O fp32 [C_a, D], m and l [C_a, H]
+        p->off_ost = attn_end;
+        p->off_mst = round_up(p->off_ost + 4 * size_t(p->ca) * Dz, A);
+        p->off_lst = round_up(p->off_mst + 4 * size_t(p->ca) * size_t(p->heads), A);
+        attn_end = round_up(p->off_lst + 4 * size_t(p->ca) * size_t(p->heads), A);
+    }
     // MLP phase (aliases the attention phase: the two never overlap in time)
     p->off_b = phase;
     p->off_h = round_up(p->off_b + 2 * size_t(p->cm) * Dz, A);
@@ -207,6 +221,41 @@ dit_status_t dit_block_bind_weight_scratch(dit_plan_t *p, void *dev_ptr, size_t 
     if (bytes < dit_block_weight_scratch_bytes(p)) return DIT_ERR_WORKSPACE_TOO_SMALL;
     p->wscratch = static_cast<uint8_t *>(dev_ptr);
     p->wscratch_bytes = bytes;
+    return DIT_OK;
+}
+
+dit_status_t dit_block_plan_set_kv_offload(dit_plan_t *p, int key_block_tokens) {
+    if (!p || p->ws) return DIT_ERR_INVALID_ARG;
+    if (key_block_tokens < 0) return DIT_ERR_INVALID_ARG;
+    if (key_block_tokens % 128) return DIT_ERR_CHUNK_ALIGN;
+    p->kvb = key_block_tokens;
+    layout(p);
+    return DIT_OK;
+}
+
+size_t dit_block_kv_host_bytes(const dit_plan_t *p) {
+    if (!p) return 0;
+    return 2 * size_t(p->T) * size_t(p->D) + 2 * size_t(p->D) * size_t(p->t_pad);
+}
+
+dit_status_t dit_block_bind_kv_host(dit_plan_t *p, void *host_ptr, size_t bytes) {
+    if (!p || !host_ptr) return DIT_ERR_INVALID_ARG;
+    if (!aligned16(host_ptr)) return DIT_ERR_ALIGN;
+    if (bytes < dit_block_kv_host_bytes(p)) return DIT_ERR_WORKSPACE_TOO_SMALL;
+    void *dev = nullptr;
+    cudaError_t e = cudaHostGetDevicePointer(&dev, host_ptr, 0);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (!p->copy_stream) {
+        e = cudaStreamCreateWithFlags(&p->copy_stream, cudaStreamNonBlocking);
+        for (int i = 0; i < 2 && e == cudaSuccess; ++i) {
+            e = cudaEventCreateWithFlags(&p->ev_filled[i], cudaEventDisableTiming);
+            if (e == cudaSuccess) e = cudaEventCreateWithFlags(&p->ev_used[i], cudaEventDisableTiming);
+        }
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&p->ev_pass1, cudaEventDisableTiming);
+        if (e != cudaSuccess) return cuda_fail(e);
+    }
+    p->kv_host = static_cast<uint8_t *>(dev);
+    p->kv_host_bytes = bytes;
     return DIT_OK;
 }
 
@@ -317,6 +366,10 @@ dit_status_t dit_block_plan(int64_t T, int D, int heads, int ffn, int mlp_chunk_
 void dit_block_plan_destroy(dit_plan_t *plan) {
     if (!plan) return;
     for (cudaEvent_t e : plan->pool) cudaEventDestroy(e);
+    for (cudaEvent_t e : {plan->ev_filled[0], plan->ev_filled[1], plan->ev_used[0],
+                          plan->ev_used[1], plan->ev_pass1})
+        if (e) cudaEventDestroy(e);
+    if (plan->copy_stream) cudaStreamDestroy(plan->copy_stream);
     delete plan;
 }
 
@@ -417,7 +470,7 @@ dit_status_t dit_block_forward_ex(const dit_plan_t *cp, float *x, const dit_bloc
             if (!aligned16(l->a) || !aligned16(l->b)) return DIT_ERR_ALIGN;
         }
     }
-    if (!p->ws) return DIT_ERR_NO_WORKSPACE;
+    if (!p->ws || (p->kvb && !p->kv_host)) return DIT_ERR_NO_WORKSPACE;
     if (!w->wqkv || !w->wo || !w->wgate || !w->wup || !w->wdown) return DIT_ERR_INVALID_ARG;
     if (!aligned16(x) || !aligned16(mod) || !aligned16(w->wqkv) || !aligned16(w->wo) ||
         !aligned16(w->wgate) || !aligned16(w->wup) || !aligned16(w->wdown))
@@ -443,8 +496,11 @@ dit_status_t dit_block_forward_ex(const dit_plan_t *cp, float *x, const dit_bloc
     const int D = p->D, F = p->F;
     const int64_t Dl = D;
     int *status = reinterpret_cast<int *>(p->ws);
-    void *K = p->ws + p->off_k;
-    void *Vt = p->ws + p->off_vt;
+    // K [T, D] and V^T [D, T_pad]: in the workspace, or (offload) in the
+    // host buffer, written there by pass one through its device mapping
+    void *K = p->kvb ? static_cast<void *>(p->kv_host) : static_cast<void *>(p->ws + p->off_k);
+    void *Vt = p->kvb ? static_cast<void *>(p->kv_host + 2 * size_t(T) * size_t(D))
+                      : static_cast<void *>(p->ws + p->off_vt);
     void *a = p->ws + p->off_a;
     void *Q = p->ws + p->off_q;
     void *b = p->ws + p->off_b;
@@ -572,6 +628,37 @@ dit_status_t dit_block_forward_ex(const dit_plan_t *cp, float *x, const dit_bloc
                        [&] { return launch_gemm(g, status, st); })) != DIT_OK)
             return r;
     }
+    // K/V offload: key blocks come back through the two ring slots, copied
+    // one block ahead of the attention on the plan's copy stream
+    const int64_t kvb = p->kvb;
+    const int64_t n_kb = kvb ? (T + kvb - 1) / kvb : 0;
+    const int64_t n_total = kvb ? n_kb * ((T + p->ca - 1) / p->ca) : 0;
+    cudaStream_t cs = p->copy_stream;
+    auto slot_k = [&](int slot) { return p->ws + p->off_ring + size_t(slot) * p->ring_slot; };
+    auto slot_vt = [&](int slot) { return slot_k(slot) + 2 * size_t(kvb) * size_t(D); };
+    auto fetch = [&](int64_t c) -> dit_status_t {  // c-th block of pass two
+        const int slot = int(c & 1);
+        const int64_t k0 = (c % n_kb) * kvb;
+        const int64_t kb = (T - k0 < kvb) ? T - k0 : kvb;
+        cudaError_t e = cudaStreamWaitEvent(cs, p->ev_used[slot], 0);
+        if (e == cudaSuccess)
+            e = cudaMemcpyAsync(slot_k(slot), static_cast<const uint8_t *>(K) + 2 * k0 * Dl,
+                                size_t(2 * kb * Dl), cudaMemcpyHostToDevice, cs);
+        if (e == cudaSuccess)
+            e = cudaMemcpy2DAsync(slot_vt(slot), size_t(2 * kvb),
+                                  static_cast<const uint8_t *>(Vt) + 2 * k0, size_t(2 * p->t_pad),
+                                  size_t(2 * kb), size_t(D), cudaMemcpyHostToDevice, cs);
+        if (e == cudaSuccess) e = cudaEventRecord(p->ev_filled[slot], cs);
+        return e == cudaSuccess ? DIT_OK : cuda_fail(e);
+    };
+    int64_t kv_c = 0;  // blocks of pass two consumed so far
+    if (kvb) {
+        // the host copies of K/V are complete once pass one's GEMMs are
+        cudaError_t e = cudaEventRecord(p->ev_pass1, st);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(cs, p->ev_pass1, 0);
+        if (e != cudaSuccess) return cuda_fail(e);
+        if ((r = fetch(0)) != DIT_OK) return r;
+    }
     // pass 2: Q per slab, attention against all keys, O-projection into x
     for (int64_t s = 0; s < T; s += p->ca) {
         const int64_t rows = (T - s < p->ca) ? T - s : p->ca;
@@ -601,11 +688,33 @@ dit_status_t dit_block_forward_ex(const dit_plan_t *cp, float *x, const dit_bloc
                        [&] { return launch_gemm(g, status, st); })) != DIT_OK)
             return r;
         // O_s overwrites a_s (dead once Q_s exists)
-        if ((r = timed(p, st, DIT_K_ATTENTION, 4.0 * rows * double(T) * D, [&] {
-                 return launch_attention(Q, rows, D, K, D, Vt, p->t_pad, T, p->heads,
-                                         p->head_dim, a, D, status, st);
-             })) != DIT_OK)
-            return r;
+        if (!kvb) {
+            if ((r = timed(p, st, DIT_K_ATTENTION, 4.0 * rows * double(T) * D, [&] {
+                     return launch_attention(Q, rows, D, K, D, Vt, p->t_pad, T, p->heads,
+                                             p->head_dim, a, D, status, st);
+                 })) != DIT_OK)
+                return r;
+        } else {
+            for (int64_t b = 0; b < n_kb; ++b, ++kv_c) {
+                if (kv_c + 1 < n_total && (r = fetch(kv_c + 1)) != DIT_OK) return r;
+                const int slot = int(kv_c & 1);
+                const int64_t kb = (T - b * kvb < kvb) ? T - b * kvb : kvb;
+                cudaError_t e = cudaStreamWaitEvent(st, p->ev_filled[slot], 0);
+                if (e != cudaSuccess) return cuda_fail(e);
+                AttnState as{reinterpret_cast<float *>(p->ws + p->off_ost),
+                             reinterpret_cast<float *>(p->ws + p->off_mst),
+                             reinterpret_cast<float *>(p->ws + p->off_lst), Dl, b == 0,
+                             b == n_kb - 1};
+                if ((r = timed(p, st, DIT_K_ATTENTION, 4.0 * rows * double(kb) * D, [&] {
+                         return launch_attention(Q, rows, D, slot_k(slot), D, slot_vt(slot),
+                                                 kvb, kb, p->heads, p->head_dim, a, D, status,
+                                                 st, &as);
+                     })) != DIT_OK)
+                    return r;
+                e = cudaEventRecord(p->ev_used[slot], st);
+                if (e != cudaSuccess) return cuda_fail(e);
+            }
+        }
         if (on(l_o) && (r = lora_u(a, D, rows, D, l_o, 0, D, u_o, nullptr, 0, 1)) != DIT_OK)
             return r;
         dit_gemm_args_t o{};
@@ -743,6 +852,16 @@ dit_status_t dit_modln_cast(const float *x, int64_t rows, int D, const float *sh
 dit_status_t dit_gemm(const dit_gemm_args_t *args, int *dev_status, dit_stream_t stream) {
     if (!args) return DIT_ERR_INVALID_ARG;
     return launch_gemm(*args, dev_status, static_cast<cudaStream_t>(stream));
+}
+
+dit_status_t dit_attention_part(const void *q, int64_t Tq, int64_t ldq, const void *k,
+                                int64_t ldk, const void *vt, int64_t ldvt, int64_t T_block,
+                                int heads, int head_dim, void *o, int64_t ldo, float *o_state,
+                                float *m_state, float *l_state, int64_t ld_state, int first,
+                                int last, int *dev_status, dit_stream_t stream) {
+    AttnState as{o_state, m_state, l_state, ld_state, first != 0, last != 0};
+    return launch_attention(q, Tq, ldq, k, ldk, vt, ldvt, T_block, heads, head_dim, o, ldo,
+                            dev_status, static_cast<cudaStream_t>(stream), &as);
 }
 
 dit_status_t dit_attention(const void *q, int64_t Tq, int64_t ldq, const void *k, int64_t ldk,

@@ -60,6 +60,15 @@ struct AttnParams {
     __nv_bfloat16 *o;
     int64_t ldo;
     int *status;
+    // Keys in several launches (a block each, in ascending order): the
+    // running max m, sum l and unnormalised fp32 O of every (query, head)
+    // carried between them.  first: no state yet; last: normalise and store
+    // O.  One launch over all keys is first = last = 1.
+    float *o_state;           // [Tq, H*HD], row stride ld_state
+    float *m_state, *l_state; // [Tq, H]
+    int64_t ld_state;
+    int heads;
+    int first, last;
 };
 
 DEV float ex2(float x) {
@@ -265,7 +274,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int kk = 0; kk < kBKV / 16; ++kk) {
                     const uint32_t offv = (kk >> 2) * (HD * 128) + (kk & 3) * 32;
                     mma_bf16_ts(d, pt + uint32_t(8 * kk), desc_sw128(vb + offv), ID_PV,
-                                (j > 0 || kk > 0) ? 1u : 0u);
+                                (j > 0 || kk > 0 || !p.first) ? 1u : 0u);
                 }
             };
             bool ok = mbar_wait(bar(B_Q), 0, wc) && ring_wait(0);
@@ -322,7 +331,31 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t oaddr = lane_base + uint32_t(C::COL_O + x * HD);
         const float sl2 = p.scale_log2;
         const int last_valid = int(p.T - int64_t(n_kv - 1) * kBKV);  // keys in last tile
+        const int64_t qrow = (2 * int64_t(qpair) + x) * kBQ + row;
         float m = -INFINITY, l = 0.f;
+        if (!p.first) {
+            // carried state of the earlier key blocks: m, l and O (into TMEM,
+            // before this tile's first PV MMA, which accumulates onto it)
+            const bool valid = qrow < p.Tq;
+            m = valid ? p.m_state[qrow * p.heads + head] : 0.f;
+            l = valid ? p.l_state[qrow * p.heads + head] : 0.f;
+            const float4 *src = reinterpret_cast<const float4 *>(
+                p.o_state + qrow * p.ld_state + int64_t(head) * HD);
+#pragma unroll
+            for (int c0 = 0; c0 < HD; c0 += 32) {
+                uint32_t r[32];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const float4 v = valid ? src[(c0 >> 2) + i] : make_float4(0.f, 0.f, 0.f, 0.f);
+                    r[4 * i] = __float_as_uint(v.x);
+                    r[4 * i + 1] = __float_as_uint(v.y);
+                    r[4 * i + 2] = __float_as_uint(v.z);
+                    r[4 * i + 3] = __float_as_uint(v.w);
+                }
+                __syncwarp();
+                tmem_st32_sync(oaddr + c0, r);
+            }
+        }
         bool ok = true;
         for (int j = 0; j < n_kv; ++j) {
             bool w = mbar_wait(bar(B_SF + x), uint32_t(j & 1), wc);
@@ -336,7 +369,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float mx =
                 (masked ? tile_max<true>(saddr, last_valid) : tile_max<false>(saddr, kBKV)) *
                 sl2;
-            if (j == 0) {
+            if (j == 0 && p.first) {  // no reference max yet: the tile's own
                 m = mx;
             } else if (__any_sync(0xffffffffu, mx > m + kRescaleLog2)) {
                 // Move the reference max of the rows that need it: O_row *=
@@ -370,8 +403,31 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool w = mbar_wait(bar(B_O), 0, wc);
             ok = __all_sync(0xffffffffu, w);
         }
-        const int64_t qrow = (2 * int64_t(qpair) + x) * kBQ + row;
-        if (ok) {
+        if (ok && !p.last) {
+            // hand the state to the next key block's launch
+            tc_fence_after();
+            if (qrow < p.Tq) {
+                p.m_state[qrow * p.heads + head] = m;
+                p.l_state[qrow * p.heads + head] = l;
+            }
+            float4 *dst = reinterpret_cast<float4 *>(p.o_state + qrow * p.ld_state +
+                                                     int64_t(head) * HD);
+#pragma unroll
+            for (int c0 = 0; c0 < HD; c0 += 32) {
+                uint32_t r[32];
+                __syncwarp();
+                tmem_ld32(oaddr + c0, r);
+                tmem_ld_wait(r);
+                if (qrow < p.Tq) {
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        dst[(c0 >> 2) + i] =
+                            make_float4(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]),
+                                        __uint_as_float(r[4 * i + 2]),
+                                        __uint_as_float(r[4 * i + 3]));
+                }
+            }
+        } else if (ok) {
             tc_fence_after();
             const float inv = 1.0f / l;
             uint4 *dst = reinterpret_cast<uint4 *>(p.o + qrow * p.ldo + int64_t(head) * HD);
@@ -411,7 +467,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int HD>
 dit_status_t run(const void *q, int64_t Tq, int64_t ldq, const void *k, int64_t ldk,
                  const void *vt, int64_t ldvt, int64_t T, int heads, void *o, int64_t ldo,
-                 int *dev_status, cudaStream_t s) {
+                 const AttnState *state, int *dev_status, cudaStream_t s) {
     using C = ACfg<HD>;
     const uint64_t D = uint64_t(heads) * HD;
     const CUtensorMapDataType bf16 = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
@@ -428,6 +484,16 @@ dit_status_t run(const void *q, int64_t Tq, int64_t ldq, const void *k, int64_t 
     p.o = reinterpret_cast<__nv_bfloat16 *>(o);
     p.ldo = ldo;
     p.status = dev_status;
+    p.heads = heads;
+    p.first = p.last = 1;
+    if (state) {
+        p.o_state = state->o;
+        p.m_state = state->m;
+        p.l_state = state->l;
+        p.ld_state = state->ld;
+        p.first = state->first;
+        p.last = state->last;
+    }
     static bool attr_done = false;
     if (!attr_done) {
         cudaError_t e = cudaFuncSetAttribute(
@@ -446,7 +512,7 @@ dit_status_t run(const void *q, int64_t Tq, int64_t ldq, const void *k, int64_t 
 dit_status_t launch_attention(const void *q, int64_t Tq, int64_t ldq, const void *k,
                               int64_t ldk, const void *vt, int64_t ldvt, int64_t T,
                               int heads, int head_dim, void *o, int64_t ldo, int *dev_status,
-                              cudaStream_t s) {
+                              cudaStream_t s, const AttnState *state) {
     if (Tq < 0 || T <= 0 || heads <= 0 || (head_dim != 64 && head_dim != 128))
         return DIT_ERR_INVALID_ARG;
     if (!q || !k || !vt || !o) return DIT_ERR_INVALID_ARG;
@@ -456,10 +522,15 @@ dit_status_t launch_attention(const void *q, int64_t Tq, int64_t ldq, const void
     if (ldq % 8 || ldk % 8 || ldo % 8 || ldvt % 8) return DIT_ERR_INVALID_ARG;
     if (Tq > (int64_t(1) << 31) - 2 * kBQ || T > (int64_t(1) << 31) - kBKV || heads > 65535)
         return DIT_ERR_INVALID_ARG;
+    if (state) {
+        if (!state->o || !state->m || !state->l) return DIT_ERR_INVALID_ARG;
+        if (!aligned16(state->o) || state->ld < D || state->ld % 4) return DIT_ERR_ALIGN;
+        if (T % kBKV && !state->last) return DIT_ERR_INVALID_ARG;  // only the last block ragged
+    }
     if (Tq == 0) return DIT_OK;
     if (head_dim == 64)
-        return run<64>(q, Tq, ldq, k, ldk, vt, ldvt, T, heads, o, ldo, dev_status, s);
-    return run<128>(q, Tq, ldq, k, ldk, vt, ldvt, T, heads, o, ldo, dev_status, s);
+        return run<64>(q, Tq, ldq, k, ldk, vt, ldvt, T, heads, o, ldo, state, dev_status, s);
+    return run<128>(q, Tq, ldq, k, ldk, vt, ldvt, T, heads, o, ldo, state, dev_status, s);
 }
 
 }  // namespace ds

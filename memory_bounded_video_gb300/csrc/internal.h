@@ -25,6 +25,17 @@ struct dit_plan {
     // optional bf16 scratch for int8 weights expanded ahead of their GEMMs
     uint8_t *wscratch = nullptr;
     size_t wscratch_bytes = 0;
+    // K/V offload: key block size (0: K/V resident), the device ring and the
+    // carried attention state in the workspace, the host K/V buffer and the
+    // copy stream with its events (slot filled / slot used)
+    int kvb = 0;
+    size_t off_ring = 0, ring_slot = 0, off_ost = 0, off_mst = 0, off_lst = 0;
+    uint8_t *kv_host = nullptr;      // device address of the pinned host buffer
+    size_t kv_host_bytes = 0;
+    cudaStream_t copy_stream = nullptr;
+    cudaEvent_t ev_filled[2] = {nullptr, nullptr};
+    cudaEvent_t ev_used[2] = {nullptr, nullptr};
+    cudaEvent_t ev_pass1 = nullptr;
     // per-kernel timing (dit_block_profile_*)
     struct Rec {
         int kind;
@@ -61,10 +72,19 @@ dit_status_t launch_modln(const float *x, int64_t rows, int D, const float *shif
 
 dit_status_t launch_gemm(const dit_gemm_args_t &a, int *dev_status, cudaStream_t s);
 
+// Carried softmax state for attention over keys in several launches.
+struct AttnState {
+    float *o;        // unnormalised fp32 O [Tq, H*d], row stride ld
+    float *m, *l;    // running max and sum [Tq, H]
+    int64_t ld;
+    int first, last; // this launch has the first / last key block
+};
+
 dit_status_t launch_attention(const void *q, int64_t Tq, int64_t ldq, const void *k,
                               int64_t ldk, const void *vt, int64_t ldvt, int64_t T,
                               int heads, int head_dim, void *o, int64_t ldo,
-                              int *dev_status, cudaStream_t s);
+                              int *dev_status, cudaStream_t s,
+                              const AttnState *state = nullptr);
 
 dit_status_t launch_final(const float *x, int64_t T, int D, const void *wf,
                           const float *wf_scale, const float *mod_f, float *out,

@@ -51,6 +51,8 @@ SYMBOLS = (
     "dit_block_forward_static", "dit_block_plan_auto", "dit_block_forward_qk",
     "dit_block_forward_ex", "dit_block_plan_set_lora_rank", "dit_lora_prepare",
     "dit_block_weight_scratch_bytes", "dit_block_bind_weight_scratch", "dit_int8_to_bf16",
+    "dit_block_plan_set_kv_offload", "dit_block_kv_host_bytes", "dit_block_bind_kv_host",
+    "dit_attention_part",
 )
 
 STATIC_SCRATCH_BYTES = 64 << 20
@@ -165,6 +167,12 @@ def _declare(lib):
         "dit_block_weight_scratch_bytes": (c_size, [vp]),
         "dit_block_bind_weight_scratch": (c_int, [vp, vp, c_size]),
         "dit_int8_to_bf16": (c_int, [vp, c_int64, vp, vp]),
+        "dit_block_plan_set_kv_offload": (c_int, [vp, c_int]),
+        "dit_block_kv_host_bytes": (c_size, [vp]),
+        "dit_block_bind_kv_host": (c_int, [vp, vp, c_size]),
+        "dit_attention_part": (c_int, [vp, c_int64, c_int64, vp, c_int64, vp, c_int64,
+                                       c_int64, c_int, c_int, vp, c_int64, vp, vp, vp,
+                                       c_int64, c_int, c_int, vp, vp]),
         "dit_lora_prepare": (c_int, [vp, c_int64, c_int, c_int64, ctypes.c_float, vp, vp,
                                      c_int64, vp]),
     }
@@ -297,6 +305,23 @@ class BlockPlan:
                    "dit_block_bind_weight_scratch")
         self._wscratch = buf
 
+    def set_kv_offload(self, key_block_tokens: int):
+        """K/V of all tokens in pinned host memory, streamed back in key
+        blocks (before binding a workspace)."""
+        _check(load().dit_block_plan_set_kv_offload(self._h, key_block_tokens),
+               "dit_block_plan_set_kv_offload")
+
+    def kv_host_bytes(self) -> int:
+        return int(load().dit_block_kv_host_bytes(self._h))
+
+    def bind_kv_host(self, buf, nbytes: Optional[int] = None):
+        """Bind a pinned host buffer (e.g. ``torch.empty(..., pin_memory=True)``)."""
+        if nbytes is None:
+            nbytes = buf.numel() * buf.element_size()
+        _check(load().dit_block_bind_kv_host(self._h, ptr(buf), nbytes),
+               "dit_block_bind_kv_host")
+        self._kv_host = buf
+
     def set_lora_rank(self, max_rank: int):
         """Reserve workspace for adapters of rank <= max_rank (before binding)."""
         _check(load().dit_block_plan_set_lora_rank(self._h, max_rank),
@@ -385,6 +410,16 @@ def block_lora(**adapters) -> BlockLora:
     for name, (a, b, rank) in adapters.items():
         setattr(bl, name, LoraArgs(ptr(a), ptr(b), rank))
     return bl
+
+
+def attention_part(q, Tq, ldq, k, ldk, vt, ldvt, T_block, heads, head_dim, o, ldo,
+                   o_state, m_state, l_state, ld_state, first, last, dev_status=None,
+                   stream=None):
+    _check(load().dit_attention_part(ptr(q), Tq, ldq, ptr(k), ldk, ptr(vt), ldvt, T_block,
+                                     heads, head_dim, ptr(o), ldo, ptr(o_state),
+                                     ptr(m_state), ptr(l_state), ld_state, int(first),
+                                     int(last), ptr(dev_status), stream_handle(stream)),
+           "dit_attention_part")
 
 
 def int8_to_bf16(q, n, out, stream=None):

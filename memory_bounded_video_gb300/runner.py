@@ -101,11 +101,17 @@ class DitStack:
     layer's output when there is one."""
 
     def __init__(self, T, D, heads, F, mlp_chunk, attn_chunk, ffn_slice=0,
-                 device="cuda", lora_rank=0, weight_scratch=False):
+                 device="cuda", lora_rank=0, weight_scratch=False, kv_offload=0):
         self.plan = ditstream.block_plan(T, D, heads, F, mlp_chunk, attn_chunk,
                                          ffn_slice)
         if lora_rank:
             self.plan.set_lora_rank(lora_rank)
+        self.kv_host = None
+        if kv_offload:  # K/V of all tokens in pinned host memory
+            self.plan.set_kv_offload(kv_offload)
+            self.kv_host = torch.empty(self.plan.kv_host_bytes(), dtype=torch.uint8,
+                                       pin_memory=True)
+            self.plan.bind_kv_host(self.kv_host)
         self.weight_scratch = None
         if weight_scratch:  # int8 weights expanded to bf16 ahead of the GEMMs
             self.weight_scratch = torch.empty(self.plan.weight_scratch_bytes(),

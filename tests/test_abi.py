@@ -119,6 +119,21 @@ def rup(v, a=1024):
     return (v + a - 1) // a * a
 
 
+def expected_workspace_offload(T, D, H, F, cm, ca, fs, kvb):
+    """dit_block_workspace_bytes with K/V offload: the two ring slots and the
+    carried attention state replace K and V^T."""
+    cm = T if cm == 0 or cm >= T else cm
+    ca = T if ca == 0 or ca >= T else ca
+    fs = fs or F
+    phase = 1024 + 2 * rup(4 * kvb * D)
+    attn = rup(rup(phase + 2 * ca * D) + 2 * ca * D)
+    attn = rup(rup(rup(attn + 4 * ca * D) + 4 * ca * H) + 4 * ca * H)
+    mlp = rup(rup(phase + 2 * cm * D) + 2 * cm * fs)
+    if fs < F:
+        mlp = rup(mlp + 4 * cm * D)
+    return max(attn, mlp)
+
+
 def expected_workspace(T, D, F, cm, ca, fs, R=0):
     """The layout documented for dit_block_workspace_bytes (and, with a
     LoRA rank R, dit_block_plan_set_lora_rank), restated."""
@@ -233,6 +248,40 @@ def test_weight_scratch_size_and_binding(lib, D, F):
     assert lib.dit_block_bind_weight_scratch(p.handle, None, 0) == ds.OK  # unbind
     assert lib.dit_int8_to_bf16(16, 24, 16, None) == ds.ERR_INVALID_ARG   # n % 16
     assert lib.dit_int8_to_bf16(8, 32, 16, None) == ds.ERR_ALIGN
+
+
+@pytest.mark.parametrize("cfg", [
+    (65536, 3072, 24, 8192, 4096, 4096, 2048, 4096),
+    (1000, 256, 4, 704, 128, 384, 0, 256),
+    (32768, 3072, 24, 8192, 8192, 8192, 0, 8192),
+])
+def test_kv_offload_workspace_does_not_grow_with_T(lib, cfg):
+    T, D, H, F, cm, ca, fs, kvb = cfg
+    p = ds.block_plan(T, D, H, F, cm, ca, fs)
+    p.set_kv_offload(kvb)
+    assert p.workspace_bytes() == expected_workspace_offload(T, D, H, F, cm, ca, fs, kvb)
+    assert p.kv_host_bytes() == 2 * T * D + 2 * D * rup(T, 128)
+    q = ds.block_plan(2 * T, D, H, F, cm, ca, fs)
+    q.set_kv_offload(kvb)
+    assert q.workspace_bytes() == p.workspace_bytes()   # independent of T
+    if T == 65536:  # below the resident K/V floor alone (4*T*D = 768 MiB)
+        assert p.workspace_bytes() < 4 * T * D / 3
+
+
+def test_kv_offload_rules(lib):
+    p = ds.block_plan(1000, 256, 4, 704, 128, 128)
+    with pytest.raises(ds.DitError) as e:
+        p.set_kv_offload(100)
+    assert e.value.status == ds.ERR_CHUNK_ALIGN
+    p.set_kv_offload(256)
+    assert lib.dit_block_bind_kv_host(p.handle, None, 1 << 20) == ds.ERR_INVALID_ARG
+    assert lib.dit_block_bind_kv_host(p.handle, 8, 1 << 20) == ds.ERR_ALIGN
+    assert lib.dit_block_bind_kv_host(p.handle, 16, 100) == ds.ERR_WORKSPACE_TOO_SMALL
+    # an offloading plan without its host buffer fails closed
+    w = ds.block_weights(16, 16, 16, 16, 16)
+    with pytest.raises(ds.DitError) as e:
+        p.forward(16, w, 16)
+    assert e.value.status == ds.ERR_NO_WORKSPACE
 
 
 def test_workspace_beyond_kv_floor_is_bounded_by_chunk():
