@@ -60,6 +60,9 @@ def parse_args(argv=None):
     ap.add_argument("--weight-scratch", choices=("on", "off"), default="on",
                     help="int8 blocks: expand each phase's weights to bf16 in a "
                          "scratch ahead of the GEMMs (exact; same result bits)")
+    ap.add_argument("--kv-offload", type=int, default=0,
+                    help="key block size: keep K/V of all tokens in pinned host memory "
+                         "and stream them back in blocks of this many keys (0: resident)")
     ap.add_argument("--lora", type=int, default=0,
                     help="rank of activation-space LoRA adapters on all five "
                          "linears of every block (0: none)")
@@ -304,7 +307,7 @@ def run_ours(args, rank, world, local_rank):
     scratch = cfg["int8"] and args.weight_scratch == "on"
     stack = runner.DitStack(T, D, H, F, cfg["mlp_chunk"], cfg["attn_chunk"],
                             cfg["ffn_slice"], device=dev_name, lora_rank=args.lora,
-                            weight_scratch=scratch)
+                            weight_scratch=scratch, kv_offload=args.kv_offload)
     loras = dls = None
     if args.lora:
         loras = [synth.make_lora(D, F, args.lora, seed=100 * rank + i)
@@ -411,6 +414,7 @@ def run_ours(args, rank, world, local_rank):
                    "qk_transform": (None if qk is None else
                                     f"q/k rmsnorm + {args.qk} rotary"),
                    "lora_rank": args.lora or None,
+                   "kv_offload_key_block": args.kv_offload or None,
                    "int8_weight_scratch_gib": (round(stack.plan.weight_scratch_bytes()
                                                      / 2**30, 4) if scratch else None),
                    "parallelism": f"replicas x{world}"},
@@ -419,7 +423,7 @@ def run_ours(args, rank, world, local_rank):
         "tensor_peak_frac_burst": round(tflops / peaks["bf16_tflops"], 4),
         "peak_activation_gib": round(stack.plan.workspace_bytes() / 2**30, 4),
         "activation_beyond_kv_gib": round(
-            (stack.plan.workspace_bytes() - 4 * T * D) / 2**30, 4),
+            (stack.plan.workspace_bytes() - (0 if args.kv_offload else 4 * T * D)) / 2**30, 4),
         "measured_forward_alloc_gib": round(peak_fwd / 2**30, 4),
         "roofline": roof,
         "kernels": kernels,

@@ -52,7 +52,7 @@
 extern "C" {
 #endif
 
-#define DITSTREAM_ABI_VERSION 5
+#define DITSTREAM_ABI_VERSION 6
 
 #if defined(__GNUC__)
 #define DIT_API __attribute__((visibility("default")))
@@ -177,8 +177,8 @@ DIT_API dit_status_t dit_block_bind_workspace(dit_plan_t *plan, void *dev_ptr,
  * key_block_tokens > 0 (a multiple of 128) K [T, D] and V^T [D, T_pad] of
  * all tokens live in caller-owned pinned host memory instead of the device
  * workspace:
- *   - pass one's K/V projection writes them there directly (the buffer is
- *     mapped into the device's address space);
+ *   - pass one's K/V projection writes each key block into a device ring
+ *     slot, copied out to the host buffer on the plan's copy stream;
  *   - pass two streams them back, per query slab, in blocks of
  *     key_block_tokens keys through a two-slot device ring (copies on the
  *     plan's own copy stream, one block ahead of the attention), and the
@@ -191,7 +191,9 @@ DIT_API dit_status_t dit_block_bind_workspace(dit_plan_t *plan, void *dev_ptr,
  * grows with T.
  * dit_block_plan_set_kv_offload: before a workspace is bound (else
  * DIT_ERR_INVALID_ARG); 0 turns it off (the default).
- * dit_block_kv_host_bytes: bytes of the host buffer (2 T D + 2 D T_pad).
+ * dit_block_kv_host_bytes: bytes of the host buffer, 2 T D + 2 D kvb n_kb
+ * (K [T, D], then V^T per key block [n_kb][D][kvb], n_kb = ceil(T / kvb),
+ * so that every copy is one contiguous range); 0 when offload is off.
  * dit_block_bind_kv_host: bind the host buffer (allocated with
  * cudaHostAlloc or registered with cudaHostRegister, so that the device can
  * address it; 16-byte aligned, >= dit_block_kv_host_bytes) and create the
@@ -448,7 +450,7 @@ typedef struct {
     int64_t ldo;
     void *out2;             /* KV: V^T */
     int64_t ldo2;
-    int64_t row_offset;     /* KV: token index of A's row 0; rotary position of row 0 */
+    int64_t row_offset;     /* KV: row of K (column of V^T) that A's row 0 lands in */
     int split_n;            /* KV: first V column */
     float *x;               /* RESID, DOWN */
     int64_t ldx;
@@ -461,8 +463,7 @@ typedef struct {
     /* Q/K transform (see dit_qk_t) on STORE_BF16 output and on the K columns
      * (n < split_n) of KV output; off when qk_norm and rope_cos are NULL.
      * Heads are head_dim (64 or 128) consecutive columns; the rotary position
-     * of row m is row_offset + m (in STORE_BF16 mode row_offset moves the
-     * position only, not the output row). */
+     * of row m is rope_pos0 + m. */
     const float *qk_norm;   /* [head_dim] or NULL */
     const float *rope_cos;  /* [positions, head_dim / 2] or NULL */
     const float *rope_sin;
@@ -484,6 +485,7 @@ typedef struct {
     const void *lora_l1;
     int64_t lora_ldl1;
     int lora_rank1;
+    int64_t rope_pos0;      /* rotary position of A's row 0 (Q/K transform) */
 } dit_gemm_args_t;
 
 /* Test hook for failure detection: CTA 0's producer arms its first

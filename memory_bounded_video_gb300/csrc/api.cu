@@ -234,8 +234,9 @@ dit_status_t dit_block_plan_set_kv_offload(dit_plan_t *p, int key_block_tokens) 
 }
 
 size_t dit_block_kv_host_bytes(const dit_plan_t *p) {
-    if (!p) return 0;
-    return 2 * size_t(p->T) * size_t(p->D) + 2 * size_t(p->D) * size_t(p->t_pad);
+    if (!p || !p->kvb) return 0;
+    const size_t n_kb = (size_t(p->T) + p->kvb - 1) / p->kvb;
+    return 2 * size_t(p->T) * size_t(p->D) + 2 * size_t(p->D) * size_t(p->kvb) * n_kb;
 }
 
 dit_status_t dit_block_bind_kv_host(dit_plan_t *p, void *host_ptr, size_t bytes) {
@@ -247,11 +248,10 @@ dit_status_t dit_block_bind_kv_host(dit_plan_t *p, void *host_ptr, size_t bytes)
     if (e != cudaSuccess) return cuda_fail(e);
     if (!p->copy_stream) {
         e = cudaStreamCreateWithFlags(&p->copy_stream, cudaStreamNonBlocking);
-        for (int i = 0; i < 2 && e == cudaSuccess; ++i) {
-            e = cudaEventCreateWithFlags(&p->ev_filled[i], cudaEventDisableTiming);
-            if (e == cudaSuccess) e = cudaEventCreateWithFlags(&p->ev_used[i], cudaEventDisableTiming);
-        }
-        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&p->ev_pass1, cudaEventDisableTiming);
+        for (int i = 0; i < 2 && e == cudaSuccess; ++i)
+            for (cudaEvent_t *ev : {&p->ev_filled[i], &p->ev_used[i], &p->ev_written[i],
+                                    &p->ev_free[i]})
+                if (e == cudaSuccess) e = cudaEventCreateWithFlags(ev, cudaEventDisableTiming);
         if (e != cudaSuccess) return cuda_fail(e);
     }
     p->kv_host = static_cast<uint8_t *>(dev);
@@ -366,9 +366,10 @@ dit_status_t dit_block_plan(int64_t T, int D, int heads, int ffn, int mlp_chunk_
 void dit_block_plan_destroy(dit_plan_t *plan) {
     if (!plan) return;
     for (cudaEvent_t e : plan->pool) cudaEventDestroy(e);
-    for (cudaEvent_t e : {plan->ev_filled[0], plan->ev_filled[1], plan->ev_used[0],
-                          plan->ev_used[1], plan->ev_pass1})
-        if (e) cudaEventDestroy(e);
+    for (int i = 0; i < 2; ++i)
+        for (cudaEvent_t e : {plan->ev_filled[i], plan->ev_used[i], plan->ev_written[i],
+                              plan->ev_free[i]})
+            if (e) cudaEventDestroy(e);
     if (plan->copy_stream) cudaStreamDestroy(plan->copy_stream);
     delete plan;
 }
@@ -596,6 +597,36 @@ dit_status_t dit_block_forward_ex(const dit_plan_t *cp, float *x, const dit_bloc
         return on(l) ? 2.0 * rows * n_out * l.rank : 0.0;
     };
 
+    // K/V offload: the two ring slots stage pass one's K/V on their way to
+    // the host buffer and bring key blocks back in pass two; the copies run
+    // on the plan's copy stream, ordered against the kernels by events.  The
+    // host buffer holds K [T, D] and, per key block b, V^T_b [D, kvb]: every
+    // copy is one contiguous range (a strided V^T copy ran at a third of the
+    // contiguous copy's bandwidth).
+    const int64_t kvb = p->kvb;
+    const int64_t n_kb = kvb ? (T + kvb - 1) / kvb : 0;
+    const int64_t n_total = kvb ? n_kb * ((T + p->ca - 1) / p->ca) : 0;
+    cudaStream_t cs = p->copy_stream;
+    auto slot_k = [&](int slot) { return p->ws + p->off_ring + size_t(slot) * p->ring_slot; };
+    auto slot_vt = [&](int slot) { return slot_k(slot) + 2 * size_t(kvb) * size_t(D); };
+    uint8_t *hK = static_cast<uint8_t *>(K);
+    uint8_t *hVt = static_cast<uint8_t *>(Vt);  // offload: V^T blocks [n_kb][D][kvb]
+    const size_t vt_block_bytes = 2 * size_t(kvb) * size_t(D);
+    auto fetch = [&](int64_t c) -> dit_status_t {  // c-th block of pass two
+        const int slot = int(c & 1);
+        const int64_t b = c % n_kb, k0 = b * kvb;
+        const int64_t kb = (T - k0 < kvb) ? T - k0 : kvb;
+        cudaError_t e = cudaStreamWaitEvent(cs, p->ev_used[slot], 0);
+        if (e == cudaSuccess)
+            e = cudaMemcpyAsync(slot_k(slot), hK + 2 * k0 * Dl, size_t(2 * kb * Dl),
+                                cudaMemcpyDefault, cs);
+        if (e == cudaSuccess)
+            e = cudaMemcpyAsync(slot_vt(slot), hVt + size_t(b) * vt_block_bytes, vt_block_bytes,
+                                cudaMemcpyDefault, cs);
+        if (e == cudaSuccess) e = cudaEventRecord(p->ev_filled[slot], cs);
+        return e == cudaSuccess ? DIT_OK : cuda_fail(e);
+    };
+
     // pass 1: K and V of every token
     for (int64_t s = 0; s < T; s += p->ca) {
         const int64_t rows = (T - s < p->ca) ? T - s : p->ca;
@@ -605,60 +636,72 @@ dit_status_t dit_block_forward_ex(const dit_plan_t *cp, float *x, const dit_bloc
             return r;
         if (on(l_qkv) && (r = lora_u(a, D, rows, D, l_qkv, 0, D, u_q, nullptr, 0, 1)) != DIT_OK)
             return r;
-        dit_gemm_args_t g{};
-        g.mode = DIT_EPI_KV;
-        g.M = rows;
-        g.N = 2 * D;
-        g.K = D;
-        g.a = a;
-        g.lda = D;
-        g.b0 = wqkv + Dl * Dl * el;  // rows D..3D-1: Wk then Wv
-        g.ldb = D;
-        g.b_dtype = bdt;
-        g.b0_scale = i8 ? w->wqkv_scale + Dl : nullptr;
-        g.out = K;
-        g.ldo = D;
-        g.out2 = Vt;
-        g.ldo2 = p->t_pad;
-        g.row_offset = s;
-        g.split_n = D;
-        set_qk(g, 1);
-        if (on(l_qkv)) attach(g, 0, u_q, l_qkv, Dl);
-        if ((r = timed(p, st, DIT_K_GEMM_KV, 2.0 * rows * 2 * D * D + lflops(l_qkv, rows, 2 * D),
-                       [&] { return launch_gemm(g, status, st); })) != DIT_OK)
-            return r;
+        // resident: one GEMM into K / V^T; offload: one per part of a key
+        // block in the slab, into the block's ring slot (slot b % 2, part at
+        // the block's column t0 % kvb), copied out when the block is complete
+        for (int64_t t0 = s; t0 < s + rows;) {
+            const int64_t b = kvb ? t0 / kvb : 0;
+            const int64_t c0 = kvb ? t0 - b * kvb : 0;
+            const int64_t t1 = kvb ? ((s + rows < (b + 1) * kvb) ? s + rows : (b + 1) * kvb)
+                                   : s + rows;
+            const int64_t sr = t1 - t0;
+            const int slot = int(b & 1);
+            dit_gemm_args_t g{};
+            g.mode = DIT_EPI_KV;
+            g.M = sr;
+            g.N = 2 * D;
+            g.K = D;
+            g.a = static_cast<const uint8_t *>(a) + 2 * (t0 - s) * Dl;
+            g.lda = D;
+            g.b0 = wqkv + Dl * Dl * el;  // rows D..3D-1: Wk then Wv
+            g.ldb = D;
+            g.b_dtype = bdt;
+            g.b0_scale = i8 ? w->wqkv_scale + Dl : nullptr;
+            g.ldo = D;
+            g.split_n = D;
+            g.rope_pos0 = t0;
+            if (!kvb) {
+                g.out = K;
+                g.out2 = Vt;
+                g.ldo2 = p->t_pad;
+                g.row_offset = s;
+            } else {
+                if (c0 == 0) {  // the block's first part: its slot must be copied out
+                    cudaError_t e = cudaStreamWaitEvent(st, p->ev_free[slot], 0);
+                    if (e != cudaSuccess) return cuda_fail(e);
+                }
+                g.out = slot_k(slot);
+                g.out2 = slot_vt(slot);
+                g.ldo2 = kvb;
+                g.row_offset = c0;
+            }
+            set_qk(g, 1);
+            if (on(l_qkv))
+                attach(g, 0, static_cast<const uint8_t *>(u_q) + 2 * (t0 - s) * l_qkv.rank,
+                       l_qkv, Dl);
+            if ((r = timed(p, st, DIT_K_GEMM_KV, 2.0 * sr * 2 * D * D + lflops(l_qkv, sr, 2 * D),
+                           [&] { return launch_gemm(g, status, st); })) != DIT_OK)
+                return r;
+            if (kvb && (t1 % kvb == 0 || t1 == T)) {  // block b complete
+                const int64_t k0 = b * kvb;
+                cudaError_t e = cudaEventRecord(p->ev_written[slot], st);
+                if (e == cudaSuccess) e = cudaStreamWaitEvent(cs, p->ev_written[slot], 0);
+                if (e == cudaSuccess)
+                    e = cudaMemcpyAsync(hK + 2 * k0 * Dl, slot_k(slot), size_t(2 * (t1 - k0) * Dl),
+                                        cudaMemcpyDefault, cs);
+                if (e == cudaSuccess)
+                    e = cudaMemcpyAsync(hVt + size_t(b) * vt_block_bytes, slot_vt(slot),
+                                        vt_block_bytes, cudaMemcpyDefault, cs);
+                if (e == cudaSuccess) e = cudaEventRecord(p->ev_free[slot], cs);
+                if (e != cudaSuccess) return cuda_fail(e);
+            }
+            t0 = t1;
+        }
     }
-    // K/V offload: key blocks come back through the two ring slots, copied
-    // one block ahead of the attention on the plan's copy stream
-    const int64_t kvb = p->kvb;
-    const int64_t n_kb = kvb ? (T + kvb - 1) / kvb : 0;
-    const int64_t n_total = kvb ? n_kb * ((T + p->ca - 1) / p->ca) : 0;
-    cudaStream_t cs = p->copy_stream;
-    auto slot_k = [&](int slot) { return p->ws + p->off_ring + size_t(slot) * p->ring_slot; };
-    auto slot_vt = [&](int slot) { return slot_k(slot) + 2 * size_t(kvb) * size_t(D); };
-    auto fetch = [&](int64_t c) -> dit_status_t {  // c-th block of pass two
-        const int slot = int(c & 1);
-        const int64_t k0 = (c % n_kb) * kvb;
-        const int64_t kb = (T - k0 < kvb) ? T - k0 : kvb;
-        cudaError_t e = cudaStreamWaitEvent(cs, p->ev_used[slot], 0);
-        if (e == cudaSuccess)
-            e = cudaMemcpyAsync(slot_k(slot), static_cast<const uint8_t *>(K) + 2 * k0 * Dl,
-                                size_t(2 * kb * Dl), cudaMemcpyHostToDevice, cs);
-        if (e == cudaSuccess)
-            e = cudaMemcpy2DAsync(slot_vt(slot), size_t(2 * kvb),
-                                  static_cast<const uint8_t *>(Vt) + 2 * k0, size_t(2 * p->t_pad),
-                                  size_t(2 * kb), size_t(D), cudaMemcpyHostToDevice, cs);
-        if (e == cudaSuccess) e = cudaEventRecord(p->ev_filled[slot], cs);
-        return e == cudaSuccess ? DIT_OK : cuda_fail(e);
-    };
     int64_t kv_c = 0;  // blocks of pass two consumed so far
-    if (kvb) {
-        // the host copies of K/V are complete once pass one's GEMMs are
-        cudaError_t e = cudaEventRecord(p->ev_pass1, st);
-        if (e == cudaSuccess) e = cudaStreamWaitEvent(cs, p->ev_pass1, 0);
-        if (e != cudaSuccess) return cuda_fail(e);
-        if ((r = fetch(0)) != DIT_OK) return r;
-    }
+    // pass two's first block; the copy stream is in order, so it follows
+    // pass one's copies to the host
+    if (kvb && (r = fetch(0)) != DIT_OK) return r;
     // pass 2: Q per slab, attention against all keys, O-projection into x
     for (int64_t s = 0; s < T; s += p->ca) {
         const int64_t rows = (T - s < p->ca) ? T - s : p->ca;
@@ -681,7 +724,7 @@ dit_status_t dit_block_forward_ex(const dit_plan_t *cp, float *x, const dit_bloc
         g.b0_scale = i8 ? w->wqkv_scale : nullptr;
         g.out = Q;
         g.ldo = D;
-        g.row_offset = s;  // rotary position of the slab's first token
+        g.rope_pos0 = s;  // rotary position of the slab's first token
         set_qk(g, 0);
         if (on(l_qkv)) attach(g, 0, u_q, l_qkv, 0);
         if ((r = timed(p, st, DIT_K_GEMM_Q, 2.0 * rows * D * D + lflops(l_qkv, rows, D),

@@ -51,6 +51,7 @@ struct GemmParams {
     void *out2;
     int64_t ldo2;
     int64_t row_offset;
+    int64_t pos0;  // rotary position of row 0 (Q/K transform)
     int split_n;
     float *x;
     int64_t ldx;
@@ -233,9 +234,10 @@ DEV void epilogue_qk_tile(const GemmParams &p, uint32_t taddr, int64_t m, int nb
     using C = Cfg<MODE, I8>;
     const bool row_ok = m < p.M;
     const int d = p.head_dim;
-    const int64_t pos = p.row_offset + m;
+    const int64_t pos = p.pos0 + m;           // rotary position
+    const int64_t tok = p.row_offset + m;     // KV: destination row of K, column of V^T
     __nv_bfloat16 *orow = reinterpret_cast<__nv_bfloat16 *>(p.out) +
-                          (MODE == DIT_EPI_KV ? pos : m) * p.ldo;
+                          (MODE == DIT_EPI_KV ? tok : m) * p.ldo;
 #pragma unroll 1
     for (int h0 = 0; h0 < C::OUT_COLS; h0 += d) {
         const int nh = nb * C::BN + h0;  // first column of the head (warp-uniform)
@@ -248,7 +250,7 @@ DEV void epilogue_qk_tile(const GemmParams &p, uint32_t taddr, int64_t m, int nb
                 load_chunk<I8>(p, taddr + h0 + c0, nh + c0, f);
                 if (!row_ok) continue;
                 __nv_bfloat16 *vt = reinterpret_cast<__nv_bfloat16 *>(p.out2) +
-                                    int64_t(nh + c0 - p.split_n) * p.ldo2 + pos;
+                                    int64_t(nh + c0 - p.split_n) * p.ldo2 + tok;
 #pragma unroll
                 for (int j = 0; j < 32; ++j) vt[int64_t(j) * p.ldo2] = __float2bfloat16_rn(f[j]);
             }
@@ -815,6 +817,7 @@ dit_status_t run(const dit_gemm_args_t &a, int *dev_status, cudaStream_t s) {
     p.out2 = a.out2;
     p.ldo2 = a.ldo2;
     p.row_offset = a.row_offset;
+    p.pos0 = a.rope_pos0;
     p.split_n = a.split_n;
     p.x = a.x;
     p.ldx = a.ldx;
@@ -884,7 +887,7 @@ dit_status_t launch_gemm(const dit_gemm_args_t &a, int *dev_status, cudaStream_t
         if (a.head_dim != 64 && a.head_dim != 128) return DIT_ERR_INVALID_ARG;
         if (a.N % a.head_dim || (a.mode == DIT_EPI_KV && a.split_n % a.head_dim))
             return DIT_ERR_INVALID_ARG;
-        if (!a.rope_cos != !a.rope_sin || a.row_offset < 0) return DIT_ERR_INVALID_ARG;
+        if (!a.rope_cos != !a.rope_sin || a.rope_pos0 < 0) return DIT_ERR_INVALID_ARG;
         if (a.qk_norm && !(a.qk_eps > 0.0f)) return DIT_ERR_INVALID_ARG;
         if (!aligned16(a.qk_norm) || !aligned16(a.rope_cos) || !aligned16(a.rope_sin))
             return DIT_ERR_ALIGN;

@@ -33,9 +33,10 @@ struct dit_plan {
     uint8_t *kv_host = nullptr;      // device address of the pinned host buffer
     size_t kv_host_bytes = 0;
     cudaStream_t copy_stream = nullptr;
-    cudaEvent_t ev_filled[2] = {nullptr, nullptr};
-    cudaEvent_t ev_used[2] = {nullptr, nullptr};
-    cudaEvent_t ev_pass1 = nullptr;
+    cudaEvent_t ev_filled[2] = {nullptr, nullptr};   // pass 2: slot holds a key block
+    cudaEvent_t ev_used[2] = {nullptr, nullptr};     // pass 2: attention done with slot
+    cudaEvent_t ev_written[2] = {nullptr, nullptr};  // pass 1: GEMM wrote slot
+    cudaEvent_t ev_free[2] = {nullptr, nullptr};     // pass 1: slot copied out
     // per-kernel timing (dit_block_profile_*)
     struct Rec {
         int kind;

@@ -107,7 +107,8 @@ class GemmArgs(ctypes.Structure):
                 ("lora_rank0", ctypes.c_int),
                 ("lora_u1", ctypes.c_void_p), ("lora_ldu1", ctypes.c_int64),
                 ("lora_l1", ctypes.c_void_p), ("lora_ldl1", ctypes.c_int64),
-                ("lora_rank1", ctypes.c_int)]
+                ("lora_rank1", ctypes.c_int),
+                ("rope_pos0", ctypes.c_int64)]
 
 
 class LoraArgs(ctypes.Structure):

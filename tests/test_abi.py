@@ -260,7 +260,7 @@ def test_kv_offload_workspace_does_not_grow_with_T(lib, cfg):
     p = ds.block_plan(T, D, H, F, cm, ca, fs)
     p.set_kv_offload(kvb)
     assert p.workspace_bytes() == expected_workspace_offload(T, D, H, F, cm, ca, fs, kvb)
-    assert p.kv_host_bytes() == 2 * T * D + 2 * D * rup(T, 128)
+    assert p.kv_host_bytes() == 2 * T * D + 2 * D * kvb * ((T + kvb - 1) // kvb)
     q = ds.block_plan(2 * T, D, H, F, cm, ca, fs)
     q.set_kv_offload(kvb)
     assert q.workspace_bytes() == p.workspace_bytes()   # independent of T
@@ -333,7 +333,7 @@ def test_qk_transform_arguments_validated_before_launch(lib):
         (dict(rope_cos=16), ds.ERR_INVALID_ARG),                  # sin missing
         (dict(rope_sin=16), ds.ERR_INVALID_ARG),
         (dict(qk_norm=16, qk_eps=0.0), ds.ERR_INVALID_ARG),
-        (dict(qk_norm=16, row_offset=-1), ds.ERR_INVALID_ARG),
+        (dict(qk_norm=16, rope_pos0=-1), ds.ERR_INVALID_ARG),
         (dict(qk_norm=8), ds.ERR_ALIGN),
         (dict(rope_cos=16, rope_sin=24), ds.ERR_ALIGN),
         (dict(mode=ds.EPI_KV, out2=16, ldo2=4096, split_n=192, N=384, ldo=192,

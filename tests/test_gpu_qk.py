@@ -82,7 +82,7 @@ def test_q_projection_with_transform(d, angles, norm, int8):
     out = torch.full((M, D), float("nan"), dtype=torch.bfloat16, device="cuda")
     args = ds.GemmArgs(mode=ds.EPI_STORE_BF16, M=M, N=D, K=D, a=ds.ptr(keep[0]), lda=D,
                        b0=ds.ptr(keep[1]), ldb=D, b_dtype=ds.W_BF16, out=ds.ptr(out),
-                       ldo=D, row_offset=off, qk_norm=ds.ptr(keep[2]),
+                       ldo=D, rope_pos0=off, qk_norm=ds.ptr(keep[2]),
                        rope_cos=ds.ptr(keep[3]), rope_sin=ds.ptr(keep[4]), head_dim=d,
                        qk_eps=1e-6)
     for k, v in extra.items():
@@ -118,7 +118,7 @@ def test_kv_projection_transforms_k_only(d, int8):
     Vt = torch.zeros(D, T_pad, dtype=torch.bfloat16, device="cuda")
     args = ds.GemmArgs(mode=ds.EPI_KV, M=M, N=2 * D, K=D, a=ds.ptr(keep[0]), lda=D,
                        b0=ds.ptr(keep[1]), ldb=D, b_dtype=ds.W_BF16, out=ds.ptr(K), ldo=D,
-                       out2=ds.ptr(Vt), ldo2=T_pad, row_offset=off, split_n=D,
+                       out2=ds.ptr(Vt), ldo2=T_pad, row_offset=off, rope_pos0=off, split_n=D,
                        qk_norm=ds.ptr(keep[2]), rope_cos=ds.ptr(keep[3]),
                        rope_sin=ds.ptr(keep[4]), head_dim=d, qk_eps=1e-6)
     for k, v in extra.items():
