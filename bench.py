@@ -57,9 +57,16 @@ def parse_args(argv=None):
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--workload", default=HEADLINE)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
-    ap.add_argument("--weight-scratch", choices=("on", "off"), default="on",
+    ap.add_argument("--weight-scratch", choices=("on", "off"), default="off",
                     help="int8 blocks: expand each phase's weights to bf16 in a "
-                         "scratch ahead of the GEMMs (exact; same result bits)")
+                         "scratch ahead of the GEMMs (exact; same result bits) "
+                         "instead of converting them in the GEMM main loop")
+    ap.add_argument("--no-alt", action="store_true",
+                    help="skip the extra int8 weight-scratch measurement")
+    ap.add_argument("--mlp-chunk", type=int, default=None,
+                    help="override the workload's MLP token chunk (0: all tokens)")
+    ap.add_argument("--attn-chunk", type=int, default=None,
+                    help="override the workload's attention query slab (0: all tokens)")
     ap.add_argument("--kv-offload", type=int, default=0,
                     help="key block size: keep K/V of all tokens in pinned host memory "
                          "and stream them back in blocks of this many keys (0: resident)")
@@ -296,6 +303,10 @@ def run_ours(args, rank, world, local_rank):
     from oracle import block as ob
 
     cfg = dict(synth.WORKLOADS[args.workload])
+    if args.mlp_chunk is not None:
+        cfg["mlp_chunk"] = args.mlp_chunk
+    if args.attn_chunk is not None:
+        cfg["attn_chunk"] = args.attn_chunk
     T, D, H, F = cfg["T"], cfg["D"], cfg["heads"], cfg["F"]
     dev_name = f"cuda:{local_rank}"
     torch.cuda.set_device(local_rank)
@@ -463,6 +474,42 @@ def run_ours(args, rank, world, local_rank):
                        "h2d_bytes_per_step": 4 * T * D,
                        "d2h_bytes_per_step": 4 * res_shape[0] * res_shape[1],
                        "steps": k_e2e}
+
+    # int8 workloads: the same plan and inputs with the bf16 weight scratch
+    # bound (weights expanded ahead of the GEMMs instead of converted in
+    # their main loop; same output bits), timed the same way
+    if cfg["int8"] and not scratch and not args.no_alt:
+        buf = torch.empty(stack.plan.weight_scratch_bytes(), dtype=torch.uint8,
+                          device=dev_name)
+        stack.plan.bind_weight_scratch(buf)
+        for _ in range(2):
+            stack.forward(x, dev, stream, qk=dqk, lora=dls)
+        stack.check(stream)
+        barrier()
+        torch.cuda.synchronize()
+        a0 = torch.cuda.Event(enable_timing=True)
+        a1 = torch.cuda.Event(enable_timing=True)
+        a0.record(stream)
+        for _ in range(args.steps):
+            stack.forward(x, dev, stream, qk=dqk, lora=dls)
+        a1.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+        stack.check(stream)
+        ms_alt = max_over_ranks(a0.elapsed_time(a1), world, dev_name) / args.steps
+        stack.plan.bind_weight_scratch(None)
+        del buf
+        tf_alt = flops_step / (ms_alt / 1e3) / 1e12
+        line["int8_weight_scratch"] = {
+            "note": "same workload, int8 weights expanded to bf16 (exact) into a "
+                    "scratch ahead of the GEMMs instead of converted in the GEMM "
+                    "main loop; same output bits",
+            "ms_per_step": round(ms_alt, 4),
+            "value": round(replica_throughput(tokens_per_step, world, ms_alt), 1),
+            "unit": "block-tokens/s",
+            "tflops": round(tf_alt, 2),
+            "tensor_peak_frac": round(tf_alt / peaks["bf16_tflops_sustained"], 4),
+            "scratch_gib": round(stack.plan.weight_scratch_bytes() / 2**30, 4)}
 
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         v, per, sample, _ = cpu_sample(cfg, inp, args.cpu_rows, qk=qk, loras=loras)

@@ -211,3 +211,28 @@ def test_weight_scratch_full_size_block_T4096_D3072():
     x0, _ = run_scratch(inp, 2048, 2048, 0, False)
     x1, _ = run_scratch(inp, 2048, 2048, 0, True)
     assert torch.equal(x0, x1)
+
+
+def test_headline_stack_chunk_sweep_is_bit_identical():
+    """The 4-block int8 + final workload at full size (T = 32768) for query
+    slabs and MLP chunks from 256 to 32768 tokens: every setting gives the
+    same bits as the unchunked run."""
+    name = "dit4_int8_final_T32768_D3072"
+    inp = synth.make_workload(name, seed=1)
+    T, D = inp.x.shape
+    dev = runner.upload(inp)
+    stream = torch.cuda.current_stream()
+    ref = None
+    settings = [(c, c) for c in (256, 512, 1024, 2048, 4096, 8192, 16384, 32768)]
+    settings += [(256, 32768), (32768, 256), (1024, 8192), (0, 0)]
+    for cm, ca in settings:
+        st = runner.DitStack(T, D, 24, 8192, cm, ca, weight_scratch=(cm == ca))
+        x = dev.x.clone()
+        out = st.forward(x, dev, stream)
+        st.check()
+        if ref is None:
+            ref = (x, out)
+        else:
+            assert torch.equal(x, ref[0]), (cm, ca)
+            assert torch.equal(out, ref[1]), (cm, ca)
+        del st
