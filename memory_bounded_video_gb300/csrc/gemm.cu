@@ -78,13 +78,19 @@ struct GemmParams {
 constexpr int kLoraRows = 128;                    // rows of a half's L tile
 constexpr int kLoraStageBytes = (kBM + kLoraRows) * kBK * 2;
 
-template <int MODE, bool I8>
+// MH: 128-row halves of the M tile.  MH = 2 (int8 B, no LoRA) runs two
+// M = 128 MMAs per K-step on one converted B tile, which halves the int8
+// conversion per multiply-add (the conversion's ALU throughput bounds the
+// int8 main loop); the N tile is halved so that both halves' accumulators
+// still fit TMEM twice.
+template <int MODE, bool I8, int MH = 1>
 struct Cfg {
     static constexpr int NB = (MODE == DIT_EPI_SWIGLU) ? 2 : 1;  // B operands
-    static constexpr int BN = (MODE == DIT_EPI_SWIGLU) ? 128 : 256;
+    static constexpr int BN = ((MODE == DIT_EPI_SWIGLU) ? 128 : 256) / MH;
+    static constexpr int BM = kBM * MH;                   // rows of A per tile
     static constexpr int CONV_WARPS = 4;                   // int8 only
     static constexpr int THREADS = I8 ? 192 + 32 * CONV_WARPS : 192;
-    static constexpr int A_BYTES = kBM * kBK * 2;
+    static constexpr int A_BYTES = BM * kBK * 2;
     static constexpr int B_BYTES = BN * kBK * 2;         // one bf16 B tile
     static constexpr int BQ_BYTES = NB * BN * kBK;       // int8 B staging
     // TMA ring: bf16: A + B (4 stages); int8: A + int8 B (4 stages).
@@ -96,7 +102,8 @@ struct Cfg {
     static constexpr int CSTAGES = I8 ? 3 : 0;
     static constexpr int C_BYTES = NB * B_BYTES;
     static constexpr int OFF_C = STAGES * STAGE_BYTES;
-    static constexpr int ACC_COLS = NB * BN;  // fp32 TMEM columns per accumulator
+    static constexpr int HALF_COLS = NB * BN;      // fp32 TMEM columns per M half
+    static constexpr int ACC_COLS = MH * HALF_COLS;  // per accumulator buffer
     static constexpr int TMEM_COLS = 2 * ACC_COLS;
     static constexpr int OUT_COLS = BN;       // output columns per tile
     static constexpr int BAR_BYTES = 256;
@@ -120,17 +127,17 @@ DEV void tile_of(const GemmParams &p, int t, int &mb, int &nb) {
 // LoRA half h of output tile nb: whether it has work, and the first row of
 // its L tile (the tile's rows h*128.. for one B operand; SwiGLU: the tile's
 // rows of the gate (h = 0) or up (h = 1) adapter).
-template <int MODE, bool I8>
+template <int MODE, bool I8, int MH>
 DEV bool lora_half_on(const GemmParams &p, int h, int nb) {
-    using C = Cfg<MODE, I8>;
+    using C = Cfg<MODE, I8, MH>;
     if (h == 0) return p.lora_on0 != 0;
     if (C::NB == 2) return p.lora_on1 != 0;
     return p.lora_on1 != 0 && nb * C::BN + kLoraRows < p.N;
 }
 
-template <int MODE, bool I8>
+template <int MODE, bool I8, int MH>
 DEV int lora_row(int h, int nb) {
-    using C = Cfg<MODE, I8>;
+    using C = Cfg<MODE, I8, MH>;
     return C::NB == 2 ? nb * C::BN : nb * C::BN + h * kLoraRows;
 }
 
@@ -229,9 +236,9 @@ DEV void load_chunk(const GemmParams &p, uint32_t taddr, int n, float (&f)[32]) 
 // models", attention section (Q normalisation and positional transform on
 // each bounded Q region).  V columns of KV pass through as in the plain
 // epilogue.
-template <int MODE, bool I8>
+template <int MODE, bool I8, int MH>
 DEV void epilogue_qk_tile(const GemmParams &p, uint32_t taddr, int64_t m, int nb) {
-    using C = Cfg<MODE, I8>;
+    using C = Cfg<MODE, I8, MH>;
     const bool row_ok = m < p.M;
     const int d = p.head_dim;
     const int64_t pos = p.pos0 + m;           // rotary position
@@ -309,12 +316,12 @@ DEV void epilogue_qk_tile(const GemmParams &p, uint32_t taddr, int64_t m, int nb
     }
 }
 
-template <int MODE, bool I8>
+template <int MODE, bool I8, int MH>
 DEV void epilogue_tile(const GemmParams &p, uint32_t taddr, int64_t m, int nb) {
-    using C = Cfg<MODE, I8>;
+    using C = Cfg<MODE, I8, MH>;
     if constexpr (MODE == DIT_EPI_STORE_BF16 || MODE == DIT_EPI_KV) {
         if (p.qk) {
-            epilogue_qk_tile<MODE, I8>(p, taddr, m, nb);
+            epilogue_qk_tile<MODE, I8, MH>(p, taddr, m, nb);
             return;
         }
     }
@@ -382,9 +389,9 @@ DEV void epilogue_tile(const GemmParams &p, uint32_t taddr, int64_t m, int nb) {
 
 // DOWN with acc_load: write the carried fp32 accumulator of tile t into the
 // TMEM buffer before the tile's MMAs start (they then accumulate onto it).
-template <bool I8>
+template <int MODE, bool I8, int MH>
 DEV void preload_tile(const GemmParams &p, uint32_t taddr, int64_t m, int nb) {
-    using C = Cfg<DIT_EPI_DOWN, I8>;
+    using C = Cfg<MODE, I8, MH>;
     const bool row_ok = m < p.M;
 #pragma unroll 1
     for (int c0 = 0; c0 < C::OUT_COLS; c0 += 32) {
@@ -409,8 +416,8 @@ DEV void preload_tile(const GemmParams &p, uint32_t taddr, int64_t m, int nb) {
     }
 }
 
-template <int MODE, bool I8>
-__global__ void __launch_bounds__(Cfg<MODE, I8>::THREADS, 1)
+template <int MODE, bool I8, int MH>
+__global__ void __launch_bounds__(Cfg<MODE, I8, MH>::THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                    const __grid_constant__ CUtensorMap tmB0,
                    const __grid_constant__ CUtensorMap tmB1,
@@ -418,7 +425,7 @@ __global__ void __launch_bounds__(Cfg<MODE, I8>::THREADS, 1)
                    const __grid_constant__ CUtensorMap tmL0,
                    const __grid_constant__ CUtensorMap tmU1,
                    const __grid_constant__ CUtensorMap tmL1, const GemmParams p) {
-    using C = Cfg<MODE, I8>;
+    using C = Cfg<MODE, I8, MH>;
     constexpr int S = C::STAGES;
     constexpr int CS = C::CSTAGES;
     extern __shared__ uint8_t smem_raw[];
@@ -503,7 +510,7 @@ __global__ void __launch_bounds__(Cfg<MODE, I8>::THREADS, 1)
                     // transaction count then never completes)
                     const bool withhold = p.inject_stall && blockIdx.x == 0 && issued == 0;
                     if (!withhold) {
-                        tma_load_2d(sA, &tmA, full_bar(stage), kb * kBK, mb * kBM);
+                        tma_load_2d(sA, &tmA, full_bar(stage), kb * kBK, mb * C::BM);
                         tma_load_2d(sB, &tmB0, full_bar(stage), kb * kBK, nb * C::BN);
                         if (C::NB == 2)
                             tma_load_2d(sB + b_step, &tmB1, full_bar(stage), kb * kBK,
@@ -523,12 +530,12 @@ __global__ void __launch_bounds__(Cfg<MODE, I8>::THREADS, 1)
                             break;
                         }
                         const uint32_t sA = smem_u32(tiles + stage * C::STAGE_BYTES);
-                        if (lora_half_on<MODE, I8>(p, h, nb)) {
+                        if (lora_half_on<MODE, I8, MH>(p, h, nb)) {
                             mbar_arrive_expect_tx(full_bar(stage), kLoraStageBytes);
                             tma_load_2d(sA, h ? &tmU1 : &tmU0, full_bar(stage), lk * kBK,
                                         mb * kBM);
                             tma_load_2d(sA + C::A_BYTES, h ? &tmL1 : &tmL0, full_bar(stage),
-                                        lk * kBK, lora_row<MODE, I8>(h, nb));
+                                        lk * kBK, lora_row<MODE, I8, MH>(h, nb));
                         } else {
                             mbar_arrive(full_bar(stage));  // nothing to load
                         }
@@ -579,8 +586,11 @@ __global__ void __launch_bounds__(Cfg<MODE, I8>::THREADS, 1)
 #pragma unroll
                     for (int k = 0; k < kBK / 16; ++k) {
                         const uint32_t accum = (kb | k) != 0 || preload;
-                        mma_bf16_ss(d, desc_sw128(sA + 32u * k), desc_sw128(sB + 32u * k),
-                                    IDESC, accum);
+#pragma unroll
+                        for (int mh = 0; mh < MH; ++mh)
+                            mma_bf16_ss(d + uint32_t(mh * C::HALF_COLS),
+                                        desc_sw128(sA + uint32_t(mh * kBM * 128) + 32u * k),
+                                        desc_sw128(sB + 32u * k), IDESC, accum);
                     }
                     mma_commit(empty_bar(stage));
                     if (++stage == S) {
@@ -605,7 +615,7 @@ __global__ void __launch_bounds__(Cfg<MODE, I8>::THREADS, 1)
                             break;
                         }
                         tc_fence_after();
-                        if (lora_half_on<MODE, I8>(p, h, nb)) {
+                        if (lora_half_on<MODE, I8, MH>(p, h, nb)) {
                             const uint32_t sU = smem_u32(tiles + stage * C::STAGE_BYTES);
                             const uint32_t sL = sU + C::A_BYTES;
 #pragma unroll
@@ -642,7 +652,11 @@ __global__ void __launch_bounds__(Cfg<MODE, I8>::THREADS, 1)
         if (preload && t < num_tiles) {
             int mb0, nb0;
             tile_of(p, t, mb0, nb0);
-            preload_tile<I8>(p, lane_base, int64_t(mb0) * kBM + q * 32 + lane, nb0);
+#pragma unroll
+            for (int mh = 0; mh < MH; ++mh)
+                preload_tile<MODE, I8, MH>(p, lane_base + uint32_t(mh * C::HALF_COLS),
+                                           int64_t(mb0) * C::BM + mh * kBM + q * 32 + lane,
+                                           nb0);
             tc_fence_before();
             mbar_arrive(tempty_bar(0));
         }
@@ -652,8 +666,11 @@ __global__ void __launch_bounds__(Cfg<MODE, I8>::THREADS, 1)
                 if (tn < num_tiles) {
                     int mbn, nbn;
                     tile_of(p, tn, mbn, nbn);
-                    preload_tile<I8>(p, lane_base + uint32_t((buf ^ 1) * C::ACC_COLS),
-                                     int64_t(mbn) * kBM + q * 32 + lane, nbn);
+#pragma unroll
+                    for (int mh = 0; mh < MH; ++mh)
+                        preload_tile<MODE, I8, MH>(
+                            p, lane_base + uint32_t((buf ^ 1) * C::ACC_COLS + mh * C::HALF_COLS),
+                            int64_t(mbn) * C::BM + mh * kBM + q * 32 + lane, nbn);
                     tc_fence_before();
                     mbar_arrive(tempty_bar(buf ^ 1));
                 }
@@ -664,8 +681,11 @@ __global__ void __launch_bounds__(Cfg<MODE, I8>::THREADS, 1)
             tc_fence_after();
             int mb, nb;
             tile_of(p, t, mb, nb);
-            epilogue_tile<MODE, I8>(p, lane_base + uint32_t(buf * C::ACC_COLS),
-                                    int64_t(mb) * kBM + q * 32 + lane, nb);
+#pragma unroll 1
+            for (int mh = 0; mh < MH; ++mh)
+                epilogue_tile<MODE, I8, MH>(
+                    p, lane_base + uint32_t(buf * C::ACC_COLS + mh * C::HALF_COLS),
+                    int64_t(mb) * C::BM + mh * kBM + q * 32 + lane, nb);
             if (!preload) {
                 tc_fence_before();
                 mbar_arrive(tempty_bar(buf));
@@ -745,19 +765,19 @@ __global__ void __launch_bounds__(Cfg<MODE, I8>::THREADS, 1)
     }
 }
 
-int &attr_flag(int mode, bool i8) {
-    static int done[8][2][64] = {};  // per mode, B type, device
+int &attr_flag(int mode, bool i8, int mh) {
+    static int done[8][2][2][64] = {};  // per mode, B type, M halves, device
     int dev = 0;
     cudaGetDevice(&dev);
-    return done[mode][i8 ? 1 : 0][dev & 63];
+    return done[mode][i8 ? 1 : 0][mh - 1][dev & 63];
 }
 
-template <int MODE, bool I8>
+template <int MODE, bool I8, int MH>
 dit_status_t run(const dit_gemm_args_t &a, int *dev_status, cudaStream_t s) {
-    using C = Cfg<MODE, I8>;
+    using C = Cfg<MODE, I8, MH>;
     CUtensorMap tA, tB0, tB1;
     if (!make_tmap_2d(&tA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.a, uint64_t(a.K), uint64_t(a.M),
-                      uint64_t(a.lda) * 2, kBK, kBM))
+                      uint64_t(a.lda) * 2, kBK, C::BM))
         return DIT_ERR_INVALID_ARG;
     const CUtensorMapDataType bdt =
         I8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
@@ -803,7 +823,7 @@ dit_status_t run(const dit_gemm_args_t &a, int *dev_status, cudaStream_t s) {
     p.M = a.M;
     p.N = a.N;
     p.K = a.K;
-    p.num_m = int((a.M + kBM - 1) / kBM);
+    p.num_m = int((a.M + C::BM - 1) / C::BM);
     p.num_n = (a.N + C::BN - 1) / C::BN;
     p.num_k = a.K / kBK;
     {  // N-blocks per tile group: the group's B tiles within ~48 MB of L2
@@ -841,9 +861,9 @@ dit_status_t run(const dit_gemm_args_t &a, int *dev_status, cudaStream_t s) {
     p.lora_on0 = a.lora_l0 != nullptr;
     p.lora_on1 = C::NB == 2 ? a.lora_l1 != nullptr : a.lora_l0 != nullptr;
 
-    int &done = attr_flag(MODE, I8);
+    int &done = attr_flag(MODE, I8, MH);
     if (!done) {
-        cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<MODE, I8>,
+        cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<MODE, I8, MH>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              C::SMEM_BYTES);
         if (e != cudaSuccess) return cuda_fail(e);
@@ -851,15 +871,18 @@ dit_status_t run(const dit_gemm_args_t &a, int *dev_status, cudaStream_t s) {
     }
     const int tiles = p.num_m * p.num_n;
     const int grid = tiles < sm_count() ? tiles : sm_count();
-    gemm_tc_kernel<MODE, I8><<<grid, C::THREADS, C::SMEM_BYTES, s>>>(tA, tB0, tB1, tU0, tL0,
+    gemm_tc_kernel<MODE, I8, MH><<<grid, C::THREADS, C::SMEM_BYTES, s>>>(tA, tB0, tB1, tU0, tL0,
                                                                      tU1, tL1, p);
     return check_launch();
 }
 
 template <int MODE>
 dit_status_t run_b(const dit_gemm_args_t &a, int *dev_status, cudaStream_t s) {
-    return a.b_dtype == DIT_W_INT8 ? run<MODE, true>(a, dev_status, s)
-                                   : run<MODE, false>(a, dev_status, s);
+    if (a.b_dtype != DIT_W_INT8) return run<MODE, false, 1>(a, dev_status, s);
+    // int8: two M halves per converted B tile, except with LoRA K-steps (their
+    // stages are laid out for one 128-row half)
+    const bool lora = a.lora_l0 || a.lora_l1;
+    return lora ? run<MODE, true, 1>(a, dev_status, s) : run<MODE, true, 2>(a, dev_status, s);
 }
 
 bool ld_ok(int64_t ld, int64_t min_ld, int elem_bytes) {
