@@ -107,12 +107,16 @@ DEV float tile_max(uint32_t saddr, int nvalid) {
 
 // P = exp2(S * sl2 - m) for one row, as bf16 written over the consumed S
 // columns (keys 2i, 2i+1 -> column i), returns the sum of the fp32
-// probabilities.  Chunk c (keys 32c..32c+31) is read before its P (columns
+// probabilities.  The scale-and-shift and the four running sums use packed
+// two-lane fp32 instructions (each lane rounds as the scalar instruction
+// would, in the same order), which cuts the instructions the softmax issues
+// per score: the softmax is bound by issue, not by the exponential unit.  Chunk c (keys 32c..32c+31) is read before its P (columns
 // 16c..16c+15) is written, so the write never clobbers unread S.
 template <bool MASK>
 DEV float tile_exp(uint32_t saddr, float sl2, float m, int nvalid) {
-    float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
-    const float neg_m = -m;
+    uint64_t s01 = 0, s23 = 0;  // (s0, s1), (s2, s3): four running sums
+    const uint64_t sl2x2 = (uint64_t(__float_as_uint(sl2)) << 32) | __float_as_uint(sl2);
+    const uint64_t negm2 = (uint64_t(__float_as_uint(-m)) << 32) | __float_as_uint(-m);
 #pragma unroll
     for (int c0 = 0; c0 < kBKV; c0 += 32) {
         uint32_t r[32];
@@ -121,25 +125,33 @@ DEV float tile_exp(uint32_t saddr, float sl2, float m, int nvalid) {
         uint32_t pk[16];
 #pragma unroll
         for (int c = 0; c < 32; c += 4) {
-            float p0 = ex2(__fmaf_rn(__uint_as_float(r[c]), sl2, neg_m));
-            float p1 = ex2(__fmaf_rn(__uint_as_float(r[c + 1]), sl2, neg_m));
-            float p2 = ex2(__fmaf_rn(__uint_as_float(r[c + 2]), sl2, neg_m));
-            float p3 = ex2(__fmaf_rn(__uint_as_float(r[c + 3]), sl2, neg_m));
+            // x = s * sl2 - m for two scores per instruction (each lane rounds
+            // as a scalar fma would)
+            uint64_t x01 = (uint64_t(r[c + 1]) << 32) | r[c];
+            uint64_t x23 = (uint64_t(r[c + 3]) << 32) | r[c + 2];
+            asm("fma.rn.f32x2 %0, %0, %1, %2;" : "+l"(x01) : "l"(sl2x2), "l"(negm2));
+            asm("fma.rn.f32x2 %0, %0, %1, %2;" : "+l"(x23) : "l"(sl2x2), "l"(negm2));
+            float p0 = ex2(__uint_as_float(uint32_t(x01)));
+            float p1 = ex2(__uint_as_float(uint32_t(x01 >> 32)));
+            float p2 = ex2(__uint_as_float(uint32_t(x23)));
+            float p3 = ex2(__uint_as_float(uint32_t(x23 >> 32)));
             if (MASK) {
                 if (c0 + c >= nvalid) p0 = 0.f;
                 if (c0 + c + 1 >= nvalid) p1 = 0.f;
                 if (c0 + c + 2 >= nvalid) p2 = 0.f;
                 if (c0 + c + 3 >= nvalid) p3 = 0.f;
             }
-            s0 += p0;
-            s1 += p1;
-            s2 += p2;
-            s3 += p3;
+            const uint64_t p01 = (uint64_t(__float_as_uint(p1)) << 32) | __float_as_uint(p0);
+            const uint64_t p23 = (uint64_t(__float_as_uint(p3)) << 32) | __float_as_uint(p2);
+            asm("add.rn.f32x2 %0, %0, %1;" : "+l"(s01) : "l"(p01));
+            asm("add.rn.f32x2 %0, %0, %1;" : "+l"(s23) : "l"(p23));
             pk[c >> 1] = pack_bf16x2(p0, p1);
             pk[(c >> 1) + 1] = pack_bf16x2(p2, p3);
         }
         tmem_st16(saddr + (c0 >> 1), pk);
     }
+    const float s0 = __uint_as_float(uint32_t(s01)), s1 = __uint_as_float(uint32_t(s01 >> 32));
+    const float s2 = __uint_as_float(uint32_t(s23)), s3 = __uint_as_float(uint32_t(s23 >> 32));
     return (s0 + s1) + (s2 + s3);
 }
 
