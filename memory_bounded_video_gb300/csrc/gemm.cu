@@ -11,7 +11,7 @@
 //               K=16) into one of two TMEM accumulators
 //   warps 2..5  epilogue: tcgen05.ld of the accumulator (one token row per
 //               thread), the fused math, stores to global
-//   warps 6..9  (int8 B only) dequantise: each int8 B tile staged by TMA is
+//   warps 6-8,10 (int8 B only) dequantise: each int8 B tile staged by TMA is
 //               converted to bf16 (exact: |q| <= 127) into the swizzled layout
 //               of the MMA operand; the per-row scale multiplies the fp32
 //               accumulator in the epilogue (W = s_row * q, "MiniMax-H3-Comfy-
@@ -61,6 +61,7 @@ struct GemmParams {
     int acc_load, acc_final;
     const float *s0, *s1;  // int8 per-row scales of B0 / B1
     int bscale;            // bf16 B holding int8 values: apply s0 / s1 too
+    int k4;                // int8 B in the (k0, k2, k1, k3) group order
     int inject_stall;      // DIT_GEMM_FLAG_INJECT_STALL test hook
     int *status;
     // Q/K transform (STORE_BF16, and K columns of KV); qk == 0: off
@@ -89,7 +90,11 @@ struct Cfg {
     static constexpr int BN = ((MODE == DIT_EPI_SWIGLU) ? 128 : 256) / MH;
     static constexpr int BM = kBM * MH;                   // rows of A per tile
     static constexpr int CONV_WARPS = 4;                   // int8 only
-    static constexpr int THREADS = I8 ? 192 + 32 * CONV_WARPS : 192;
+    // int8: 12 warps, converters on warps 6, 7, 8 and 10 (sub-partitions 2, 3,
+    // 0, 2) and warps 9, 11 idle, so that the MMA-issuing warp 1 shares its
+    // sub-partition with no converter: measured 7-10 % faster than converters
+    // on warps 6..9, whose ALU stream slowed the MMA issue.
+    static constexpr int THREADS = I8 ? 384 : 192;
     static constexpr int A_BYTES = BM * kBK * 2;
     static constexpr int B_BYTES = BN * kBK * 2;         // one bf16 B tile
     static constexpr int BQ_BYTES = NB * BN * kBK;       // int8 B staging
@@ -207,6 +212,27 @@ DEV uint2 int8x4_to_bf16x4(uint32_t u) {
     r.x = hi_halves(uint32_t(a), uint32_t(a >> 32));
     r.y = hi_halves(uint32_t(b), uint32_t(b >> 32));
     return r;
+}
+
+// Four int8 stored as (k0, k2, k1, k3) -> bf16 pairs (k0, k1), (k2, k3),
+// exact.  For a byte b of q, 0x4300 | (b & 0x7f) is the bf16 value
+// 128 + (b & 0x7f) and 0x4300 | (b & 0x80) is 128 (q >= 0) or 256 (q < 0),
+// so one packed subtraction leaves q; the even bytes (k0, k1) are already in
+// the two 16-bit halves' low bytes, the odd ones (k2, k3) after a shift.
+DEV uint2 int8x4k4_to_bf16x4(uint32_t w) {
+    const uint32_t wo = w >> 8;
+    const uint32_t te = (w & 0x007f007fu) | 0x43004300u, se = (w & 0x00800080u) | 0x43004300u;
+    const uint32_t to = (wo & 0x007f007fu) | 0x43004300u, so = (wo & 0x00800080u) | 0x43004300u;
+    uint2 r;
+    asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(r.x) : "r"(te), "r"(se));
+    asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(r.y) : "r"(to), "r"(so));
+    return r;
+}
+
+DEV uint4 int8x8k4_to_bf16x8(uint2 w) {
+    const uint2 lo = int8x4k4_to_bf16x4(w.x);
+    const uint2 hi = int8x4k4_to_bf16x4(w.y);
+    return make_uint4(lo.x, lo.y, hi.x, hi.y);
 }
 
 // Eight int8 (two words) -> eight bf16 (four bf16x2 words), exact.
@@ -583,14 +609,18 @@ __global__ void __launch_bounds__(Cfg<MODE, I8, MH>::THREADS, 1)
                     const uint32_t sA = smem_u32(tiles + stage * C::STAGE_BYTES);
                     const uint32_t sB = I8 ? smem_u32(tiles + C::OFF_C + cstage * C::C_BYTES)
                                            : sA + C::A_BYTES;
+                    // descriptors of the stage's tiles, stepped through K (16
+                    // elements = 32 bytes = 2 in the address field) and the M
+                    // halves (128 rows = 16 KB); the field cannot overflow
+                    const uint64_t da = desc_sw128(sA), db = desc_sw128(sB);
 #pragma unroll
                     for (int k = 0; k < kBK / 16; ++k) {
                         const uint32_t accum = (kb | k) != 0 || preload;
 #pragma unroll
                         for (int mh = 0; mh < MH; ++mh)
                             mma_bf16_ss(d + uint32_t(mh * C::HALF_COLS),
-                                        desc_sw128(sA + uint32_t(mh * kBM * 128) + 32u * k),
-                                        desc_sw128(sB + 32u * k), IDESC, accum);
+                                        da + uint64_t(mh * (kBM * 128 / 16) + 2 * k),
+                                        db + uint64_t(2 * k), IDESC, accum);
                     }
                     mma_commit(empty_bar(stage));
                     if (++stage == S) {
@@ -695,13 +725,13 @@ __global__ void __launch_bounds__(Cfg<MODE, I8, MH>::THREADS, 1)
                 bph ^= 1u;
             }
         }
-    } else if (I8) {
+    } else if (I8 && warp != 9 && warp != 11) {
         // -------------------------------------------------- int8 -> bf16
         // Staged int8 rows (64 bytes each, NB*BN rows) become 128-byte bf16
         // rows of a converted-B stage; 16-byte chunk c of row r lands at
         // chunk c ^ (r % 8) of the row (the 128-byte swizzle), rows in 8-row
         // groups of 1024 bytes.
-        const int tid = threadIdx.x - 192;
+        const int tid = (warp == 10 ? 3 : warp - 6) * 32 + lane;
         int stage = 0, cstage = 0;
         uint32_t ph = 0, cph = 0;
         bool ok = true;
@@ -731,10 +761,17 @@ __global__ void __launch_bounds__(Cfg<MODE, I8, MH>::THREADS, 1)
 #pragma unroll
                     for (int i = 0; i < kBatch; ++i)
                         w8[i] = *reinterpret_cast<const uint2 *>(src + (i0 + i) * (kConv / 8) * kBK);
+                    if (p.k4) {
 #pragma unroll
-                    for (int i = 0; i < kBatch; ++i)
-                        *reinterpret_cast<uint4 *>(dst + (i0 + i) * (kConv / 8) * 128) =
-                            int8x8_to_bf16x8(w8[i]);
+                        for (int i = 0; i < kBatch; ++i)
+                            *reinterpret_cast<uint4 *>(dst + (i0 + i) * (kConv / 8) * 128) =
+                                int8x8k4_to_bf16x8(w8[i]);
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < kBatch; ++i)
+                            *reinterpret_cast<uint4 *>(dst + (i0 + i) * (kConv / 8) * 128) =
+                                int8x8_to_bf16x8(w8[i]);
+                    }
                 }
                 fence_proxy_async_smem();  // the tensor core reads what we wrote
                 mbar_arrive(cfull_bar(cstage));
@@ -849,6 +886,7 @@ dit_status_t run(const dit_gemm_args_t &a, int *dev_status, cudaStream_t s) {
     p.s0 = a.b0_scale;
     p.s1 = a.b1_scale;
     p.bscale = (!I8 && a.b0_scale) ? 1 : 0;
+    p.k4 = a.b_dtype == DIT_W_INT8_K4;
     p.inject_stall = (a.flags & DIT_GEMM_FLAG_INJECT_STALL) != 0;
     p.status = dev_status;
     p.qk = (a.qk_norm || a.rope_cos) ? 1 : 0;
@@ -878,7 +916,7 @@ dit_status_t run(const dit_gemm_args_t &a, int *dev_status, cudaStream_t s) {
 
 template <int MODE>
 dit_status_t run_b(const dit_gemm_args_t &a, int *dev_status, cudaStream_t s) {
-    if (a.b_dtype != DIT_W_INT8) return run<MODE, false, 1>(a, dev_status, s);
+    if (a.b_dtype == DIT_W_BF16) return run<MODE, false, 1>(a, dev_status, s);
     // int8: two M halves per converted B tile, except with LoRA K-steps (their
     // stages are laid out for one 128-row half)
     const bool lora = a.lora_l0 || a.lora_l1;
@@ -894,9 +932,10 @@ bool ld_ok(int64_t ld, int64_t min_ld, int elem_bytes) {
 dit_status_t launch_gemm(const dit_gemm_args_t &a, int *dev_status, cudaStream_t s) {
     if (a.M < 0 || a.N <= 0 || a.K <= 0 || a.N % 32 || a.K % kBK) return DIT_ERR_INVALID_ARG;
     if (a.M > (int64_t(1) << 31) - kBM) return DIT_ERR_INVALID_ARG;
-    if (a.b_dtype != DIT_W_BF16 && a.b_dtype != DIT_W_INT8) return DIT_ERR_INVALID_ARG;
+    if (a.b_dtype != DIT_W_BF16 && a.b_dtype != DIT_W_INT8 && a.b_dtype != DIT_W_INT8_K4)
+        return DIT_ERR_INVALID_ARG;
     if (a.flags & ~DIT_GEMM_FLAG_INJECT_STALL) return DIT_ERR_INVALID_ARG;
-    const bool i8 = a.b_dtype == DIT_W_INT8;
+    const bool i8 = a.b_dtype != DIT_W_BF16;
     if (!a.a || !a.b0) return DIT_ERR_INVALID_ARG;
     if (!aligned16(a.a) || !aligned16(a.b0)) return DIT_ERR_ALIGN;
     if (!ld_ok(a.lda, a.K, 2) || !ld_ok(a.ldb, a.K, i8 ? 1 : 2)) return DIT_ERR_INVALID_ARG;
