@@ -61,10 +61,6 @@ def parse_args(argv=None):
                     help="int8 blocks: expand each phase's weights to bf16 in a "
                          "scratch ahead of the GEMMs (exact; same result bits) "
                          "instead of converting them in the GEMM main loop")
-    ap.add_argument("--int8-layout", choices=("k4", "plain"), default="plain",
-                    help="int8 weights in the (k0, k2, k1, k3) group order the GEMM "
-                         "converts with fewer instructions (reordered once at upload), "
-                         "or in their plain order")
     ap.add_argument("--no-alt", action="store_true",
                     help="skip the extra int8 weight-scratch measurement")
     ap.add_argument("--mlp-chunk", type=int, default=None,
@@ -318,7 +314,7 @@ def run_ours(args, rank, world, local_rank):
     ditstream.load()
 
     inp = synth.make_workload(args.workload, seed=rank)
-    dev = runner.upload(inp, dev_name, prepack=cfg["int8"] and args.int8_layout == "k4")
+    dev = runner.upload(inp, dev_name)
     scratch = cfg["int8"] and args.weight_scratch == "on"
     stack = runner.DitStack(T, D, H, F, cfg["mlp_chunk"], cfg["attn_chunk"],
                             cfg["ffn_slice"], device=dev_name, lora_rank=args.lora,
@@ -430,9 +426,6 @@ def run_ours(args, rank, world, local_rank):
                                     f"q/k rmsnorm + {args.qk} rotary"),
                    "lora_rank": args.lora or None,
                    "kv_offload_key_block": args.kv_offload or None,
-                   "int8_layout": ((args.int8_layout + " (byte order within 4-column "
-                                    "groups; same values and scales)")
-                                   if cfg["int8"] else None),
                    "int8_weight_scratch_gib": (round(stack.plan.weight_scratch_bytes()
                                                      / 2**30, 4) if scratch else None),
                    "parallelism": f"replicas x{world}"},

@@ -61,7 +61,6 @@ struct GemmParams {
     int acc_load, acc_final;
     const float *s0, *s1;  // int8 per-row scales of B0 / B1
     int bscale;            // bf16 B holding int8 values: apply s0 / s1 too
-    int k4;                // int8 B in the (k0, k2, k1, k3) group order
     int inject_stall;      // DIT_GEMM_FLAG_INJECT_STALL test hook
     int *status;
     // Q/K transform (STORE_BF16, and K columns of KV); qk == 0: off
@@ -212,27 +211,6 @@ DEV uint2 int8x4_to_bf16x4(uint32_t u) {
     r.x = hi_halves(uint32_t(a), uint32_t(a >> 32));
     r.y = hi_halves(uint32_t(b), uint32_t(b >> 32));
     return r;
-}
-
-// Four int8 stored as (k0, k2, k1, k3) -> bf16 pairs (k0, k1), (k2, k3),
-// exact.  For a byte b of q, 0x4300 | (b & 0x7f) is the bf16 value
-// 128 + (b & 0x7f) and 0x4300 | (b & 0x80) is 128 (q >= 0) or 256 (q < 0),
-// so one packed subtraction leaves q; the even bytes (k0, k1) are already in
-// the two 16-bit halves' low bytes, the odd ones (k2, k3) after a shift.
-DEV uint2 int8x4k4_to_bf16x4(uint32_t w) {
-    const uint32_t wo = w >> 8;
-    const uint32_t te = (w & 0x007f007fu) | 0x43004300u, se = (w & 0x00800080u) | 0x43004300u;
-    const uint32_t to = (wo & 0x007f007fu) | 0x43004300u, so = (wo & 0x00800080u) | 0x43004300u;
-    uint2 r;
-    asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(r.x) : "r"(te), "r"(se));
-    asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(r.y) : "r"(to), "r"(so));
-    return r;
-}
-
-DEV uint4 int8x8k4_to_bf16x8(uint2 w) {
-    const uint2 lo = int8x4k4_to_bf16x4(w.x);
-    const uint2 hi = int8x4k4_to_bf16x4(w.y);
-    return make_uint4(lo.x, lo.y, hi.x, hi.y);
 }
 
 // Eight int8 (two words) -> eight bf16 (four bf16x2 words), exact.
@@ -761,17 +739,10 @@ __global__ void __launch_bounds__(Cfg<MODE, I8, MH>::THREADS, 1)
 #pragma unroll
                     for (int i = 0; i < kBatch; ++i)
                         w8[i] = *reinterpret_cast<const uint2 *>(src + (i0 + i) * (kConv / 8) * kBK);
-                    if (p.k4) {
 #pragma unroll
-                        for (int i = 0; i < kBatch; ++i)
-                            *reinterpret_cast<uint4 *>(dst + (i0 + i) * (kConv / 8) * 128) =
-                                int8x8k4_to_bf16x8(w8[i]);
-                    } else {
-#pragma unroll
-                        for (int i = 0; i < kBatch; ++i)
-                            *reinterpret_cast<uint4 *>(dst + (i0 + i) * (kConv / 8) * 128) =
-                                int8x8_to_bf16x8(w8[i]);
-                    }
+                    for (int i = 0; i < kBatch; ++i)
+                        *reinterpret_cast<uint4 *>(dst + (i0 + i) * (kConv / 8) * 128) =
+                            int8x8_to_bf16x8(w8[i]);
                 }
                 fence_proxy_async_smem();  // the tensor core reads what we wrote
                 mbar_arrive(cfull_bar(cstage));
@@ -886,7 +857,6 @@ dit_status_t run(const dit_gemm_args_t &a, int *dev_status, cudaStream_t s) {
     p.s0 = a.b0_scale;
     p.s1 = a.b1_scale;
     p.bscale = (!I8 && a.b0_scale) ? 1 : 0;
-    p.k4 = a.b_dtype == DIT_W_INT8_K4;
     p.inject_stall = (a.flags & DIT_GEMM_FLAG_INJECT_STALL) != 0;
     p.status = dev_status;
     p.qk = (a.qk_norm || a.rope_cos) ? 1 : 0;
@@ -932,7 +902,7 @@ bool ld_ok(int64_t ld, int64_t min_ld, int elem_bytes) {
 dit_status_t launch_gemm(const dit_gemm_args_t &a, int *dev_status, cudaStream_t s) {
     if (a.M < 0 || a.N <= 0 || a.K <= 0 || a.N % 32 || a.K % kBK) return DIT_ERR_INVALID_ARG;
     if (a.M > (int64_t(1) << 31) - kBM) return DIT_ERR_INVALID_ARG;
-    if (a.b_dtype != DIT_W_BF16 && a.b_dtype != DIT_W_INT8 && a.b_dtype != DIT_W_INT8_K4)
+    if (a.b_dtype != DIT_W_BF16 && a.b_dtype != DIT_W_INT8)
         return DIT_ERR_INVALID_ARG;
     if (a.flags & ~DIT_GEMM_FLAG_INJECT_STALL) return DIT_ERR_INVALID_ARG;
     const bool i8 = a.b_dtype != DIT_W_BF16;
