@@ -52,7 +52,7 @@
 extern "C" {
 #endif
 
-#define DITSTREAM_ABI_VERSION 6
+#define DITSTREAM_ABI_VERSION 7
 
 #if defined(__GNUC__)
 #define DIT_API __attribute__((visibility("default")))
@@ -532,6 +532,40 @@ DIT_API dit_status_t dit_attention(const void *q, int64_t Tq, int64_t ldq,
                            int64_t ldvt, int64_t T, int heads, int head_dim,
                            void *o, int64_t ldo, int *dev_status,
                            dit_stream_t stream);
+
+/* dit_attention with the persistent kernel's work split.  The (query pair,
+ * head) units of a launch are spread over at most max_ctas CTAs (0: one per
+ * multiprocessor); the units that would form a last, partial wave are cut
+ * into key ranges shared by all CTAs, each range continuing the running max,
+ * sum and fp32 output of the range before it, so that every CTA gets the
+ * same number of key tiles.  Key tiles are still visited in ascending order
+ * with the same arithmetic: the result equals dit_attention bit for bit.
+ * split_ws: device memory of dit_attention_split_bytes(head_dim, slots)
+ * bytes, 16-byte aligned, zero before its first use (the call leaves it so
+ * after a successful launch); bytes [0, 1024) hold one flag per slot, the
+ * rest the hand-off state of `slots` slots (slots = (split_bytes - 1024) /
+ * (1024 * (head_dim + 2)), at most 160).  A launch splits only if it needs no
+ * more slots than that; split_ws = NULL never splits.  Launches sharing one
+ * split_ws must not overlap on the device.  Errors: as dit_attention. */
+DIT_API size_t dit_attention_split_bytes(int head_dim, int slots);
+DIT_API dit_status_t dit_attention_ex(const void *q, int64_t Tq, int64_t ldq,
+                                      const void *k, int64_t ldk, const void *vt,
+                                      int64_t ldvt, int64_t T, int heads, int head_dim,
+                                      void *o, int64_t ldo, void *split_ws,
+                                      size_t split_bytes, int max_ctas, int *dev_status,
+                                      dit_stream_t stream);
+
+/* The persistent attention's work list, computed on the host exactly as the
+ * kernel computes it: `units` (query pair, head) units of n_kv key tiles on
+ * at most max_ctas CTAs with `slots` hand-off slots.  Writes the CTA count
+ * and the number of CTAs that share the remainder (0: none), and, while
+ * they fit in `cap` rows, one row of 7 ints per work item in each CTA's
+ * processing order: (cta, index, unit, first key tile, end key tile, slot
+ * read at the start or -1, slot written at the end or -1); *n_items is the
+ * total.  Host only; for checking the schedule. */
+DIT_API dit_status_t dit_attention_schedule(int units, int n_kv, int max_ctas, int slots,
+                                            int *n_cta, int *n_split, int *items,
+                                            int64_t cap, int64_t *n_items);
 
 #ifdef __cplusplus
 }

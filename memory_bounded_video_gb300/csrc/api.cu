@@ -23,6 +23,7 @@
 #include <new>
 #include <vector>
 
+#include "attn_sched.h"
 #include "internal.h"
 
 namespace ds {
@@ -163,11 +164,11 @@ void layout(dit_plan *p) {
     size_t phase;
     if (p->kvb) {  // K/V in host memory: a two-slot ring of key blocks
         p->off_k = p->off_vt = 0;
-        p->off_ring = A;  // [0, 256): device status words
+        p->off_ring = A;  // [0, 1024): header (status word, attention flags)
         p->ring_slot = round_up(4 * size_t(p->kvb) * Dz, A);
         phase = p->off_ring + 2 * p->ring_slot;
     } else {
-        p->off_k = A;  // [0, 256): device status words
+        p->off_k = A;  // [0, 1024): header (status word, attention flags)
         p->off_vt = round_up(p->off_k + 2 * size_t(p->T) * Dz, A);
         phase = round_up(p->off_vt + 2 * Dz * size_t(p->t_pad), A);
     }
@@ -183,6 +184,15 @@ void layout(dit_plan *p) {
         p->off_mst = round_up(p->off_ost + 4 * size_t(p->ca) * Dz, A);
         p->off_lst = round_up(p->off_mst + 4 * size_t(p->ca) * size_t(p->heads), A);
         attn_end = round_up(p->off_lst + 4 * size_t(p->ca) * size_t(p->heads), A);
+    }
+    // hand-off state of the attention's split units, when a slab has enough
+    // (query pair, head) units to leave a partial wave on some device
+    const int64_t units = (int64_t(p->ca) + 255) / 256 * p->heads;
+    p->split_slots = units < (int64_t(1) << 30) ? attn_slots_needed(int(units)) : 0;
+    p->off_split = 0;
+    if (p->split_slots) {
+        p->off_split = attn_end;
+        attn_end = round_up(p->off_split + attn_split_state_bytes(p->split_slots, p->head_dim), A);
     }
     // MLP phase (aliases the attention phase: the two never overlap in time)
     p->off_b = phase;
@@ -432,7 +442,7 @@ dit_status_t dit_block_bind_workspace(dit_plan_t *p, void *dev_ptr, size_t bytes
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
     if (e != cudaSuccess) return cuda_fail(e);
     if (major != 10 || minor != 3) return DIT_ERR_UNSUPPORTED_ARCH;
-    e = cudaMemset(dev_ptr, 0, 256);
+    e = cudaMemset(dev_ptr, 0, kHeaderBytes);
     if (e != cudaSuccess) return cuda_fail(e);
     p->ws = static_cast<uint8_t *>(dev_ptr);
     p->ws_bytes = bytes;
@@ -698,6 +708,9 @@ dit_status_t dit_block_forward_ex(const dit_plan_t *cp, float *x, const dit_bloc
             t0 = t1;
         }
     }
+    // the attention's hand-off space for split units
+    const AttnSplit split{reinterpret_cast<int *>(p->ws + kFlagsOffset),
+                          reinterpret_cast<float *>(p->ws + p->off_split), p->split_slots, 0};
     int64_t kv_c = 0;  // blocks of pass two consumed so far
     // pass two's first block; the copy stream is in order, so it follows
     // pass one's copies to the host
@@ -734,7 +747,7 @@ dit_status_t dit_block_forward_ex(const dit_plan_t *cp, float *x, const dit_bloc
         if (!kvb) {
             if ((r = timed(p, st, DIT_K_ATTENTION, 4.0 * rows * double(T) * D, [&] {
                      return launch_attention(Q, rows, D, K, D, Vt, p->t_pad, T, p->heads,
-                                             p->head_dim, a, D, status, st);
+                                             p->head_dim, a, D, status, st, nullptr, &split);
                  })) != DIT_OK)
                 return r;
         } else {
@@ -751,7 +764,7 @@ dit_status_t dit_block_forward_ex(const dit_plan_t *cp, float *x, const dit_bloc
                 if ((r = timed(p, st, DIT_K_ATTENTION, 4.0 * rows * double(kb) * D, [&] {
                          return launch_attention(Q, rows, D, slot_k(slot), D, slot_vt(slot),
                                                  kvb, kb, p->heads, p->head_dim, a, D, status,
-                                                 st, &as);
+                                                 st, &as, &split);
                      })) != DIT_OK)
                     return r;
                 e = cudaEventRecord(p->ev_used[slot], st);
@@ -869,7 +882,10 @@ dit_status_t dit_block_sync_status(const dit_plan_t *p, dit_stream_t stream) {
     if (!p->ws) return DIT_OK;
     int v = 0;
     e = cudaMemcpyAsync(&v, p->ws, sizeof(int), cudaMemcpyDeviceToHost, st);
-    if (e == cudaSuccess && v != 0) e = cudaMemsetAsync(p->ws, 0, sizeof(int), st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    // after a failure the hand-off flags may be left set: clear them with
+    // the status word
+    if (e == cudaSuccess && v != 0) e = cudaMemsetAsync(p->ws, 0, kHeaderBytes, st);
     if (e == cudaSuccess) e = cudaStreamSynchronize(st);
     if (e != cudaSuccess) return cuda_fail(e);
     return v == 0 ? DIT_OK : (v == DIT_ERR_TIMEOUT ? DIT_ERR_TIMEOUT : DIT_ERR_CUDA);
@@ -905,6 +921,59 @@ dit_status_t dit_attention_part(const void *q, int64_t Tq, int64_t ldq, const vo
     AttnState as{o_state, m_state, l_state, ld_state, first != 0, last != 0};
     return launch_attention(q, Tq, ldq, k, ldk, vt, ldvt, T_block, heads, head_dim, o, ldo,
                             dev_status, static_cast<cudaStream_t>(stream), &as);
+}
+
+size_t dit_attention_split_bytes(int head_dim, int slots) {
+    if ((head_dim != 64 && head_dim != 128) || slots < 0 || slots > kAttnSplitSlots) return 0;
+    return kHeaderBytes + attn_split_state_bytes(slots, head_dim);
+}
+
+dit_status_t dit_attention_ex(const void *q, int64_t Tq, int64_t ldq, const void *k,
+                              int64_t ldk, const void *vt, int64_t ldvt, int64_t T, int heads,
+                              int head_dim, void *o, int64_t ldo, void *split_ws,
+                              size_t split_bytes, int max_ctas, int *dev_status,
+                              dit_stream_t stream) {
+    if (max_ctas < 0 || (head_dim != 64 && head_dim != 128)) return DIT_ERR_INVALID_ARG;
+    AttnSplit split{nullptr, nullptr, 0, max_ctas};
+    if (split_ws) {
+        if (!aligned16(split_ws)) return DIT_ERR_ALIGN;
+        if (split_bytes < kHeaderBytes) return DIT_ERR_WORKSPACE_TOO_SMALL;
+        const size_t per = attn_split_state_bytes(1, head_dim);
+        size_t n = (split_bytes - kHeaderBytes) / per;
+        if (n > size_t(kAttnSplitSlots)) n = kAttnSplitSlots;
+        split.flags = static_cast<int *>(split_ws);
+        split.state = reinterpret_cast<float *>(static_cast<uint8_t *>(split_ws) + kHeaderBytes);
+        split.slots = int(n);
+    }
+    return launch_attention(q, Tq, ldq, k, ldk, vt, ldvt, T, heads, head_dim, o, ldo, dev_status,
+                            static_cast<cudaStream_t>(stream), nullptr, &split);
+}
+
+dit_status_t dit_attention_schedule(int units, int n_kv, int max_ctas, int slots, int *n_cta,
+                                    int *n_split, int *items, int64_t cap, int64_t *n_items) {
+    if (units <= 0 || n_kv <= 0 || max_ctas <= 0 || slots < 0 || cap < 0)
+        return DIT_ERR_INVALID_ARG;
+    const AttnGrid g = attn_grid(units, n_kv, max_ctas, slots);
+    if (n_cta) *n_cta = g.n_cta;
+    if (n_split) *n_split = g.n_pc;
+    int64_t n = 0;
+    for (int c = 0; c < g.n_cta; ++c) {
+        const AttnCta cs = attn_cta(g, c);
+        for (int i = 0; i < cs.count; ++i, ++n) {
+            if (!items || n >= cap) continue;
+            const AttnItem it = attn_item(g, cs, c, i);
+            int *row = items + 7 * n;
+            row[0] = c;
+            row[1] = i;
+            row[2] = it.u;
+            row[3] = it.k0;
+            row[4] = it.k1;
+            row[5] = it.src;
+            row[6] = it.dst;
+        }
+    }
+    if (n_items) *n_items = n;
+    return DIT_OK;
 }
 
 dit_status_t dit_attention(const void *q, int64_t Tq, int64_t ldq, const void *k, int64_t ldk,

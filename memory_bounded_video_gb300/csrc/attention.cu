@@ -6,9 +6,15 @@
 // the key loop runs over all T keys in tiles of 128, always in ascending
 // order, so a query's output does not depend on the slab it belongs to.
 //
-// Roles (384 threads, one CTA per SM):
-//   warp 0        TMA: both Q tiles once, then K_j and V_j^T tiles through one
-//                 shared ring (K_0, V_0, K_1, V_1, ...)
+// Persistent: one CTA per SM works through a list of (unit, key range)
+// items (attn_sched.h), where a unit is one head and one pair of query tiles;
+// the last, partial wave of units is cut into key ranges shared by all CTAs,
+// handing the softmax state from CTA to CTA, so that every SM gets the same
+// number of key tiles.
+//
+// Roles (384 threads):
+//   warp 0        TMA: per item both Q tiles, then K_j and V_j^T tiles
+//                 through one shared ring (K_0, V_0, K_1, V_1, ...)
 //   warp 1        TMEM owner; one lane issues the tcgen05.mma:
 //                   S_X  = Q_X K_j^T  (M=128, N=128, K=d)     -> TMEM S[X]
 //                   O_X += P_X V_j    (M=128, N=d,   K=128)   -> TMEM O[X]
@@ -28,6 +34,7 @@
 //
 // V arrives transposed (V^T [H*d, T], written so by the K/V projection's
 // epilogue), which makes both MMAs K-major in both operands.
+#include "attn_sched.h"
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -48,7 +55,7 @@ struct ACfg {
     static constexpr int OFF_Q = 0;
     static constexpr int OFF_RING = OFF_Q + 2 * Q_BYTES;
     static constexpr int OFF_BAR = OFF_RING + RING * TILE_BYTES;
-    static constexpr int SMEM_BYTES = OFF_BAR + 256 + 1024;
+    static constexpr int SMEM_BYTES = OFF_BAR + 512 + 1024;  // + barriers, schedule
     static constexpr int TMEM_COLS = 512;
     static constexpr int COL_O = 2 * kBKV;                // S_A S_B | O_A O_B
 };
@@ -69,7 +76,38 @@ struct AttnParams {
     int64_t ld_state;
     int heads;
     int first, last;
+    // persistent schedule and the hand-off space of split units
+    AttnGrid g;
+    int n_qpairs;             // query-tile pairs per head
+    int *split_flags;         // [slots]
+    float *split_state;       // [slots][256 * (HD + 2)]: m, l, O
 };
+
+// Release / acquire of the hand-off flags (device scope).
+DEV void flag_release(int *f) {
+    asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(f), "r"(1) : "memory");
+}
+DEV int flag_acquire(const int *f) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(f) : "memory");
+    return v;
+}
+
+// Bounded wait for a hand-off flag; false (with the timeout recorded) if it
+// was not set within the limit or another wait of this CTA gave up.
+DEV bool flag_wait(const int *f, const WaitCtx &w) {
+    if (flag_acquire(f)) return true;
+    const uint64_t t0 = globaltimer();
+    while (true) {
+        __nanosleep(128);
+        if (flag_acquire(f)) return true;
+        if (*w.abort) return false;
+        if (globaltimer() - t0 > kWaitLimitNs) {
+            record_timeout(w);
+            return false;
+        }
+    }
+}
 
 DEV float ex2(float x) {
     float y;
@@ -161,22 +199,29 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const AttnParams p) {
     using C = ACfg<HD>;
+    constexpr int kSlotFloats = 2 * kBQ * (HD + 2);  // m, l, O of 256 rows
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + C::OFF_BAR);
     // bars: q_full, ring_full[RING], ring_empty[RING], s_full[2], p_full[2],
-    //       o_full, drain
+    //       o_full, drain, q_empty, handed (split state written)
     constexpr int B_Q = 0, B_RF = 1, B_RE = B_RF + C::RING, B_SF = B_RE + C::RING,
-                  B_PF = B_SF + 2, B_O = B_PF + 2, B_DR = B_O + 1, NBAR = B_DR + 1;
+                  B_PF = B_SF + 2, B_O = B_PF + 2, B_DR = B_O + 1, B_QE = B_DR + 1,
+                  B_HD = B_QE + 1, NBAR = B_HD + 1;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + NBAR);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     const uint32_t bar0 = smem_u32(bars);
     auto bar = [&](int i) { return bar0 + 8u * i; };
 
     const int warp = warp_id(), lane = lane_id();
-    const int qpair = blockIdx.x, head = blockIdx.y;
+    const int cta = blockIdx.x;
     const int n_kv = p.n_kv;
+    // this CTA's pieces, in shared memory (kept out of the registers of the
+    // softmax loop)
+    AttnCta *cs_smem = reinterpret_cast<AttnCta *>(sm + C::OFF_BAR + 256);
+    if (threadIdx.x == 0) *cs_smem = attn_cta(p.g, cta);
+    const AttnCta &cs = *cs_smem;
 
     if (threadIdx.x == 0) {
         mbar_init(bar(B_Q), 1);
@@ -190,6 +235,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mbar_init(bar(B_O), 1);
         mbar_init(bar(B_DR), 1);
+        mbar_init(bar(B_QE), 1);
+        mbar_init(bar(B_HD), 2 * 128);
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -221,113 +268,176 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0) {
         if (lane == 0) {
             // ------------------------------------------------ TMA producer
-            mbar_arrive_expect_tx(bar(B_Q), 2 * C::Q_BYTES);
-#pragma unroll
-            for (int x = 0; x < 2; ++x)
-#pragma unroll
-                for (int b = 0; b < HD / 64; ++b)
-                    tma_load_2d(sQ + x * C::Q_BYTES + b * (kBQ * 128), &tmQ, bar(B_Q),
-                                head * HD + 64 * b, (2 * qpair + x) * kBQ);
-            int seq = 0;
+            int rs = 0, nq = 0;             // ring stage; Q loads
+            int nl = 0;                     // ring loads issued
+            uint32_t rph = 0;               // ring pass parity
             bool ok = true;
-            for (int j = 0; ok && j < n_kv; ++j) {
-                for (int kind = 0; ok && kind < 2; ++kind, ++seq) {
-                    const int s = seq % C::RING;
-                    if (!mbar_wait(bar(B_RE + s), uint32_t((seq / C::RING) & 1) ^ 1u, wc)) {
-                        ok = false;
-                        break;
-                    }
-                    mbar_arrive_expect_tx(bar(B_RF + s), C::TILE_BYTES);
-                    const uint32_t dst = sRing + s * C::TILE_BYTES;
-                    if (kind == 0) {
+            auto ring_load = [&](int head, int j, int kind) -> bool {
+                if (!mbar_wait(bar(B_RE + rs), rph ^ 1u, wc)) return false;
+                mbar_arrive_expect_tx(bar(B_RF + rs), C::TILE_BYTES);
+                const uint32_t dst = sRing + rs * C::TILE_BYTES;
+                if (kind == 0) {
 #pragma unroll
-                        for (int b = 0; b < HD / 64; ++b)
-                            tma_load_2d(dst + b * (kBKV * 128), &tmK, bar(B_RF + s),
-                                        head * HD + 64 * b, j * kBKV);
-                    } else {
+                    for (int b = 0; b < HD / 64; ++b)
+                        tma_load_2d(dst + b * (kBKV * 128), &tmK, bar(B_RF + rs),
+                                    head * HD + 64 * b, j * kBKV);
+                } else {
 #pragma unroll
-                        for (int b = 0; b < kBKV / 64; ++b)
-                            tma_load_2d(dst + b * (HD * 128), &tmV, bar(B_RF + s),
-                                        j * kBKV + 64 * b, head * HD);
-                    }
+                    for (int b = 0; b < kBKV / 64; ++b)
+                        tma_load_2d(dst + b * (HD * 128), &tmV, bar(B_RF + rs),
+                                    j * kBKV + 64 * b, head * HD);
                 }
+                ++nl;
+                if (++rs == C::RING) {
+                    rs = 0;
+                    rph ^= 1u;
+                }
+                return true;
+            };
+            for (int idx = 0; ok && idx < cs.count; ++idx) {
+                const AttnItem it = attn_item(p.g, cs, cta, idx);
+                const int qpair = it.u % p.n_qpairs, head = it.u / p.n_qpairs;
+                // the item's first K/V tiles go ahead of its Q, which must
+                // wait until the previous item's last S MMAs have read Q
+                ok = ring_load(head, it.k0, 0) && ring_load(head, it.k0, 1);
+                if (ok && idx > 0) ok = mbar_wait(bar(B_QE), uint32_t((idx - 1) & 1), wc);
+                if (!ok) break;
+                mbar_arrive_expect_tx(bar(B_Q), 2 * C::Q_BYTES);
+#pragma unroll
+                for (int x = 0; x < 2; ++x)
+#pragma unroll
+                    for (int b = 0; b < HD / 64; ++b)
+                        tma_load_2d(sQ + x * C::Q_BYTES + b * (kBQ * 128), &tmQ, bar(B_Q),
+                                    head * HD + 64 * b, (2 * qpair + x) * kBQ);
+                ++nq;
+                for (int j = it.k0 + 1; ok && j < it.k1; ++j)
+                    ok = ring_load(head, j, 0) && ring_load(head, j, 1);
             }
             if (!ok) {  // let the copies in flight land before the CTA exits
-                mbar_wait_quiet(bar(B_Q), 0, kWaitLimitNs);
-                for (int i = seq > C::RING ? seq - C::RING : 0; i < seq; ++i)
-                    mbar_wait_quiet(bar(B_RF + i % C::RING), uint32_t((i / C::RING) & 1),
-                                    kWaitLimitNs);
+                if (nq > 0) mbar_wait_quiet(bar(B_Q), uint32_t((nq - 1) & 1), kWaitLimitNs);
+                for (int i = 0; i < C::RING && i < nl; ++i) {  // the last loads issued
+                    if (--rs < 0) {
+                        rs = C::RING - 1;
+                        rph ^= 1u;
+                    }
+                    mbar_wait_quiet(bar(B_RF + rs), rph, kWaitLimitNs);
+                }
             }
         }
     } else if (warp == 1) {
         if (lane == 0) {
             // ------------------------------------------------ MMA issuer
+            // One thread issues 32 MMAs per key tile (~1,000 tensor cycles at
+            // d = 128), so every instruction of this loop is on the critical
+            // path: shared-memory descriptors are computed once and stepped by
+            // constant offsets (16 bytes per unit of the address field, which
+            // cannot overflow), and the last key tile of an item is peeled so
+            // that the loop body has no branches but the waits.
             constexpr uint32_t ID_S = idesc_bf16_f32(kBQ, kBKV);
             constexpr uint32_t ID_PV = idesc_bf16_f32(kBQ, HD);
-            auto ring_wait = [&](int seq) {
-                return mbar_wait(bar(B_RF + seq % C::RING), uint32_t((seq / C::RING) & 1), wc);
-            };
-            auto issue_s = [&](int x, int seq) {
-                const uint32_t kb = sRing + (seq % C::RING) * C::TILE_BYTES;
-                const uint32_t qb = sQ + x * C::Q_BYTES;
+            const uint64_t dq0 = desc_sw128(sQ), dring = desc_sw128(sRing);
+            auto issue_s = [&](int x, int stage) {
+                const uint64_t dq = dq0 + uint64_t(x * (C::Q_BYTES >> 4));
+                const uint64_t dk = dring + uint64_t(stage * (C::TILE_BYTES >> 4));
                 const uint32_t d = tmem + uint32_t(x * kBKV);
 #pragma unroll
                 for (int kk = 0; kk < HD / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * (kBQ * 128) + (kk & 3) * 32;
-                    mma_bf16_ss(d, desc_sw128(qb + off), desc_sw128(kb + off), ID_S, kk > 0);
+                    const uint64_t off = uint64_t(((kk >> 2) * (kBQ * 128) + (kk & 3) * 32) >> 4);
+                    mma_bf16_ss(d, dq + off, dk + off, ID_S, kk > 0);
                 }
                 mma_commit(bar(B_SF + x));
             };
-            auto issue_pv = [&](int x, int seq, int j) {
-                const uint32_t vb = sRing + (seq % C::RING) * C::TILE_BYTES;
+            auto issue_pv = [&](int x, int stage, bool acc) {
+                const uint64_t dv = dring + uint64_t(stage * (C::TILE_BYTES >> 4));
                 const uint32_t pt = tmem + uint32_t(x * kBKV);  // P_X: lanes 0..127
                 const uint32_t d = tmem + uint32_t(C::COL_O + x * HD);
 #pragma unroll
                 for (int kk = 0; kk < kBKV / 16; ++kk) {
-                    const uint32_t offv = (kk >> 2) * (HD * 128) + (kk & 3) * 32;
-                    mma_bf16_ts(d, pt + uint32_t(8 * kk), desc_sw128(vb + offv), ID_PV,
-                                (j > 0 || kk > 0 || !p.first) ? 1u : 0u);
+                    const uint64_t offv = uint64_t(((kk >> 2) * (HD * 128) + (kk & 3) * 32) >> 4);
+                    mma_bf16_ts(d, pt + uint32_t(8 * kk), dv + offv, ID_PV,
+                                (acc || kk > 0) ? 1u : 0u);
                 }
             };
-            bool ok = mbar_wait(bar(B_Q), 0, wc) && ring_wait(0);
-            if (ok) {
-                tc_fence_after();
-                issue_s(0, 0);
-                issue_s(1, 0);
-                mma_commit(bar(B_RE + 0));
-            }
-            for (int j = 0; ok && j < n_kv; ++j) {
-                const int seq_v = 2 * j + 1, seq_k = 2 * j + 2;
-                const bool more = j + 1 < n_kv;
-                if (!ring_wait(seq_v) || !mbar_wait(bar(B_PF + 0), uint32_t(j & 1), wc)) {
+            // ring entries are read in the order they were filled (K_0, V_0,
+            // K_1, ...): the stage and its fill parity advance one by one
+            int rs = 0;
+            uint32_t rph = 0, tph = 0;  // ring pass parity; key tile parity
+            auto advance = [&]() {
+                if (++rs == C::RING) {
+                    rs = 0;
+                    rph ^= 1u;
+                }
+            };
+            bool ok = true;
+            for (int idx = 0; ok && idx < cs.count; ++idx) {
+                const AttnItem it = attn_item(p.g, cs, cta, idx);
+                const int nt = it.k1 - it.k0;
+                // O starts from a carried state unless this is the start of
+                // the unit's first launch
+                const bool carried = it.k0 > 0 || !p.first;
+                if (!mbar_wait(bar(B_Q), uint32_t(idx & 1), wc) ||
+                    !mbar_wait(bar(B_RF + rs), rph, wc)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                issue_pv(0, seq_v, j);
-                if (more) {
-                    if (!ring_wait(seq_k)) {
+                issue_s(0, rs);
+                issue_s(1, rs);
+                mma_commit(bar(B_RE + rs));
+                advance();
+                for (int jj = 0; jj + 1 < nt; ++jj) {
+                    const int sv = rs;  // V_j
+                    if (!mbar_wait(bar(B_RF + sv), rph, wc) || !mbar_wait(bar(B_PF + 0), tph, wc)) {
+                        ok = false;
+                        break;
+                    }
+                    advance();
+                    tc_fence_after();
+                    issue_pv(0, sv, jj > 0 || carried);
+                    const int sk = rs;  // K_{j+1}
+                    if (!mbar_wait(bar(B_RF + sk), rph, wc)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    issue_s(0, seq_k);
+                    issue_s(0, sk);
+                    if (!mbar_wait(bar(B_PF + 1), tph, wc)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    issue_pv(1, sv, jj > 0 || carried);
+                    mma_commit(bar(B_RE + sv));
+                    issue_s(1, sk);
+                    mma_commit(bar(B_RE + sk));
+                    advance();
+                    tph ^= 1u;
                 }
-                if (!mbar_wait(bar(B_PF + 1), uint32_t(j & 1), wc)) {
-                    ok = false;
-                    break;
+                if (!ok) break;
+                // the item's last S MMAs are issued: Q may be reloaded once
+                // they are complete
+                mma_commit(bar(B_QE));
+                {  // last key tile: PV only
+                    const int sv = rs;
+                    if (!mbar_wait(bar(B_RF + sv), rph, wc) || !mbar_wait(bar(B_PF + 0), tph, wc)) {
+                        ok = false;
+                        break;
+                    }
+                    advance();
+                    tc_fence_after();
+                    issue_pv(0, sv, nt > 1 || carried);
+                    if (!mbar_wait(bar(B_PF + 1), tph, wc)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    issue_pv(1, sv, nt > 1 || carried);
+                    mma_commit(bar(B_RE + sv));
+                    tph ^= 1u;
                 }
-                tc_fence_after();
-                issue_pv(1, seq_v, j);
-                mma_commit(bar(B_RE + seq_v % C::RING));
-                if (more) {
-                    issue_s(1, seq_k);
-                    mma_commit(bar(B_RE + seq_k % C::RING));
-                }
-            }
-            if (ok) {
                 mma_commit(bar(B_O));
-            } else {
+            }
+            if (!ok) {
                 mma_commit(bar(B_DR));
                 mbar_wait_quiet(bar(B_DR), 0, kWaitLimitNs);
             }
@@ -338,27 +448,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int x = (warp - 4) >> 2;          // tile A or B
         const int qd = warp & 3;                // TMEM lane quadrant
         const int row = qd * 32 + lane;         // query row within the tile
+        const int urow = x * kBQ + row;         // row within the unit's 256
         const uint32_t lane_base = tmem + (uint32_t(qd * 32) << 16);
         const uint32_t saddr = lane_base + uint32_t(x * kBKV);
         const uint32_t oaddr = lane_base + uint32_t(C::COL_O + x * HD);
         const float sl2 = p.scale_log2;
         const int last_valid = int(p.T - int64_t(n_kv - 1) * kBKV);  // keys in last tile
-        const int64_t qrow = (2 * int64_t(qpair) + x) * kBQ + row;
-        float m = -INFINITY, l = 0.f;
-        if (!p.first) {
-            // carried state of the earlier key blocks: m, l and O (into TMEM,
-            // before this tile's first PV MMA, which accumulates onto it)
-            const bool valid = qrow < p.Tq;
-            m = valid ? p.m_state[qrow * p.heads + head] : 0.f;
-            l = valid ? p.l_state[qrow * p.heads + head] : 0.f;
-            const float4 *src = reinterpret_cast<const float4 *>(
-                p.o_state + qrow * p.ld_state + int64_t(head) * HD);
+        // O of this row (HD fp32 values at src) into TMEM; rows beyond the
+        // queries read zeros
+        auto o_to_tmem = [&](const float *src, bool valid) {
+            const float4 *s4 = reinterpret_cast<const float4 *>(src);
 #pragma unroll
             for (int c0 = 0; c0 < HD; c0 += 32) {
                 uint32_t r[32];
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
-                    const float4 v = valid ? src[(c0 >> 2) + i] : make_float4(0.f, 0.f, 0.f, 0.f);
+                    const float4 v = valid ? s4[(c0 >> 2) + i] : make_float4(0.f, 0.f, 0.f, 0.f);
                     r[4 * i] = __float_as_uint(v.x);
                     r[4 * i + 1] = __float_as_uint(v.y);
                     r[4 * i + 2] = __float_as_uint(v.z);
@@ -367,104 +472,184 @@ __global__ void __launch_bounds__(kThreads, 1)
                 __syncwarp();
                 tmem_st32_sync(oaddr + c0, r);
             }
-        }
-        bool ok = true;
-        for (int j = 0; j < n_kv; ++j) {
-            bool w = mbar_wait(bar(B_SF + x), uint32_t(j & 1), wc);
-            w = __all_sync(0xffffffffu, w);
-            if (!w) {
-                ok = false;
-                break;
-            }
-            tc_fence_after();
-            const bool masked = (j == n_kv - 1) && last_valid < kBKV;
-            const float mx =
-                (masked ? tile_max<true>(saddr, last_valid) : tile_max<false>(saddr, kBKV)) *
-                sl2;
-            if (j == 0 && p.first) {  // no reference max yet: the tile's own
-                m = mx;
-            } else if (__any_sync(0xffffffffu, mx > m + kRescaleLog2)) {
-                // Move the reference max of the rows that need it: O_row *=
-                // 2^(m - m_new), l likewise.  The branch is warp-uniform (the
-                // TMEM accesses are warp-collective); the other rows keep m
-                // and are multiplied by exactly 1, so each row's result
-                // depends on that row alone.
-                const float m_new = (mx > m + kRescaleLog2) ? mx : m;
-                const float alpha = ex2(m - m_new);
-#pragma unroll
-                for (int c0 = 0; c0 < HD; c0 += 32) {
-                    uint32_t r[32];
-                    tmem_ld32(oaddr + c0, r);
-                    tmem_ld_wait(r);
-#pragma unroll
-                    for (int c = 0; c < 32; ++c)
-                        r[c] = __float_as_uint(__uint_as_float(r[c]) * alpha);
-                    tmem_st32_sync(oaddr + c0, r);
-                }
-                l *= alpha;
-                m = m_new;
-            }
-            const float sum = masked ? tile_exp<true>(saddr, sl2, m, last_valid)
-                                     : tile_exp<false>(saddr, sl2, m, kBKV);
-            l += sum;
-            tmem_st_wait();    // P is in tensor memory before the PV MMA reads it
-            tc_fence_before(); // S/O/P accesses finish before the next MMAs
-            mbar_arrive(bar(B_PF + x));
-        }
-        if (ok) {
-            bool w = mbar_wait(bar(B_O), 0, wc);
-            ok = __all_sync(0xffffffffu, w);
-        }
-        if (ok && !p.last) {
-            // hand the state to the next key block's launch
-            tc_fence_after();
-            if (qrow < p.Tq) {
-                p.m_state[qrow * p.heads + head] = m;
-                p.l_state[qrow * p.heads + head] = l;
-            }
-            float4 *dst = reinterpret_cast<float4 *>(p.o_state + qrow * p.ld_state +
-                                                     int64_t(head) * HD);
+        };
+        // O of this row from TMEM to dst (fp32), if valid
+        auto o_from_tmem = [&](float *dst, bool valid) {
+            float4 *d4 = reinterpret_cast<float4 *>(dst);
 #pragma unroll
             for (int c0 = 0; c0 < HD; c0 += 32) {
                 uint32_t r[32];
                 __syncwarp();
                 tmem_ld32(oaddr + c0, r);
                 tmem_ld_wait(r);
-                if (qrow < p.Tq) {
+                if (valid) {
 #pragma unroll
                     for (int i = 0; i < 8; ++i)
-                        dst[(c0 >> 2) + i] =
+                        d4[(c0 >> 2) + i] =
                             make_float4(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]),
                                         __uint_as_float(r[4 * i + 2]),
                                         __uint_as_float(r[4 * i + 3]));
                 }
             }
-        } else if (ok) {
+        };
+        // query row of this thread in item `it` (global index) and its head
+        auto qrow_of = [&](const AttnItem &it) {
+            return (2 * int64_t(it.u % p.n_qpairs) + x) * kBQ + row;
+        };
+        bool ok = true;
+        int tc = 0;  // key tiles done
+        for (int idx = 0; ok && idx < cs.count; ++idx) {
+            float m = -INFINITY, l = 0.f;
+            int k0, nt;
+            {
+                const AttnItem it = attn_item(p.g, cs, cta, idx);
+                k0 = it.k0;
+                nt = it.k1 - it.k0;
+                // the state this item starts from: the CTA before's at k0
+                // (the unit's earlier keys ran there), or the earlier
+                // launches' (earlier key blocks); O goes into TMEM before
+                // this item's first PV MMA, which accumulates onto it
+                const float *src = nullptr;
+                bool valid = true;
+                if (it.k0 > 0) {
+                    const bool w = flag_wait(p.split_flags + it.src, wc);
+                    if (!__all_sync(0xffffffffu, w)) {
+                        ok = false;
+                        break;
+                    }
+                    const float *slot = p.split_state + size_t(it.src) * kSlotFloats;
+                    m = slot[urow];
+                    l = slot[2 * kBQ + urow];
+                    src = slot + 4 * kBQ + size_t(urow) * HD;
+                } else if (!p.first) {
+                    const int64_t qrow = qrow_of(it);
+                    const int head = it.u / p.n_qpairs;
+                    valid = qrow < p.Tq;
+                    m = valid ? p.m_state[qrow * p.heads + head] : 0.f;
+                    l = valid ? p.l_state[qrow * p.heads + head] : 0.f;
+                    src = p.o_state + qrow * p.ld_state + int64_t(head) * HD;
+                }
+                if (src) o_to_tmem(src, valid);
+            }
+            const bool fresh = k0 == 0 && p.first;
+            for (int jj = 0; jj < nt; ++jj) {
+                const int j = k0 + jj;
+                bool w = mbar_wait(bar(B_SF + x), uint32_t((tc + jj) & 1), wc);
+                w = __all_sync(0xffffffffu, w);
+                if (!w) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const bool masked = (j == n_kv - 1) && last_valid < kBKV;
+                const float mx =
+                    (masked ? tile_max<true>(saddr, last_valid) : tile_max<false>(saddr, kBKV)) *
+                    sl2;
+                if (jj == 0 && fresh) {  // no reference max yet: the tile's own
+                    m = mx;
+                } else if (__any_sync(0xffffffffu, mx > m + kRescaleLog2)) {
+                    // Move the reference max of the rows that need it: O_row *=
+                    // 2^(m - m_new), l likewise.  The branch is warp-uniform (the
+                    // TMEM accesses are warp-collective); the other rows keep m
+                    // and are multiplied by exactly 1, so each row's result
+                    // depends on that row alone.
+                    const float m_new = (mx > m + kRescaleLog2) ? mx : m;
+                    const float alpha = ex2(m - m_new);
+#pragma unroll
+                    for (int c0 = 0; c0 < HD; c0 += 32) {
+                        uint32_t r[32];
+                        tmem_ld32(oaddr + c0, r);
+                        tmem_ld_wait(r);
+#pragma unroll
+                        for (int c = 0; c < 32; ++c)
+                            r[c] = __float_as_uint(__uint_as_float(r[c]) * alpha);
+                        tmem_st32_sync(oaddr + c0, r);
+                    }
+                    l *= alpha;
+                    m = m_new;
+                }
+                const float sum = masked ? tile_exp<true>(saddr, sl2, m, last_valid)
+                                         : tile_exp<false>(saddr, sl2, m, kBKV);
+                l += sum;
+                tmem_st_wait();    // P is in tensor memory before the PV MMA reads it
+                tc_fence_before(); // S/O/P accesses finish before the next MMAs
+                mbar_arrive(bar(B_PF + x));
+            }
+            if (!ok) break;
+            // the item is looked up again rather than kept in registers
+            // across the key loop
+            const AttnItem it = attn_item(p.g, cs, cta, idx);
+            const int64_t qrow = qrow_of(it);
+            const int head = it.u / p.n_qpairs;
+            const bool valid = qrow < p.Tq;
+            {
+                const bool w = mbar_wait(bar(B_O), uint32_t(idx & 1), wc);
+                if (!__all_sync(0xffffffffu, w)) {
+                    ok = false;
+                    break;
+                }
+            }
             tc_fence_after();
-            const float inv = 1.0f / l;
-            uint4 *dst = reinterpret_cast<uint4 *>(p.o + qrow * p.ldo + int64_t(head) * HD);
+            if (it.k1 < n_kv || !p.last) {
+                // hand m, l and O at key tile k1 on: to the CTA that continues
+                // the unit (all 256 rows write, then one thread sets the flag;
+                // a CTA hands on at most once, since only its range's end can
+                // fall inside a unit), or to the next key block's launch
+                const bool split = it.k1 < n_kv;
+                float *slot = p.split_state + size_t(split ? it.dst : 0) * kSlotFloats;
+                float *mp = split ? slot + urow : p.m_state + qrow * p.heads + head;
+                float *lp = split ? slot + 2 * kBQ + urow : p.l_state + qrow * p.heads + head;
+                float *dst = split ? slot + 4 * kBQ + size_t(urow) * HD
+                                   : p.o_state + qrow * p.ld_state + int64_t(head) * HD;
+                const bool v = split || valid;
+                if (v) {
+                    *mp = m;
+                    *lp = l;
+                }
+                o_from_tmem(dst, v);
+                if (split) {
+                    __threadfence();
+                    mbar_arrive(bar(B_HD));
+                    if (x == 0 && row == 0) {
+                        if (!mbar_wait(bar(B_HD), 0u, wc)) {
+                            ok = false;
+                        } else {
+                            __threadfence();
+                            flag_release(p.split_flags + it.dst);
+                        }
+                    }
+                    ok = __all_sync(0xffffffffu, ok);
+                }
+            } else {
+                const float inv = 1.0f / l;
+                uint4 *dst = reinterpret_cast<uint4 *>(p.o + qrow * p.ldo + int64_t(head) * HD);
 #pragma unroll
-            for (int c0 = 0; c0 < HD; c0 += 32) {
-                uint32_t r[32];
-                __syncwarp();
-                tmem_ld32(oaddr + c0, r);
-                tmem_ld_wait(r);
-                if (qrow < p.Tq) {
+                for (int c0 = 0; c0 < HD; c0 += 32) {
+                    uint32_t r[32];
+                    __syncwarp();
+                    tmem_ld32(oaddr + c0, r);
+                    tmem_ld_wait(r);
+                    if (valid) {
 #pragma unroll
-                    for (int c = 0; c < 32; c += 8) {
-                        uint4 v;
-                        v.x = pack_bf16x2(__uint_as_float(r[c]) * inv,
-                                          __uint_as_float(r[c + 1]) * inv);
-                        v.y = pack_bf16x2(__uint_as_float(r[c + 2]) * inv,
-                                          __uint_as_float(r[c + 3]) * inv);
-                        v.z = pack_bf16x2(__uint_as_float(r[c + 4]) * inv,
-                                          __uint_as_float(r[c + 5]) * inv);
-                        v.w = pack_bf16x2(__uint_as_float(r[c + 6]) * inv,
-                                          __uint_as_float(r[c + 7]) * inv);
-                        dst[(c0 + c) >> 3] = v;
+                        for (int c = 0; c < 32; c += 8) {
+                            uint4 v;
+                            v.x = pack_bf16x2(__uint_as_float(r[c]) * inv,
+                                              __uint_as_float(r[c + 1]) * inv);
+                            v.y = pack_bf16x2(__uint_as_float(r[c + 2]) * inv,
+                                              __uint_as_float(r[c + 3]) * inv);
+                            v.z = pack_bf16x2(__uint_as_float(r[c + 4]) * inv,
+                                              __uint_as_float(r[c + 5]) * inv);
+                            v.w = pack_bf16x2(__uint_as_float(r[c + 6]) * inv,
+                                              __uint_as_float(r[c + 7]) * inv);
+                            dst[(c0 + c) >> 3] = v;
+                        }
                     }
                 }
             }
+            // this item's TMEM reads are done before the next item's MMAs
+            // write O (the first PV waits for this thread's P arrival)
+            tc_fence_before();
+            tc += nt;
         }
     }
 
@@ -474,12 +659,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         tmem_dealloc(tmem, C::TMEM_COLS);
     }
+    // every thread of this CTA is past its wait on the flag it consumed:
+    // leave it zero for the next launch
+    if (threadIdx.x == 0 && cs.has_a && cs.a.src >= 0) p.split_flags[cs.a.src] = 0;
 }
 
 template <int HD>
 dit_status_t run(const void *q, int64_t Tq, int64_t ldq, const void *k, int64_t ldk,
                  const void *vt, int64_t ldvt, int64_t T, int heads, void *o, int64_t ldo,
-                 const AttnState *state, int *dev_status, cudaStream_t s) {
+                 const AttnState *state, const AttnSplit *split, int *dev_status,
+                 cudaStream_t s) {
     using C = ACfg<HD>;
     const uint64_t D = uint64_t(heads) * HD;
     const CUtensorMapDataType bf16 = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
@@ -506,6 +695,16 @@ dit_status_t run(const void *q, int64_t Tq, int64_t ldq, const void *k, int64_t 
         p.first = state->first;
         p.last = state->last;
     }
+    const int64_t qtiles = (Tq + kBQ - 1) / kBQ;
+    p.n_qpairs = int((qtiles + 1) / 2);
+    int max_cta = sm_count();
+    if (split && split->max_ctas > 0 && split->max_ctas < max_cta) max_cta = split->max_ctas;
+    const int slots = (split && split->flags && split->state) ? split->slots : 0;
+    p.g = attn_grid(p.n_qpairs * heads, p.n_kv, max_cta, slots);
+    if (p.g.n_pc > 0) {
+        p.split_flags = split->flags;
+        p.split_state = split->state;
+    }
     static bool attr_done = false;
     if (!attr_done) {
         cudaError_t e = cudaFuncSetAttribute(
@@ -513,9 +712,20 @@ dit_status_t run(const void *q, int64_t Tq, int64_t ldq, const void *k, int64_t 
         if (e != cudaSuccess) return cuda_fail(e);
         attr_done = true;
     }
-    const int64_t qtiles = (Tq + kBQ - 1) / kBQ;
-    const dim3 grid(unsigned((qtiles + 1) / 2), unsigned(heads));
-    attn_fwd_kernel<HD><<<grid, kThreads, C::SMEM_BYTES, s>>>(tQ, tK, tV, p);
+    // CTAs that hand state to one another must all be resident at once: a
+    // cooperative launch guarantees it (one CTA per SM, at most one per SM)
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(unsigned(p.g.n_cta));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = C::SMEM_BYTES;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = p.g.n_pc > 0 ? 1 : 0;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, attn_fwd_kernel<HD>, tQ, tK, tV, p);
+    if (e != cudaSuccess) return cuda_fail(e);
     return check_launch();
 }
 
@@ -524,7 +734,8 @@ dit_status_t run(const void *q, int64_t Tq, int64_t ldq, const void *k, int64_t 
 dit_status_t launch_attention(const void *q, int64_t Tq, int64_t ldq, const void *k,
                               int64_t ldk, const void *vt, int64_t ldvt, int64_t T,
                               int heads, int head_dim, void *o, int64_t ldo, int *dev_status,
-                              cudaStream_t s, const AttnState *state) {
+                              cudaStream_t s, const AttnState *state,
+                              const AttnSplit *split) {
     if (Tq < 0 || T <= 0 || heads <= 0 || (head_dim != 64 && head_dim != 128))
         return DIT_ERR_INVALID_ARG;
     if (!q || !k || !vt || !o) return DIT_ERR_INVALID_ARG;
@@ -532,8 +743,14 @@ dit_status_t launch_attention(const void *q, int64_t Tq, int64_t ldq, const void
     const int64_t D = int64_t(heads) * head_dim;
     if (ldq < D || ldk < D || ldo < D || ldvt < T) return DIT_ERR_INVALID_ARG;
     if (ldq % 8 || ldk % 8 || ldo % 8 || ldvt % 8) return DIT_ERR_INVALID_ARG;
-    if (Tq > (int64_t(1) << 31) - 2 * kBQ || T > (int64_t(1) << 31) - kBKV || heads > 65535)
+    if (Tq > (int64_t(1) << 31) - 2 * kBQ || T > (int64_t(1) << 31) - kBKV ||
+        (Tq + 2 * kBQ - 1) / (2 * kBQ) * heads > (int64_t(1) << 30))
         return DIT_ERR_INVALID_ARG;
+    if (split && split->slots > 0) {
+        if (!split->flags || !split->state || split->slots > kAttnSplitSlots)
+            return DIT_ERR_INVALID_ARG;
+        if (!aligned16(split->state)) return DIT_ERR_ALIGN;
+    }
     if (state) {
         if (!state->o || !state->m || !state->l) return DIT_ERR_INVALID_ARG;
         if (!aligned16(state->o) || state->ld < D || state->ld % 4) return DIT_ERR_ALIGN;
@@ -541,8 +758,10 @@ dit_status_t launch_attention(const void *q, int64_t Tq, int64_t ldq, const void
     }
     if (Tq == 0) return DIT_OK;
     if (head_dim == 64)
-        return run<64>(q, Tq, ldq, k, ldk, vt, ldvt, T, heads, o, ldo, state, dev_status, s);
-    return run<128>(q, Tq, ldq, k, ldk, vt, ldvt, T, heads, o, ldo, state, dev_status, s);
+        return run<64>(q, Tq, ldq, k, ldk, vt, ldvt, T, heads, o, ldo, state, split, dev_status,
+                       s);
+    return run<128>(q, Tq, ldq, k, ldk, vt, ldvt, T, heads, o, ldo, state, split, dev_status,
+                    s);
 }
 
 }  // namespace ds

@@ -1,0 +1,171 @@
+// Work schedule of the persistent attention kernel (host and device code).
+//
+// A unit is one head and one pair of 128-query tiles, attended against all
+// n_kv key tiles in ascending order.  With U units on G CTAs (G = min(U,
+// SMs)), CTA c takes the F = U / G whole units c, c + G, ..., c + (F-1) G,
+// the order in which a one-unit-per-CTA grid would run them.  The R = U % G
+// remaining units would otherwise run as a last, mostly idle wave; instead
+// their R * n_kv key tiles, laid out unit by unit, are cut into n_pc equal
+// contiguous ranges, one per CTA c < n_pc.  A range covers the end of one
+// unit (piece A) and possibly the start of the next (piece B).
+//
+// A unit cut between CTAs is still computed as one pass over its keys: the
+// CTA holding keys [k0, k1) takes over the running max, sum and unnormalised
+// fp32 output at k0 from the CTA before it (slot c, flag c) and, if the unit
+// goes on past k1, hands them to the CTA after it (slot c + 1), so every
+// output element sees the same operations in the same order as in one CTA.
+// A piece that starts a unit has no input and is run first; the piece that
+// continues a unit at chain position p (p CTAs before it hold earlier keys of
+// that unit) is run after p whole units, by which time the piece before it,
+// run at position p - 1 on the CTA before, has long finished.  Positions are
+// at most F when n_pc <= R * F, since a unit then spans at most F + 1
+// ranges, or when every unit is cut into the same q <= F + 1 aligned ranges;
+// a larger position is clamped to F (correct, only slower).
+#pragma once
+
+#include <stdint.h>
+
+#if defined(__CUDACC__)
+#define DS_HD __host__ __device__ __forceinline__
+#else
+#define DS_HD inline
+#endif
+
+namespace ds {
+
+// Most CTAs that may share the remainder: one state slot and one flag each.
+constexpr int kAttnSplitSlots = 160;
+
+
+struct AttnItem {
+    int u;       // unit: query pair u % n_qpairs, head u / n_qpairs
+    int k0, k1;  // key tiles [k0, k1)
+    int src;     // slot holding the state at k0 (k0 > 0), else -1
+    int dst;     // slot to hand the state at k1 to (k1 < n_kv), else -1
+};
+
+struct AttnGrid {
+    int units, n_kv, n_cta;
+    int full;           // whole units per CTA (split mode); 0: round robin
+    int n_pc;           // CTAs sharing the remainder (0: no split)
+    int64_t rem_tiles;  // remainder key tiles R * n_kv
+    int rem_u0;         // first remainder unit, full * n_cta
+};
+
+// Grid and split for U units of n_kv key tiles on at most max_cta CTAs;
+// slots: state slots available (0: no split; slot c is used by CTAs c - 1
+// and c, for 0 < c < n_pc).
+DS_HD AttnGrid attn_grid(int units, int n_kv, int max_cta, int slots) {
+    AttnGrid g{};
+    g.units = units;
+    g.n_kv = n_kv;
+    g.n_cta = units < max_cta ? units : max_cta;
+    if (g.n_cta < 1) g.n_cta = 1;
+    const int F = units / g.n_cta, R = units % g.n_cta;
+    if (R > 0) {
+        // Ranges of any length at least n_kv / F keep every unit within
+        // F + 1 ranges; ranges of exactly n_kv / q (q of them per unit,
+        // aligned to the units) allow q = F + 1.  The more CTAs share the
+        // remainder, the shorter the longest range.
+        int64_t n1 = g.n_cta;
+        if (int64_t(R) * F < n1) n1 = int64_t(R) * F;
+        if (int64_t(R) * n_kv < n1) n1 = int64_t(R) * n_kv;
+        int64_t q = F + 1;
+        if (g.n_cta / R < q) q = g.n_cta / R;
+        if (n_kv < q) q = n_kv;
+        const int64_t n = n1 > R * q ? n1 : R * q;
+        // split only if the longest range is shorter than a unit (else every
+        // remainder unit stays whole, round robin, as it does when the
+        // hand-off space has too few slots)
+        const int64_t longest = (int64_t(R) * n_kv + n - 1) / n;
+        if (longest < n_kv && n <= slots) {
+            g.full = F;
+            g.n_pc = int(n);
+            g.rem_tiles = int64_t(R) * n_kv;
+            g.rem_u0 = F * g.n_cta;
+        }
+    }
+    return g;
+}
+
+// Multiprocessor counts a plan sizes its hand-off space for (the plan is
+// made without a device; a device outside the range may split less).
+constexpr int kAttnMinSms = 128, kAttnMaxSms = 160;
+
+// State slots that units of an attention slab may need on any device with
+// kAttnMinSms..kAttnMaxSms multiprocessors, whatever its key count.
+inline int attn_slots_needed(int units) {
+    int need = 0;
+    for (int sm = kAttnMinSms; sm <= kAttnMaxSms; ++sm) {
+        const AttnGrid g = attn_grid(units, 1 << 20, sm, kAttnSplitSlots);
+        if (g.n_pc > need) need = g.n_pc;
+    }
+    return need;
+}
+
+// The pieces of CTA c and where piece A goes among its whole units.
+struct AttnCta {
+    int count;  // items
+    int has_a, has_b, pos_a;
+    AttnItem a, b;
+};
+
+DS_HD AttnCta attn_cta(const AttnGrid &g, int c) {
+    AttnCta s{};
+    if (g.n_pc == 0) {  // round robin: units c, c + G, ... below U
+        s.count = c < g.units ? (g.units - c + g.n_cta - 1) / g.n_cta : 0;
+        return s;
+    }
+    s.count = g.full;
+    if (c >= g.n_pc) return s;
+    const int64_t nkv = g.n_kv;
+    const int64_t lo = int64_t(c) * g.rem_tiles / g.n_pc;
+    const int64_t hi = int64_t(c + 1) * g.rem_tiles / g.n_pc;
+    const int64_t ja = lo / nkv;
+    const int64_t end_a = hi < (ja + 1) * nkv ? hi : (ja + 1) * nkv;
+    s.has_a = 1;
+    s.a.u = int(g.rem_u0 + ja);
+    s.a.k0 = int(lo - ja * nkv);
+    s.a.k1 = int(end_a - ja * nkv);
+    s.a.src = s.a.k0 > 0 ? c : -1;
+    s.a.dst = s.a.k1 < nkv ? c + 1 : -1;
+    if (hi > (ja + 1) * nkv) {  // the range goes on into the next unit
+        s.has_b = 1;
+        s.b.u = s.a.u + 1;
+        s.b.k0 = 0;
+        s.b.k1 = int(hi - (ja + 1) * nkv);
+        s.b.src = -1;
+        s.b.dst = s.b.k1 < nkv ? c + 1 : -1;
+    }
+    if (s.a.k0 > 0) {
+        // chain position: CTAs before c whose ranges hold keys of unit ja;
+        // the first is the one whose range holds its key tile 0
+        const int64_t first = ((ja * nkv + 1) * g.n_pc - 1) / g.rem_tiles;
+        int64_t pos = c - first;
+        if (pos > g.full) pos = g.full;
+        s.pos_a = int(pos);
+    }
+    s.count += s.has_a + s.has_b;
+    return s;
+}
+
+// Item idx (0 <= idx < count) of CTA c, in processing order.
+DS_HD AttnItem attn_item(const AttnGrid &g, const AttnCta &s, int c, int idx) {
+    int i = idx;
+    if (s.has_b) {
+        if (i == 0) return s.b;
+        --i;
+    }
+    if (s.has_a) {
+        if (i == s.pos_a) return s.a;
+        if (i > s.pos_a) --i;
+    }
+    AttnItem w;
+    w.u = c + i * g.n_cta;
+    w.k0 = 0;
+    w.k1 = g.n_kv;
+    w.src = w.dst = -1;
+    return w;
+}
+
+}  // namespace ds

@@ -30,6 +30,10 @@ struct dit_plan {
     // copy stream with its events (slot filled / slot used)
     int kvb = 0;
     size_t off_ring = 0, ring_slot = 0, off_ost = 0, off_mst = 0, off_lst = 0;
+    // hand-off state of the persistent attention's split units (slots of
+    // it; 0: none) in the attention phase; their flags sit in the header
+    int split_slots = 0;
+    size_t off_split = 0;
     uint8_t *kv_host = nullptr;      // device address of the pinned host buffer
     size_t kv_host_bytes = 0;
     cudaStream_t copy_stream = nullptr;
@@ -50,6 +54,11 @@ struct dit_plan {
 };
 
 namespace ds {
+
+// Workspace header: the device status word at byte 0, the attention
+// hand-off flags at kFlagsOffset; zeroed when the workspace is bound.
+constexpr size_t kFlagsOffset = 256;
+constexpr size_t kHeaderBytes = 1024;
 
 // Record a CUDA error for dit_last_cuda_error() and return DIT_ERR_CUDA.
 dit_status_t cuda_fail(cudaError_t e);
@@ -81,11 +90,28 @@ struct AttnState {
     int first, last; // this launch has the first / last key block
 };
 
+// Hand-off space of the persistent attention kernel's split units: a flag
+// per slot (zero before a launch; a launch leaves the flags it used zero
+// again) and per slot the running max and sum of 256 query rows and their
+// unnormalised fp32 output [256, head_dim].  slots = 0: no split.
+struct AttnSplit {
+    int *flags;    // [slots]
+    float *state;  // [slots][256 * (head_dim + 2)]
+    int slots;
+    int max_ctas;  // CTAs at most (0: one per multiprocessor)
+};
+
+// Bytes of the split state for `slots` slots (the flags not included).
+inline size_t attn_split_state_bytes(int slots, int head_dim) {
+    return size_t(slots) * 256 * size_t(head_dim + 2) * 4;
+}
+
 dit_status_t launch_attention(const void *q, int64_t Tq, int64_t ldq, const void *k,
                               int64_t ldk, const void *vt, int64_t ldvt, int64_t T,
                               int heads, int head_dim, void *o, int64_t ldo,
                               int *dev_status, cudaStream_t s,
-                              const AttnState *state = nullptr);
+                              const AttnState *state = nullptr,
+                              const AttnSplit *split = nullptr);
 
 dit_status_t launch_final(const float *x, int64_t T, int D, const void *wf,
                           const float *wf_scale, const float *mod_f, float *out,

@@ -49,9 +49,10 @@ extern "C" dit_status_t dit_block_forward_static(const dit_plan_t *plan, float *
     }
     uint8_t *scratch = static_cast<uint8_t *>(g_scratch_addr[dev]);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    // Only the status word must start at zero: every other region is
-    // written before it is read within one forward.
-    e = cudaMemsetAsync(scratch, 0, 256, st);
+    // Only the header (the status word and the attention's hand-off flags)
+    // must start at zero: every other region is written before it is read
+    // within one forward.
+    e = cudaMemsetAsync(scratch, 0, ds::kHeaderBytes, st);
     if (e != cudaSuccess) return ds::cuda_fail(e);
     // Run the ordinary schedule with the plan pointed at the static scratch
     // for the duration of the (host-side, asynchronous) enqueue.

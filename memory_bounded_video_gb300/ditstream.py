@@ -52,7 +52,8 @@ SYMBOLS = (
     "dit_block_forward_ex", "dit_block_plan_set_lora_rank", "dit_lora_prepare",
     "dit_block_weight_scratch_bytes", "dit_block_bind_weight_scratch", "dit_int8_to_bf16",
     "dit_block_plan_set_kv_offload", "dit_block_kv_host_bytes", "dit_block_bind_kv_host",
-    "dit_attention_part",
+    "dit_attention_part", "dit_attention_split_bytes", "dit_attention_ex",
+    "dit_attention_schedule",
 )
 
 STATIC_SCRATCH_BYTES = 64 << 20
@@ -176,6 +177,12 @@ def _declare(lib):
                                        c_int64, c_int, c_int, vp, vp]),
         "dit_lora_prepare": (c_int, [vp, c_int64, c_int, c_int64, ctypes.c_float, vp, vp,
                                      c_int64, vp]),
+        "dit_attention_split_bytes": (c_size, [c_int, c_int]),
+        "dit_attention_ex": (c_int, [vp, c_int64, c_int64, vp, c_int64, vp, c_int64,
+                                     c_int64, c_int, c_int, vp, c_int64, vp, c_size, c_int,
+                                     vp, vp]),
+        "dit_attention_schedule": (c_int, [c_int, c_int, c_int, c_int, vp, vp, vp,
+                                           c_int64, vp]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -444,3 +451,31 @@ def attention(q, Tq, ldq, k, ldk, vt, ldvt, T, heads, head_dim, o, ldo,
     _check(load().dit_attention(ptr(q), Tq, ldq, ptr(k), ldk, ptr(vt), ldvt, T,
                                 heads, head_dim, ptr(o), ldo, ptr(dev_status),
                                 stream_handle(stream)), "dit_attention")
+
+
+def attention_split_bytes(head_dim, slots):
+    return int(load().dit_attention_split_bytes(head_dim, slots))
+
+
+def attention_ex(q, Tq, ldq, k, ldk, vt, ldvt, T, heads, head_dim, o, ldo, split_ws=None,
+                 split_bytes=0, max_ctas=0, dev_status=None, stream=None):
+    _check(load().dit_attention_ex(ptr(q), Tq, ldq, ptr(k), ldk, ptr(vt), ldvt, T, heads,
+                                   head_dim, ptr(o), ldo, ptr(split_ws), split_bytes,
+                                   max_ctas, ptr(dev_status), stream_handle(stream)),
+           "dit_attention_ex")
+
+
+def attention_schedule(units, n_kv, max_ctas, slots):
+    """(n_cta, n_split, items): the persistent attention's work list, each
+    item (cta, index, unit, k0, k1, src_slot, dst_slot)."""
+    lib = load()
+    n_cta, n_split, n = ctypes.c_int(), ctypes.c_int(), ctypes.c_int64()
+    _check(lib.dit_attention_schedule(units, n_kv, max_ctas, slots, ctypes.byref(n_cta),
+                                      ctypes.byref(n_split), None, 0, ctypes.byref(n)),
+           "dit_attention_schedule")
+    buf = (ctypes.c_int * (7 * max(n.value, 1)))()
+    _check(lib.dit_attention_schedule(units, n_kv, max_ctas, slots, ctypes.byref(n_cta),
+                                      ctypes.byref(n_split), buf, n.value, ctypes.byref(n)),
+           "dit_attention_schedule")
+    items = [tuple(buf[7 * i:7 * i + 7]) for i in range(n.value)]
+    return n_cta.value, n_split.value, items

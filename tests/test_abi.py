@@ -119,6 +119,17 @@ def rup(v, a=1024):
     return (v + a - 1) // a * a
 
 
+def split_region(ca, H, hd):
+    """Bytes of the attention hand-off state: slots for the most CTAs that
+    share a slab's partial last wave on a 128..160-multiprocessor device,
+    256 rows x (head_dim + 2) fp32 values each (the rule is restated in
+    test_attention_schedule.grid)."""
+    from test_attention_schedule import grid
+    units = -(-ca // 256) * H
+    slots = max(grid(units, 1 << 20, sm, 160)[1] for sm in range(128, 161))
+    return slots * 256 * (hd + 2) * 4
+
+
 def expected_workspace_offload(T, D, H, F, cm, ca, fs, kvb):
     """dit_block_workspace_bytes with K/V offload: the two ring slots and the
     carried attention state replace K and V^T."""
@@ -128,13 +139,14 @@ def expected_workspace_offload(T, D, H, F, cm, ca, fs, kvb):
     phase = 1024 + 2 * rup(4 * kvb * D)
     attn = rup(rup(phase + 2 * ca * D) + 2 * ca * D)
     attn = rup(rup(rup(attn + 4 * ca * D) + 4 * ca * H) + 4 * ca * H)
+    attn = rup(attn + split_region(ca, H, D // H))
     mlp = rup(rup(phase + 2 * cm * D) + 2 * cm * fs)
     if fs < F:
         mlp = rup(mlp + 4 * cm * D)
     return max(attn, mlp)
 
 
-def expected_workspace(T, D, F, cm, ca, fs, R=0):
+def expected_workspace(T, D, F, cm, ca, fs, R=0, H=24):
     """The layout documented for dit_block_workspace_bytes (and, with a
     LoRA rank R, dit_block_plan_set_lora_rank), restated."""
     cm = T if cm == 0 or cm >= T else cm
@@ -152,6 +164,7 @@ def expected_workspace(T, D, F, cm, ca, fs, R=0):
         mlp = rup(rup(rup(mlp + 2 * cm * R) + 2 * cm * R) + 2 * cm * R)  # gate, up, down
         if fs < F:
             mlp = rup(mlp + 4 * cm * R)                     # down's fp32 carry
+    attn = rup(attn + split_region(ca, H, D // H))          # attention hand-off state
     return max(attn, mlp)
 
 
@@ -165,7 +178,7 @@ def expected_workspace(T, D, F, cm, ca, fs, R=0):
 def test_workspace_layout_and_info(lib, cfg):
     T, D, H, F, cm, ca, fs = cfg
     p = ds.block_plan(T, D, H, F, cm, ca, fs)
-    assert p.workspace_bytes() == expected_workspace(T, D, F, cm, ca, fs)
+    assert p.workspace_bytes() == expected_workspace(T, D, F, cm, ca, fs, H=H)
     info = p.info()
     assert info["T"] == T and info["D"] == D and info["heads"] == H
     assert info["mlp_chunk"] == (T if cm == 0 or cm >= T else cm)
@@ -182,9 +195,9 @@ def test_workspace_with_lora_rank(lib, cfg):
     T, D, H, F, cm, ca, fs, R = cfg
     p = ds.block_plan(T, D, H, F, cm, ca, fs)
     p.set_lora_rank(R)
-    assert p.workspace_bytes() == expected_workspace(T, D, F, cm, ca, fs, R)
+    assert p.workspace_bytes() == expected_workspace(T, D, F, cm, ca, fs, R, H=H)
     p.set_lora_rank(0)
-    assert p.workspace_bytes() == expected_workspace(T, D, F, cm, ca, fs)
+    assert p.workspace_bytes() == expected_workspace(T, D, F, cm, ca, fs, H=H)
 
 
 def test_lora_rank_rules(lib):

@@ -1,0 +1,179 @@
+"""CPU checks of the persistent attention kernel's work list.
+
+The kernel computes its items from the same host/device code that
+dit_attention_schedule runs on the host, so these checks cover what the
+device executes: every (unit, key tile) once, each cut unit a chain of key
+ranges handing state from CTA to CTA through distinct slots, a processing
+order in which no CTA waits for a hand-off, and the balance of key tiles
+per CTA that removes the partial last wave."""
+
+import random
+
+import pytest
+
+from memory_bounded_video_gb300 import build as dbuild
+from memory_bounded_video_gb300 import ditstream as ds
+
+
+@pytest.fixture(scope="module", autouse=True)
+def lib():
+    dbuild.build()
+    return ds.load()
+
+
+def grid(units, n_kv, max_cta, slots):
+    """(CTAs, CTAs sharing the remainder, whole units each, remainder units),
+    restating the documented rule: F = U // G whole units per CTA and the
+    R = U % G remaining units cut into n ranges, n the larger of
+    min(G, R*F, R*n_kv) (any ranges of at least n_kv / F tiles) and R*q,
+    q = min(F + 1, G // R, n_kv) (q aligned ranges per unit), used when
+    n <= slots and the longest range, ceil(R * n_kv / n), is shorter than a
+    unit."""
+    G = max(1, min(units, max_cta))
+    F, R = divmod(units, G)
+    if R == 0:
+        return G, 0, F, 0
+    n1 = min(G, R * F, R * n_kv)
+    q = min(F + 1, G // R, n_kv)
+    n = max(n1, R * q)
+    if n <= slots and -(-R * n_kv // n) < n_kv:
+        return G, n, F, R
+    return G, 0, F, R
+
+
+CASES = [
+    (768, 256, 148, 160),    # 32k keys, 8192-query slab, 24 heads (the bench)
+    (384, 256, 148, 160),    # 4096-query slab
+    (1536, 256, 148, 160),   # 16384-query slab
+    (3072, 256, 148, 160),   # all 32768 queries
+    (384, 512, 148, 160),    # 64k keys, 4096-query slab
+    (200, 256, 148, 160),    # one whole unit per CTA plus a cut remainder
+    (256, 32, 148, 160),     # 4096 tokens, 16 heads of 64
+    (768, 256, 148, 0),      # no hand-off space: round robin
+    (768, 256, 152, 160),
+    (100, 256, 148, 160),    # fewer units than multiprocessors
+    (50, 8, 7, 8), (23, 5, 7, 8), (40, 3, 7, 8), (1000, 1, 13, 13),
+    (97, 64, 13, 13), (13, 4, 13, 13), (5, 9, 13, 13), (29, 2, 9, 9),
+    (17, 17, 16, 16), (33, 6, 16, 3),
+]
+_rng = random.Random(11)
+CASES += [(_rng.randint(1, 400), _rng.randint(1, 40), _rng.randint(1, 40), 40)
+          for _ in range(60)]
+
+
+def by_cta(items):
+    out = {}
+    for c, i, u, k0, k1, src, dst in items:
+        out.setdefault(c, []).append((i, u, k0, k1, src, dst))
+    for c in out:
+        out[c].sort()
+        assert [it[0] for it in out[c]] == list(range(len(out[c])))
+    return out
+
+
+@pytest.mark.parametrize("units,n_kv,max_cta,slots", CASES)
+def test_schedule_covers_every_key_tile_once_as_chains(units, n_kv, max_cta, slots):
+    n_cta, n_split, items = ds.attention_schedule(units, n_kv, max_cta, slots)
+    G, n_pc, F, R = grid(units, n_kv, max_cta, slots)
+    assert (n_cta, n_split) == (G, n_pc)
+    pieces = {}
+    for c, i, u, k0, k1, src, dst in items:
+        assert 0 <= c < n_cta and 0 <= u < units and 0 <= k0 < k1 <= n_kv
+        pieces.setdefault(u, []).append((k0, k1, c, src, dst))
+    assert sorted(pieces) == list(range(units))
+    written, read = set(), set()
+    for u, ps in pieces.items():
+        ps.sort()
+        assert ps[0][0] == 0 and ps[0][3] == -1          # starts fresh
+        assert ps[-1][1] == n_kv and ps[-1][4] == -1     # ends with the output
+        for a, b in zip(ps, ps[1:]):
+            assert a[1] == b[0]                          # contiguous key ranges
+            assert a[4] == b[3] != -1                    # handed through one slot
+            assert b[2] == a[2] + 1 == a[4]              # to the next CTA, slot c
+            assert 0 < a[4] < max(n_split, 1)
+            written.add(a[4])
+            read.add(b[3])
+    assert len(written) == len(read) == sum(len(ps) - 1 for ps in pieces.values())
+    if n_split == 0:  # round robin: units c, c + G, ... whole
+        for c, its in by_cta(items).items():
+            assert [it[1] for it in its] == list(range(c, units, n_cta))
+            assert all(it[2:] == (0, n_kv, -1, -1) for it in its)
+
+
+@pytest.mark.parametrize("units,n_kv,max_cta,slots", CASES)
+def test_schedule_never_waits_and_balances_key_tiles(units, n_kv, max_cta, slots):
+    """Every CTA runs its items back to back, an item taking its key tiles
+    in time; an item that continues a unit must not start before the piece
+    before it has ended on the CTA before."""
+    n_cta, n_split, items = ds.attention_schedule(units, n_kv, max_cta, slots)
+    G, n_pc, F, R = grid(units, n_kv, max_cta, slots)
+    per = by_cta(items)
+    start, end = {}, {}
+    for c, its in per.items():
+        t = 0
+        for i, u, k0, k1, src, dst in its:
+            start[(u, k0)] = t
+            t += k1 - k0
+            end[(u, k1)] = t
+    for (u, k0), t in start.items():
+        if k0 > 0:
+            assert end[(u, k0)] <= t, (u, k0)
+    loads = [sum(k1 - k0 for _, _, k0, k1, _, _ in its) for its in per.values()]
+    assert sum(loads) == units * n_kv
+    if n_pc:
+        assert max(loads) == F * n_kv + -(-R * n_kv // n_pc)
+        assert max(loads) < (F + 1) * n_kv  # shorter than with a last wave
+    else:
+        assert max(loads) == -(-units // n_cta) * n_kv
+
+
+def test_schedule_of_the_32k_token_slab():
+    # 8192-query slabs of 24 heads against 32768 keys on 148 SMs: 768 units,
+    # 5.19 waves.  One CTA per unit needs 6 waves (1536 key tiles on the
+    # busiest SM); the split needs 1332, the mean being 1328.4.
+    n_cta, n_split, items = ds.attention_schedule(768, 256, 148, 160)
+    assert (n_cta, n_split) == (148, 140)
+    loads = {}
+    for c, i, u, k0, k1, src, dst in items:
+        loads[c] = loads.get(c, 0) + k1 - k0
+    assert max(loads.values()) == 1332 and min(loads.values()) == 1280
+
+
+def test_plan_workspace_holds_the_hand_off_space():
+    # a 8192-query slab of 24 heads needs hand-off slots, a 4096-token block
+    # of 16 heads (256 units, one per SM and a remainder too large to cut)
+    # does not
+    big = ds.block_plan(32768, 3072, 24, 8192, 8192, 8192)
+    small = ds.block_plan(4096, 1024, 16, 2816, 4096, 4096)
+    slots = max(grid(768, 1 << 20, sm, 160)[1] for sm in range(128, 161))
+    assert slots == 160
+    base = 1024 + 2 * 32768 * 3072 + 2 * 3072 * 32768
+    attn = base + 4 * 8192 * 3072 + slots * 256 * 130 * 4
+    mlp = base + 2 * 8192 * 3072 + 2 * 8192 * 8192
+    assert big.workspace_bytes() == max(attn, mlp)
+    assert max(grid(256, 1 << 20, sm, 160)[1] for sm in range(128, 161)) == 0
+    assert small.workspace_bytes() == (1024 + 4 * 4096 * 1024 + 2 * 4096 * 1024
+                                       + 2 * 4096 * 2816)
+
+
+def test_split_bytes_and_arguments(lib):
+    assert ds.attention_split_bytes(128, 160) == 1024 + 160 * 256 * 130 * 4
+    assert ds.attention_split_bytes(64, 1) == 1024 + 256 * 66 * 4
+    assert ds.attention_split_bytes(96, 4) == 0
+    assert ds.attention_split_bytes(128, 161) == 0
+    for bad in ((0, 4, 4, 4), (4, 0, 4, 4), (4, 4, 0, 4), (4, 4, 4, -1)):
+        with pytest.raises(ds.DitError) as e:
+            ds.attention_schedule(*bad)
+        assert e.value.status == ds.ERR_INVALID_ARG
+    # argument checks before any launch: head_dim, alignment, too small
+    with pytest.raises(ds.DitError) as e:
+        ds.attention_ex(16, 256, 1024, 16, 1024, 16, 256, 256, 8, 96, 16, 1024)
+    assert e.value.status == ds.ERR_INVALID_ARG
+    with pytest.raises(ds.DitError) as e:
+        ds.attention_ex(16, 256, 1024, 16, 1024, 16, 256, 256, 8, 128, 16, 1024,
+                        split_ws=8, split_bytes=4096)
+    assert e.value.status == ds.ERR_ALIGN
+    with pytest.raises(ds.DitError) as e:
+        ds.attention_ex(16, 256, 1024, 16, 1024, 16, 256, 256, 8, 128, 16, 1024,
+                        split_ws=16, split_bytes=512)
+    assert e.value.status == ds.ERR_WORKSPACE_TOO_SMALL
