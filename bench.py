@@ -43,8 +43,8 @@ TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0,
                   "bf16_tflops_sustained": 1700.0}
 
-# kernel kind -> source file whose hash keys the ncu traffic figure
-KIND_SOURCE = {"attention": "attention.cu", "modln": "modln.cu",
+# kernel kind -> source file(s) whose hash keys the ncu traffic figure
+KIND_SOURCE = {"attention": ("attention.cu", "attn_sched.h"), "modln": "modln.cu",
                "final": "final.cu", "gemm_kv": "gemm.cu", "gemm_q": "gemm.cu",
                "gemm_o": "gemm.cu", "gemm_swiglu": "gemm.cu",
                "gemm_down": "gemm.cu"}
@@ -94,10 +94,13 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
-def source_sha(name):
-    path = os.path.join(ROOT, "memory_bounded_video_gb300", "csrc", name)
-    with open(path, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+def source_sha(names):
+    """First 16 hex digits of the sha256 of the kernel's source file(s)."""
+    h = hashlib.sha256()
+    for name in ((names,) if isinstance(names, str) else names):
+        with open(os.path.join(ROOT, "memory_bounded_video_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
 
 
 def traffic_for(kind, workload):

@@ -154,17 +154,23 @@ DIT_API dit_status_t dit_block_plan_info(const dit_plan_t *plan, int64_t *T, int
                                  int *attn_chunk, int *ffn_slice);
 
 /* Exact device workspace bytes the plan needs:
- *   256 (status words) + K [T, D] bf16 + V^T [D, roundup(T, 128)] bf16
- *   + max(attention phase 4 * C_a * D,
+ *   1024 (header: status word, attention hand-off flags)
+ *   + K [T, D] bf16 + V^T [D, roundup(T, 128)] bf16
+ *   + max(attention phase 4 * C_a * D + hand-off state,
  *         MLP phase 2 * C_m * D + 2 * C_m * F_s + (F_s < F ? 4 * C_m * D : 0))
  * each region rounded up to 1 KiB, plus the LoRA regions when the plan has a
- * LoRA rank (dit_block_plan_set_lora_rank).  K/V for all tokens is the floor that
- * grows with T ("Where people get burned": K and V of the whole sequence
- * stay resident); everything else is bounded by the chunk sizes. */
+ * LoRA rank (dit_block_plan_set_lora_rank).  The hand-off state is that of
+ * dit_attention_ex: slots x 1024 * (head_dim + 2) bytes, slots the most CTAs
+ * that would share the partial last wave of ceil(C_a / 256) * heads units on a
+ * device of 128 to 160 multiprocessors (0 when no such device would split;
+ * at most 160).  K/V for all tokens is the floor that grows with T ("Where
+ * people get burned": K and V of the whole sequence stay resident);
+ * everything else is bounded by the chunk sizes. */
 DIT_API size_t dit_block_workspace_bytes(const dit_plan_t *plan);
 
 /* Bind caller-owned device memory (>= dit_block_workspace_bytes, 256-byte
- * aligned) as the plan's workspace and clear its status words.  The current
+ * aligned) as the plan's workspace and clear its header (status word and
+ * hand-off flags).  The current
  * device must be of compute capability 10.3.  The library never allocates
  * device memory itself.  Errors: DIT_ERR_INVALID_ARG, DIT_ERR_ALIGN,
  * DIT_ERR_WORKSPACE_TOO_SMALL, DIT_ERR_UNSUPPORTED_ARCH, DIT_ERR_CUDA. */
@@ -341,9 +347,10 @@ DIT_API dit_status_t dit_block_forward_ex(const dit_plan_t *plan, float *x,
  *   - All calls share one scratch, which keeps the last call's contents:
  *     calls whose work overlaps on the GPU (concurrent streams, several
  *     host threads) race and give wrong results.  Serialise them.
- *   - The scratch's status word is cleared at the start of each call; a
- *     bounded device wait that runs out is recorded there but not reported
- *     (dit_block_sync_status reads the plan's bound workspace only).
+ *   - The scratch's header (status word, attention hand-off flags) is
+ *     cleared at the start of each call; a bounded device wait that runs
+ *     out is recorded there but not reported (dit_block_sync_status reads
+ *     the plan's bound workspace only).
  *   - Calls no cudaMalloc/cudaFree or any other allocating routine.
  * Errors: as dit_block_forward, plus DIT_ERR_WORKSPACE_TOO_SMALL and
  * DIT_ERR_UNSUPPORTED_ARCH. */
@@ -353,8 +360,9 @@ DIT_API dit_status_t dit_block_forward_static(const dit_plan_t *plan, float *x,
                                               const float *modulation,
                                               dit_stream_t stream);
 
-/* Synchronise `stream`, read and clear the plan's device status word.
- * Returns DIT_OK, DIT_ERR_TIMEOUT or DIT_ERR_CUDA. */
+/* Synchronise `stream`, read and clear the plan's device status word (after
+ * a failure also the attention hand-off flags, which a launch that gave up
+ * may have left set).  Returns DIT_OK, DIT_ERR_TIMEOUT or DIT_ERR_CUDA. */
 DIT_API dit_status_t dit_block_sync_status(const dit_plan_t *plan, dit_stream_t stream);
 
 /* Final layer (output head), fp32 arithmetic, unsliced:

@@ -3,7 +3,7 @@
     python -m memory_bounded_video_gb300.profile_case gemm --mode swiglu \\
         --int8 --M 2048 --N 8192 --K 3072 --reps 3
     python -m memory_bounded_video_gb300.profile_case attention --Tq 2048 \\
-        --T 8192 --heads 4 --head-dim 128 --reps 3
+        --T 8192 --heads 4 --head-dim 128 --reps 3 [--no-split]
     python -m memory_bounded_video_gb300.profile_case modln --M 8192 --D 3072
     python -m memory_bounded_video_gb300.profile_case final --M 8192 --D 3072
     python -m memory_bounded_video_gb300.profile_case expand --M 8192 --D 3072
@@ -79,10 +79,17 @@ def attention_case(a):
     ldvt = (a.T + 127) // 128 * 128
     vt = torch.randn(D, ldvt, device="cuda", generator=g).to(torch.bfloat16)
     o = torch.empty(a.Tq, D, device="cuda", dtype=torch.bfloat16)
-    keep = (q, k, vt, o)
     flops = 4 * a.Tq * a.T * D
-    return (lambda: ds.attention(q, a.Tq, D, k, D, vt, ldvt, a.T, a.heads,
-                                 a.head_dim, o, D)), flops, keep
+    if a.no_split:  # whole units only, one after another per CTA
+        keep = (q, k, vt, o)
+        return (lambda: ds.attention(q, a.Tq, D, k, D, vt, ldvt, a.T, a.heads,
+                                     a.head_dim, o, D)), flops, keep
+    # the block forward's launch: the last wave's units cut into key ranges
+    nb = ds.attention_split_bytes(a.head_dim, 160)
+    ws = torch.zeros(nb, dtype=torch.uint8, device="cuda")
+    keep = (q, k, vt, o, ws)
+    return (lambda: ds.attention_ex(q, a.Tq, D, k, D, vt, ldvt, a.T, a.heads, a.head_dim,
+                                    o, D, split_ws=ws, split_bytes=nb)), flops, keep
 
 
 def modln_case(a):
@@ -126,6 +133,8 @@ def main(argv=None):
     ap.add_argument("--heads", type=int, default=4)
     ap.add_argument("--head-dim", type=int, default=128)
     ap.add_argument("--reps", type=int, default=3)
+    ap.add_argument("--no-split", action="store_true",
+                    help="attention: no key-range split of the last wave's units")
     a = ap.parse_args(argv)
     dbuild.build()
     ds.load()
