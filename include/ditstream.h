@@ -158,12 +158,16 @@ DIT_API dit_status_t dit_block_plan_info(const dit_plan_t *plan, int64_t *T, int
  *   + K [T, D] bf16 + V^T [D, roundup(T, 128)] bf16
  *   + max(attention phase 4 * C_a * D + hand-off state,
  *         MLP phase 2 * C_m * D + 2 * C_m * F_s + (F_s < F ? 4 * C_m * D : 0))
+ *   + the GEMMs' hand-off state
  * each region rounded up to 1 KiB, plus the LoRA regions when the plan has a
- * LoRA rank (dit_block_plan_set_lora_rank).  The hand-off state is that of
- * dit_attention_ex: slots x 1024 * (head_dim + 2) bytes, slots the most CTAs
- * that would share the partial last wave of ceil(C_a / 256) * heads units on a
- * device of 128 to 160 multiprocessors (0 when no such device would split;
- * at most 160).  K/V for all tokens is the floor that grows with T ("Where
+ * LoRA rank (dit_block_plan_set_lora_rank).  The attention's hand-off state
+ * is that of dit_attention_ex: slots x 1024 * (head_dim + 2) bytes, slots the
+ * most CTAs that would share the partial last wave of ceil(C_a / 256) * heads
+ * units on a device of 128 to 160 multiprocessors (0 when no such device
+ * would split; at most 160).  The GEMMs' is that of dit_gemm_ex: 128 KiB per
+ * slot, slots the most that any of the plan's GEMM launches (K/V, Q, O,
+ * gate/up, down, at full and ragged chunk and slice sizes, in either tile
+ * shape) would use on such a device, at most 64.  K/V for all tokens is the floor that grows with T ("Where
  * people get burned": K and V of the whole sequence stay resident);
  * everything else is bounded by the chunk sizes. */
 DIT_API size_t dit_block_workspace_bytes(const dit_plan_t *plan);
@@ -505,6 +509,24 @@ typedef struct {
 
 DIT_API dit_status_t dit_gemm(const dit_gemm_args_t *args, int *dev_status,
                       dit_stream_t stream);
+
+/* dit_gemm with the work split of its persistent grid: the output tiles of
+ * a launch go to at most max_ctas CTAs (0: one per multiprocessor); when the
+ * tiles that would form a last, partial wave are worth cutting, their K-steps
+ * (64 wide) are cut into ranges shared by all CTAs, each continuing the raw
+ * fp32 accumulator of the range before it, so every output element is still
+ * one accumulation over K in the same order: the result equals dit_gemm bit
+ * for bit.  split_ws: device memory of dit_gemm_split_bytes(slots) bytes,
+ * 16-byte aligned, zero before its first use (a successful launch leaves it
+ * so); bytes [0, 1024) hold one flag per slot, the rest `slots` accumulator
+ * slots of 128 KiB (slots = (split_bytes - 1024) / 131072, at most 64).  A
+ * launch splits only if it needs no more slots than that; split_ws = NULL
+ * never splits.  Launches sharing one split_ws must not overlap on the
+ * device.  Errors: as dit_gemm. */
+DIT_API size_t dit_gemm_split_bytes(int slots);
+DIT_API dit_status_t dit_gemm_ex(const dit_gemm_args_t *args, void *split_ws,
+                                 size_t split_bytes, int max_ctas, int *dev_status,
+                                 dit_stream_t stream);
 
 /* dit_attention over one block of a longer key sequence (keys k0 .. k0 +
  * T_block - 1 of it, k and vt pointing at that block), carrying the softmax

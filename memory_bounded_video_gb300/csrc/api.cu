@@ -209,6 +209,35 @@ void layout(dit_plan *p) {
         if (p->fs < p->F) mlp_end = round_up(p->off_udc + 4 * size_t(p->cm) * R, A);
     }
     p->total = attn_end > mlp_end ? attn_end : mlp_end;
+    // the GEMMs' hand-off state, used within single launches of every phase:
+    // slots for the most CTAs that any of the plan's GEMM launches (either
+    // tile shape, full and ragged chunks and FFN slices) may cut its last
+    // wave over on a device of 128 to 160 SMs, at most kGemmSplitSlots
+    int gs = 0;
+    auto need = [&](int64_t M, int N, int K, bool two_b) {
+        if (M <= 0 || N <= 0 || K <= 0) return;
+        for (bool r256 : {false, true}) {
+            const int n = attn_slots_needed(gemm_units(M, N, two_b, r256), K / 64,
+                                            kGemmSplitSlots);
+            if (n > gs) gs = n;
+        }
+    };
+    const int D = p->D;
+    for (int64_t M : {int64_t(p->ca), p->T % p->ca}) {
+        need(M, 2 * D, D, false);  // K, V
+        need(M, D, D, false);      // Q, O
+    }
+    for (int64_t M : {int64_t(p->cm), p->T % p->cm})
+        for (int fw : {p->fs, p->F % p->fs}) {
+            need(M, fw, D, true);   // gate / up
+            need(M, D, fw, false);  // down
+        }
+    p->gsplit_slots = gs;
+    p->off_gsplit = 0;
+    if (gs) {
+        p->off_gsplit = round_up(p->total, A);
+        p->total = round_up(p->off_gsplit + size_t(gs) * kGemmSlotBytes, A);
+    }
 }
 
 }  // namespace
@@ -507,6 +536,10 @@ dit_status_t dit_block_forward_ex(const dit_plan_t *cp, float *x, const dit_bloc
     const int D = p->D, F = p->F;
     const int64_t Dl = D;
     int *status = reinterpret_cast<int *>(p->ws);
+    // the GEMMs' hand-off space for split tiles (flags shared with the
+    // attention's: every launch leaves the flags it used zero)
+    const AttnSplit gsplit{reinterpret_cast<int *>(p->ws + kFlagsOffset),
+                           reinterpret_cast<float *>(p->ws + p->off_gsplit), p->gsplit_slots, 0};
     // K [T, D] and V^T [D, T_pad]: in the workspace, or (offload) in the
     // host buffer, written there by pass one through its device mapping
     void *K = p->kvb ? static_cast<void *>(p->kv_host) : static_cast<void *>(p->ws + p->off_k);
@@ -577,7 +610,7 @@ dit_status_t dit_block_forward_ex(const dit_plan_t *cp, float *x, const dit_bloc
             g.acc_final = 0;
         }
         return timed(p, st, DIT_K_LORA_U, 2.0 * rows * l.rank * K_,
-                     [&] { return launch_gemm(g, status, st); });
+                     [&] { return launch_gemm(g, status, st, &gsplit); });
     };
     // LoRA K-steps of a GEMM: u [rows, rank] and rows row0.. of the prepared B
     auto attach = [&](dit_gemm_args_t &g, int half, const void *u, const dit_lora_t &l,
@@ -690,7 +723,7 @@ dit_status_t dit_block_forward_ex(const dit_plan_t *cp, float *x, const dit_bloc
                 attach(g, 0, static_cast<const uint8_t *>(u_q) + 2 * (t0 - s) * l_qkv.rank,
                        l_qkv, Dl);
             if ((r = timed(p, st, DIT_K_GEMM_KV, 2.0 * sr * 2 * D * D + lflops(l_qkv, sr, 2 * D),
-                           [&] { return launch_gemm(g, status, st); })) != DIT_OK)
+                           [&] { return launch_gemm(g, status, st, &gsplit); })) != DIT_OK)
                 return r;
             if (kvb && (t1 % kvb == 0 || t1 == T)) {  // block b complete
                 const int64_t k0 = b * kvb;
@@ -741,7 +774,7 @@ dit_status_t dit_block_forward_ex(const dit_plan_t *cp, float *x, const dit_bloc
         set_qk(g, 0);
         if (on(l_qkv)) attach(g, 0, u_q, l_qkv, 0);
         if ((r = timed(p, st, DIT_K_GEMM_Q, 2.0 * rows * D * D + lflops(l_qkv, rows, D),
-                       [&] { return launch_gemm(g, status, st); })) != DIT_OK)
+                       [&] { return launch_gemm(g, status, st, &gsplit); })) != DIT_OK)
             return r;
         // O_s overwrites a_s (dead once Q_s exists)
         if (!kvb) {
@@ -789,7 +822,7 @@ dit_status_t dit_block_forward_ex(const dit_plan_t *cp, float *x, const dit_bloc
         o.gate = gate1;
         if (on(l_o)) attach(o, 0, u_o, l_o, 0);
         if ((r = timed(p, st, DIT_K_GEMM_O, 2.0 * rows * D * D + lflops(l_o, rows, D),
-                       [&] { return launch_gemm(o, status, st); })) != DIT_OK)
+                       [&] { return launch_gemm(o, status, st, &gsplit); })) != DIT_OK)
             return r;
     }
     // MLP: token chunks x FFN feature slices
@@ -839,7 +872,7 @@ dit_status_t dit_block_forward_ex(const dit_plan_t *cp, float *x, const dit_bloc
             if (on(l_u)) attach(g, 1, u_u, l_u, f);
             if ((r = timed(p, st, DIT_K_GEMM_SWIGLU,
                            4.0 * rows * fw * D + lflops(l_g, rows, fw) + lflops(l_u, rows, fw),
-                           [&] { return launch_gemm(g, status, st); })) != DIT_OK)
+                           [&] { return launch_gemm(g, status, st, &gsplit); })) != DIT_OK)
                 return r;
             // the down adapter's u = h A_d^T accumulates over the FFN slices
             // (fp32 carry; bf16 after the last), in the unsliced K order
@@ -867,7 +900,7 @@ dit_status_t dit_block_forward_ex(const dit_plan_t *cp, float *x, const dit_bloc
             if (last && on(l_d)) attach(d, 0, u_d, l_d, 0);
             if ((r = timed(p, st, DIT_K_GEMM_DOWN,
                            2.0 * rows * D * fw + (last ? lflops(l_d, rows, D) : 0.0),
-                           [&] { return launch_gemm(d, status, st); })) != DIT_OK)
+                           [&] { return launch_gemm(d, status, st, &gsplit); })) != DIT_OK)
                 return r;
         }
     }
@@ -911,6 +944,27 @@ dit_status_t dit_modln_cast(const float *x, int64_t rows, int D, const float *sh
 dit_status_t dit_gemm(const dit_gemm_args_t *args, int *dev_status, dit_stream_t stream) {
     if (!args) return DIT_ERR_INVALID_ARG;
     return launch_gemm(*args, dev_status, static_cast<cudaStream_t>(stream));
+}
+
+size_t dit_gemm_split_bytes(int slots) {
+    if (slots < 0 || slots > kGemmSplitSlots) return 0;
+    return kHeaderBytes + size_t(slots) * kGemmSlotBytes;
+}
+
+dit_status_t dit_gemm_ex(const dit_gemm_args_t *args, void *split_ws, size_t split_bytes,
+                         int max_ctas, int *dev_status, dit_stream_t stream) {
+    if (!args || max_ctas < 0) return DIT_ERR_INVALID_ARG;
+    AttnSplit split{nullptr, nullptr, 0, max_ctas};
+    if (split_ws) {
+        if (!aligned16(split_ws)) return DIT_ERR_ALIGN;
+        if (split_bytes < kHeaderBytes) return DIT_ERR_WORKSPACE_TOO_SMALL;
+        size_t n = (split_bytes - kHeaderBytes) / kGemmSlotBytes;
+        if (n > size_t(kGemmSplitSlots)) n = kGemmSplitSlots;
+        split.flags = static_cast<int *>(split_ws);
+        split.state = reinterpret_cast<float *>(static_cast<uint8_t *>(split_ws) + kHeaderBytes);
+        split.slots = int(n);
+    }
+    return launch_gemm(*args, dev_status, static_cast<cudaStream_t>(stream), &split);
 }
 
 dit_status_t dit_attention_part(const void *q, int64_t Tq, int64_t ldq, const void *k,

@@ -83,32 +83,6 @@ struct AttnParams {
     float *split_state;       // [slots][256 * (HD + 2)]: m, l, O
 };
 
-// Release / acquire of the hand-off flags (device scope).
-DEV void flag_release(int *f) {
-    asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(f), "r"(1) : "memory");
-}
-DEV int flag_acquire(const int *f) {
-    int v;
-    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(f) : "memory");
-    return v;
-}
-
-// Bounded wait for a hand-off flag; false (with the timeout recorded) if it
-// was not set within the limit or another wait of this CTA gave up.
-DEV bool flag_wait(const int *f, const WaitCtx &w) {
-    if (flag_acquire(f)) return true;
-    const uint64_t t0 = globaltimer();
-    while (true) {
-        __nanosleep(128);
-        if (flag_acquire(f)) return true;
-        if (*w.abort) return false;
-        if (globaltimer() - t0 > kWaitLimitNs) {
-            record_timeout(w);
-            return false;
-        }
-    }
-}
-
 DEV float ex2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -231,12 +205,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int x = 0; x < 2; ++x) {
             mbar_init(bar(B_SF + x), 1);
-            mbar_init(bar(B_PF + x), 128);
+            mbar_init(bar(B_PF + x), 4);  // one arrival per softmax warp
         }
         mbar_init(bar(B_O), 1);
         mbar_init(bar(B_DR), 1);
         mbar_init(bar(B_QE), 1);
-        mbar_init(bar(B_HD), 2 * 128);
+        mbar_init(bar(B_HD), 8);  // one arrival per softmax warp
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -454,16 +428,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t oaddr = lane_base + uint32_t(C::COL_O + x * HD);
         const float sl2 = p.scale_log2;
         const int last_valid = int(p.T - int64_t(n_kv - 1) * kBKV);  // keys in last tile
-        // O of this row (HD fp32 values at src) into TMEM; rows beyond the
-        // queries read zeros
-        auto o_to_tmem = [&](const float *src, bool valid) {
+        // O of this row (HD fp32 values, 4 columns per float4, consecutive
+        // float4s `step` apart) into TMEM; rows beyond the queries read zeros
+        auto o_to_tmem = [&](const float *src, size_t step, bool valid) {
             const float4 *s4 = reinterpret_cast<const float4 *>(src);
 #pragma unroll
             for (int c0 = 0; c0 < HD; c0 += 32) {
                 uint32_t r[32];
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
-                    const float4 v = valid ? s4[(c0 >> 2) + i] : make_float4(0.f, 0.f, 0.f, 0.f);
+                    const float4 v = valid ? s4[size_t((c0 >> 2) + i) * step]
+                                           : make_float4(0.f, 0.f, 0.f, 0.f);
                     r[4 * i] = __float_as_uint(v.x);
                     r[4 * i + 1] = __float_as_uint(v.y);
                     r[4 * i + 2] = __float_as_uint(v.z);
@@ -473,8 +448,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem_st32_sync(oaddr + c0, r);
             }
         };
-        // O of this row from TMEM to dst (fp32), if valid
-        auto o_from_tmem = [&](float *dst, bool valid) {
+        // O of this row from TMEM to dst (fp32, the same layout), if valid
+        auto o_from_tmem = [&](float *dst, size_t step, bool valid) {
             float4 *d4 = reinterpret_cast<float4 *>(dst);
 #pragma unroll
             for (int c0 = 0; c0 < HD; c0 += 32) {
@@ -485,7 +460,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (valid) {
 #pragma unroll
                     for (int i = 0; i < 8; ++i)
-                        d4[(c0 >> 2) + i] =
+                        d4[size_t((c0 >> 2) + i) * step] =
                             make_float4(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]),
                                         __uint_as_float(r[4 * i + 2]),
                                         __uint_as_float(r[4 * i + 3]));
@@ -510,6 +485,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // launches' (earlier key blocks); O goes into TMEM before
                 // this item's first PV MMA, which accumulates onto it
                 const float *src = nullptr;
+                size_t step = 1;  // float4s between column groups
                 bool valid = true;
                 if (it.k0 > 0) {
                     const bool w = flag_wait(p.split_flags + it.src, wc);
@@ -520,7 +496,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const float *slot = p.split_state + size_t(it.src) * kSlotFloats;
                     m = slot[urow];
                     l = slot[2 * kBQ + urow];
-                    src = slot + 4 * kBQ + size_t(urow) * HD;
+                    src = slot + 4 * kBQ + 4 * size_t(urow);  // column-group major
+                    step = 2 * kBQ;
                 } else if (!p.first) {
                     const int64_t qrow = qrow_of(it);
                     const int head = it.u / p.n_qpairs;
@@ -529,7 +506,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     l = valid ? p.l_state[qrow * p.heads + head] : 0.f;
                     src = p.o_state + qrow * p.ld_state + int64_t(head) * HD;
                 }
-                if (src) o_to_tmem(src, valid);
+                if (src) o_to_tmem(src, step, valid);
             }
             const bool fresh = k0 == 0 && p.first;
             for (int jj = 0; jj < nt; ++jj) {
@@ -573,7 +550,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 l += sum;
                 tmem_st_wait();    // P is in tensor memory before the PV MMA reads it
                 tc_fence_before(); // S/O/P accesses finish before the next MMAs
-                mbar_arrive(bar(B_PF + x));
+                mbar_arrive_warp(bar(B_PF + x));
             }
             if (!ok) break;
             // the item is looked up again rather than kept in registers
@@ -599,17 +576,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                 float *slot = p.split_state + size_t(split ? it.dst : 0) * kSlotFloats;
                 float *mp = split ? slot + urow : p.m_state + qrow * p.heads + head;
                 float *lp = split ? slot + 2 * kBQ + urow : p.l_state + qrow * p.heads + head;
-                float *dst = split ? slot + 4 * kBQ + size_t(urow) * HD
+                // the slot's O is column-group major (float4 j of row r at
+                // j * 256 + r: a warp's rows move 512 contiguous bytes)
+                float *dst = split ? slot + 4 * kBQ + 4 * size_t(urow)
                                    : p.o_state + qrow * p.ld_state + int64_t(head) * HD;
                 const bool v = split || valid;
                 if (v) {
                     *mp = m;
                     *lp = l;
                 }
-                o_from_tmem(dst, v);
+                o_from_tmem(dst, split ? size_t(2 * kBQ) : size_t(1), v);
                 if (split) {
                     __threadfence();
-                    mbar_arrive(bar(B_HD));
+                    mbar_arrive_warp(bar(B_HD));
                     if (x == 0 && row == 0) {
                         if (!mbar_wait(bar(B_HD), 0u, wc)) {
                             ok = false;

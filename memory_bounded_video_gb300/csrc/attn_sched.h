@@ -92,15 +92,30 @@ DS_HD AttnGrid attn_grid(int units, int n_kv, int max_cta, int slots) {
 // made without a device; a device outside the range may split less).
 constexpr int kAttnMinSms = 128, kAttnMaxSms = 160;
 
-// State slots that units of an attention slab may need on any device with
-// kAttnMinSms..kAttnMaxSms multiprocessors, whatever its key count.
-inline int attn_slots_needed(int units) {
+// State slots that `units` units of n_kv key tiles may need on any device
+// with kAttnMinSms..kAttnMaxSms multiprocessors when at most `cap` slots
+// are available (0: none would split).
+inline int attn_slots_needed(int units, int n_kv = 1 << 20, int cap = kAttnSplitSlots) {
     int need = 0;
     for (int sm = kAttnMinSms; sm <= kAttnMaxSms; ++sm) {
-        const AttnGrid g = attn_grid(units, 1 << 20, sm, kAttnSplitSlots);
+        const AttnGrid g = attn_grid(units, n_kv, sm, cap);
         if (g.n_pc > need) need = g.n_pc;
     }
     return need;
+}
+
+// The tensor-core GEMM uses the same split with output tiles as units and
+// K-steps of 64 as key tiles: a slot holds one tile's raw fp32 accumulator
+// (256 x 128 or 128 x 256 values), and a plan provides at most 64 slots.
+constexpr int kGemmSplitSlots = 64;
+constexpr size_t kGemmSlotBytes = size_t(128) * 256 * 4;
+
+// GEMM tiles of an M x N output in either tile shape the GEMM uses (256 x
+// BN/2 or 128 x BN, BN = 256 or, with two B operands, 128 per operand).
+inline int gemm_units(int64_t M, int N, bool two_b, bool rows256) {
+    const int bm = rows256 ? 256 : 128;
+    const int bn = (two_b ? 128 : 256) / (rows256 ? 2 : 1);
+    return int((M + bm - 1) / bm) * ((N + bn - 1) / bn);
 }
 
 // The pieces of CTA c and where piece A goes among its whole units.

@@ -19,6 +19,14 @@
 // The accumulator is double-buffered, so the epilogue of tile i overlaps the
 // main loop of tile i+1.
 //
+// Work split (attn_sched.h, output tiles as units and K-steps as key tiles):
+// each CTA runs its whole tiles in the order of a one-tile-per-CTA grid, and
+// when the last, partial wave is worth cutting, its tiles' K-steps are cut
+// into equal ranges shared by all CTAs.  A range that continues a tile starts
+// from the raw fp32 accumulator the CTA before handed on (a state slot and a
+// release/acquire flag; cooperative launch), so every output element is
+// still one accumulation over K in the same order.
+//
 // Activation-space LoRA ("ComfyUI-StaticPipeline", "Activation-space LoRA
 // (bypass mode)": y = W x + alpha B (A x)) continues the same accumulation:
 // after W's K-steps, each 64-wide K-step of U L^T (U = x A^T, L = alpha B)
@@ -32,6 +40,7 @@
 // Per-row exactness: every output element is the same fp32 accumulation over
 // K in the same order (k-blocks of 64, MMAs of 16), whatever M, the tile
 // schedule or the grid — so results do not depend on how tokens are chunked.
+#include "attn_sched.h"
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -70,6 +79,11 @@ struct GemmParams {
     int head_dim;
     float qk_eps;
     int group_n;  // tile order: groups of group_n N-blocks, M-blocks within
+    // work split: tiles as units, K-steps as key tiles (attn_sched.h); the
+    // hand-off flags and slots of raw fp32 accumulators [MH*128][HALF_COLS]
+    AttnGrid g;
+    int *split_flags;
+    float *split_state;
     // LoRA: K-steps of U L^T after the main ones (two half stages each)
     int num_lk;
     int lora_on0, lora_on1;
@@ -110,7 +124,8 @@ struct Cfg {
     static constexpr int ACC_COLS = MH * HALF_COLS;  // per accumulator buffer
     static constexpr int TMEM_COLS = 2 * ACC_COLS;
     static constexpr int OUT_COLS = BN;       // output columns per tile
-    static constexpr int BAR_BYTES = 256;
+    static constexpr int SLOT_FLOATS = MH * kBM * HALF_COLS;  // one tile's accumulator
+    static constexpr int BAR_BYTES = 512;  // barriers, TMEM slot, abort flag, schedule
     static constexpr int SMEM_BYTES = OFF_C + CSTAGES * C_BYTES + BAR_BYTES + 1024;
 };
 
@@ -391,6 +406,46 @@ DEV void epilogue_tile(const GemmParams &p, uint32_t taddr, int64_t m, int nb) {
     }
 }
 
+// A thread's row of a raw fp32 accumulator between TMEM (COLS columns from
+// taddr) and a hand-off slot of ROWS rows.  The slot is column-group major:
+// the 4 columns 4j..4j+3 of row r are float4 number j * ROWS + r, so a warp's
+// 32 rows move 512 contiguous bytes per access (row-major slots cost a cache
+// line per thread and made each hand-off several times slower).
+template <int COLS, int ROWS>
+DEV void slot_to_tmem(const float *slot, int row, uint32_t taddr) {
+    const float4 *s4 = reinterpret_cast<const float4 *>(slot) + row;
+#pragma unroll 1
+    for (int c0 = 0; c0 < COLS; c0 += 32) {
+        uint32_t r[32];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const float4 v = s4[size_t((c0 >> 2) + i) * ROWS];
+            r[4 * i] = __float_as_uint(v.x);
+            r[4 * i + 1] = __float_as_uint(v.y);
+            r[4 * i + 2] = __float_as_uint(v.z);
+            r[4 * i + 3] = __float_as_uint(v.w);
+        }
+        __syncwarp();
+        tmem_st32_sync(taddr + c0, r);
+    }
+}
+template <int COLS, int ROWS>
+DEV void tmem_to_slot(uint32_t taddr, float *slot, int row) {
+    float4 *d4 = reinterpret_cast<float4 *>(slot) + row;
+#pragma unroll 1
+    for (int c0 = 0; c0 < COLS; c0 += 32) {
+        uint32_t r[32];
+        __syncwarp();
+        tmem_ld32(taddr + c0, r);
+        tmem_ld_wait(r);
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            d4[size_t((c0 >> 2) + i) * ROWS] = make_float4(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]),
+                                            __uint_as_float(r[4 * i + 2]),
+                                            __uint_as_float(r[4 * i + 3]));
+    }
+}
+
 // DOWN with acc_load: write the carried fp32 accumulator of tile t into the
 // TMEM buffer before the tile's MMAs start (they then accumulate onto it).
 template <int MODE, bool I8, int MH>
@@ -436,9 +491,14 @@ __global__ void __launch_bounds__(Cfg<MODE, I8, MH>::THREADS, 1)
     uint8_t *tiles = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *bars = reinterpret_cast<uint64_t *>(tiles + C::OFF_C + CS * C::C_BYTES);
-    // bars: full[S], empty[S], cfull[4], cempty[4], tfull[2], tempty[2], drain
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * S + 8 + 5);
+    // bars: full[S], empty[S], cfull[4], cempty[4], tfull[2], tempty[2], drain,
+    // handed (split accumulator written); then the TMEM slot, the abort flag
+    // and (at byte 256) this CTA's work list
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * S + 8 + 6);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    AttnCta *cs_smem = reinterpret_cast<AttnCta *>(reinterpret_cast<uint8_t *>(bars) + 256);
+    if (threadIdx.x == 0) *cs_smem = attn_cta(p.g, blockIdx.x);
+    const AttnCta &cs = *cs_smem;
 
     const int warp = warp_id();
     const int lane = lane_id();
@@ -450,6 +510,7 @@ __global__ void __launch_bounds__(Cfg<MODE, I8, MH>::THREADS, 1)
     auto tfull_bar = [&](int b) { return bar0 + 8u * (2 * S + 8 + b); };
     auto tempty_bar = [&](int b) { return bar0 + 8u * (2 * S + 10 + b); };
     const uint32_t drain_bar = bar0 + 8u * (2 * S + 12);
+    const uint32_t handed_bar = bar0 + 8u * (2 * S + 13);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
@@ -465,6 +526,7 @@ __global__ void __launch_bounds__(Cfg<MODE, I8, MH>::THREADS, 1)
             mbar_init(tempty_bar(b), 128);
         }
         mbar_init(drain_bar, 1);
+        mbar_init(handed_bar, 4);  // one arrival per epilogue warp
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -488,7 +550,7 @@ __global__ void __launch_bounds__(Cfg<MODE, I8, MH>::THREADS, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     const WaitCtx wc{abort_flag, p.status};
-    const int num_tiles = p.num_m * p.num_n;
+    const int cta = blockIdx.x;
     const bool preload = (MODE == DIT_EPI_DOWN || MODE == DIT_EPI_STORE_BF16) && p.acc_load;
 
     if (warp == 0) {
@@ -498,10 +560,11 @@ __global__ void __launch_bounds__(Cfg<MODE, I8, MH>::THREADS, 1)
             uint32_t ph = 0;
             int64_t issued = 0;
             bool ok = true;
-            for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+            for (int idx = 0; idx < cs.count && ok; ++idx) {
+                const AttnItem it = attn_item(p.g, cs, cta, idx);
                 int mb, nb;
-                tile_of(p, t, mb, nb);
-                for (int kb = 0; kb < p.num_k; ++kb) {
+                tile_of(p, it.u, mb, nb);
+                for (int kb = it.k0; kb < it.k1; ++kb) {
                     if (!mbar_wait(empty_bar(stage), ph ^ 1u, wc)) {
                         ok = false;
                         break;
@@ -526,8 +589,10 @@ __global__ void __launch_bounds__(Cfg<MODE, I8, MH>::THREADS, 1)
                         ph ^= 1u;
                     }
                 }
-                // LoRA K-steps: U and L tiles, one half stage per accumulator half
-                for (int lk = 0; lk < p.num_lk && ok; ++lk) {
+                // LoRA K-steps (after the tile's last W K-step): U and L
+                // tiles, one half stage per accumulator half
+                const int num_lk = it.k1 == p.num_k ? p.num_lk : 0;
+                for (int lk = 0; lk < num_lk && ok; ++lk) {
                     for (int h = 0; h < 2; ++h) {
                         if (!mbar_wait(empty_bar(stage), ph ^ 1u, wc)) {
                             ok = false;
@@ -567,38 +632,46 @@ __global__ void __launch_bounds__(Cfg<MODE, I8, MH>::THREADS, 1)
             constexpr uint32_t IDESC_L = idesc_bf16_f32(kBM, kLoraRows);
             int stage = 0, cstage = 0;
             uint32_t ph = 0, cph = 0;
-            int buf = 0;
-            uint32_t bph = 0;
+            // descriptors of the first TMA stage and the first converted-B stage
+            const uint64_t da0 = desc_sw128(smem_u32(tiles));
+            const uint64_t dc0 = desc_sw128(smem_u32(tiles + C::OFF_C));
             bool ok = true;
-            for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
-                if (!mbar_wait(tempty_bar(buf), preload ? bph : (bph ^ 1u), wc)) {
+            for (int idx = 0; idx < cs.count && ok; ++idx) {
+                const AttnItem it = attn_item(p.g, cs, cta, idx);
+                // accumulator buffer idx % 2, ready (drained, and holding the
+                // carry if the item starts from one) once per use
+                const int buf = idx & 1;
+                if (!mbar_wait(tempty_bar(buf), uint32_t((idx >> 1) & 1), wc)) {
                     ok = false;
                     break;
                 }
+                // the first K-step accumulates onto a carry: the CTA before's
+                // partial sum at k0, or the caller's accumulator
+                const bool carried = it.k0 > 0 || preload;
                 tc_fence_after();
                 const uint32_t d = tmem + uint32_t(buf * C::ACC_COLS);
-                for (int kb = 0; kb < p.num_k; ++kb) {
+                for (int kb = it.k0; kb < it.k1; ++kb) {
                     if (!mbar_wait(full_bar(stage), ph, wc) ||
                         (I8 && !mbar_wait(cfull_bar(cstage), cph, wc))) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t sA = smem_u32(tiles + stage * C::STAGE_BYTES);
-                    const uint32_t sB = I8 ? smem_u32(tiles + C::OFF_C + cstage * C::C_BYTES)
-                                           : sA + C::A_BYTES;
-                    // descriptors of the stage's tiles, stepped through K (16
-                    // elements = 32 bytes = 2 in the address field) and the M
-                    // halves (128 rows = 16 KB); the field cannot overflow
-                    const uint64_t da = desc_sw128(sA), db = desc_sw128(sB);
+                    // descriptors of the stage's tiles, stepped from the ring's
+                    // first stage by whole stages and through K (16 elements =
+                    // 32 bytes = 2 in the address field) and the M halves (128
+                    // rows = 16 KB); the field cannot overflow
+                    const uint64_t da = da0 + uint64_t(stage * (C::STAGE_BYTES >> 4));
+                    const uint64_t db = I8 ? dc0 + uint64_t(cstage * (C::C_BYTES >> 4))
+                                           : da + uint64_t(C::A_BYTES >> 4);
+                    const uint32_t accum0 = kb != it.k0 || carried;
 #pragma unroll
                     for (int k = 0; k < kBK / 16; ++k) {
-                        const uint32_t accum = (kb | k) != 0 || preload;
 #pragma unroll
                         for (int mh = 0; mh < MH; ++mh)
                             mma_bf16_ss(d + uint32_t(mh * C::HALF_COLS),
                                         da + uint64_t(mh * (kBM * 128 / 16) + 2 * k),
-                                        db + uint64_t(2 * k), IDESC, accum);
+                                        db + uint64_t(2 * k), IDESC, k == 0 ? accum0 : 1u);
                     }
                     mma_commit(empty_bar(stage));
                     if (++stage == S) {
@@ -615,8 +688,9 @@ __global__ void __launch_bounds__(Cfg<MODE, I8, MH>::THREADS, 1)
                 }
                 if (!ok) break;
                 int mb, nb;
-                tile_of(p, t, mb, nb);
-                for (int lk = 0; lk < p.num_lk && ok; ++lk) {
+                tile_of(p, it.u, mb, nb);
+                const int num_lk = it.k1 == p.num_k ? p.num_lk : 0;
+                for (int lk = 0; lk < num_lk && ok; ++lk) {
                     for (int h = 0; h < 2; ++h) {
                         if (!mbar_wait(full_bar(stage), ph, wc)) {
                             ok = false;
@@ -640,10 +714,6 @@ __global__ void __launch_bounds__(Cfg<MODE, I8, MH>::THREADS, 1)
                 }
                 if (!ok) break;
                 mma_commit(tfull_bar(buf));
-                if (++buf == 2) {
-                    buf = 0;
-                    bph ^= 1u;
-                }
             }
             if (!ok) {  // every issued MMA must finish before TMEM is freed
                 mma_commit(drain_bar);
@@ -654,54 +724,76 @@ __global__ void __launch_bounds__(Cfg<MODE, I8, MH>::THREADS, 1)
         // -------------------------------------------------- epilogue
         const int q = warp & 3;  // TMEM lane quadrant this warp may access
         const uint32_t lane_base = tmem + (uint32_t(q * 32) << 16);
-        int buf = 0;
-        uint32_t bph = 0;
-        int t = blockIdx.x;
-        if (preload && t < num_tiles) {
-            int mb0, nb0;
-            tile_of(p, t, mb0, nb0);
-#pragma unroll
-            for (int mh = 0; mh < MH; ++mh)
-                preload_tile<MODE, I8, MH>(p, lane_base + uint32_t(mh * C::HALF_COLS),
-                                           int64_t(mb0) * C::BM + mh * kBM + q * 32 + lane,
-                                           nb0);
-            tc_fence_before();
-            mbar_arrive(tempty_bar(0));
-        }
-        for (; t < num_tiles; t += gridDim.x) {
-            if (preload) {
-                const int tn = t + gridDim.x;
-                if (tn < num_tiles) {
-                    int mbn, nbn;
-                    tile_of(p, tn, mbn, nbn);
-#pragma unroll
-                    for (int mh = 0; mh < MH; ++mh)
-                        preload_tile<MODE, I8, MH>(
-                            p, lane_base + uint32_t((buf ^ 1) * C::ACC_COLS + mh * C::HALF_COLS),
-                            int64_t(mbn) * C::BM + mh * kBM + q * 32 + lane, nbn);
-                    tc_fence_before();
-                    mbar_arrive(tempty_bar(buf ^ 1));
-                }
-            }
-            bool ok = mbar_wait(tfull_bar(buf), bph, wc);
-            ok = __all_sync(0xffffffffu, ok);
-            if (!ok) break;
-            tc_fence_after();
-            int mb, nb;
-            tile_of(p, t, mb, nb);
+        // Buffer j % 2 ready for item j: drained (this warp's epilogue of item
+        // j - 2 is done, by program order) and, if the item starts from a
+        // carry, holding it: the CTA before's raw accumulator at K-step k0
+        // (waited for by its flag), or the caller's accumulator.
+        auto prepare = [&](int j) -> bool {
+            const AttnItem it = attn_item(p.g, cs, cta, j);
+            const uint32_t base = lane_base + uint32_t((j & 1) * C::ACC_COLS);
+            if (it.k0 > 0) {
+                const bool w = flag_wait(p.split_flags + it.src, wc);
+                if (!__all_sync(0xffffffffu, w)) return false;
+                const float *slot = p.split_state + size_t(it.src) * C::SLOT_FLOATS;
 #pragma unroll 1
-            for (int mh = 0; mh < MH; ++mh)
-                epilogue_tile<MODE, I8, MH>(
-                    p, lane_base + uint32_t(buf * C::ACC_COLS + mh * C::HALF_COLS),
-                    int64_t(mb) * C::BM + mh * kBM + q * 32 + lane, nb);
-            if (!preload) {
-                tc_fence_before();
-                mbar_arrive(tempty_bar(buf));
+                for (int mh = 0; mh < MH; ++mh)
+                    slot_to_tmem<C::HALF_COLS, MH * kBM>(slot, mh * kBM + q * 32 + lane,
+                                                         base + uint32_t(mh * C::HALF_COLS));
+            } else if (preload) {
+                int mb, nb;
+                tile_of(p, it.u, mb, nb);
+#pragma unroll 1
+                for (int mh = 0; mh < MH; ++mh)
+                    preload_tile<MODE, I8, MH>(p, base + uint32_t(mh * C::HALF_COLS),
+                                               int64_t(mb) * C::BM + mh * kBM + q * 32 + lane,
+                                               nb);
             }
-            if (++buf == 2) {
-                buf = 0;
-                bph ^= 1u;
+            tc_fence_before();
+            mbar_arrive(tempty_bar(j & 1));
+            return true;
+        };
+        bool ok = true;
+        for (int j = 0; ok && j < 2 && j < cs.count; ++j) ok = prepare(j);
+        for (int idx = 0; ok && idx < cs.count; ++idx) {
+            const int buf = idx & 1;
+            {
+                const bool w = mbar_wait(tfull_bar(buf), uint32_t((idx >> 1) & 1), wc);
+                if (!__all_sync(0xffffffffu, w)) break;
             }
+            tc_fence_after();
+            const AttnItem it = attn_item(p.g, cs, cta, idx);
+            const uint32_t base = lane_base + uint32_t(buf * C::ACC_COLS);
+            if (it.k1 < p.num_k) {
+                // hand the raw accumulator at K-step k1 to the CTA that
+                // continues the tile: all rows write, then one thread sets the
+                // flag (a CTA hands on at most once: only its range's end can
+                // fall inside a tile)
+                float *slot = p.split_state + size_t(it.dst) * C::SLOT_FLOATS;
+#pragma unroll 1
+                for (int mh = 0; mh < MH; ++mh)
+                    tmem_to_slot<C::HALF_COLS, MH * kBM>(base + uint32_t(mh * C::HALF_COLS), slot,
+                                                         mh * kBM + q * 32 + lane);
+                __threadfence();
+                mbar_arrive_warp(handed_bar);
+                if (warp == 2 && lane == 0) {
+                    if (!mbar_wait(handed_bar, 0u, wc)) {
+                        ok = false;
+                    } else {
+                        __threadfence();
+                        flag_release(p.split_flags + it.dst);
+                    }
+                }
+                ok = __all_sync(0xffffffffu, ok);
+            } else {
+                int mb, nb;
+                tile_of(p, it.u, mb, nb);
+#pragma unroll 1
+                for (int mh = 0; mh < MH; ++mh)
+                    epilogue_tile<MODE, I8, MH>(
+                        p, base + uint32_t(mh * C::HALF_COLS),
+                        int64_t(mb) * C::BM + mh * kBM + q * 32 + lane, nb);
+            }
+            if (ok && idx + 2 < cs.count) ok = prepare(idx + 2);
         }
     } else if (I8 && warp != 9 && warp != 11) {
         // -------------------------------------------------- int8 -> bf16
@@ -713,8 +805,9 @@ __global__ void __launch_bounds__(Cfg<MODE, I8, MH>::THREADS, 1)
         int stage = 0, cstage = 0;
         uint32_t ph = 0, cph = 0;
         bool ok = true;
-        for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
-            for (int kb = 0; kb < p.num_k; ++kb) {
+        for (int idx = 0; ok && idx < cs.count; ++idx) {
+            const AttnItem it = attn_item(p.g, cs, cta, idx);
+            for (int kb = it.k0; kb < it.k1; ++kb) {
                 bool w = mbar_wait(full_bar(stage), ph, wc) &&
                          mbar_wait(cempty_bar(cstage), cph ^ 1u, wc);
                 w = __all_sync(0xffffffffu, w);
@@ -745,6 +838,9 @@ __global__ void __launch_bounds__(Cfg<MODE, I8, MH>::THREADS, 1)
                             int8x8_to_bf16x8(w8[i]);
                 }
                 fence_proxy_async_smem();  // the tensor core reads what we wrote
+                // every converter thread arrives as soon as its own stores are
+                // fenced (one arrival per warp after __syncwarp measured 3-5 %
+                // slower int8 launches)
                 mbar_arrive(cfull_bar(cstage));
                 if (++stage == S) {
                     stage = 0;
@@ -756,7 +852,8 @@ __global__ void __launch_bounds__(Cfg<MODE, I8, MH>::THREADS, 1)
                 }
             }
             // the tile's LoRA stages hold bf16 tiles the MMA reads directly
-            for (int i = 0; ok && i < 2 * p.num_lk; ++i) {
+            const int num_lk = it.k1 == p.num_k ? p.num_lk : 0;
+            for (int i = 0; ok && i < 2 * num_lk; ++i) {
                 if (++stage == S) {
                     stage = 0;
                     ph ^= 1u;
@@ -771,6 +868,9 @@ __global__ void __launch_bounds__(Cfg<MODE, I8, MH>::THREADS, 1)
         tc_fence_after();
         tmem_dealloc(tmem, C::TMEM_COLS);
     }
+    // every thread of this CTA is past its wait on the flag it consumed:
+    // leave it zero for the next launch
+    if (threadIdx.x == 0 && cs.has_a && cs.a.src >= 0) p.split_flags[cs.a.src] = 0;
 }
 
 int &attr_flag(int mode, bool i8, int mh) {
@@ -781,8 +881,10 @@ int &attr_flag(int mode, bool i8, int mh) {
 }
 
 template <int MODE, bool I8, int MH>
-dit_status_t run(const dit_gemm_args_t &a, int *dev_status, cudaStream_t s) {
+dit_status_t run(const dit_gemm_args_t &a, int *dev_status, cudaStream_t s,
+                 const AttnSplit *split) {
     using C = Cfg<MODE, I8, MH>;
+    static_assert(size_t(C::SLOT_FLOATS) * 4 == kGemmSlotBytes, "hand-off slot size");
     CUtensorMap tA, tB0, tB1;
     if (!make_tmap_2d(&tA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.a, uint64_t(a.K), uint64_t(a.M),
                       uint64_t(a.lda) * 2, kBK, C::BM))
@@ -878,19 +980,45 @@ dit_status_t run(const dit_gemm_args_t &a, int *dev_status, cudaStream_t s) {
         done = 1;
     }
     const int tiles = p.num_m * p.num_n;
-    const int grid = tiles < sm_count() ? tiles : sm_count();
-    gemm_tc_kernel<MODE, I8, MH><<<grid, C::THREADS, C::SMEM_BYTES, s>>>(tA, tB0, tB1, tU0, tL0,
-                                                                     tU1, tL1, p);
+    int max_cta = sm_count();
+    if (split && split->max_ctas > 0 && split->max_ctas < max_cta) max_cta = split->max_ctas;
+    // No split where the epilogue, not the main loop, bounds a tile: the bf16
+    // gated-residual launch's fp32 read-modify-write (about 20 us per 128 x
+    // 256 tile against 16 us of MMAs, measured) would only gain work.
+    const bool split_pays = I8 || MODE != DIT_EPI_RESID;
+    const int slots = (split_pays && split && split->flags && split->state) ? split->slots : 0;
+    p.g = attn_grid(tiles, p.num_k, max_cta, slots);
+    if (p.g.n_pc > 0) {
+        p.split_flags = split->flags;
+        p.split_state = split->state;
+    }
+    // CTAs that hand accumulators to one another must all be resident at
+    // once: a cooperative launch guarantees it (at most one CTA per SM)
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(unsigned(p.g.n_cta));
+    cfg.blockDim = dim3(C::THREADS);
+    cfg.dynamicSmemBytes = C::SMEM_BYTES;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = p.g.n_pc > 0 ? 1 : 0;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_tc_kernel<MODE, I8, MH>, tA, tB0, tB1,
+                                             tU0, tL0, tU1, tL1, p);
+    if (e != cudaSuccess) return cuda_fail(e);
     return check_launch();
 }
 
 template <int MODE>
-dit_status_t run_b(const dit_gemm_args_t &a, int *dev_status, cudaStream_t s) {
-    if (a.b_dtype == DIT_W_BF16) return run<MODE, false, 1>(a, dev_status, s);
+dit_status_t run_b(const dit_gemm_args_t &a, int *dev_status, cudaStream_t s,
+                   const AttnSplit *split) {
+    if (a.b_dtype == DIT_W_BF16) return run<MODE, false, 1>(a, dev_status, s, split);
     // int8: two M halves per converted B tile, except with LoRA K-steps (their
     // stages are laid out for one 128-row half)
     const bool lora = a.lora_l0 || a.lora_l1;
-    return lora ? run<MODE, true, 1>(a, dev_status, s) : run<MODE, true, 2>(a, dev_status, s);
+    return lora ? run<MODE, true, 1>(a, dev_status, s, split)
+                : run<MODE, true, 2>(a, dev_status, s, split);
 }
 
 bool ld_ok(int64_t ld, int64_t min_ld, int elem_bytes) {
@@ -899,7 +1027,8 @@ bool ld_ok(int64_t ld, int64_t min_ld, int elem_bytes) {
 
 }  // namespace
 
-dit_status_t launch_gemm(const dit_gemm_args_t &a, int *dev_status, cudaStream_t s) {
+dit_status_t launch_gemm(const dit_gemm_args_t &a, int *dev_status, cudaStream_t s,
+                         const AttnSplit *split) {
     if (a.M < 0 || a.N <= 0 || a.K <= 0 || a.N % 32 || a.K % kBK) return DIT_ERR_INVALID_ARG;
     if (a.M > (int64_t(1) << 31) - kBM) return DIT_ERR_INVALID_ARG;
     if (a.b_dtype != DIT_W_BF16 && a.b_dtype != DIT_W_INT8)
@@ -938,6 +1067,11 @@ dit_status_t launch_gemm(const dit_gemm_args_t &a, int *dev_status, cudaStream_t
             e = half_ok(a.lora_u1, a.lora_ldu1, a.lora_l1, a.lora_ldl1, a.lora_rank1);
         if (e != DIT_OK) return e;
     }
+    if (split && split->slots > 0) {
+        if (!split->flags || !split->state || split->slots > kGemmSplitSlots)
+            return DIT_ERR_INVALID_ARG;
+        if (!aligned16(split->state)) return DIT_ERR_ALIGN;
+    }
     if (a.M == 0) return DIT_OK;
     switch (a.mode) {
         case DIT_EPI_STORE_BF16:
@@ -947,26 +1081,26 @@ dit_status_t launch_gemm(const dit_gemm_args_t &a, int *dev_status, cudaStream_t
                 if (!a.acc || !aligned16(a.acc)) return DIT_ERR_ALIGN;
                 if (!ld_ok(a.ldacc, a.N, 4)) return DIT_ERR_INVALID_ARG;
             }
-            return run_b<DIT_EPI_STORE_BF16>(a, dev_status, s);
+            return run_b<DIT_EPI_STORE_BF16>(a, dev_status, s, split);
         case DIT_EPI_STORE_F32:
             if (!a.out || !aligned16(a.out)) return DIT_ERR_ALIGN;
             if (!ld_ok(a.ldo, a.N, 4)) return DIT_ERR_INVALID_ARG;
-            return run_b<DIT_EPI_STORE_F32>(a, dev_status, s);
+            return run_b<DIT_EPI_STORE_F32>(a, dev_status, s, split);
         case DIT_EPI_KV:
             if (!a.out || !a.out2 || !aligned16(a.out)) return DIT_ERR_ALIGN;
             if (a.split_n < 0 || a.split_n % 32 || a.split_n > a.N || a.row_offset < 0)
                 return DIT_ERR_INVALID_ARG;
             if (!ld_ok(a.ldo, a.split_n, 2) || a.ldo2 < a.row_offset + a.M)
                 return DIT_ERR_INVALID_ARG;
-            return run_b<DIT_EPI_KV>(a, dev_status, s);
+            return run_b<DIT_EPI_KV>(a, dev_status, s, split);
         case DIT_EPI_RESID:
             if (!a.x || !a.gate || !aligned16(a.x) || !aligned16(a.gate)) return DIT_ERR_ALIGN;
             if (!ld_ok(a.ldx, a.N, 4)) return DIT_ERR_INVALID_ARG;
-            return run_b<DIT_EPI_RESID>(a, dev_status, s);
+            return run_b<DIT_EPI_RESID>(a, dev_status, s, split);
         case DIT_EPI_SWIGLU:
             if (!a.b1 || !aligned16(a.b1) || !a.out || !aligned16(a.out)) return DIT_ERR_ALIGN;
             if (!ld_ok(a.ldo, a.N, 2)) return DIT_ERR_INVALID_ARG;
-            return run_b<DIT_EPI_SWIGLU>(a, dev_status, s);
+            return run_b<DIT_EPI_SWIGLU>(a, dev_status, s, split);
         case DIT_EPI_DOWN:
             if (a.acc_final) {
                 if (!a.x || !a.gate || !aligned16(a.x) || !aligned16(a.gate))
@@ -977,7 +1111,7 @@ dit_status_t launch_gemm(const dit_gemm_args_t &a, int *dev_status, cudaStream_t
                 if (!a.acc || !aligned16(a.acc)) return DIT_ERR_ALIGN;
                 if (!ld_ok(a.ldacc, a.N, 4)) return DIT_ERR_INVALID_ARG;
             }
-            return run_b<DIT_EPI_DOWN>(a, dev_status, s);
+            return run_b<DIT_EPI_DOWN>(a, dev_status, s, split);
         default:
             return DIT_ERR_INVALID_ARG;
     }

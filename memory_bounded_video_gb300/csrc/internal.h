@@ -34,6 +34,9 @@ struct dit_plan {
     // it; 0: none) in the attention phase; their flags sit in the header
     int split_slots = 0;
     size_t off_split = 0;
+    // the GEMMs' hand-off state (slots of kGemmSlotBytes), outside the phases
+    int gsplit_slots = 0;
+    size_t off_gsplit = 0;
     uint8_t *kv_host = nullptr;      // device address of the pinned host buffer
     size_t kv_host_bytes = 0;
     cudaStream_t copy_stream = nullptr;
@@ -80,7 +83,11 @@ bool make_tmap_2d(CUtensorMap *m, CUtensorMapDataType dt, const void *base,
 dit_status_t launch_modln(const float *x, int64_t rows, int D, const float *shift,
                           const float *scale, void *out, cudaStream_t s);
 
-dit_status_t launch_gemm(const dit_gemm_args_t &a, int *dev_status, cudaStream_t s);
+struct AttnSplit;
+// split: the hand-off space of the work split (flags, kGemmSlotBytes slots);
+// null or no slots: whole tiles only.
+dit_status_t launch_gemm(const dit_gemm_args_t &a, int *dev_status, cudaStream_t s,
+                         const AttnSplit *split = nullptr);
 
 // Carried softmax state for attention over keys in several launches.
 struct AttnState {

@@ -45,6 +45,14 @@ DEV void mbar_arrive(uint32_t bar) {
     asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(bar)
                  : "memory");
 }
+// One arrival for the whole warp (the barrier counts warps, not threads):
+// after __syncwarp, lane 0 arrives with release semantics, so every lane's
+// earlier writes and fences are ordered before the arrival.  One atomic on
+// the barrier word instead of 32.  All lanes of the warp must call it.
+DEV void mbar_arrive_warp(uint32_t bar) {
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
+}
 DEV void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
     asm volatile(
         "mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(bar),
@@ -99,6 +107,34 @@ DEV void mbar_wait_quiet(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
     const uint64_t t0 = globaltimer();
     while (!mbar_try_wait(bar, parity)) {
         if (globaltimer() - t0 > limit_ns) return;
+    }
+}
+
+// ------------------------------------------------------------ hand-off flags
+// A CTA that continues another CTA's partial result waits for that CTA's
+// flag (global int, 0 or 1): release / acquire at device scope.
+DEV void flag_release(int *f) {
+    asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(f), "r"(1) : "memory");
+}
+DEV int flag_acquire(const int *f) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(f) : "memory");
+    return v;
+}
+
+// Bounded wait for a hand-off flag; false (with the timeout recorded) if it
+// was not set within the limit or another wait of this CTA gave up.
+DEV bool flag_wait(const int *f, const WaitCtx &w) {
+    if (flag_acquire(f)) return true;
+    const uint64_t t0 = globaltimer();
+    while (true) {
+        __nanosleep(128);
+        if (flag_acquire(f)) return true;
+        if (*w.abort) return false;
+        if (globaltimer() - t0 > kWaitLimitNs) {
+            record_timeout(w);
+            return false;
+        }
     }
 }
 

@@ -53,7 +53,7 @@ SYMBOLS = (
     "dit_block_weight_scratch_bytes", "dit_block_bind_weight_scratch", "dit_int8_to_bf16",
     "dit_block_plan_set_kv_offload", "dit_block_kv_host_bytes", "dit_block_bind_kv_host",
     "dit_attention_part", "dit_attention_split_bytes", "dit_attention_ex",
-    "dit_attention_schedule",
+    "dit_attention_schedule", "dit_gemm_split_bytes", "dit_gemm_ex",
 )
 
 STATIC_SCRATCH_BYTES = 64 << 20
@@ -178,6 +178,8 @@ def _declare(lib):
         "dit_lora_prepare": (c_int, [vp, c_int64, c_int, c_int64, ctypes.c_float, vp, vp,
                                      c_int64, vp]),
         "dit_attention_split_bytes": (c_size, [c_int, c_int]),
+        "dit_gemm_split_bytes": (c_size, [c_int]),
+        "dit_gemm_ex": (c_int, [ctypes.POINTER(GemmArgs), vp, c_size, c_int, vp, vp]),
         "dit_attention_ex": (c_int, [vp, c_int64, c_int64, vp, c_int64, vp, c_int64,
                                      c_int64, c_int, c_int, vp, c_int64, vp, c_size, c_int,
                                      vp, vp]),
@@ -479,3 +481,13 @@ def attention_schedule(units, n_kv, max_ctas, slots):
            "dit_attention_schedule")
     items = [tuple(buf[7 * i:7 * i + 7]) for i in range(n.value)]
     return n_cta.value, n_split.value, items
+
+
+def gemm_split_bytes(slots):
+    return int(load().dit_gemm_split_bytes(slots))
+
+
+def gemm_ex(args: GemmArgs, split_ws=None, split_bytes=0, max_ctas=0, dev_status=None,
+            stream=None):
+    _check(load().dit_gemm_ex(ctypes.byref(args), ptr(split_ws), split_bytes, max_ctas,
+                              ptr(dev_status), stream_handle(stream)), "dit_gemm_ex")

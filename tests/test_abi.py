@@ -130,6 +130,36 @@ def split_region(ca, H, hd):
     return slots * 256 * (hd + 2) * 4
 
 
+def gemm_region(T, D, F, cm, ca, fs):
+    """Bytes of the GEMMs' hand-off state: 128 KiB slots for the most CTAs
+    that any of the plan's GEMM launches (K/V, Q, O, gate/up, down at full
+    and ragged chunk / slice sizes, in 256 x BN/2 or 128 x BN tiles) would
+    cut its last wave over on a 128..160-SM device, at most 64."""
+    from test_attention_schedule import grid
+
+    def units(M, N, two_b, r256):
+        bm = 256 if r256 else 128
+        bn = (128 if two_b else 256) // (2 if r256 else 1)
+        return -(-M // bm) * -(-N // bn)
+
+    slots = 0
+    def need(M, N, K, two_b):
+        nonlocal slots
+        if M <= 0 or N <= 0 or K <= 0:
+            return
+        for r256 in (False, True):
+            u = units(M, N, two_b, r256)
+            slots = max([slots] + [grid(u, K // 64, sm, 64)[1] for sm in range(128, 161)])
+    for M in (ca, T % ca):
+        need(M, 2 * D, D, False)
+        need(M, D, D, False)
+    for M in (cm, T % cm):
+        for fw in (fs, F % fs):
+            need(M, fw, D, True)
+            need(M, D, fw, False)
+    return slots * 128 * 1024
+
+
 def expected_workspace_offload(T, D, H, F, cm, ca, fs, kvb):
     """dit_block_workspace_bytes with K/V offload: the two ring slots and the
     carried attention state replace K and V^T."""
@@ -143,7 +173,8 @@ def expected_workspace_offload(T, D, H, F, cm, ca, fs, kvb):
     mlp = rup(rup(phase + 2 * cm * D) + 2 * cm * fs)
     if fs < F:
         mlp = rup(mlp + 4 * cm * D)
-    return max(attn, mlp)
+    g = gemm_region(T, D, F, cm, ca, fs)
+    return rup(max(attn, mlp) + g) if g else max(attn, mlp)
 
 
 def expected_workspace(T, D, F, cm, ca, fs, R=0, H=24):
@@ -165,7 +196,8 @@ def expected_workspace(T, D, F, cm, ca, fs, R=0, H=24):
         if fs < F:
             mlp = rup(mlp + 4 * cm * R)                     # down's fp32 carry
     attn = rup(attn + split_region(ca, H, D // H))          # attention hand-off state
-    return max(attn, mlp)
+    g = gemm_region(T, D, F, cm, ca, fs)                    # GEMM hand-off state
+    return rup(max(attn, mlp) + g) if g else max(attn, mlp)
 
 
 @pytest.mark.parametrize("cfg", [

@@ -150,10 +150,17 @@ def test_plan_workspace_holds_the_hand_off_space():
     base = 1024 + 2 * 32768 * 3072 + 2 * 3072 * 32768
     attn = base + 4 * 8192 * 3072 + slots * 256 * 130 * 4
     mlp = base + 2 * 8192 * 3072 + 2 * 8192 * 8192
-    assert big.workspace_bytes() == max(attn, mlp)
+    # plus the GEMMs' hand-off state: 8192-row chunks of 3072 outputs are 768
+    # tiles (5.05 waves on 152 SMs: 8 left over, each cut into 6 K ranges)
+    from test_abi import gemm_region
+    g = gemm_region(32768, 3072, 8192, 8192, 8192, 8192)
+    assert g == 48 * 128 * 1024
+    assert ds.attention_schedule(768, 48, 152, 64)[1] == 48
+    assert big.workspace_bytes() == max(attn, mlp) + g
     assert max(grid(256, 1 << 20, sm, 160)[1] for sm in range(128, 161)) == 0
     assert small.workspace_bytes() == (1024 + 4 * 4096 * 1024 + 2 * 4096 * 1024
-                                       + 2 * 4096 * 2816)
+                                       + 2 * 4096 * 2816
+                                       + gemm_region(4096, 1024, 2816, 4096, 4096, 2816))
 
 
 def test_split_bytes_and_arguments(lib):
