@@ -73,12 +73,14 @@ DS_HD AttnGrid attn_grid(int units, int n_kv, int max_cta, int slots) {
         int64_t q = F + 1;
         if (g.n_cta / R < q) q = g.n_cta / R;
         if (n_kv < q) q = n_kv;
-        const int64_t n = n1 > R * q ? n1 : R * q;
+        int64_t n = n1 > R * q ? n1 : R * q;
+        // with fewer slots than that, as many contiguous ranges as there are
+        // slots (still at most R * F of them)
+        if (n > slots) n = n1 < slots ? n1 : slots;
         // split only if the longest range is shorter than a unit (else every
-        // remainder unit stays whole, round robin, as it does when the
-        // hand-off space has too few slots)
-        const int64_t longest = (int64_t(R) * n_kv + n - 1) / n;
-        if (longest < n_kv && n <= slots) {
+        // remainder unit stays whole, round robin)
+        const int64_t longest = n > 0 ? (int64_t(R) * n_kv + n - 1) / n : n_kv;
+        if (longest < n_kv) {
             g.full = F;
             g.n_pc = int(n);
             g.rem_tiles = int64_t(R) * n_kv;

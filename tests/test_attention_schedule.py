@@ -26,9 +26,9 @@ def grid(units, n_kv, max_cta, slots):
     restating the documented rule: F = U // G whole units per CTA and the
     R = U % G remaining units cut into n ranges, n the larger of
     min(G, R*F, R*n_kv) (any ranges of at least n_kv / F tiles) and R*q,
-    q = min(F + 1, G // R, n_kv) (q aligned ranges per unit), used when
-    n <= slots and the longest range, ceil(R * n_kv / n), is shorter than a
-    unit."""
+    q = min(F + 1, G // R, n_kv) (q aligned ranges per unit), or, when that
+    exceeds the slots, min(the first, slots); used when the longest range,
+    ceil(R * n_kv / n), is shorter than a unit."""
     G = max(1, min(units, max_cta))
     F, R = divmod(units, G)
     if R == 0:
@@ -36,7 +36,9 @@ def grid(units, n_kv, max_cta, slots):
     n1 = min(G, R * F, R * n_kv)
     q = min(F + 1, G // R, n_kv)
     n = max(n1, R * q)
-    if n <= slots and -(-R * n_kv // n) < n_kv:
+    if n > slots:
+        n = min(n1, slots)
+    if n > 0 and -(-R * n_kv // n) < n_kv:
         return G, n, F, R
     return G, 0, F, R
 
@@ -151,11 +153,14 @@ def test_plan_workspace_holds_the_hand_off_space():
     attn = base + 4 * 8192 * 3072 + slots * 256 * 130 * 4
     mlp = base + 2 * 8192 * 3072 + 2 * 8192 * 8192
     # plus the GEMMs' hand-off state: 8192-row chunks of 3072 outputs are 768
-    # tiles (5.05 waves on 152 SMs: 8 left over, each cut into 6 K ranges)
+    # tiles (5.05 waves on 152 SMs: 8 left over, each cut into 6 K ranges);
+    # the K/V projection's 1536 tiles (10.1 waves) would use 152 slots and
+    # get the 64 there are
     from test_abi import gemm_region
     g = gemm_region(32768, 3072, 8192, 8192, 8192, 8192)
-    assert g == 48 * 128 * 1024
+    assert g == 64 * 128 * 1024
     assert ds.attention_schedule(768, 48, 152, 64)[1] == 48
+    assert ds.attention_schedule(1536, 48, 152, 64)[1] == 64
     assert big.workspace_bytes() == max(attn, mlp) + g
     assert max(grid(256, 1 << 20, sm, 160)[1] for sm in range(128, 161)) == 0
     assert small.workspace_bytes() == (1024 + 4 * 4096 * 1024 + 2 * 4096 * 1024
