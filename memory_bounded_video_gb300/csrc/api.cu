@@ -216,9 +216,8 @@ void layout(dit_plan *p) {
     int gs = 0;
     auto need = [&](int64_t M, int N, int K, bool two_b) {
         if (M <= 0 || N <= 0 || K <= 0) return;
-        for (bool r256 : {false, true}) {
-            const int n = attn_slots_needed(gemm_units(M, N, two_b, r256), K / 64,
-                                            kGemmSplitSlots);
+        for (bool pair : {false, true}) {
+            const int n = gemm_slots_needed(gemm_units(M, N, two_b, pair), K / 64, pair);
             if (n > gs) gs = n;
         }
     };

@@ -107,17 +107,31 @@ inline int attn_slots_needed(int units, int n_kv = 1 << 20, int cap = kAttnSplit
 }
 
 // The tensor-core GEMM uses the same split with output tiles as units and
-// K-steps of 64 as key tiles: a slot holds one tile's raw fp32 accumulator
-// (256 x 128 or 128 x 256 values), and a plan provides at most 64 slots.
+// K-steps of 64 as key tiles: a slot holds one CTA's raw fp32 accumulator
+// (128 x 256 values), and a plan provides at most 64 slots.
 constexpr int kGemmSplitSlots = 64;
 constexpr size_t kGemmSlotBytes = size_t(128) * 256 * 4;
 
-// GEMM tiles of an M x N output in either tile shape the GEMM uses (256 x
-// BN/2 or 128 x BN, BN = 256 or, with two B operands, 128 per operand).
-inline int gemm_units(int64_t M, int N, bool two_b, bool rows256) {
-    const int bm = rows256 ? 256 : 128;
-    const int bn = (two_b ? 128 : 256) / (rows256 ? 2 : 1);
+// GEMM tiles of an M x N output in either tile shape the GEMM uses: 128 x BN
+// on one CTA, or 256 x BN on a cluster pair (BN = 256, or with two B operands
+// 128 per operand).
+inline int gemm_units(int64_t M, int N, bool two_b, bool pair) {
+    const int bm = pair ? 256 : 128;
+    const int bn = two_b ? 128 : 256;
     return int((M + bm - 1) / bm) * ((N + bn - 1) / bn);
+}
+
+// Hand-off slots a GEMM launch of `units` tiles and `k_steps` K-steps may use
+// on a device of 128 to 160 SMs (pair tiles: 64 to 80 pairs, two slots per
+// cut, one per CTA), at most kGemmSplitSlots.
+inline int gemm_slots_needed(int units, int k_steps, bool pair) {
+    if (!pair) return attn_slots_needed(units, k_steps, kGemmSplitSlots);
+    int need = 0;
+    for (int w = kAttnMinSms / 2; w <= kAttnMaxSms / 2; ++w) {
+        const AttnGrid g = attn_grid(units, k_steps, w, kGemmSplitSlots / 2);
+        if (2 * g.n_pc > need) need = 2 * g.n_pc;
+    }
+    return need;
 }
 
 // The pieces of CTA c and where piece A goes among its whole units.

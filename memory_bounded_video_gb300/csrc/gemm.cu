@@ -97,36 +97,61 @@ constexpr int kLoraStageBytes = (kBM + kLoraRows) * kBK * 2;
 // conversion per multiply-add (the conversion's ALU throughput bounds the
 // int8 main loop); the N tile is halved so that both halves' accumulators
 // still fit TMEM twice.
-template <int MODE, bool I8, int MH = 1>
+//
+// P (pair): a cluster of two CTAs computes a 256 x 256 output tile (SwiGLU:
+// 256 rows x 128 features of gate and of up) with M = 256, N = 256 MMAs
+// issued by the leading CTA (cta_group::2).  Each CTA stages its own 128 rows
+// of A and half of the B rows (the N-block's first or second 128 rows; for
+// SwiGLU the gate or the up tile) and keeps its 128 rows x 256 columns of the
+// accumulator in its own tensor memory, so its epilogue is the MH = 1 one.
+// Per K-step a CTA then moves 64 KB through shared memory for bf16 B (TMA
+// writes of A and its B half, the MMA's reads of both) against 96 KB for the
+// one-CTA 128 x 256 tile, and 80 KB against 128 KB for int8 B with MH = 2:
+// the one-CTA tiles' main loops are bound by that traffic (78-80 % tensor
+// pipe activity for bf16).
+template <int MODE, bool I8, int MH = 1, bool P = false>
 struct Cfg {
+    static_assert(!P || MH == 1, "pair tiles hold one 128-row half per CTA");
     static constexpr int NB = (MODE == DIT_EPI_SWIGLU) ? 2 : 1;  // B operands
     static constexpr int BN = ((MODE == DIT_EPI_SWIGLU) ? 128 : 256) / MH;
-    static constexpr int BM = kBM * MH;                   // rows of A per tile
+    static constexpr int A_ROWS = kBM * MH;                 // rows of A per CTA
+    static constexpr int BM = A_ROWS * (P ? 2 : 1);         // rows of A per tile
+    static constexpr int B_ROWS = P ? 128 : NB * BN;        // B rows staged per CTA
+    static constexpr int B_BOX = P ? 128 : BN;              // rows of one B TMA box
+    static constexpr int MMA_M = P ? 256 : kBM;
     static constexpr int CONV_WARPS = 4;                   // int8 only
     // int8: 12 warps, converters on warps 6, 7, 8 and 10 (sub-partitions 2, 3,
     // 0, 2) and warps 9, 11 idle, so that the MMA-issuing warp 1 shares its
     // sub-partition with no converter: measured 7-10 % faster than converters
     // on warps 6..9, whose ALU stream slowed the MMA issue.
     static constexpr int THREADS = I8 ? 384 : 192;
-    static constexpr int A_BYTES = BM * kBK * 2;
-    static constexpr int B_BYTES = BN * kBK * 2;         // one bf16 B tile
-    static constexpr int BQ_BYTES = NB * BN * kBK;       // int8 B staging
-    // TMA ring: bf16: A + B (4 stages); int8: A + int8 B (4 stages).
-    static constexpr int STAGES = 4;
-    static constexpr int STAGE_BYTES = A_BYTES + (I8 ? BQ_BYTES : NB * B_BYTES);
+    static constexpr int A_BYTES = A_ROWS * kBK * 2;
+    static constexpr int BQ_BYTES = B_ROWS * kBK;          // int8 B staging
+    // TMA ring: bf16: A + B; int8: A + int8 B.
+    static constexpr int STAGES = P ? (I8 ? 5 : 6) : 4;
+    static constexpr int STAGE_BYTES = A_BYTES + (I8 ? BQ_BYTES : B_ROWS * kBK * 2);
     static constexpr int TMA_BYTES = STAGE_BYTES;
-    // int8 only: ring of converted bf16 B tiles read by the MMA (3 stages),
-    // decoupled from the TMA ring so TMA latency and conversion overlap.
-    static constexpr int CSTAGES = I8 ? 3 : 0;
-    static constexpr int C_BYTES = NB * B_BYTES;
+    // int8 only: ring of converted bf16 B tiles read by the MMA, decoupled
+    // from the TMA ring (3 stages) so TMA latency and conversion overlap.
+    // Pair tiles keep it in lockstep with the TMA ring instead: one commit per
+    // K-step then frees both (a multicast commit costs the MMA-issuing thread
+    // about one bf16 K-step: with two per K-step the int8 pair ran at 524 ns
+    // per K-step against 272 for bf16), and a TMA stage that has landed again
+    // proves the converted stage of the same index free.
+    static constexpr bool LOCK = P && I8;
+    static constexpr int CSTAGES = I8 ? (LOCK ? STAGES : 3) : 0;
+    static constexpr int C_BYTES = B_ROWS * kBK * 2;
     static constexpr int OFF_C = STAGES * STAGE_BYTES;
     static constexpr int HALF_COLS = NB * BN;      // fp32 TMEM columns per M half
     static constexpr int ACC_COLS = MH * HALF_COLS;  // per accumulator buffer
     static constexpr int TMEM_COLS = 2 * ACC_COLS;
     static constexpr int OUT_COLS = BN;       // output columns per tile
-    static constexpr int SLOT_FLOATS = MH * kBM * HALF_COLS;  // one tile's accumulator
-    static constexpr int BAR_BYTES = 512;  // barriers, TMEM slot, abort flag, schedule
+    static constexpr int SLOT_FLOATS = MH * kBM * HALF_COLS;  // one CTA's accumulator
+    // barriers (up to byte 384), TMEM slot, abort flag; this CTA's work list
+    // at byte 384
+    static constexpr int BAR_BYTES = 512;
     static constexpr int SMEM_BYTES = OFF_C + CSTAGES * C_BYTES + BAR_BYTES + 1024;
+    static_assert(2 * STAGES + 24 <= 48 && CSTAGES <= 8, "barriers overlap the work list");
 };
 
 // Output tile of persistent work index t.  Tiles go in groups of group_n
@@ -475,8 +500,8 @@ DEV void preload_tile(const GemmParams &p, uint32_t taddr, int64_t m, int nb) {
     }
 }
 
-template <int MODE, bool I8, int MH>
-__global__ void __launch_bounds__(Cfg<MODE, I8, MH>::THREADS, 1)
+template <int MODE, bool I8, int MH, bool P>
+__global__ void __launch_bounds__(Cfg<MODE, I8, MH, P>::THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                    const __grid_constant__ CUtensorMap tmB0,
                    const __grid_constant__ CUtensorMap tmB1,
@@ -484,20 +509,28 @@ __global__ void __launch_bounds__(Cfg<MODE, I8, MH>::THREADS, 1)
                    const __grid_constant__ CUtensorMap tmL0,
                    const __grid_constant__ CUtensorMap tmU1,
                    const __grid_constant__ CUtensorMap tmL1, const GemmParams p) {
-    using C = Cfg<MODE, I8, MH>;
+    using C = Cfg<MODE, I8, MH, P>;
     constexpr int S = C::STAGES;
     constexpr int CS = C::CSTAGES;
+    constexpr int G = P ? 2 : 1;  // cta_group of every tcgen05 instruction here
     extern __shared__ uint8_t smem_raw[];
     uint8_t *tiles = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *bars = reinterpret_cast<uint64_t *>(tiles + C::OFF_C + CS * C::C_BYTES);
-    // bars: full[S], empty[S], cfull[4], cempty[4], tfull[2], tempty[2], drain,
-    // handed (split accumulator written); then the TMEM slot, the abort flag
-    // and (at byte 256) this CTA's work list
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * S + 8 + 6);
+    // bars: full[S], empty[S], cfull[8], cempty[8], tfull[2], tempty[2], drain,
+    // handed (split accumulator written); then the TMEM slot and the abort
+    // flag; this CTA's work list at byte 384; 16 bytes per converter warp at
+    // byte 448 (int8 pair: completion-signal copies)
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * S + 22);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
-    AttnCta *cs_smem = reinterpret_cast<AttnCta *>(reinterpret_cast<uint8_t *>(bars) + 256);
-    if (threadIdx.x == 0) *cs_smem = attn_cta(p.g, blockIdx.x);
+    AttnCta *cs_smem = reinterpret_cast<AttnCta *>(reinterpret_cast<uint8_t *>(bars) + 384);
+    const uint32_t sig0 = smem_u32(bars) + 448u;
+    // work unit owner: the CTA, or the cluster pair; rank 0 of a pair issues
+    // the MMAs for both
+    const int cta = P ? int(cluster_id_x()) : int(blockIdx.x);
+    const int rank = P ? int(cluster_ctarank()) : 0;
+    const bool leader = rank == 0;
+    if (threadIdx.x == 0) *cs_smem = attn_cta(p.g, cta);
     const AttnCta &cs = *cs_smem;
 
     const int warp = warp_id();
@@ -506,24 +539,28 @@ __global__ void __launch_bounds__(Cfg<MODE, I8, MH>::THREADS, 1)
     auto full_bar = [&](int s) { return bar0 + 8u * s; };
     auto empty_bar = [&](int s) { return bar0 + 8u * (S + s); };
     auto cfull_bar = [&](int s) { return bar0 + 8u * (2 * S + s); };
-    auto cempty_bar = [&](int s) { return bar0 + 8u * (2 * S + 4 + s); };
-    auto tfull_bar = [&](int b) { return bar0 + 8u * (2 * S + 8 + b); };
-    auto tempty_bar = [&](int b) { return bar0 + 8u * (2 * S + 10 + b); };
-    const uint32_t drain_bar = bar0 + 8u * (2 * S + 12);
-    const uint32_t handed_bar = bar0 + 8u * (2 * S + 13);
+    auto cempty_bar = [&](int s) { return bar0 + 8u * (2 * S + 8 + s); };
+    auto tfull_bar = [&](int b) { return bar0 + 8u * (2 * S + 16 + b); };
+    auto tempty_bar = [&](int b) { return bar0 + 8u * (2 * S + 18 + b); };
+    const uint32_t drain_bar = bar0 + 8u * (2 * S + 20);
+    const uint32_t handed_bar = bar0 + 8u * (2 * S + 21);
+    // the leader's copy of a barrier (pair: where the peer reports to)
+    auto lead = [&](uint32_t bar) { return P ? mapa_shared(bar, 0) : bar; };
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
             mbar_init(full_bar(s), 1);
             mbar_init(empty_bar(s), 1);
         }
+        // converters per thread (a pair's leader: plus 16 bytes of
+        // completion-signal copy per converter warp of the peer)
         for (int s = 0; s < CS; ++s) {
             mbar_init(cfull_bar(s), 32 * C::CONV_WARPS);
             mbar_init(cempty_bar(s), 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(tfull_bar(b), 1);
-            mbar_init(tempty_bar(b), 128);
+            mbar_init(tempty_bar(b), 128 + (P ? 4 : 0));  // pair: + the peer's 4 warps
         }
         mbar_init(drain_bar, 1);
         mbar_init(handed_bar, 4);  // one arrival per epilogue warp
@@ -542,15 +579,15 @@ __global__ void __launch_bounds__(Cfg<MODE, I8, MH>::THREADS, 1)
         }
     }
     if (warp == 1) {
-        tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
-        tmem_relinquish();
+        tmem_alloc<G>(smem_u32(tmem_slot), C::TMEM_COLS);
+        tmem_relinquish<G>();
     }
     tc_fence_before();
     __syncthreads();
+    if constexpr (P) cluster_sync();  // both CTAs' barriers exist before any remote arrival
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     const WaitCtx wc{abort_flag, p.status};
-    const int cta = blockIdx.x;
     const bool preload = (MODE == DIT_EPI_DOWN || MODE == DIT_EPI_STORE_BF16) && p.acc_load;
 
     if (warp == 0) {
@@ -560,10 +597,14 @@ __global__ void __launch_bounds__(Cfg<MODE, I8, MH>::THREADS, 1)
             uint32_t ph = 0;
             int64_t issued = 0;
             bool ok = true;
+            // this CTA's B operand and rows within the N-block (pair: its half)
+            const CUtensorMap *tb = (P && C::NB == 2 && rank == 1) ? &tmB1 : &tmB0;
+            const int b_row0 = (P && C::NB == 1) ? rank * C::B_BOX : 0;
             for (int idx = 0; idx < cs.count && ok; ++idx) {
                 const AttnItem it = attn_item(p.g, cs, cta, idx);
                 int mb, nb;
                 tile_of(p, it.u, mb, nb);
+                const int a_row = mb * C::BM + rank * C::A_ROWS;
                 for (int kb = it.k0; kb < it.k1; ++kb) {
                     if (!mbar_wait(empty_bar(stage), ph ^ 1u, wc)) {
                         ok = false;
@@ -571,17 +612,27 @@ __global__ void __launch_bounds__(Cfg<MODE, I8, MH>::THREADS, 1)
                     }
                     const uint32_t sA = smem_u32(tiles + stage * C::STAGE_BYTES);
                     const uint32_t sB = sA + C::A_BYTES;
-                    const uint32_t b_step = I8 ? C::BN * kBK : C::B_BYTES;
-                    mbar_arrive_expect_tx(full_bar(stage), C::TMA_BYTES);
                     // test hook: CTA 0 withholds its first copy (the stage's
                     // transaction count then never completes)
                     const bool withhold = p.inject_stall && blockIdx.x == 0 && issued == 0;
-                    if (!withhold) {
-                        tma_load_2d(sA, &tmA, full_bar(stage), kb * kBK, mb * C::BM);
-                        tma_load_2d(sB, &tmB0, full_bar(stage), kb * kBK, nb * C::BN);
-                        if (C::NB == 2)
-                            tma_load_2d(sB + b_step, &tmB1, full_bar(stage), kb * kBK,
-                                        nb * C::BN);
+                    if (P && !I8) {
+                        // bf16 pair: both CTAs' tiles complete on the leader's
+                        // barrier, armed by the leader for both
+                        if (leader) mbar_arrive_expect_tx(full_bar(stage), 2 * C::TMA_BYTES);
+                        if (!withhold) {
+                            const uint32_t fb = lead(full_bar(stage));
+                            tma_load_2d_pair(sA, &tmA, fb, kb * kBK, a_row);
+                            tma_load_2d_pair(sB, tb, fb, kb * kBK, nb * C::BN + b_row0);
+                        }
+                    } else {
+                        mbar_arrive_expect_tx(full_bar(stage), C::TMA_BYTES);
+                    }
+                    if (!withhold && !(P && !I8)) {
+                        tma_load_2d(sA, &tmA, full_bar(stage), kb * kBK, a_row);
+                        tma_load_2d(sB, tb, full_bar(stage), kb * kBK, nb * C::BN + b_row0);
+                        if (!P && C::NB == 2)
+                            tma_load_2d(sB + C::B_BOX * kBK * (I8 ? 1 : 2), &tmB1,
+                                        full_bar(stage), kb * kBK, nb * C::BN);
                     }
                     ++issued;
                     if (++stage == S) {
@@ -590,8 +641,8 @@ __global__ void __launch_bounds__(Cfg<MODE, I8, MH>::THREADS, 1)
                     }
                 }
                 // LoRA K-steps (after the tile's last W K-step): U and L
-                // tiles, one half stage per accumulator half
-                const int num_lk = it.k1 == p.num_k ? p.num_lk : 0;
+                // tiles, one half stage per accumulator half (one-CTA tiles)
+                const int num_lk = (!P && it.k1 == p.num_k) ? p.num_lk : 0;
                 for (int lk = 0; lk < num_lk && ok; ++lk) {
                     for (int h = 0; h < 2; ++h) {
                         if (!mbar_wait(empty_bar(stage), ph ^ 1u, wc)) {
@@ -617,19 +668,34 @@ __global__ void __launch_bounds__(Cfg<MODE, I8, MH>::THREADS, 1)
                 }
             }
             if (!ok) {  // let the copies already in flight land before exit
-                const int64_t first = issued > S ? issued - S : 0;
-                for (int64_t i = first; i < issued; ++i)
-                    mbar_wait_quiet(full_bar(int(i % S)), uint32_t((i / S) & 1), kWaitLimitNs);
+                if (P && !I8 && !leader) {
+                    // they complete on the leader's barriers: give them time
+                    const uint64_t t0 = globaltimer();
+                    while (globaltimer() - t0 < 200000ull) __nanosleep(1000);
+                } else {
+                    const int64_t first = issued > S ? issued - S : 0;
+                    for (int64_t i = first; i < issued; ++i)
+                        mbar_wait_quiet(full_bar(int(i % S)), uint32_t((i / S) & 1),
+                                        kWaitLimitNs);
+                }
             }
         }
-    } else if (warp == 1) {
+    } else if (warp == 1 && (!P || leader)) {
         if (lane == 0) {
             // ---------------------------------------------- MMA issuer
             // The NB B tiles are contiguous in shared memory (rows of B1 follow
-            // those of B0), so one MMA with N = NB * BN covers both; its
-            // accumulator columns BN.. are the B1 results.
-            constexpr uint32_t IDESC = idesc_bf16_f32(kBM, C::NB * C::BN);
+            // those of B0; pair: the peer's half follows this CTA's), so one
+            // MMA with N = NB * BN covers both; its accumulator columns BN..
+            // are the B1 results.
+            constexpr uint32_t IDESC = idesc_bf16_f32(C::MMA_M, C::NB * C::BN);
             constexpr uint32_t IDESC_L = idesc_bf16_f32(kBM, kLoraRows);
+            constexpr uint16_t kPairMask = 0x3;
+            auto commit = [&](uint32_t bar) {
+                if constexpr (P)
+                    mma_commit_pair_mc(bar, kPairMask);  // the same barrier in both CTAs
+                else
+                    mma_commit(bar);
+            };
             int stage = 0, cstage = 0;
             uint32_t ph = 0, cph = 0;
             // descriptors of the first TMA stage and the first converted-B stage
@@ -651,6 +717,9 @@ __global__ void __launch_bounds__(Cfg<MODE, I8, MH>::THREADS, 1)
                 tc_fence_after();
                 const uint32_t d = tmem + uint32_t(buf * C::ACC_COLS);
                 for (int kb = it.k0; kb < it.k1; ++kb) {
+                    // the stage's tiles (bf16 pair: both CTAs'); int8: the
+                    // converted B (pair: both halves; the peer's arrives once
+                    // its stage has landed and been converted)
                     if (!mbar_wait(full_bar(stage), ph, wc) ||
                         (I8 && !mbar_wait(cfull_bar(cstage), cph, wc))) {
                         ok = false;
@@ -667,19 +736,24 @@ __global__ void __launch_bounds__(Cfg<MODE, I8, MH>::THREADS, 1)
                     const uint32_t accum0 = kb != it.k0 || carried;
 #pragma unroll
                     for (int k = 0; k < kBK / 16; ++k) {
+                        if constexpr (P) {
+                            mma_bf16_ss_pair(d, da + uint64_t(2 * k), db + uint64_t(2 * k), IDESC,
+                                             k == 0 ? accum0 : 1u);
+                        } else {
 #pragma unroll
-                        for (int mh = 0; mh < MH; ++mh)
-                            mma_bf16_ss(d + uint32_t(mh * C::HALF_COLS),
-                                        da + uint64_t(mh * (kBM * 128 / 16) + 2 * k),
-                                        db + uint64_t(2 * k), IDESC, k == 0 ? accum0 : 1u);
+                            for (int mh = 0; mh < MH; ++mh)
+                                mma_bf16_ss(d + uint32_t(mh * C::HALF_COLS),
+                                            da + uint64_t(mh * (kBM * 128 / 16) + 2 * k),
+                                            db + uint64_t(2 * k), IDESC, k == 0 ? accum0 : 1u);
+                        }
                     }
-                    mma_commit(empty_bar(stage));
+                    commit(empty_bar(stage));
                     if (++stage == S) {
                         stage = 0;
                         ph ^= 1u;
                     }
                     if (I8) {
-                        mma_commit(cempty_bar(cstage));
+                        if (!C::LOCK) commit(cempty_bar(cstage));
                         if (++cstage == CS) {
                             cstage = 0;
                             cph ^= 1u;
@@ -687,43 +761,53 @@ __global__ void __launch_bounds__(Cfg<MODE, I8, MH>::THREADS, 1)
                     }
                 }
                 if (!ok) break;
-                int mb, nb;
-                tile_of(p, it.u, mb, nb);
-                const int num_lk = it.k1 == p.num_k ? p.num_lk : 0;
-                for (int lk = 0; lk < num_lk && ok; ++lk) {
-                    for (int h = 0; h < 2; ++h) {
-                        if (!mbar_wait(full_bar(stage), ph, wc)) {
-                            ok = false;
-                            break;
-                        }
-                        tc_fence_after();
-                        if (lora_half_on<MODE, I8, MH>(p, h, nb)) {
-                            const uint32_t sU = smem_u32(tiles + stage * C::STAGE_BYTES);
-                            const uint32_t sL = sU + C::A_BYTES;
+                if constexpr (!P) {
+                    int mb, nb;
+                    tile_of(p, it.u, mb, nb);
+                    const int num_lk = it.k1 == p.num_k ? p.num_lk : 0;
+                    for (int lk = 0; lk < num_lk && ok; ++lk) {
+                        for (int h = 0; h < 2; ++h) {
+                            if (!mbar_wait(full_bar(stage), ph, wc)) {
+                                ok = false;
+                                break;
+                            }
+                            tc_fence_after();
+                            if (lora_half_on<MODE, I8, MH>(p, h, nb)) {
+                                const uint32_t sU = smem_u32(tiles + stage * C::STAGE_BYTES);
+                                const uint32_t sL = sU + C::A_BYTES;
 #pragma unroll
-                            for (int k = 0; k < kBK / 16; ++k)
-                                mma_bf16_ss(d + uint32_t(h * kLoraRows), desc_sw128(sU + 32u * k),
-                                            desc_sw128(sL + 32u * k), IDESC_L, 1u);
-                        }
-                        mma_commit(empty_bar(stage));
-                        if (++stage == S) {
-                            stage = 0;
-                            ph ^= 1u;
+                                for (int k = 0; k < kBK / 16; ++k)
+                                    mma_bf16_ss(d + uint32_t(h * kLoraRows),
+                                                desc_sw128(sU + 32u * k),
+                                                desc_sw128(sL + 32u * k), IDESC_L, 1u);
+                            }
+                            mma_commit(empty_bar(stage));
+                            if (++stage == S) {
+                                stage = 0;
+                                ph ^= 1u;
+                            }
                         }
                     }
+                    if (!ok) break;
                 }
-                if (!ok) break;
-                mma_commit(tfull_bar(buf));
+                commit(tfull_bar(buf));
             }
             if (!ok) {  // every issued MMA must finish before TMEM is freed
-                mma_commit(drain_bar);
+                if constexpr (P)
+                    mma_commit_pair_mc(drain_bar, 0x1);  // this CTA's barrier only
+                else
+                    mma_commit(drain_bar);
                 mbar_wait_quiet(drain_bar, 0, kWaitLimitNs);
             }
         }
+    } else if (warp == 1) {
+        // (pair: the second CTA's warp 1 has nothing to do)
     } else if (warp < 6) {
         // -------------------------------------------------- epilogue
         const int q = warp & 3;  // TMEM lane quadrant this warp may access
         const uint32_t lane_base = tmem + (uint32_t(q * 32) << 16);
+        // hand-off flags and slots: one per CTA of a pair
+        auto hslot = [&](int i) { return P ? 2 * i + rank : i; };
         // Buffer j % 2 ready for item j: drained (this warp's epilogue of item
         // j - 2 is done, by program order) and, if the item starts from a
         // carry, holding it: the CTA before's raw accumulator at K-step k0
@@ -732,9 +816,9 @@ __global__ void __launch_bounds__(Cfg<MODE, I8, MH>::THREADS, 1)
             const AttnItem it = attn_item(p.g, cs, cta, j);
             const uint32_t base = lane_base + uint32_t((j & 1) * C::ACC_COLS);
             if (it.k0 > 0) {
-                const bool w = flag_wait(p.split_flags + it.src, wc);
+                const bool w = flag_wait(p.split_flags + hslot(it.src), wc);
                 if (!__all_sync(0xffffffffu, w)) return false;
-                const float *slot = p.split_state + size_t(it.src) * C::SLOT_FLOATS;
+                const float *slot = p.split_state + size_t(hslot(it.src)) * C::SLOT_FLOATS;
 #pragma unroll 1
                 for (int mh = 0; mh < MH; ++mh)
                     slot_to_tmem<C::HALF_COLS, MH * kBM>(slot, mh * kBM + q * 32 + lane,
@@ -744,12 +828,15 @@ __global__ void __launch_bounds__(Cfg<MODE, I8, MH>::THREADS, 1)
                 tile_of(p, it.u, mb, nb);
 #pragma unroll 1
                 for (int mh = 0; mh < MH; ++mh)
-                    preload_tile<MODE, I8, MH>(p, base + uint32_t(mh * C::HALF_COLS),
-                                               int64_t(mb) * C::BM + mh * kBM + q * 32 + lane,
-                                               nb);
+                    preload_tile<MODE, I8, MH>(
+                        p, base + uint32_t(mh * C::HALF_COLS),
+                        int64_t(mb) * C::BM + rank * C::A_ROWS + mh * kBM + q * 32 + lane, nb);
             }
             tc_fence_before();
-            mbar_arrive(tempty_bar(j & 1));
+            if (P && !leader)
+                mbar_arrive_remote_warp(lead(tempty_bar(j & 1)));
+            else
+                mbar_arrive(tempty_bar(j & 1));
             return true;
         };
         bool ok = true;
@@ -768,7 +855,7 @@ __global__ void __launch_bounds__(Cfg<MODE, I8, MH>::THREADS, 1)
                 // continues the tile: all rows write, then one thread sets the
                 // flag (a CTA hands on at most once: only its range's end can
                 // fall inside a tile)
-                float *slot = p.split_state + size_t(it.dst) * C::SLOT_FLOATS;
+                float *slot = p.split_state + size_t(hslot(it.dst)) * C::SLOT_FLOATS;
 #pragma unroll 1
                 for (int mh = 0; mh < MH; ++mh)
                     tmem_to_slot<C::HALF_COLS, MH * kBM>(base + uint32_t(mh * C::HALF_COLS), slot,
@@ -780,7 +867,7 @@ __global__ void __launch_bounds__(Cfg<MODE, I8, MH>::THREADS, 1)
                         ok = false;
                     } else {
                         __threadfence();
-                        flag_release(p.split_flags + it.dst);
+                        flag_release(p.split_flags + hslot(it.dst));
                     }
                 }
                 ok = __all_sync(0xffffffffu, ok);
@@ -791,13 +878,13 @@ __global__ void __launch_bounds__(Cfg<MODE, I8, MH>::THREADS, 1)
                 for (int mh = 0; mh < MH; ++mh)
                     epilogue_tile<MODE, I8, MH>(
                         p, base + uint32_t(mh * C::HALF_COLS),
-                        int64_t(mb) * C::BM + mh * kBM + q * 32 + lane, nb);
+                        int64_t(mb) * C::BM + rank * C::A_ROWS + mh * kBM + q * 32 + lane, nb);
             }
             if (ok && idx + 2 < cs.count) ok = prepare(idx + 2);
         }
     } else if (I8 && warp != 9 && warp != 11) {
         // -------------------------------------------------- int8 -> bf16
-        // Staged int8 rows (64 bytes each, NB*BN rows) become 128-byte bf16
+        // Staged int8 rows (64 bytes each, B_ROWS rows) become 128-byte bf16
         // rows of a converted-B stage; 16-byte chunk c of row r lands at
         // chunk c ^ (r % 8) of the row (the 128-byte swizzle), rows in 8-row
         // groups of 1024 bytes.
@@ -809,7 +896,7 @@ __global__ void __launch_bounds__(Cfg<MODE, I8, MH>::THREADS, 1)
             const AttnItem it = attn_item(p.g, cs, cta, idx);
             for (int kb = it.k0; kb < it.k1; ++kb) {
                 bool w = mbar_wait(full_bar(stage), ph, wc) &&
-                         mbar_wait(cempty_bar(cstage), cph ^ 1u, wc);
+                         (C::LOCK || mbar_wait(cempty_bar(cstage), cph ^ 1u, wc));
                 w = __all_sync(0xffffffffu, w);
                 if (!w) {
                     ok = false;
@@ -822,7 +909,7 @@ __global__ void __launch_bounds__(Cfg<MODE, I8, MH>::THREADS, 1)
                 // the same for all of them.  Loads are batched ahead of the
                 // conversions so their latency overlaps.
                 constexpr int kConv = 32 * C::CONV_WARPS;
-                constexpr int kPieces = C::NB * C::BN * 8 / kConv;
+                constexpr int kPieces = C::B_ROWS * 8 / kConv;
                 constexpr int kBatch = kPieces < 8 ? kPieces : 8;
                 const uint8_t *src = sq + (tid >> 3) * kBK + (tid & 7) * 8;
                 uint8_t *dst = dst0 + (tid >> 3) * 128 + (((tid & 7) ^ ((tid >> 3) & 7)) << 4);
@@ -840,8 +927,23 @@ __global__ void __launch_bounds__(Cfg<MODE, I8, MH>::THREADS, 1)
                 fence_proxy_async_smem();  // the tensor core reads what we wrote
                 // every converter thread arrives as soon as its own stores are
                 // fenced (one arrival per warp after __syncwarp measured 3-5 %
-                // slower int8 launches)
-                mbar_arrive(cfull_bar(cstage));
+                // slower int8 launches).  A pair's second CTA signals the
+                // leader instead, one 16-byte copy per warp completing on the
+                // leader's barrier (it also says this CTA's A tile landed):
+                // with a remote mbarrier arrival per K-step, which keeps the
+                // issuing thread waiting several hundred ns, the int8 pair
+                // ran at 480-520 ns per K-step
+                if (!P) {
+                    mbar_arrive(cfull_bar(cstage));
+                } else if (!leader) {
+                    __syncwarp();
+                    const uint32_t sig = sig0 + 16u * uint32_t(tid >> 5);
+                    if (lane == 0) bulk_signal_remote(lead(sig), sig, 16u, lead(cfull_bar(cstage)));
+                } else if (tid == 0) {
+                    mbar_arrive_expect_tx(cfull_bar(cstage), 16u * C::CONV_WARPS);
+                } else {
+                    mbar_arrive(cfull_bar(cstage));
+                }
                 if (++stage == S) {
                     stage = 0;
                     ph ^= 1u;
@@ -852,7 +954,7 @@ __global__ void __launch_bounds__(Cfg<MODE, I8, MH>::THREADS, 1)
                 }
             }
             // the tile's LoRA stages hold bf16 tiles the MMA reads directly
-            const int num_lk = it.k1 == p.num_k ? p.num_lk : 0;
+            const int num_lk = (!P && it.k1 == p.num_k) ? p.num_lk : 0;
             for (int i = 0; ok && i < 2 * num_lk; ++i) {
                 if (++stage == S) {
                     stage = 0;
@@ -864,41 +966,48 @@ __global__ void __launch_bounds__(Cfg<MODE, I8, MH>::THREADS, 1)
 
     tc_fence_before();
     __syncthreads();
+    // pair: neither CTA frees its tensor memory or leaves (its barriers may
+    // still take the other's arrivals) before both are done
+    if constexpr (P) cluster_sync();
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem, C::TMEM_COLS);
+        tmem_dealloc<G>(tmem, C::TMEM_COLS);
     }
     // every thread of this CTA is past its wait on the flag it consumed:
     // leave it zero for the next launch
-    if (threadIdx.x == 0 && cs.has_a && cs.a.src >= 0) p.split_flags[cs.a.src] = 0;
+    if (threadIdx.x == 0 && cs.has_a && cs.a.src >= 0)
+        p.split_flags[P ? 2 * cs.a.src + rank : cs.a.src] = 0;
 }
 
-int &attr_flag(int mode, bool i8, int mh) {
-    static int done[8][2][2][64] = {};  // per mode, B type, M halves, device
+// Per (mode, B type, tile shape, device): 0 until the kernel's shared-memory
+// attribute is set; then, for pair kernels, the most clusters of two that can
+// be resident at once (queried once).
+int &attr_flag(int mode, bool i8, int shape) {
+    static int done[8][2][3][64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
-    return done[mode][i8 ? 1 : 0][mh - 1][dev & 63];
+    return done[mode][i8 ? 1 : 0][shape][dev & 63];
 }
 
-template <int MODE, bool I8, int MH>
+template <int MODE, bool I8, int MH, bool P>
 dit_status_t run(const dit_gemm_args_t &a, int *dev_status, cudaStream_t s,
                  const AttnSplit *split) {
-    using C = Cfg<MODE, I8, MH>;
+    using C = Cfg<MODE, I8, MH, P>;
     static_assert(size_t(C::SLOT_FLOATS) * 4 == kGemmSlotBytes, "hand-off slot size");
     CUtensorMap tA, tB0, tB1;
     if (!make_tmap_2d(&tA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.a, uint64_t(a.K), uint64_t(a.M),
-                      uint64_t(a.lda) * 2, kBK, C::BM))
+                      uint64_t(a.lda) * 2, kBK, C::A_ROWS))
         return DIT_ERR_INVALID_ARG;
     const CUtensorMapDataType bdt =
         I8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     const uint64_t bel = I8 ? 1 : 2;
     const CUtensorMapSwizzle bsw = I8 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B;
     if (!make_tmap_2d(&tB0, bdt, a.b0, uint64_t(a.K), uint64_t(a.N), uint64_t(a.ldb) * bel, kBK,
-                      C::BN, bsw))
+                      C::B_BOX, bsw))
         return DIT_ERR_INVALID_ARG;
     tB1 = tB0;
     if (C::NB == 2 && !make_tmap_2d(&tB1, bdt, a.b1, uint64_t(a.K), uint64_t(a.N),
-                                    uint64_t(a.ldb) * bel, kBK, C::BN, bsw))
+                                    uint64_t(a.ldb) * bel, kBK, C::B_BOX, bsw))
         return DIT_ERR_INVALID_ARG;
 
     // LoRA operand maps (unused ones alias A's map)
@@ -928,6 +1037,7 @@ dit_status_t run(const dit_gemm_args_t &a, int *dev_status, cudaStream_t s,
         tU1 = tU0;
         tL1 = tL0;
     }
+    if (P && rmax) return DIT_ERR_INVALID_ARG;  // LoRA K-steps use one-CTA tiles
 
     GemmParams p{};
     p.M = a.M;
@@ -971,41 +1081,77 @@ dit_status_t run(const dit_gemm_args_t &a, int *dev_status, cudaStream_t s,
     p.lora_on0 = a.lora_l0 != nullptr;
     p.lora_on1 = C::NB == 2 ? a.lora_l1 != nullptr : a.lora_l0 != nullptr;
 
-    int &done = attr_flag(MODE, I8, MH);
+    cudaLaunchConfig_t cfg = {};
+    cfg.blockDim = dim3(C::THREADS);
+    cfg.dynamicSmemBytes = C::SMEM_BYTES;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeCooperative;
+    attr[1].val.cooperative = 1;
+
+    const int shape = P ? 2 : MH - 1;
+    int &done = attr_flag(MODE, I8, shape);
     if (!done) {
-        cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<MODE, I8, MH>,
+        cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<MODE, I8, MH, P>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              C::SMEM_BYTES);
         if (e != cudaSuccess) return cuda_fail(e);
         done = 1;
+        if (P) {
+            cfg.gridDim = dim3(2u * unsigned(sm_count() / 2));
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            int n = 0;
+            e = cudaOccupancyMaxActiveClusters(&n, gemm_tc_kernel<MODE, I8, MH, P>, &cfg);
+            if (e != cudaSuccess) return cuda_fail(e);
+            if (n < 1) return DIT_ERR_CUDA;
+            done = n;
+        }
     }
-    const int tiles = p.num_m * p.num_n;
-    int max_cta = sm_count();
-    if (split && split->max_ctas > 0 && split->max_ctas < max_cta) max_cta = split->max_ctas;
+    // workers: CTAs, or resident pairs
+    const int units = p.num_m * p.num_n;
+    int max_w = P ? done : sm_count();
+    if (split && split->max_ctas > 0) {
+        const int cap = P ? (split->max_ctas >= 2 ? split->max_ctas / 2 : 1) : split->max_ctas;
+        if (cap < max_w) max_w = cap;
+    }
     // No split where the epilogue, not the main loop, bounds a tile: the bf16
     // gated-residual launch's fp32 read-modify-write (about 20 us per 128 x
     // 256 tile against 16 us of MMAs, measured) would only gain work.
     const bool split_pays = I8 || MODE != DIT_EPI_RESID;
-    const int slots = (split_pays && split && split->flags && split->state) ? split->slots : 0;
-    p.g = attn_grid(tiles, p.num_k, max_cta, slots);
+    int slots = (split_pays && split && split->flags && split->state) ? split->slots : 0;
+    if (P) slots /= 2;  // a cut pair tile hands on two slots, one per CTA
+    p.g = attn_grid(units, p.num_k, max_w, slots);
     if (p.g.n_pc > 0) {
         p.split_flags = split->flags;
         p.split_state = split->state;
     }
     // CTAs that hand accumulators to one another must all be resident at
     // once: a cooperative launch guarantees it (at most one CTA per SM)
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(unsigned(p.g.n_cta));
-    cfg.blockDim = dim3(C::THREADS);
-    cfg.dynamicSmemBytes = C::SMEM_BYTES;
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeCooperative;
-    attr[0].val.cooperative = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = p.g.n_pc > 0 ? 1 : 0;
-    const cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_tc_kernel<MODE, I8, MH>, tA, tB0, tB1,
-                                             tU0, tL0, tU1, tL1, p);
+    auto launch = [&]() {
+        cudaLaunchAttribute used[2];
+        int na = 0;
+        if (P) used[na++] = attr[0];
+        if (p.g.n_pc > 0) used[na++] = attr[1];
+        cfg.gridDim = dim3(unsigned(p.g.n_cta * (P ? 2 : 1)));
+        cfg.attrs = used;
+        cfg.numAttrs = na;
+        return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<MODE, I8, MH, P>, tA, tB0, tB1, tU0, tL0,
+                                  tU1, tL1, p);
+    };
+    cudaError_t e = launch();
+    if (e != cudaSuccess && P && p.g.n_pc > 0) {
+        // no cooperative launch of clusters here: run whole tiles only
+        (void)cudaGetLastError();
+        p.g = attn_grid(units, p.num_k, max_w, 0);
+        p.split_flags = nullptr;
+        p.split_state = nullptr;
+        e = launch();
+    }
     if (e != cudaSuccess) return cuda_fail(e);
     return check_launch();
 }
@@ -1013,12 +1159,14 @@ dit_status_t run(const dit_gemm_args_t &a, int *dev_status, cudaStream_t s,
 template <int MODE>
 dit_status_t run_b(const dit_gemm_args_t &a, int *dev_status, cudaStream_t s,
                    const AttnSplit *split) {
-    if (a.b_dtype == DIT_W_BF16) return run<MODE, false, 1>(a, dev_status, s, split);
-    // int8: two M halves per converted B tile, except with LoRA K-steps (their
-    // stages are laid out for one 128-row half)
+    // LoRA K-steps are laid out for one-CTA tiles of 128 rows; everything
+    // else runs on pair tiles
     const bool lora = a.lora_l0 || a.lora_l1;
-    return lora ? run<MODE, true, 1>(a, dev_status, s, split)
-                : run<MODE, true, 2>(a, dev_status, s, split);
+    if (a.b_dtype == DIT_W_BF16)
+        return lora ? run<MODE, false, 1, false>(a, dev_status, s, split)
+                    : run<MODE, false, 1, true>(a, dev_status, s, split);
+    return lora ? run<MODE, true, 1, false>(a, dev_status, s, split)
+                : run<MODE, true, 1, true>(a, dev_status, s, split);
 }
 
 bool ld_ok(int64_t ld, int64_t min_ld, int elem_bytes) {

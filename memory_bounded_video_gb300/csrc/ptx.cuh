@@ -110,6 +110,47 @@ DEV void mbar_wait_quiet(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
     }
 }
 
+// ------------------------------------------------------------ clusters
+DEV uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+DEV uint32_t cluster_id_x() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+    return r;
+}
+// All threads of every CTA of the cluster: arrive (release) and wait
+// (acquire).  Only reached on paths every thread takes; every other wait in
+// the kernels that use it is bounded, so it cannot wait forever.
+DEV void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
+                 "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// Shared-memory address of the same variable in CTA `rank` of the cluster.
+DEV uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+    return r;
+}
+// Arrive on a barrier of another CTA of the cluster (address from
+// mapa_shared), with release semantics at CTA scope, the form used for
+// cross-CTA pipeline barriers in tensor-core GEMMs; at cluster scope the
+// arrival cost the issuing thread about 400 ns more (measured: the pair
+// GEMM's K-step went from 365 to 742 ns with one such arrival per K-step).
+// The issuing thread still waits several hundred ns for it, so pipelines
+// keep it off their per-K-step critical threads.
+DEV void mbar_arrive_remote(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.release.cta.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+                 : "memory");
+}
+// One such arrival for the whole warp; all lanes call it.
+DEV void mbar_arrive_remote_warp(uint32_t cluster_addr) {
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive_remote(cluster_addr);
+}
+
 // ------------------------------------------------------------ hand-off flags
 // A CTA that continues another CTA's partial result waits for that CTA's
 // flag (global int, 0 or 1): release / acquire at device scope.
@@ -153,20 +194,69 @@ DEV void tma_load_2d(uint32_t dst, const CUtensorMap *m, uint32_t bar, int x, in
         : "memory");
 }
 
+// Pair form: a CTA of a cluster pair loads into its own shared memory and
+// completes the bytes on barrier `cluster_bar` of either CTA of the pair
+// (mapa_shared address), so the pair's leader can wait for both CTAs' tiles
+// on one barrier armed with both CTAs' bytes.
+DEV void tma_load_2d_pair(uint32_t dst, const CUtensorMap *m, uint32_t cluster_bar, int x,
+                          int y) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes."
+        "cta_group::2 [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(m)), "r"(cluster_bar), "r"(x), "r"(y)
+        : "memory");
+}
+
+// Completion signal to another CTA of the cluster through the bulk-copy
+// engine: `bytes` (a multiple of 16) copied from this CTA's shared memory
+// `src` to `dst` in the other CTA (mapa_shared address), completing them on
+// that CTA's barrier `cluster_bar`.  The issuing thread does not wait for
+// it, unlike a remote mbarrier arrival; the copy follows the shared-memory
+// writes this thread (or its warp, after __syncwarp) fenced to the async
+// proxy before it.
+DEV void bulk_signal_remote(uint32_t dst, uint32_t src, uint32_t bytes, uint32_t cluster_bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, "
+        "[%3];" ::"r"(dst),
+        "r"(src), "r"(bytes), "r"(cluster_bar)
+        : "memory");
+}
+
 // ------------------------------------------------------------ tcgen05
+// G = 1: this CTA's tensor memory.  G = 2: the same columns in both CTAs of
+// a cluster pair, for MMAs issued with cta_group::2; one warp of each CTA of
+// the pair executes the allocation (and later the deallocation) together.
+// A kernel uses one value of G for all of its tcgen05 instructions.
+template <int G = 1>
 DEV void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                     dst_smem),
-                 "r"(ncols)
-                 : "memory");
+    if constexpr (G == 1)
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         dst_smem),
+                     "r"(ncols)
+                     : "memory");
+    else
+        asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         dst_smem),
+                     "r"(ncols)
+                     : "memory");
 }
+template <int G = 1>
 DEV void tmem_relinquish() {
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    if constexpr (G == 1)
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    else
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
 }
+template <int G = 1>
 DEV void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr),
-                 "r"(ncols)
-                 : "memory");
+    if constexpr (G == 1)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr),
+                     "r"(ncols)
+                     : "memory");
+    else
+        asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr),
+                     "r"(ncols)
+                     : "memory");
 }
 DEV void tc_fence_before() {
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
@@ -207,6 +297,30 @@ DEV void mma_commit(uint32_t bar) {
     asm volatile(
         "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
             bar)
+        : "memory");
+}
+
+// Pair form (cta_group::2), issued by one thread of the pair's leading CTA:
+// D (M = 256: rows 0..127 in the leader's tensor memory, 128..255 in the
+// peer's, same columns) (+)= A * B^T, where each CTA holds its 128 rows of A
+// and its half of B's N rows (the leader rows 0..N/2-1) at the same
+// shared-memory offsets the descriptors give.
+DEV void mma_bf16_ss_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                          uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+// Arrive once on barrier `bar` (same offset) in every CTA of `cta_mask` when
+// all pair MMAs issued so far by this thread have completed.
+DEV void mma_commit_pair_mc(uint32_t bar, uint16_t cta_mask) {
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster."
+        "b64 [%0], %1;" ::"r"(bar),
+        "h"(cta_mask)
         : "memory");
 }
 

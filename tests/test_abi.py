@@ -133,13 +133,14 @@ def split_region(ca, H, hd):
 def gemm_region(T, D, F, cm, ca, fs):
     """Bytes of the GEMMs' hand-off state: 128 KiB slots for the most CTAs
     that any of the plan's GEMM launches (K/V, Q, O, gate/up, down at full
-    and ragged chunk / slice sizes, in 256 x BN/2 or 128 x BN tiles) would
-    cut its last wave over on a 128..160-SM device, at most 64."""
+    and ragged chunk / slice sizes, in 128 x BN one-CTA tiles or 256 x BN
+    pair tiles, two slots per cut pair tile) would cut its last wave over on
+    a 128..160-SM device, at most 64."""
     from test_attention_schedule import grid
 
-    def units(M, N, two_b, r256):
-        bm = 256 if r256 else 128
-        bn = (128 if two_b else 256) // (2 if r256 else 1)
+    def units(M, N, two_b, pair):
+        bm = 256 if pair else 128
+        bn = 128 if two_b else 256
         return -(-M // bm) * -(-N // bn)
 
     slots = 0
@@ -147,9 +148,10 @@ def gemm_region(T, D, F, cm, ca, fs):
         nonlocal slots
         if M <= 0 or N <= 0 or K <= 0:
             return
-        for r256 in (False, True):
-            u = units(M, N, two_b, r256)
-            slots = max([slots] + [grid(u, K // 64, sm, 64)[1] for sm in range(128, 161)])
+        u = units(M, N, two_b, False)
+        slots = max([slots] + [grid(u, K // 64, sm, 64)[1] for sm in range(128, 161)])
+        u = units(M, N, two_b, True)
+        slots = max([slots] + [2 * grid(u, K // 64, w, 32)[1] for w in range(64, 81)])
     for M in (ca, T % ca):
         need(M, 2 * D, D, False)
         need(M, D, D, False)

@@ -3,10 +3,12 @@ into K ranges handed from CTA to CTA must not change a bit.
 
 Every epilogue (Q store with and without the Q/K transform, K/V store,
 gated residual, SwiGLU, the down projection with and without its carried
-accumulator) runs with bf16 and int8 weights (the int8 path in both of its
-tile shapes, with and without LoRA K-steps), once whole tiles only (dit_gemm)
+accumulator) runs with bf16 and int8 weights (in both tile shapes: without
+and with LoRA K-steps), once whole tiles only (dit_gemm)
 and twice with the split (dit_gemm_ex with a CTA cap that makes small cases
-cut tiles), on the same inputs; the outputs must be equal bit for bit.  The
+cut tiles), on the same inputs; the outputs must be equal bit for bit.
+Launches without LoRA run on cluster pairs of CTAs (256-row tiles), those
+with LoRA on one-CTA tiles.  The
 unsplit results are checked against the oracle in test_gpu_kernels.py and
 test_gpu_lora.py."""
 
@@ -25,9 +27,9 @@ def lib():
     return ds.load()
 
 
-def gemm_units(M, N, two_b, rows256):
-    bm = 256 if rows256 else 128
-    bn = (128 if two_b else 256) // (2 if rows256 else 1)
+def gemm_units(M, N, two_b, pair):
+    bm = 256 if pair else 128
+    bn = 128 if two_b else 256
     return -(-M // bm) * -(-N // bn)
 
 
@@ -101,7 +103,10 @@ class Case:
             args.lora_u0, args.lora_ldu0 = ds.ptr(u), lora
             args.lora_l0, args.lora_ldl0, args.lora_rank0 = ds.ptr(l), lora, lora
         self.args = args
-        self.tiles = gemm_units(M, N, two_b, int8 and not lora)
+        # launches without LoRA run on cluster pairs (256-row tiles, one
+        # worker per two CTAs, two hand-off slots per cut tile)
+        self.pair = not lora
+        self.tiles = gemm_units(M, N, two_b, self.pair)
         self.num_k = K // 64
 
     def run(self, split_ws=None, split_bytes=0, max_ctas=0):
@@ -124,18 +129,18 @@ class Case:
 
 CASES = [
     # (name, mode, M, N, K, int8, CTA cap, extra)
-    ("q_bf16", ds.EPI_STORE_BF16, 1000, 1024, 512, False, 7, {}),
-    ("q_int8", ds.EPI_STORE_BF16, 1000, 1024, 512, True, 7, {}),
-    ("q_qk_bf16", ds.EPI_STORE_BF16, 700, 768, 256, False, 5, {"qk": True}),
-    ("q_qk_int8", ds.EPI_STORE_BF16, 700, 768, 256, True, 5, {"qk": True}),
-    ("kv_bf16", ds.EPI_KV, 600, 1024, 512, False, 6, {}),
-    ("kv_qk_int8", ds.EPI_KV, 600, 1024, 512, True, 7, {"qk": True}),
-    ("resid_int8", ds.EPI_RESID, 900, 768, 1024, True, 5, {}),
-    ("swiglu_int8", ds.EPI_SWIGLU, 520, 640, 512, True, 7, {}),
-    ("swiglu_bf16", ds.EPI_SWIGLU, 520, 640, 512, False, 7, {}),
-    ("down_carry_int8", ds.EPI_DOWN, 700, 512, 1024, True, 5, {"acc_load": 1, "acc_final": 1}),
-    ("down_partial_bf16", ds.EPI_DOWN, 700, 512, 1024, False, 5, {"acc_load": 0, "acc_final": 0}),
-    ("down_mid_int8", ds.EPI_DOWN, 700, 512, 1024, True, 5, {"acc_load": 1, "acc_final": 0}),
+    ("q_bf16", ds.EPI_STORE_BF16, 1000, 1024, 512, False, 10, {}),
+    ("q_int8", ds.EPI_STORE_BF16, 1000, 1024, 512, True, 10, {}),
+    ("q_qk_bf16", ds.EPI_STORE_BF16, 700, 768, 256, False, 8, {"qk": True}),
+    ("q_qk_int8", ds.EPI_STORE_BF16, 700, 768, 256, True, 8, {"qk": True}),
+    ("kv_bf16", ds.EPI_KV, 600, 1024, 512, False, 10, {}),
+    ("kv_qk_int8", ds.EPI_KV, 600, 1024, 512, True, 10, {"qk": True}),
+    ("resid_int8", ds.EPI_RESID, 900, 768, 1024, True, 10, {}),
+    ("swiglu_int8", ds.EPI_SWIGLU, 520, 640, 512, True, 8, {}),
+    ("swiglu_bf16", ds.EPI_SWIGLU, 520, 640, 512, False, 8, {}),
+    ("down_carry_int8", ds.EPI_DOWN, 700, 512, 1024, True, 8, {"acc_load": 1, "acc_final": 1}),
+    ("down_partial_bf16", ds.EPI_DOWN, 700, 512, 1024, False, 10, {"acc_load": 0, "acc_final": 0}),
+    ("down_mid_int8", ds.EPI_DOWN, 700, 512, 1024, True, 8, {"acc_load": 1, "acc_final": 0}),
     ("q_lora_int8", ds.EPI_STORE_BF16, 600, 512, 512, True, 4, {"lora": 64}),
     ("swiglu_lora_bf16", ds.EPI_SWIGLU, 600, 512, 512, False, 6, {"lora": 64}),
     # the bench's launch sizes on every SM
@@ -148,7 +153,10 @@ CASES = [
 def test_split_gemm_is_bit_identical_to_unsplit(name, mode, M, N, K, int8, cap, extra):
     case = Case(mode, M, N, K, int8, seed=M + N + K, **extra)
     ctas = cap or torch.cuda.get_device_properties(0).multi_processor_count
-    _, n_split, _ = ds.attention_schedule(case.tiles, case.num_k, ctas, 64)
+    if case.pair:
+        _, n_split, _ = ds.attention_schedule(case.tiles, case.num_k, max(ctas // 2, 1), 32)
+    else:
+        _, n_split, _ = ds.attention_schedule(case.tiles, case.num_k, ctas, 64)
     assert n_split > 0, "the case must cut tiles"
     ref = case.run(max_ctas=cap)
     nbytes = ds.gemm_split_bytes(64)
