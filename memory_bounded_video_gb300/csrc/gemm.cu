@@ -119,39 +119,48 @@ struct Cfg {
     static constexpr int B_ROWS = P ? 128 : NB * BN;        // B rows staged per CTA
     static constexpr int B_BOX = P ? 128 : BN;              // rows of one B TMA box
     static constexpr int MMA_M = P ? 256 : kBM;
-    static constexpr int CONV_WARPS = 4;                   // int8 only
-    // int8: 12 warps, converters on warps 6, 7, 8 and 10 (sub-partitions 2, 3,
-    // 0, 2) and warps 9, 11 idle, so that the MMA-issuing warp 1 shares its
-    // sub-partition with no converter: measured 7-10 % faster than converters
-    // on warps 6..9, whose ALU stream slowed the MMA issue.
-    static constexpr int THREADS = I8 ? 384 : 192;
+    // Warps: 0 TMA producer, 1 MMA issuer (a pair's leader), 2 int8 B
+    // producer (int8 pair), 3 forwarder (int8 pair, second CTA), 4..7
+    // epilogue (TMEM lane quadrants 0..3), 8, 10, 11, 12, 14, 15 int8 -> bf16
+    // converters: two on each sub-partition but the MMA issuer's (1), whose
+    // single thread bounds the main loop; four converter warps took 640-700
+    // cycles per 8 KB stage, longer than a K-step of the MMAs.
+    static constexpr int CONV_WARPS = 6;                    // int8 only
+    static constexpr int THREADS = I8 ? 512 : 256;
     static constexpr int A_BYTES = A_ROWS * kBK * 2;
     static constexpr int BQ_BYTES = B_ROWS * kBK;          // int8 B staging
-    // TMA ring: bf16: A + B; int8: A + int8 B.
+    static constexpr int C_BYTES = B_ROWS * kBK * 2;       // one bf16 B tile
+    // QR (int8 pair): a ring of A tiles + converted B tiles, freed by one
+    // commit per K-step, and a separate ring of int8 B tiles freed by the
+    // converters as soon as they have read them, so the weights are fetched
+    // well ahead and their TMA latency is off the conversion's path (with A,
+    // int8 B and converted B in one stage the int8 pair ran at ~1000 cycles
+    // per K-step, 360 of them with the MMA issuer waiting for converted B).
+    static constexpr bool QR = P && I8;
+    // TMA ring: bf16: A + B; int8 one-CTA: A + int8 B; QR: A + converted B
+    // (the A tile completes on the converted-B barrier, so the MMA issuer
+    // waits once per K-step).
     static constexpr int STAGES = P ? (I8 ? 5 : 6) : 4;
-    static constexpr int STAGE_BYTES = A_BYTES + (I8 ? BQ_BYTES : B_ROWS * kBK * 2);
-    static constexpr int TMA_BYTES = STAGE_BYTES;
-    // int8 only: ring of converted bf16 B tiles read by the MMA, decoupled
-    // from the TMA ring (3 stages) so TMA latency and conversion overlap.
-    // Pair tiles keep it in lockstep with the TMA ring instead: one commit per
-    // K-step then frees both (a multicast commit costs the MMA-issuing thread
-    // about one bf16 K-step: with two per K-step the int8 pair ran at 524 ns
-    // per K-step against 272 for bf16), and a TMA stage that has landed again
-    // proves the converted stage of the same index free.
-    static constexpr bool LOCK = P && I8;
-    static constexpr int CSTAGES = I8 ? (LOCK ? STAGES : 3) : 0;
-    static constexpr int C_BYTES = B_ROWS * kBK * 2;
+    static constexpr int STAGE_BYTES = A_BYTES + (QR ? C_BYTES : I8 ? BQ_BYTES : C_BYTES);
+    static constexpr int TMA_BYTES = QR ? A_BYTES : STAGE_BYTES;
+    // int8 one-CTA: ring of converted bf16 B tiles read by the MMA (3 stages),
+    // decoupled from the TMA ring so TMA latency and conversion overlap.
+    static constexpr int CSTAGES = (I8 && !QR) ? 3 : 0;
+    static constexpr int QSTAGES = QR ? 7 : 0;               // int8 B ring (QR)
     static constexpr int OFF_C = STAGES * STAGE_BYTES;
+    static constexpr int OFF_Q = OFF_C + CSTAGES * C_BYTES;
     static constexpr int HALF_COLS = NB * BN;      // fp32 TMEM columns per M half
     static constexpr int ACC_COLS = MH * HALF_COLS;  // per accumulator buffer
     static constexpr int TMEM_COLS = 2 * ACC_COLS;
     static constexpr int OUT_COLS = BN;       // output columns per tile
     static constexpr int SLOT_FLOATS = MH * kBM * HALF_COLS;  // one CTA's accumulator
     // barriers (up to byte 384), TMEM slot, abort flag; this CTA's work list
-    // at byte 384
+    // at byte 384; completion-signal bytes at 448
     static constexpr int BAR_BYTES = 512;
-    static constexpr int SMEM_BYTES = OFF_C + CSTAGES * C_BYTES + BAR_BYTES + 1024;
-    static_assert(2 * STAGES + 24 <= 48 && CSTAGES <= 8, "barriers overlap the work list");
+    static constexpr int SMEM_BYTES = OFF_Q + QSTAGES * BQ_BYTES + BAR_BYTES + 1024;
+    static_assert(2 * STAGES + 32 <= 48 && CSTAGES <= 8 && QSTAGES <= 8,
+                  "barriers overlap the work list");
+    static_assert(SMEM_BYTES <= 232448, "shared memory");
 };
 
 // Output tile of persistent work index t.  Tiles go in groups of group_n
@@ -512,19 +521,21 @@ __global__ void __launch_bounds__(Cfg<MODE, I8, MH, P>::THREADS, 1)
     using C = Cfg<MODE, I8, MH, P>;
     constexpr int S = C::STAGES;
     constexpr int CS = C::CSTAGES;
+    constexpr int QS = C::QSTAGES;
+    constexpr bool QR = C::QR;
     constexpr int G = P ? 2 : 1;  // cta_group of every tcgen05 instruction here
     extern __shared__ uint8_t smem_raw[];
     uint8_t *tiles = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t *bars = reinterpret_cast<uint64_t *>(tiles + C::OFF_C + CS * C::C_BYTES);
-    // bars: full[S], empty[S], cfull[8], cempty[8], tfull[2], tempty[2], drain,
-    // handed (split accumulator written); then the TMEM slot and the abort
-    // flag; this CTA's work list at byte 384; 16 bytes per converter warp at
-    // byte 448 (int8 pair: completion-signal copies)
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * S + 22);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(tiles + C::OFF_Q + QS * C::BQ_BYTES);
+    // bars: full[S], empty[S], cfull[8], cempty[8] (QR: qfull), qempty[8],
+    // tfull[2], tempty[2], drain, handed (split accumulator written); then the
+    // TMEM slot and the abort flag; this CTA's work list at byte 384; 16
+    // bytes at byte 448 (QR: the completion-signal copy's source/target)
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * S + 30);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     AttnCta *cs_smem = reinterpret_cast<AttnCta *>(reinterpret_cast<uint8_t *>(bars) + 384);
-    const uint32_t sig0 = smem_u32(bars) + 448u;
+    const uint32_t sig = smem_u32(bars) + 448u;
     // work unit owner: the CTA, or the cluster pair; rank 0 of a pair issues
     // the MMAs for both
     const int cta = P ? int(cluster_id_x()) : int(blockIdx.x);
@@ -540,23 +551,32 @@ __global__ void __launch_bounds__(Cfg<MODE, I8, MH, P>::THREADS, 1)
     auto empty_bar = [&](int s) { return bar0 + 8u * (S + s); };
     auto cfull_bar = [&](int s) { return bar0 + 8u * (2 * S + s); };
     auto cempty_bar = [&](int s) { return bar0 + 8u * (2 * S + 8 + s); };
-    auto tfull_bar = [&](int b) { return bar0 + 8u * (2 * S + 16 + b); };
-    auto tempty_bar = [&](int b) { return bar0 + 8u * (2 * S + 18 + b); };
-    const uint32_t drain_bar = bar0 + 8u * (2 * S + 20);
-    const uint32_t handed_bar = bar0 + 8u * (2 * S + 21);
+    auto qfull_bar = [&](int s) { return bar0 + 8u * (2 * S + 8 + s); };  // QR only
+    auto qempty_bar = [&](int s) { return bar0 + 8u * (2 * S + 16 + s); };
+    auto tfull_bar = [&](int b) { return bar0 + 8u * (2 * S + 24 + b); };
+    auto tempty_bar = [&](int b) { return bar0 + 8u * (2 * S + 26 + b); };
+    const uint32_t drain_bar = bar0 + 8u * (2 * S + 28);
+    const uint32_t handed_bar = bar0 + 8u * (2 * S + 29);
     // the leader's copy of a barrier (pair: where the peer reports to)
     auto lead = [&](uint32_t bar) { return P ? mapa_shared(bar, 0) : bar; };
+    constexpr uint32_t kConvThreads = 32 * C::CONV_WARPS;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
             mbar_init(full_bar(s), 1);
             mbar_init(empty_bar(s), 1);
+            // QR: stage s ready: the A producer's arrival with the A tile's
+            // bytes, the converters' arrivals, and at the pair's leader the
+            // peer's 16-byte signal
+            if (QR) mbar_init(cfull_bar(s), kConvThreads + 1);
         }
-        // converters per thread (a pair's leader: plus 16 bytes of
-        // completion-signal copy per converter warp of the peer)
         for (int s = 0; s < CS; ++s) {
-            mbar_init(cfull_bar(s), 32 * C::CONV_WARPS);
+            mbar_init(cfull_bar(s), kConvThreads);
             mbar_init(cempty_bar(s), 1);
+        }
+        for (int s = 0; s < QS; ++s) {
+            mbar_init(qfull_bar(s), 1);
+            mbar_init(qempty_bar(s), kConvThreads);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(tfull_bar(b), 1);
@@ -586,6 +606,18 @@ __global__ void __launch_bounds__(Cfg<MODE, I8, MH, P>::THREADS, 1)
     __syncthreads();
     if constexpr (P) cluster_sync();  // both CTAs' barriers exist before any remote arrival
     tc_fence_after();
+    // int8 (512 threads, launched with 128 registers each): the epilogue
+    // warpgroup takes 168 from the producer / issuer warpgroup and the
+    // converters (112 + 168 + 2 x 112 per thread: 64,512 of the 65,536; the
+    // smallest split without spills)
+    if constexpr (I8) {
+        if (warp < 4)
+            asm volatile("setmaxnreg.dec.sync.aligned.u32 112;" ::: "memory");
+        else if (warp < 8)
+            asm volatile("setmaxnreg.inc.sync.aligned.u32 168;" ::: "memory");
+        else
+            asm volatile("setmaxnreg.dec.sync.aligned.u32 112;" ::: "memory");
+    }
     const uint32_t tmem = *tmem_slot;
     const WaitCtx wc{abort_flag, p.status};
     const bool preload = (MODE == DIT_EPI_DOWN || MODE == DIT_EPI_STORE_BF16) && p.acc_load;
@@ -593,6 +625,7 @@ __global__ void __launch_bounds__(Cfg<MODE, I8, MH, P>::THREADS, 1)
     if (warp == 0) {
         if (lane == 0) {
             // ---------------------------------------------- TMA producer
+            // (QR: A only; the int8 B tiles come from warp 2)
             int stage = 0;
             uint32_t ph = 0;
             int64_t issued = 0;
@@ -625,14 +658,16 @@ __global__ void __launch_bounds__(Cfg<MODE, I8, MH, P>::THREADS, 1)
                             tma_load_2d_pair(sB, tb, fb, kb * kBK, nb * C::BN + b_row0);
                         }
                     } else {
-                        mbar_arrive_expect_tx(full_bar(stage), C::TMA_BYTES);
-                    }
-                    if (!withhold && !(P && !I8)) {
-                        tma_load_2d(sA, &tmA, full_bar(stage), kb * kBK, a_row);
-                        tma_load_2d(sB, tb, full_bar(stage), kb * kBK, nb * C::BN + b_row0);
-                        if (!P && C::NB == 2)
-                            tma_load_2d(sB + C::B_BOX * kBK * (I8 ? 1 : 2), &tmB1,
-                                        full_bar(stage), kb * kBK, nb * C::BN);
+                        const uint32_t fb = QR ? cfull_bar(stage) : full_bar(stage);
+                        mbar_arrive_expect_tx(fb, C::TMA_BYTES);
+                        if (!withhold) {
+                            tma_load_2d(sA, &tmA, fb, kb * kBK, a_row);
+                            if (!QR)
+                                tma_load_2d(sB, tb, fb, kb * kBK, nb * C::BN + b_row0);
+                            if (!P && C::NB == 2)
+                                tma_load_2d(sB + C::B_BOX * kBK * (I8 ? 1 : 2), &tmB1, fb,
+                                            kb * kBK, nb * C::BN);
+                        }
                     }
                     ++issued;
                     if (++stage == S) {
@@ -668,8 +703,9 @@ __global__ void __launch_bounds__(Cfg<MODE, I8, MH, P>::THREADS, 1)
                 }
             }
             if (!ok) {  // let the copies already in flight land before exit
-                if (P && !I8 && !leader) {
-                    // they complete on the leader's barriers: give them time
+                if ((P && !I8 && !leader) || QR) {
+                    // they complete on the leader's barriers, or on barriers
+                    // that also wait for the converters: give them time
                     const uint64_t t0 = globaltimer();
                     while (globaltimer() - t0 < 200000ull) __nanosleep(1000);
                 } else {
@@ -717,11 +753,13 @@ __global__ void __launch_bounds__(Cfg<MODE, I8, MH, P>::THREADS, 1)
                 tc_fence_after();
                 const uint32_t d = tmem + uint32_t(buf * C::ACC_COLS);
                 for (int kb = it.k0; kb < it.k1; ++kb) {
-                    // the stage's tiles (bf16 pair: both CTAs'); int8: the
-                    // converted B (pair: both halves; the peer's arrives once
-                    // its stage has landed and been converted)
-                    if (!mbar_wait(full_bar(stage), ph, wc) ||
-                        (I8 && !mbar_wait(cfull_bar(cstage), cph, wc))) {
+                    // the stage's tiles (bf16 pair: both CTAs'); int8
+                    // one-CTA: and the converted B; int8 pair: one barrier
+                    // for this CTA's A tile and converted B and the peer's
+                    // signal that its stage is ready
+                    if ((QR && !mbar_wait(cfull_bar(stage), ph, wc)) ||
+                        (!QR && !mbar_wait(full_bar(stage), ph, wc)) ||
+                        (I8 && !QR && !mbar_wait(cfull_bar(cstage), cph, wc))) {
                         ok = false;
                         break;
                     }
@@ -731,8 +769,9 @@ __global__ void __launch_bounds__(Cfg<MODE, I8, MH, P>::THREADS, 1)
                     // 32 bytes = 2 in the address field) and the M halves (128
                     // rows = 16 KB); the field cannot overflow
                     const uint64_t da = da0 + uint64_t(stage * (C::STAGE_BYTES >> 4));
-                    const uint64_t db = I8 ? dc0 + uint64_t(cstage * (C::C_BYTES >> 4))
-                                           : da + uint64_t(C::A_BYTES >> 4);
+                    const uint64_t db = (I8 && !QR)
+                                            ? dc0 + uint64_t(cstage * (C::C_BYTES >> 4))
+                                            : da + uint64_t(C::A_BYTES >> 4);
                     const uint32_t accum0 = kb != it.k0 || carried;
 #pragma unroll
                     for (int k = 0; k < kBK / 16; ++k) {
@@ -752,8 +791,8 @@ __global__ void __launch_bounds__(Cfg<MODE, I8, MH, P>::THREADS, 1)
                         stage = 0;
                         ph ^= 1u;
                     }
-                    if (I8) {
-                        if (!C::LOCK) commit(cempty_bar(cstage));
+                    if (I8 && !QR) {
+                        commit(cempty_bar(cstage));
                         if (++cstage == CS) {
                             cstage = 0;
                             cph ^= 1u;
@@ -800,9 +839,67 @@ __global__ void __launch_bounds__(Cfg<MODE, I8, MH, P>::THREADS, 1)
                 mbar_wait_quiet(drain_bar, 0, kWaitLimitNs);
             }
         }
-    } else if (warp == 1) {
-        // (pair: the second CTA's warp 1 has nothing to do)
-    } else if (warp < 6) {
+    } else if (warp == 2 && QR) {
+        if (lane == 0) {
+            // ---------------------------------------------- int8 B producer (QR)
+            const CUtensorMap *tb = (C::NB == 2 && rank == 1) ? &tmB1 : &tmB0;
+            const int b_row0 = C::NB == 1 ? rank * C::B_BOX : 0;
+            int qs = 0;
+            uint32_t qph = 0;
+            int64_t issued = 0;
+            bool ok = true;
+            for (int idx = 0; idx < cs.count && ok; ++idx) {
+                const AttnItem it = attn_item(p.g, cs, cta, idx);
+                int mb, nb;
+                tile_of(p, it.u, mb, nb);
+                for (int kb = it.k0; kb < it.k1; ++kb) {
+                    if (!mbar_wait(qempty_bar(qs), qph ^ 1u, wc)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(qfull_bar(qs), C::BQ_BYTES);
+                    tma_load_2d(smem_u32(tiles + C::OFF_Q + qs * C::BQ_BYTES), tb, qfull_bar(qs),
+                                kb * kBK, nb * C::BN + b_row0);
+                    ++issued;
+                    if (++qs == QS) {
+                        qs = 0;
+                        qph ^= 1u;
+                    }
+                }
+            }
+            if (!ok) {
+                const int64_t first = issued > QS ? issued - QS : 0;
+                for (int64_t i = first; i < issued; ++i)
+                    mbar_wait_quiet(qfull_bar(int(i % QS)), uint32_t((i / QS) & 1), kWaitLimitNs);
+            }
+        }
+    } else if (warp == 3 && QR) {
+        if (!leader && lane == 0) {
+            // ---------------------------------------------- forwarder (QR)
+            // the pair's second CTA: once its converters have filled the B
+            // half of stage s and its A tile has landed there, send the leader
+            // a 16-byte copy that completes on the leader's converted-B
+            // barrier.  The bulk-copy engine carries it; the thread does not
+            // wait for it.
+            int stage = 0;
+            uint32_t ph = 0;
+            bool ok = true;
+            for (int idx = 0; idx < cs.count && ok; ++idx) {
+                const AttnItem it = attn_item(p.g, cs, cta, idx);
+                for (int kb = it.k0; kb < it.k1; ++kb) {
+                    if (!mbar_wait(cfull_bar(stage), ph, wc)) {
+                        ok = false;
+                        break;
+                    }
+                    bulk_signal_remote(lead(sig), sig, 16u, lead(cfull_bar(stage)));
+                    if (++stage == S) {
+                        stage = 0;
+                        ph ^= 1u;
+                    }
+                }
+            }
+        }
+    } else if (warp >= 4 && warp < 8) {
         // -------------------------------------------------- epilogue
         const int q = warp & 3;  // TMEM lane quadrant this warp may access
         const uint32_t lane_base = tmem + (uint32_t(q * 32) << 16);
@@ -862,7 +959,7 @@ __global__ void __launch_bounds__(Cfg<MODE, I8, MH, P>::THREADS, 1)
                                                          mh * kBM + q * 32 + lane);
                 __threadfence();
                 mbar_arrive_warp(handed_bar);
-                if (warp == 2 && lane == 0) {
+                if (warp == 4 && lane == 0) {
                     if (!mbar_wait(handed_bar, 0u, wc)) {
                         ok = false;
                     } else {
@@ -882,75 +979,91 @@ __global__ void __launch_bounds__(Cfg<MODE, I8, MH, P>::THREADS, 1)
             }
             if (ok && idx + 2 < cs.count) ok = prepare(idx + 2);
         }
-    } else if (I8 && warp != 9 && warp != 11) {
+    } else if (I8 && warp >= 8 && (warp & 3) != 1) {
         // -------------------------------------------------- int8 -> bf16
         // Staged int8 rows (64 bytes each, B_ROWS rows) become 128-byte bf16
-        // rows of a converted-B stage; 16-byte chunk c of row r lands at
-        // chunk c ^ (r % 8) of the row (the 128-byte swizzle), rows in 8-row
-        // groups of 1024 bytes.
-        const int tid = (warp == 10 ? 3 : warp - 6) * 32 + lane;
-        int stage = 0, cstage = 0;
-        uint32_t ph = 0, cph = 0;
+        // rows of a converted-B tile; 16-byte chunk c of row r lands at chunk
+        // c ^ (r % 8) of the row (the 128-byte swizzle), rows in 8-row groups
+        // of 1024 bytes.  One-CTA tiles: from the TMA stage into the
+        // converted-B ring; QR: from the int8 ring into the B half of the
+        // A + B stage, once the MMAs that read that stage's last use are done.
+        const int tid = ((warp - 8) - (warp > 9) - (warp > 13)) * 32 + lane;
+        int stage = 0, cstage = 0, qs = 0;
+        uint32_t ph = 0, cph = 0, qph = 0;
         bool ok = true;
         for (int idx = 0; ok && idx < cs.count; ++idx) {
             const AttnItem it = attn_item(p.g, cs, cta, idx);
             for (int kb = it.k0; kb < it.k1; ++kb) {
-                bool w = mbar_wait(full_bar(stage), ph, wc) &&
-                         (C::LOCK || mbar_wait(cempty_bar(cstage), cph ^ 1u, wc));
+                bool w;
+                if constexpr (QR)
+                    w = mbar_wait(qfull_bar(qs), qph, wc) &&
+                        mbar_wait(empty_bar(stage), ph ^ 1u, wc);
+                else
+                    w = mbar_wait(full_bar(stage), ph, wc) &&
+                        mbar_wait(cempty_bar(cstage), cph ^ 1u, wc);
                 w = __all_sync(0xffffffffu, w);
                 if (!w) {
                     ok = false;
                     break;
                 }
-                const uint8_t *sq = tiles + stage * C::STAGE_BYTES + C::A_BYTES;
-                uint8_t *dst0 = tiles + C::OFF_C + cstage * C::C_BYTES;
-                // Thread tid owns pieces tid + kConv * i (8 int8 each): row
-                // r = tid / 8 + (kConv / 8) i, chunk c = tid % 8, and r % 8 is
-                // the same for all of them.  Loads are batched ahead of the
-                // conversions so their latency overlaps.
-                constexpr int kConv = 32 * C::CONV_WARPS;
-                constexpr int kPieces = C::B_ROWS * 8 / kConv;
-                constexpr int kBatch = kPieces < 8 ? kPieces : 8;
-                const uint8_t *src = sq + (tid >> 3) * kBK + (tid & 7) * 8;
-                uint8_t *dst = dst0 + (tid >> 3) * 128 + (((tid & 7) ^ ((tid >> 3) & 7)) << 4);
+                const uint8_t *sq = QR ? tiles + C::OFF_Q + qs * C::BQ_BYTES
+                                       : tiles + stage * C::STAGE_BYTES + C::A_BYTES;
+                uint8_t *dst0 = QR ? tiles + stage * C::STAGE_BYTES + C::A_BYTES
+                                   : tiles + C::OFF_C + cstage * C::C_BYTES;
+                // Thread tid owns pieces of 8 int8: rows r = tid / 8 + kStep i
+                // (kStep = 24, a multiple of 8, so r % 8 is the same for all
+                // of them; the last piece is ragged), chunk c = tid % 8.
+                // Loads are batched ahead of the conversions so their latency
+                // overlaps.
+                constexpr int kStep = int(kConvThreads) / 8;
+                static_assert(kStep % 8 == 0, "rows of one thread share the swizzle phase");
+                constexpr int kPieces = (C::B_ROWS + kStep - 1) / kStep;
+                constexpr int kBatch = kPieces < 6 ? kPieces : 6;
+                const int r0 = tid >> 3;
+                const uint8_t *src = sq + r0 * kBK + (tid & 7) * 8;
+                uint8_t *dst = dst0 + r0 * 128 + (((tid & 7) ^ (r0 & 7)) << 4);
 #pragma unroll
                 for (int i0 = 0; i0 < kPieces; i0 += kBatch) {
                     uint2 w8[kBatch];
 #pragma unroll
-                    for (int i = 0; i < kBatch; ++i)
-                        w8[i] = *reinterpret_cast<const uint2 *>(src + (i0 + i) * (kConv / 8) * kBK);
+                    for (int i = 0; i < kBatch; ++i) {
+                        const bool in = i0 + i < kPieces && r0 + (i0 + i) * kStep < C::B_ROWS;
+                        w8[i] = in ? *reinterpret_cast<const uint2 *>(src + (i0 + i) * kStep * kBK)
+                                   : make_uint2(0u, 0u);
+                    }
 #pragma unroll
-                    for (int i = 0; i < kBatch; ++i)
-                        *reinterpret_cast<uint4 *>(dst + (i0 + i) * (kConv / 8) * 128) =
-                            int8x8_to_bf16x8(w8[i]);
+                    for (int i = 0; i < kBatch; ++i) {
+                        const bool in = i0 + i < kPieces && r0 + (i0 + i) * kStep < C::B_ROWS;
+                        if (in)
+                            *reinterpret_cast<uint4 *>(dst + (i0 + i) * kStep * 128) =
+                                int8x8_to_bf16x8(w8[i]);
+                    }
                 }
                 fence_proxy_async_smem();  // the tensor core reads what we wrote
                 // every converter thread arrives as soon as its own stores are
                 // fenced (one arrival per warp after __syncwarp measured 3-5 %
-                // slower int8 launches).  A pair's second CTA signals the
-                // leader instead, one 16-byte copy per warp completing on the
-                // leader's barrier (it also says this CTA's A tile landed):
-                // with a remote mbarrier arrival per K-step, which keeps the
-                // issuing thread waiting several hundred ns, the int8 pair
-                // ran at 480-520 ns per K-step
-                if (!P) {
-                    mbar_arrive(cfull_bar(cstage));
-                } else if (!leader) {
-                    __syncwarp();
-                    const uint32_t sig = sig0 + 16u * uint32_t(tid >> 5);
-                    if (lane == 0) bulk_signal_remote(lead(sig), sig, 16u, lead(cfull_bar(cstage)));
-                } else if (tid == 0) {
-                    mbar_arrive_expect_tx(cfull_bar(cstage), 16u * C::CONV_WARPS);
+                // slower); QR: the int8 tile is free again, and the leader's
+                // thread 0 also arms the peer's 16-byte signal
+                if constexpr (QR) {
+                    mbar_arrive(qempty_bar(qs));
+                    if (leader && tid == 0)
+                        mbar_arrive_expect_tx(cfull_bar(stage), 16u);
+                    else
+                        mbar_arrive(cfull_bar(stage));
+                    if (++qs == QS) {
+                        qs = 0;
+                        qph ^= 1u;
+                    }
                 } else {
                     mbar_arrive(cfull_bar(cstage));
+                    if (++cstage == CS) {
+                        cstage = 0;
+                        cph ^= 1u;
+                    }
                 }
                 if (++stage == S) {
                     stage = 0;
                     ph ^= 1u;
-                }
-                if (++cstage == CS) {
-                    cstage = 0;
-                    cph ^= 1u;
                 }
             }
             // the tile's LoRA stages hold bf16 tiles the MMA reads directly
