@@ -143,12 +143,22 @@ struct Cfg {
     static constexpr int STAGES = P ? (I8 ? 5 : 6) : 4;
     static constexpr int STAGE_BYTES = A_BYTES + (QR ? C_BYTES : I8 ? BQ_BYTES : C_BYTES);
     static constexpr int TMA_BYTES = QR ? A_BYTES : STAGE_BYTES;
+    // fp32 epilogues (gated residual, down projection, fp32 store) move each
+    // warp's 32 x 32 blocks through a padded shared-memory tile so that
+    // every global access of a warp is one contiguous 128-byte row segment
+    // (with one row per lane each access touched 32 lines, and the residual
+    // epilogue took longer than the tile's main loop); the rings give up a
+    // stage for it.
+    static constexpr bool EPI_T =
+        MODE == DIT_EPI_RESID || MODE == DIT_EPI_DOWN || MODE == DIT_EPI_STORE_F32;
+    static constexpr int T_BYTES = EPI_T ? 4 * 32 * 36 * 4 : 0;
     // int8 one-CTA: ring of converted bf16 B tiles read by the MMA (3 stages),
     // decoupled from the TMA ring so TMA latency and conversion overlap.
-    static constexpr int CSTAGES = (I8 && !QR) ? 3 : 0;
-    static constexpr int QSTAGES = QR ? 7 : 0;               // int8 B ring (QR)
+    static constexpr int CSTAGES = (I8 && !QR) ? (EPI_T ? 2 : 3) : 0;
+    static constexpr int QSTAGES = QR ? (EPI_T ? 5 : 7) : 0;  // int8 B ring (QR)
     static constexpr int OFF_C = STAGES * STAGE_BYTES;
     static constexpr int OFF_Q = OFF_C + CSTAGES * C_BYTES;
+    static constexpr int OFF_T = OFF_Q + QSTAGES * BQ_BYTES;
     static constexpr int HALF_COLS = NB * BN;      // fp32 TMEM columns per M half
     static constexpr int ACC_COLS = MH * HALF_COLS;  // per accumulator buffer
     static constexpr int TMEM_COLS = 2 * ACC_COLS;
@@ -157,7 +167,7 @@ struct Cfg {
     // barriers (up to byte 384), TMEM slot, abort flag; this CTA's work list
     // at byte 384; completion-signal bytes at 448
     static constexpr int BAR_BYTES = 512;
-    static constexpr int SMEM_BYTES = OFF_Q + QSTAGES * BQ_BYTES + BAR_BYTES + 1024;
+    static constexpr int SMEM_BYTES = OFF_T + T_BYTES + BAR_BYTES + 1024;
     static_assert(2 * STAGES + 32 <= 48 && CSTAGES <= 8 && QSTAGES <= 8,
                   "barriers overlap the work list");
     static_assert(SMEM_BYTES <= 232448, "shared memory");
@@ -369,9 +379,107 @@ DEV void epilogue_qk_tile(const GemmParams &p, uint32_t taddr, int64_t m, int nb
     }
 }
 
+// fp32 epilogues (gated residual, down projection, fp32 store) of a warp's
+// 32 rows m0.. through its shared-memory tile T (32 rows of 36 floats): per
+// 32 columns each lane writes its accumulator row into T as float4s, then
+// each group of 8 lanes reads one row back (lane & 7 picks the 16-byte
+// piece), so one warp access moves four whole 128-byte row segments instead
+// of touching 32 rows.  The row stride of 36 floats keeps both the writes
+// and the reads free of bank conflicts.  The arithmetic per element is the
+// row path's: scale, then one fused multiply-add onto x (or a plain store).
+constexpr int kEpiLd = 36;  // floats per row of an epilogue tile
 template <int MODE, bool I8, int MH>
-DEV void epilogue_tile(const GemmParams &p, uint32_t taddr, int64_t m, int nb) {
+DEV void epilogue_tile_f32(const GemmParams &p, uint32_t taddr, int64_t m0, int nb, float *T) {
     using C = Cfg<MODE, I8, MH>;
+    const int lane = lane_id();
+    const int64_t left = p.M - m0;
+    const int rows = left < 32 ? int(left) : 32;  // <= 0: no row of this warp
+    const bool scaled = (I8 || p.bscale) && !(MODE == DIT_EPI_DOWN && !p.acc_final);
+    const bool resid = MODE == DIT_EPI_RESID || (MODE == DIT_EPI_DOWN && p.acc_final);
+    const int sub = lane >> 3;       // row within a group of four
+    const int c4 = (lane & 7) * 4;   // this lane's four columns
+    float4 *tw = reinterpret_cast<float4 *>(T + lane * kEpiLd);
+#pragma unroll 1
+    for (int c0 = 0; c0 < C::OUT_COLS; c0 += 32) {
+        __syncwarp();
+        uint32_t r[32];
+        tmem_ld32(taddr + c0, r);
+        tmem_ld_wait(r);
+        const int n = nb * C::BN + c0;  // warp-uniform; N is a multiple of 32
+        if (rows <= 0 || n >= p.N) continue;
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            tw[i] = make_float4(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]),
+                                __uint_as_float(r[4 * i + 2]), __uint_as_float(r[4 * i + 3]));
+        __syncwarp();
+        const float4 s = scaled ? __ldg(reinterpret_cast<const float4 *>(p.s0 + n + c4))
+                                : make_float4(1.f, 1.f, 1.f, 1.f);
+        const float4 g = resid ? __ldg(reinterpret_cast<const float4 *>(p.gate + n + c4))
+                               : make_float4(0.f, 0.f, 0.f, 0.f);
+        float *base;
+        int64_t ld;
+        if (resid) {
+            base = p.x + m0 * p.ldx + n + c4;
+            ld = p.ldx;
+        } else if (MODE == DIT_EPI_DOWN) {
+            base = p.acc + m0 * p.ldacc + n + c4;
+            ld = p.ldacc;
+        } else {
+            base = reinterpret_cast<float *>(p.out) + m0 * p.ldo + n + c4;
+            ld = p.ldo;
+        }
+        if (resid) {
+            float4 xv[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const int i = 4 * k + sub;
+                if (i < rows) xv[k] = *reinterpret_cast<const float4 *>(base + int64_t(i) * ld);
+            }
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const int i = 4 * k + sub;
+                if (i < rows) {
+                    float4 v = *reinterpret_cast<const float4 *>(T + i * kEpiLd + c4);
+                    if (scaled) {
+                        v.x *= s.x;
+                        v.y *= s.y;
+                        v.z *= s.z;
+                        v.w *= s.w;
+                    }
+                    float4 a = xv[k];
+                    a.x = __fmaf_rn(g.x, v.x, a.x);
+                    a.y = __fmaf_rn(g.y, v.y, a.y);
+                    a.z = __fmaf_rn(g.z, v.z, a.z);
+                    a.w = __fmaf_rn(g.w, v.w, a.w);
+                    *reinterpret_cast<float4 *>(base + int64_t(i) * ld) = a;
+                }
+            }
+        } else {
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const int i = 4 * k + sub;
+                if (i < rows) {
+                    float4 v = *reinterpret_cast<const float4 *>(T + i * kEpiLd + c4);
+                    if (scaled) {
+                        v.x *= s.x;
+                        v.y *= s.y;
+                        v.z *= s.z;
+                        v.w *= s.w;
+                    }
+                    *reinterpret_cast<float4 *>(base + int64_t(i) * ld) = v;
+                }
+            }
+        }
+    }
+}
+
+template <int MODE, bool I8, int MH>
+DEV void epilogue_tile(const GemmParams &p, uint32_t taddr, int64_t m, int nb, float *T) {
+    using C = Cfg<MODE, I8, MH>;
+    if constexpr (C::EPI_T) {
+        epilogue_tile_f32<MODE, I8, MH>(p, taddr, m - lane_id(), nb, T);
+        return;
+    }
     if constexpr (MODE == DIT_EPI_STORE_BF16 || MODE == DIT_EPI_KV) {
         if (p.qk) {
             epilogue_qk_tile<MODE, I8, MH>(p, taddr, m, nb);
@@ -527,7 +635,7 @@ __global__ void __launch_bounds__(Cfg<MODE, I8, MH, P>::THREADS, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t *tiles = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t *bars = reinterpret_cast<uint64_t *>(tiles + C::OFF_Q + QS * C::BQ_BYTES);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(tiles + C::OFF_T + C::T_BYTES);
     // bars: full[S], empty[S], cfull[8], cempty[8] (QR: qfull), qempty[8],
     // tfull[2], tempty[2], drain, handed (split accumulator written); then the
     // TMEM slot and the abort flag; this CTA's work list at byte 384; 16
@@ -905,6 +1013,8 @@ __global__ void __launch_bounds__(Cfg<MODE, I8, MH, P>::THREADS, 1)
         const uint32_t lane_base = tmem + (uint32_t(q * 32) << 16);
         // hand-off flags and slots: one per CTA of a pair
         auto hslot = [&](int i) { return P ? 2 * i + rank : i; };
+        // this warp's fp32 epilogue tile (32 rows of 36 floats)
+        float *epi_t = reinterpret_cast<float *>(tiles + C::OFF_T) + q * (32 * 36);
         // Buffer j % 2 ready for item j: drained (this warp's epilogue of item
         // j - 2 is done, by program order) and, if the item starts from a
         // carry, holding it: the CTA before's raw accumulator at K-step k0
@@ -975,7 +1085,8 @@ __global__ void __launch_bounds__(Cfg<MODE, I8, MH, P>::THREADS, 1)
                 for (int mh = 0; mh < MH; ++mh)
                     epilogue_tile<MODE, I8, MH>(
                         p, base + uint32_t(mh * C::HALF_COLS),
-                        int64_t(mb) * C::BM + rank * C::A_ROWS + mh * kBM + q * 32 + lane, nb);
+                        int64_t(mb) * C::BM + rank * C::A_ROWS + mh * kBM + q * 32 + lane, nb,
+                        epi_t);
             }
             if (ok && idx + 2 < cs.count) ok = prepare(idx + 2);
         }
