@@ -238,7 +238,11 @@ DIT_API dit_status_t dit_block_bind_weight_scratch(dit_plan_t *plan, void *dev_p
  * 16-byte aligned).  modulation: device float [6, D].  Asynchronous on
  * `stream`; returns the launch-time status.  Device-side errors are read by
  * dit_block_sync_status().  Errors: DIT_ERR_INVALID_ARG, DIT_ERR_ALIGN,
- * DIT_ERR_NO_WORKSPACE, DIT_ERR_CUDA. */
+ * DIT_ERR_NO_WORKSPACE, DIT_ERR_CUDA.
+ * The GEMMs cut their last wave of output tiles into K ranges in a
+ * cooperative launch; with the environment variable DITSTREAM_GEMM_SPLIT=0
+ * (read once per process) they run whole tiles only, with the same output
+ * bits, for tools that cannot launch cooperative cluster grids. */
 DIT_API dit_status_t dit_block_forward(const dit_plan_t *plan, float *x,
                                const dit_block_weights_t *w,
                                const float *modulation, dit_stream_t stream);

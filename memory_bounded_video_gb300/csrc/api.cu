@@ -19,6 +19,7 @@
 // query attends to the pre-attention keys and values of all tokens.
 #include <cstdint>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <new>
 #include <vector>
@@ -102,6 +103,19 @@ bool make_tmap_2d(CUtensorMap *m, CUtensorMapDataType dt, const void *base, uint
                                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
+}
+
+// Whether the block's GEMMs may cut their last wave into K ranges (the work
+// split, a cooperative launch).  DITSTREAM_GEMM_SPLIT=0 in the environment
+// turns it off for the process: every GEMM then runs whole tiles, with the
+// same result bits.  This is for tools that cannot launch a cooperative grid
+// of thread-block clusters (Nsight Compute reports such a launch as failed).
+bool gemm_split_on() {
+    static const bool on = [] {
+        const char *v = std::getenv("DITSTREAM_GEMM_SPLIT");
+        return !(v && std::strcmp(v, "0") == 0);
+    }();
+    return on;
 }
 
 // Launch `fn` (returning a dit_status_t) bracketed by profiling events when
@@ -538,7 +552,8 @@ dit_status_t dit_block_forward_ex(const dit_plan_t *cp, float *x, const dit_bloc
     // the GEMMs' hand-off space for split tiles (flags shared with the
     // attention's: every launch leaves the flags it used zero)
     const AttnSplit gsplit{reinterpret_cast<int *>(p->ws + kFlagsOffset),
-                           reinterpret_cast<float *>(p->ws + p->off_gsplit), p->gsplit_slots, 0};
+                           reinterpret_cast<float *>(p->ws + p->off_gsplit),
+                           gemm_split_on() ? p->gsplit_slots : 0, 0};
     // K [T, D] and V^T [D, T_pad]: in the workspace, or (offload) in the
     // host buffer, written there by pass one through its device mapping
     void *K = p->kvb ? static_cast<void *>(p->kv_host) : static_cast<void *>(p->ws + p->off_k);

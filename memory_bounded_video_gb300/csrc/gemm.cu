@@ -126,6 +126,11 @@ struct Cfg {
     // single thread bounds the main loop; four converter warps took 640-700
     // cycles per 8 KB stage, longer than a K-step of the MMAs.
     static constexpr int CONV_WARPS = 6;                    // int8 only
+    // QR: the converter warps work in groups of two, group g converting the
+    // CTA's K-steps j with j % 3 == g, so three stages are converted at once
+    // and each group's per-stage latency (wait, loads, stores, proxy fence,
+    // arrival) overlaps the others'.
+    static constexpr int CONV_GROUPS = (P && I8) ? 3 : 1;
     static constexpr int THREADS = I8 ? 512 : 256;
     static constexpr int A_BYTES = A_ROWS * kBK * 2;
     static constexpr int BQ_BYTES = B_ROWS * kBK;          // int8 B staging
@@ -170,6 +175,12 @@ struct Cfg {
     static constexpr int SMEM_BYTES = OFF_T + T_BYTES + BAR_BYTES + 1024;
     static_assert(2 * STAGES + 32 <= 48 && CSTAGES <= 8 && QSTAGES <= 8,
                   "barriers overlap the work list");
+    // A converter group's K-steps are CONV_GROUPS apart; its wait for a ring
+    // slot's previous use to be freed is only unambiguous (mbarrier phase
+    // parity) while that use is at most one ring cycle back, which needs
+    // CONV_GROUPS <= the ring depths.
+    static_assert(!QR || (CONV_GROUPS <= STAGES && CONV_GROUPS <= QSTAGES),
+                  "converter groups outrun the rings");
     static_assert(SMEM_BYTES <= 232448, "shared memory");
 };
 
@@ -668,6 +679,7 @@ __global__ void __launch_bounds__(Cfg<MODE, I8, MH, P>::THREADS, 1)
     // the leader's copy of a barrier (pair: where the peer reports to)
     auto lead = [&](uint32_t bar) { return P ? mapa_shared(bar, 0) : bar; };
     constexpr uint32_t kConvThreads = 32 * C::CONV_WARPS;
+    constexpr uint32_t kGroupThreads = kConvThreads / C::CONV_GROUPS;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
@@ -676,15 +688,15 @@ __global__ void __launch_bounds__(Cfg<MODE, I8, MH, P>::THREADS, 1)
             // QR: stage s ready: the A producer's arrival with the A tile's
             // bytes, the converters' arrivals, and at the pair's leader the
             // peer's 16-byte signal
-            if (QR) mbar_init(cfull_bar(s), kConvThreads + 1);
+            if (QR) mbar_init(cfull_bar(s), kGroupThreads + 1);
         }
         for (int s = 0; s < CS; ++s) {
-            mbar_init(cfull_bar(s), kConvThreads);
+            mbar_init(cfull_bar(s), kGroupThreads);
             mbar_init(cempty_bar(s), 1);
         }
         for (int s = 0; s < QS; ++s) {
             mbar_init(qfull_bar(s), 1);
-            mbar_init(qempty_bar(s), kConvThreads);
+            mbar_init(qempty_bar(s), kGroupThreads);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(tfull_bar(b), 1);
@@ -1098,13 +1110,18 @@ __global__ void __launch_bounds__(Cfg<MODE, I8, MH, P>::THREADS, 1)
         // of 1024 bytes.  One-CTA tiles: from the TMA stage into the
         // converted-B ring; QR: from the int8 ring into the B half of the
         // A + B stage, once the MMAs that read that stage's last use are done.
-        const int tid = ((warp - 8) - (warp > 9) - (warp > 13)) * 32 + lane;
-        int stage = 0, cstage = 0, qs = 0;
+        const int tid_all = ((warp - 8) - (warp > 9) - (warp > 13)) * 32 + lane;
+        const int grp = tid_all / int(kGroupThreads);
+        const int tid = tid_all % int(kGroupThreads);
+        int stage = 0, cstage = 0, qs = 0, turn = 0;
         uint32_t ph = 0, cph = 0, qph = 0;
         bool ok = true;
         for (int idx = 0; ok && idx < cs.count; ++idx) {
             const AttnItem it = attn_item(p.g, cs, cta, idx);
             for (int kb = it.k0; kb < it.k1; ++kb) {
+              const bool mine = turn == grp;
+              if (++turn == C::CONV_GROUPS) turn = 0;
+              if (mine) {
                 bool w;
                 if constexpr (QR)
                     w = mbar_wait(qfull_bar(qs), qph, wc) &&
@@ -1122,17 +1139,21 @@ __global__ void __launch_bounds__(Cfg<MODE, I8, MH, P>::THREADS, 1)
                 uint8_t *dst0 = QR ? tiles + stage * C::STAGE_BYTES + C::A_BYTES
                                    : tiles + C::OFF_C + cstage * C::C_BYTES;
                 // Thread tid owns pieces of 8 int8: rows r = tid / 8 + kStep i
-                // (kStep = 24, a multiple of 8, so r % 8 is the same for all
-                // of them; the last piece is ragged), chunk c = tid % 8.
-                // Loads are batched ahead of the conversions so their latency
-                // overlaps.
-                constexpr int kStep = int(kConvThreads) / 8;
-                static_assert(kStep % 8 == 0, "rows of one thread share the swizzle phase");
+                // (kStep = the group's threads / 8; the last piece is ragged),
+                // chunk c = tid % 8.  Loads are batched ahead of the
+                // conversions so their latency overlaps.
+                constexpr int kStep = int(kGroupThreads) / 8;
                 constexpr int kPieces = (C::B_ROWS + kStep - 1) / kStep;
                 constexpr int kBatch = kPieces < 6 ? kPieces : 6;
-                const int r0 = tid >> 3;
-                const uint8_t *src = sq + r0 * kBK + (tid & 7) * 8;
-                uint8_t *dst = dst0 + r0 * 128 + (((tid & 7) ^ (r0 & 7)) << 4);
+                const int r0 = tid >> 3, c8 = tid & 7;
+                const uint8_t *src = sq + r0 * kBK + c8 * 8;
+                // row r's chunk c lands at chunk c ^ (r % 8): with kStep a
+                // multiple of 8 that is the same chunk for every piece
+                auto dst_of = [&](int i) -> uint8_t * {
+                    const int r = r0 + i * kStep;
+                    const int sw = (kStep % 8 == 0) ? (r0 & 7) : (r & 7);
+                    return dst0 + r * 128 + ((c8 ^ sw) << 4);
+                };
 #pragma unroll
                 for (int i0 = 0; i0 < kPieces; i0 += kBatch) {
                     uint2 w8[kBatch];
@@ -1145,9 +1166,7 @@ __global__ void __launch_bounds__(Cfg<MODE, I8, MH, P>::THREADS, 1)
 #pragma unroll
                     for (int i = 0; i < kBatch; ++i) {
                         const bool in = i0 + i < kPieces && r0 + (i0 + i) * kStep < C::B_ROWS;
-                        if (in)
-                            *reinterpret_cast<uint4 *>(dst + (i0 + i) * kStep * 128) =
-                                int8x8_to_bf16x8(w8[i]);
+                        if (in) *reinterpret_cast<uint4 *>(dst_of(i0 + i)) = int8x8_to_bf16x8(w8[i]);
                     }
                 }
                 fence_proxy_async_smem();  // the tensor core reads what we wrote
@@ -1161,12 +1180,16 @@ __global__ void __launch_bounds__(Cfg<MODE, I8, MH, P>::THREADS, 1)
                         mbar_arrive_expect_tx(cfull_bar(stage), 16u);
                     else
                         mbar_arrive(cfull_bar(stage));
+                } else {
+                    mbar_arrive(cfull_bar(cstage));
+                }
+              }
+                if constexpr (QR) {
                     if (++qs == QS) {
                         qs = 0;
                         qph ^= 1u;
                     }
                 } else {
-                    mbar_arrive(cfull_bar(cstage));
                     if (++cstage == CS) {
                         cstage = 0;
                         cph ^= 1u;

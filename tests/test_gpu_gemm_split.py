@@ -188,3 +188,36 @@ def test_unsplit_cta_cap_does_not_change_the_result():
     outs = [case.run(max_ctas=c)["x"] for c in (0, 1, 7)]
     for o in outs[1:]:
         assert torch.equal(outs[0].view(torch.int32), o.view(torch.int32))
+
+
+CHILD = """
+import sys, torch
+sys.path.insert(0, {root!r})
+from memory_bounded_video_gb300 import runner, synth
+inp = synth.make_inputs(8192, 1024, 16, 2816, seed=11, int8=True, jitter=True)
+dev = runner.upload(inp)
+stack = runner.DitStack(8192, 1024, 16, 2816, 2048, 2048)
+x = dev.x.clone()
+stack.forward(x, dev)
+stack.check()
+torch.save(x.cpu(), {out!r})
+"""
+
+
+def test_block_without_gemm_split_gives_the_same_bits(tmp_path):
+    """DITSTREAM_GEMM_SPLIT=0 (read once per process) makes every GEMM of the
+    block run whole tiles without a cooperative launch; the block's output
+    must keep its bits.  Both runs happen in child processes so that each
+    reads the variable afresh."""
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    outs = []
+    for flag in ("1", "0"):
+        out = str(tmp_path / f"x_{flag}.pt")
+        env = dict(os.environ, DITSTREAM_GEMM_SPLIT=flag)
+        subprocess.run([sys.executable, "-c", CHILD.format(root=root, out=out)],
+                       env=env, check=True, timeout=600)
+        outs.append(torch.load(out))
+    assert torch.equal(outs[0].view(torch.int32), outs[1].view(torch.int32))
