@@ -121,16 +121,20 @@ struct Cfg {
     static constexpr int MMA_M = P ? 256 : kBM;
     // Warps: 0 TMA producer, 1 MMA issuer (a pair's leader), 2 int8 B
     // producer (int8 pair), 3 forwarder (int8 pair, second CTA), 4..7
-    // epilogue (TMEM lane quadrants 0..3), 8, 10, 11, 12, 14, 15 int8 -> bf16
-    // converters: two on each sub-partition but the MMA issuer's (1), whose
-    // single thread bounds the main loop; four converter warps took 640-700
-    // cycles per 8 KB stage, longer than a K-step of the MMAs.
-    static constexpr int CONV_WARPS = 6;                    // int8 only
-    // QR: the converter warps work in groups of two, group g converting the
-    // CTA's K-steps j with j % 3 == g, so three stages are converted at once
-    // and each group's per-stage latency (wait, loads, stores, proxy fence,
-    // arrival) overlaps the others'.
-    static constexpr int CONV_GROUPS = (P && I8) ? 3 : 1;
+    // epilogue (TMEM lane quadrants 0..3), then the int8 -> bf16 converters.
+    // One-CTA int8 tiles: warps 8, 10, 11, 12, 14, 15, two on each
+    // sub-partition but the MMA issuer's (1), whose single thread bounds the
+    // main loop (four converter warps took 640-700 cycles per 8 KB stage,
+    // longer than a K-step of the MMAs).  Int8 pair tiles: warps 8..15 in
+    // four groups of two, group g converting the CTA's K-steps j with
+    // j % 4 == g, so four stages are converted at once and each group's
+    // per-stage latency (wait, loads, stores, proxy fence, arrival) overlaps
+    // the others' (one group of six: 0.64 ms for the SwiGLU launch of 8192 x
+    // 8192 x 3072; two groups of three 0.59; three of two 0.53; four of two,
+    // with two warps on the issuer's sub-partition, 0.52).
+    static constexpr bool QR = P && I8;
+    static constexpr int CONV_WARPS = QR ? 8 : 6;           // int8 only
+    static constexpr int CONV_GROUPS = QR ? 4 : 1;
     static constexpr int THREADS = I8 ? 512 : 256;
     static constexpr int A_BYTES = A_ROWS * kBK * 2;
     static constexpr int BQ_BYTES = B_ROWS * kBK;          // int8 B staging
@@ -141,7 +145,6 @@ struct Cfg {
     // well ahead and their TMA latency is off the conversion's path (with A,
     // int8 B and converted B in one stage the int8 pair ran at ~1000 cycles
     // per K-step, 360 of them with the MMA issuer waiting for converted B).
-    static constexpr bool QR = P && I8;
     // TMA ring: bf16: A + B; int8 one-CTA: A + int8 B; QR: A + converted B
     // (the A tile completes on the converted-B barrier, so the MMA issuer
     // waits once per K-step).
@@ -1102,7 +1105,7 @@ __global__ void __launch_bounds__(Cfg<MODE, I8, MH, P>::THREADS, 1)
             }
             if (ok && idx + 2 < cs.count) ok = prepare(idx + 2);
         }
-    } else if (I8 && warp >= 8 && (warp & 3) != 1) {
+    } else if (I8 && warp >= 8 && (QR || (warp & 3) != 1)) {
         // -------------------------------------------------- int8 -> bf16
         // Staged int8 rows (64 bytes each, B_ROWS rows) become 128-byte bf16
         // rows of a converted-B tile; 16-byte chunk c of row r lands at chunk
@@ -1110,7 +1113,8 @@ __global__ void __launch_bounds__(Cfg<MODE, I8, MH, P>::THREADS, 1)
         // of 1024 bytes.  One-CTA tiles: from the TMA stage into the
         // converted-B ring; QR: from the int8 ring into the B half of the
         // A + B stage, once the MMAs that read that stage's last use are done.
-        const int tid_all = ((warp - 8) - (warp > 9) - (warp > 13)) * 32 + lane;
+        const int tid_all =
+            (QR ? warp - 8 : (warp - 8) - (warp > 9) - (warp > 13)) * 32 + lane;
         const int grp = tid_all / int(kGroupThreads);
         const int tid = tid_all % int(kGroupThreads);
         int stage = 0, cstage = 0, qs = 0, turn = 0;

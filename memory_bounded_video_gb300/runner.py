@@ -144,6 +144,57 @@ class DitStack:
             return out
         return None
 
+    def forward_host(self, x_host: List[torch.Tensor], dev: DeviceInputs,
+                     out_host: List[torch.Tensor], stream=None,
+                     qk: Optional[DeviceQk] = None,
+                     lora: Optional[List[DeviceLora]] = None):
+        """Run the stack over a sequence of token batches held in pinned
+        host memory, writing each batch's result (the final layer's output,
+        or x without a final layer) into the matching pinned ``out_host``
+        tensor.  Two device buffers alternate: while batch i computes on
+        ``stream``, a copy stream brings batch i + 1 in and takes batch i - 1's
+        result out, so the host link overlaps the kernels.  Asynchronous:
+        ``stream`` has waited for every copy when this returns, so
+        synchronising it makes the results valid."""
+        if stream is None:
+            stream = torch.cuda.current_stream()
+        n = len(x_host)
+        if len(out_host) != n:
+            raise ValueError("one output buffer per input batch")
+        if n == 0:
+            return
+        final = dev.wf is not None
+        if getattr(self, "_io", None) is None:
+            xs = [torch.empty(self.T, self.D, dtype=torch.float32, device=self.device)
+                  for _ in range(2)]
+            outs = ([torch.empty(self.T, 64, dtype=torch.float32, device=self.device)
+                     for _ in range(2)] if final else [None, None])
+            self._io = (torch.cuda.Stream(device=self.device), xs, outs)
+        copy, xs, outs = self._io
+        if final and outs[0] is None:
+            raise ValueError("forward_host: the stack was first run without a final layer")
+        ev_in = [torch.cuda.Event() for _ in range(2)]
+        ev_done = [torch.cuda.Event() for _ in range(2)]
+        copy.wait_stream(stream)  # the buffers' previous users are done
+
+        def bring_in(i):
+            with torch.cuda.stream(copy):
+                xs[i % 2].copy_(x_host[i], non_blocking=True)
+                ev_in[i % 2].record(copy)
+
+        bring_in(0)
+        for i in range(n):
+            b = i % 2
+            if i + 1 < n:  # same stream as batch i - 1's copy-out: ordered after it
+                bring_in(i + 1)
+            stream.wait_event(ev_in[b])
+            res = self.forward(xs[b], dev, stream, out=outs[b], qk=qk, lora=lora)
+            ev_done[b].record(stream)
+            copy.wait_event(ev_done[b])
+            with torch.cuda.stream(copy):
+                out_host[i].copy_(res if res is not None else xs[b], non_blocking=True)
+        stream.wait_stream(copy)
+
     def check(self, stream=None):
         """Synchronise and raise if a kernel recorded a device-side error."""
         if stream is None:

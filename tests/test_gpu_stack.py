@@ -236,3 +236,30 @@ def test_headline_stack_chunk_sweep_is_bit_identical():
             assert torch.equal(x, ref[0]), (cm, ca)
             assert torch.equal(out, ref[1]), (cm, ca)
         del st
+
+
+@pytest.mark.parametrize("final", [True, False])
+def test_forward_host_pipeline_matches_per_batch_forwards(final):
+    # three different token batches from pinned host memory through the
+    # double-buffered host path, against one device forward per batch
+    T, D, H, F = 1000, 256, 4, 704
+    inp = synth.make_inputs(T, D, H, F, seed=21, blocks=2, int8=True, final=final,
+                            jitter=True)
+    dev = runner.upload(inp)
+    g = torch.Generator().manual_seed(5)
+    xs = [torch.randn(T, D, generator=g).pin_memory() for _ in range(3)]
+    cols = 64 if final else D
+    outs = [torch.full((T, cols), float("nan")).pin_memory() for _ in range(3)]
+    stack = runner.DitStack(T, D, H, F, 256, 384, 256)
+    for _ in range(2):  # the second call reuses the stack's buffers
+        stack.forward_host(xs, dev, outs)
+        torch.cuda.synchronize()
+        stack.check()
+        for xh, oh in zip(xs, outs):
+            x = xh.cuda()
+            ref = stack.forward(x, dev)
+            stack.check()
+            ref = (ref if final else x).cpu()
+            assert torch.equal(oh.view(torch.int32), ref.view(torch.int32))
+        for o in outs:
+            o.fill_(float("nan"))
