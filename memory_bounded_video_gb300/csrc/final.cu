@@ -5,8 +5,9 @@
 //
 // Per CTA (256 threads): row statistics (one warp per row, two passes over
 // the row), then the D axis in chunks of 64: the normalised-modulated chunk
-// and the matching W_f chunk are staged transposed in shared memory and every
-// thread accumulates a 4-row x 4-output register tile in ascending k.
+// and the matching W_f chunk are staged transposed in shared memory (each
+// thread one 4 x 4 block of each) and every thread accumulates a 4-row x
+// 4-output register tile in ascending k.
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -19,6 +20,8 @@ constexpr int kOut = 64;     // output channels
 constexpr int kKC = 64;      // k chunk
 constexpr int kPad = 68;     // padded row of the transposed tiles (floats)
 constexpr int kThreads = 256;
+static_assert(kRows == 64 && kOut == 64 && kKC == 64 && kThreads == 256,
+              "each thread stages one 4 x 4 block of the x and W chunks");
 
 template <bool INT8>
 __global__ void __launch_bounds__(kThreads)
@@ -65,45 +68,65 @@ __global__ void __launch_bounds__(kThreads)
     const int og = tid & 15;   // outputs og*4 .. og*4+3
     float acc[4][4] = {};
     for (int k0 = 0; k0 < D; k0 += kKC) {
-        // stage the modulated-normalised x chunk and the W chunk, transposed
-        for (int i = tid; i < kRows * (kKC / 4); i += kThreads) {
-            const int r = i / (kKC / 4), c4 = i % (kKC / 4);
-            const int64_t t = row0 + r;
+        // stage the modulated-normalised x chunk and the W chunk, transposed.
+        // Thread tid owns a 4 x 4 block of each (rows or outputs 4 (tid % 16)
+        // .., k 4 (tid / 16) ..): four 16-byte loads (the two half-warps
+        // read the two halves of each 32-byte sector) and four 16-byte
+        // shared stores, which hit distinct banks within each quarter-warp
+        // (one scalar store per element, with consecutive threads 272 floats
+        // apart, collided eight ways).
+        {
+            const int b4 = (tid & 15) * 4;  // first row / output of the block
+            const int c4 = tid >> 4;        // k = k0 + 4 c4 .. + 3
             const int k = k0 + 4 * c4;
-            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (t < T) {
-                const float4 xv = *reinterpret_cast<const float4 *>(x + t * D + k);
-                const float4 sc = __ldg(reinterpret_cast<const float4 *>(scale + k));
-                const float4 sh = __ldg(reinterpret_cast<const float4 *>(shift + k));
-                const float m = mean_s[r], rs = rstd_s[r];
-                v.x = __fmaf_rn((xv.x - m) * rs, 1.0f + sc.x, sh.x);
-                v.y = __fmaf_rn((xv.y - m) * rs, 1.0f + sc.y, sh.y);
-                v.z = __fmaf_rn((xv.z - m) * rs, 1.0f + sc.z, sh.z);
-                v.w = __fmaf_rn((xv.w - m) * rs, 1.0f + sc.w, sh.w);
+            float v[4][4];
+            const float4 sc = __ldg(reinterpret_cast<const float4 *>(scale + k));
+            const float4 sh = __ldg(reinterpret_cast<const float4 *>(shift + k));
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int r = b4 + i;
+                const int64_t t = row0 + r;
+                float4 xv = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (t < T) {
+                    xv = *reinterpret_cast<const float4 *>(x + t * D + k);
+                    const float m = mean_s[r], rs = rstd_s[r];
+                    xv.x = __fmaf_rn((xv.x - m) * rs, 1.0f + sc.x, sh.x);
+                    xv.y = __fmaf_rn((xv.y - m) * rs, 1.0f + sc.y, sh.y);
+                    xv.z = __fmaf_rn((xv.z - m) * rs, 1.0f + sc.z, sh.z);
+                    xv.w = __fmaf_rn((xv.w - m) * rs, 1.0f + sc.w, sh.w);
+                }
+                v[0][i] = xv.x;
+                v[1][i] = xv.y;
+                v[2][i] = xv.z;
+                v[3][i] = xv.w;
             }
-            xs[(4 * c4 + 0) * kPad + r] = v.x;
-            xs[(4 * c4 + 1) * kPad + r] = v.y;
-            xs[(4 * c4 + 2) * kPad + r] = v.z;
-            xs[(4 * c4 + 3) * kPad + r] = v.w;
-        }
-        for (int i = tid; i < kOut * (kKC / 4); i += kThreads) {
-            const int o = i / (kKC / 4), c4 = i % (kKC / 4);
-            const int k = k0 + 4 * c4;
-            float4 w;
-            if (INT8) {
-                const char4 qv = *reinterpret_cast<const char4 *>(
-                    reinterpret_cast<const int8_t *>(wf) + int64_t(o) * D + k);
-                const float s = __ldg(wscale + o);
-                w = make_float4(float(qv.x) * s, float(qv.y) * s, float(qv.z) * s,
-                                float(qv.w) * s);
-            } else {
-                w = *reinterpret_cast<const float4 *>(reinterpret_cast<const float *>(wf) +
-                                                      int64_t(o) * D + k);
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                *reinterpret_cast<float4 *>(xs + (4 * c4 + j) * kPad + b4) =
+                    make_float4(v[j][0], v[j][1], v[j][2], v[j][3]);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int o = b4 + i;
+                float4 w;
+                if (INT8) {
+                    const char4 qv = *reinterpret_cast<const char4 *>(
+                        reinterpret_cast<const int8_t *>(wf) + int64_t(o) * D + k);
+                    const float s = __ldg(wscale + o);
+                    w = make_float4(float(qv.x) * s, float(qv.y) * s, float(qv.z) * s,
+                                    float(qv.w) * s);
+                } else {
+                    w = *reinterpret_cast<const float4 *>(reinterpret_cast<const float *>(wf) +
+                                                          int64_t(o) * D + k);
+                }
+                v[0][i] = w.x;
+                v[1][i] = w.y;
+                v[2][i] = w.z;
+                v[3][i] = w.w;
             }
-            ws[(4 * c4 + 0) * kPad + o] = w.x;
-            ws[(4 * c4 + 1) * kPad + o] = w.y;
-            ws[(4 * c4 + 2) * kPad + o] = w.z;
-            ws[(4 * c4 + 3) * kPad + o] = w.w;
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                *reinterpret_cast<float4 *>(ws + (4 * c4 + j) * kPad + b4) =
+                    make_float4(v[j][0], v[j][1], v[j][2], v[j][3]);
         }
         __syncthreads();
 #pragma unroll 8
