@@ -28,7 +28,7 @@ computes that function directly, unchunked, in float64:
     b   = LN(x1) * (1 + scale2) + shift2
     x2  = x1 + gate2 * ((silu(b Wg^T) * (b Wu^T)) Wd^T)
 
-Readings where the pages are silent (the same list is kept in the design doc):
+Readings where the pages are silent:
 
 * LN is LayerNorm over the hidden axis, biased variance, eps 1e-6, no affine.
 * ``modulation`` is [6, D] with rows shift1, scale1, gate1, shift2, scale2,
