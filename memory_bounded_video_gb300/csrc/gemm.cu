@@ -131,7 +131,8 @@ struct Cfg {
     // per-stage latency (wait, loads, stores, proxy fence, arrival) overlaps
     // the others' (one group of six: 0.64 ms for the SwiGLU launch of 8192 x
     // 8192 x 3072; two groups of three 0.59; three of two 0.53; four of two,
-    // with two warps on the issuer's sub-partition, 0.52).
+    // with two warps on the issuer's sub-partition, 0.52; with the int8 tile
+    // staged in place and a 7-stage ring, 0.50).
     static constexpr bool QR = P && I8;
     static constexpr int CONV_WARPS = QR ? 8 : 6;           // int8 only
     static constexpr int CONV_GROUPS = QR ? 4 : 1;
@@ -139,16 +140,22 @@ struct Cfg {
     static constexpr int A_BYTES = A_ROWS * kBK * 2;
     static constexpr int BQ_BYTES = B_ROWS * kBK;          // int8 B staging
     static constexpr int C_BYTES = B_ROWS * kBK * 2;       // one bf16 B tile
-    // QR (int8 pair): a ring of A tiles + converted B tiles, freed by one
-    // commit per K-step, and a separate ring of int8 B tiles freed by the
-    // converters as soon as they have read them, so the weights are fetched
-    // well ahead and their TMA latency is off the conversion's path (with A,
-    // int8 B and converted B in one stage the int8 pair ran at ~1000 cycles
-    // per K-step, 360 of them with the MMA issuer waiting for converted B).
+    // QR (int8 pair): one ring of A + converted-B stages, freed by one commit
+    // per K-step.  The int8 B tile (8 KB) lands by TMA in the upper half of
+    // its stage's converted-B slot (16 KB), and a converter group reads all
+    // of it into registers before any of the group writes the bf16 tile over
+    // the slot, so no separate int8 ring takes shared memory: the ring is 7
+    // stages deep (6 with the fp32 epilogue tile) instead of 5 beside a
+    // 7-stage int8 ring.  The conversion of a stage can start only when the
+    // MMA of the stage's previous use is done, and the ring's depth is what
+    // hides that chain (conversion, proxy fence, the peer's signal, the MMA
+    // and its commit).
     // TMA ring: bf16: A + B; int8 one-CTA: A + int8 B; QR: A + converted B
     // (the A tile completes on the converted-B barrier, so the MMA issuer
     // waits once per K-step).
-    static constexpr int STAGES = P ? (I8 ? 5 : 6) : 4;
+    static constexpr bool EPI_T =
+        MODE == DIT_EPI_RESID || MODE == DIT_EPI_DOWN || MODE == DIT_EPI_STORE_F32;
+    static constexpr int STAGES = P ? (I8 ? (EPI_T ? 6 : 7) : 6) : 4;
     static constexpr int STAGE_BYTES = A_BYTES + (QR ? C_BYTES : I8 ? BQ_BYTES : C_BYTES);
     static constexpr int TMA_BYTES = QR ? A_BYTES : STAGE_BYTES;
     // fp32 epilogues (gated residual, down projection, fp32 store) move each
@@ -157,16 +164,13 @@ struct Cfg {
     // (with one row per lane each access touched 32 lines, and the residual
     // epilogue took longer than the tile's main loop); the rings give up a
     // stage for it.
-    static constexpr bool EPI_T =
-        MODE == DIT_EPI_RESID || MODE == DIT_EPI_DOWN || MODE == DIT_EPI_STORE_F32;
     static constexpr int T_BYTES = EPI_T ? 4 * 32 * 36 * 4 : 0;
     // int8 one-CTA: ring of converted bf16 B tiles read by the MMA (3 stages),
     // decoupled from the TMA ring so TMA latency and conversion overlap.
     static constexpr int CSTAGES = (I8 && !QR) ? (EPI_T ? 2 : 3) : 0;
-    static constexpr int QSTAGES = QR ? (EPI_T ? 5 : 7) : 0;  // int8 B ring (QR)
+    static constexpr int OFF_QIN = A_BYTES + BQ_BYTES;  // QR: int8 tile within a stage
     static constexpr int OFF_C = STAGES * STAGE_BYTES;
-    static constexpr int OFF_Q = OFF_C + CSTAGES * C_BYTES;
-    static constexpr int OFF_T = OFF_Q + QSTAGES * BQ_BYTES;
+    static constexpr int OFF_T = OFF_C + CSTAGES * C_BYTES;
     static constexpr int HALF_COLS = NB * BN;      // fp32 TMEM columns per M half
     static constexpr int ACC_COLS = MH * HALF_COLS;  // per accumulator buffer
     static constexpr int TMEM_COLS = 2 * ACC_COLS;
@@ -176,14 +180,15 @@ struct Cfg {
     // at byte 384; completion-signal bytes at 448
     static constexpr int BAR_BYTES = 512;
     static constexpr int SMEM_BYTES = OFF_T + T_BYTES + BAR_BYTES + 1024;
-    static_assert(2 * STAGES + 32 <= 48 && CSTAGES <= 8 && QSTAGES <= 8,
+    static_assert(2 * STAGES + 32 <= 48 && CSTAGES <= 8,
                   "barriers overlap the work list");
     // A converter group's K-steps are CONV_GROUPS apart; its wait for a ring
     // slot's previous use to be freed is only unambiguous (mbarrier phase
     // parity) while that use is at most one ring cycle back, which needs
-    // CONV_GROUPS <= the ring depths.
-    static_assert(!QR || (CONV_GROUPS <= STAGES && CONV_GROUPS <= QSTAGES),
-                  "converter groups outrun the rings");
+    // CONV_GROUPS <= the ring depth.
+    static_assert(!QR || (CONV_GROUPS <= STAGES && CONV_GROUPS <= 8),
+                  "converter groups outrun the ring");
+    static_assert(!QR || 2 * BQ_BYTES == C_BYTES, "int8 tile fills half a converted slot");
     static_assert(SMEM_BYTES <= 232448, "shared memory");
 };
 
@@ -643,14 +648,14 @@ __global__ void __launch_bounds__(Cfg<MODE, I8, MH, P>::THREADS, 1)
     using C = Cfg<MODE, I8, MH, P>;
     constexpr int S = C::STAGES;
     constexpr int CS = C::CSTAGES;
-    constexpr int QS = C::QSTAGES;
     constexpr bool QR = C::QR;
     constexpr int G = P ? 2 : 1;  // cta_group of every tcgen05 instruction here
     extern __shared__ uint8_t smem_raw[];
     uint8_t *tiles = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *bars = reinterpret_cast<uint64_t *>(tiles + C::OFF_T + C::T_BYTES);
-    // bars: full[S], empty[S], cfull[8], cempty[8] (QR: qfull), qempty[8],
+    // bars: full[S], empty[S], cfull[8], cempty[8] (QR: qfull), qempty[8]
+    // (QR: the converter groups' load-before-store barriers),
     // tfull[2], tempty[2], drain, handed (split accumulator written); then the
     // TMEM slot and the abort flag; this CTA's work list at byte 384; 16
     // bytes at byte 448 (QR: the completion-signal copy's source/target)
@@ -674,7 +679,7 @@ __global__ void __launch_bounds__(Cfg<MODE, I8, MH, P>::THREADS, 1)
     auto cfull_bar = [&](int s) { return bar0 + 8u * (2 * S + s); };
     auto cempty_bar = [&](int s) { return bar0 + 8u * (2 * S + 8 + s); };
     auto qfull_bar = [&](int s) { return bar0 + 8u * (2 * S + 8 + s); };  // QR only
-    auto qempty_bar = [&](int s) { return bar0 + 8u * (2 * S + 16 + s); };
+    auto gsync_bar = [&](int g) { return bar0 + 8u * (2 * S + 16 + g); };  // QR only
     auto tfull_bar = [&](int b) { return bar0 + 8u * (2 * S + 24 + b); };
     auto tempty_bar = [&](int b) { return bar0 + 8u * (2 * S + 26 + b); };
     const uint32_t drain_bar = bar0 + 8u * (2 * S + 28);
@@ -697,9 +702,9 @@ __global__ void __launch_bounds__(Cfg<MODE, I8, MH, P>::THREADS, 1)
             mbar_init(cfull_bar(s), kGroupThreads);
             mbar_init(cempty_bar(s), 1);
         }
-        for (int s = 0; s < QS; ++s) {
-            mbar_init(qfull_bar(s), 1);
-            mbar_init(qempty_bar(s), kGroupThreads);
+        if (QR) {
+            for (int s = 0; s < S; ++s) mbar_init(qfull_bar(s), 1);
+            for (int g = 0; g < C::CONV_GROUPS; ++g) mbar_init(gsync_bar(g), kGroupThreads);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(tfull_bar(b), 1);
@@ -965,10 +970,12 @@ __global__ void __launch_bounds__(Cfg<MODE, I8, MH, P>::THREADS, 1)
     } else if (warp == 2 && QR) {
         if (lane == 0) {
             // ---------------------------------------------- int8 B producer (QR)
+            // into the upper half of the stage's converted-B slot, once the
+            // MMAs of the stage's previous use are done
             const CUtensorMap *tb = (C::NB == 2 && rank == 1) ? &tmB1 : &tmB0;
             const int b_row0 = C::NB == 1 ? rank * C::B_BOX : 0;
-            int qs = 0;
-            uint32_t qph = 0;
+            int stage = 0;
+            uint32_t ph = 0;
             int64_t issued = 0;
             bool ok = true;
             for (int idx = 0; idx < cs.count && ok; ++idx) {
@@ -976,24 +983,24 @@ __global__ void __launch_bounds__(Cfg<MODE, I8, MH, P>::THREADS, 1)
                 int mb, nb;
                 tile_of(p, it.u, mb, nb);
                 for (int kb = it.k0; kb < it.k1; ++kb) {
-                    if (!mbar_wait(qempty_bar(qs), qph ^ 1u, wc)) {
+                    if (!mbar_wait(empty_bar(stage), ph ^ 1u, wc)) {
                         ok = false;
                         break;
                     }
-                    mbar_arrive_expect_tx(qfull_bar(qs), C::BQ_BYTES);
-                    tma_load_2d(smem_u32(tiles + C::OFF_Q + qs * C::BQ_BYTES), tb, qfull_bar(qs),
-                                kb * kBK, nb * C::BN + b_row0);
+                    mbar_arrive_expect_tx(qfull_bar(stage), C::BQ_BYTES);
+                    tma_load_2d(smem_u32(tiles + stage * C::STAGE_BYTES + C::OFF_QIN), tb,
+                                qfull_bar(stage), kb * kBK, nb * C::BN + b_row0);
                     ++issued;
-                    if (++qs == QS) {
-                        qs = 0;
-                        qph ^= 1u;
+                    if (++stage == S) {
+                        stage = 0;
+                        ph ^= 1u;
                     }
                 }
             }
             if (!ok) {
-                const int64_t first = issued > QS ? issued - QS : 0;
+                const int64_t first = issued > S ? issued - S : 0;
                 for (int64_t i = first; i < issued; ++i)
-                    mbar_wait_quiet(qfull_bar(int(i % QS)), uint32_t((i / QS) & 1), kWaitLimitNs);
+                    mbar_wait_quiet(qfull_bar(int(i % S)), uint32_t((i / S) & 1), kWaitLimitNs);
             }
         }
     } else if (warp == 3 && QR) {
@@ -1117,8 +1124,8 @@ __global__ void __launch_bounds__(Cfg<MODE, I8, MH, P>::THREADS, 1)
             (QR ? warp - 8 : (warp - 8) - (warp > 9) - (warp > 13)) * 32 + lane;
         const int grp = tid_all / int(kGroupThreads);
         const int tid = tid_all % int(kGroupThreads);
-        int stage = 0, cstage = 0, qs = 0, turn = 0;
-        uint32_t ph = 0, cph = 0, qph = 0;
+        int stage = 0, cstage = 0, turn = 0;
+        uint32_t ph = 0, cph = 0, gph = 0;
         bool ok = true;
         for (int idx = 0; ok && idx < cs.count; ++idx) {
             const AttnItem it = attn_item(p.g, cs, cta, idx);
@@ -1128,8 +1135,7 @@ __global__ void __launch_bounds__(Cfg<MODE, I8, MH, P>::THREADS, 1)
               if (mine) {
                 bool w;
                 if constexpr (QR)
-                    w = mbar_wait(qfull_bar(qs), qph, wc) &&
-                        mbar_wait(empty_bar(stage), ph ^ 1u, wc);
+                    w = mbar_wait(qfull_bar(stage), ph, wc);  // the slot was free for it
                 else
                     w = mbar_wait(full_bar(stage), ph, wc) &&
                         mbar_wait(cempty_bar(cstage), cph ^ 1u, wc);
@@ -1138,8 +1144,7 @@ __global__ void __launch_bounds__(Cfg<MODE, I8, MH, P>::THREADS, 1)
                     ok = false;
                     break;
                 }
-                const uint8_t *sq = QR ? tiles + C::OFF_Q + qs * C::BQ_BYTES
-                                       : tiles + stage * C::STAGE_BYTES + C::A_BYTES;
+                const uint8_t *sq = tiles + stage * C::STAGE_BYTES + (QR ? C::OFF_QIN : C::A_BYTES);
                 uint8_t *dst0 = QR ? tiles + stage * C::STAGE_BYTES + C::A_BYTES
                                    : tiles + C::OFF_C + cstage * C::C_BYTES;
                 // Thread tid owns pieces of 8 int8: rows r = tid / 8 + kStep i
@@ -1158,28 +1163,59 @@ __global__ void __launch_bounds__(Cfg<MODE, I8, MH, P>::THREADS, 1)
                     const int sw = (kStep % 8 == 0) ? (r0 & 7) : (r & 7);
                     return dst0 + r * 128 + ((c8 ^ sw) << 4);
                 };
+                if constexpr (QR) {
+                    // the bf16 tile overwrites the int8 tile it comes from:
+                    // the whole group's pieces go into registers first, and
+                    // the group's barrier (bounded wait) orders every load
+                    // before any store
+                    uint2 w8[kPieces];
 #pragma unroll
-                for (int i0 = 0; i0 < kPieces; i0 += kBatch) {
-                    uint2 w8[kBatch];
-#pragma unroll
-                    for (int i = 0; i < kBatch; ++i) {
-                        const bool in = i0 + i < kPieces && r0 + (i0 + i) * kStep < C::B_ROWS;
-                        w8[i] = in ? *reinterpret_cast<const uint2 *>(src + (i0 + i) * kStep * kBK)
+                    for (int i = 0; i < kPieces; ++i) {
+                        const bool in = r0 + i * kStep < C::B_ROWS;
+                        w8[i] = in ? *reinterpret_cast<const uint2 *>(src + i * kStep * kBK)
                                    : make_uint2(0u, 0u);
                     }
+                    mbar_arrive(gsync_bar(grp));
+                    bool gw = mbar_wait(gsync_bar(grp), gph, wc);
+                    gph ^= 1u;
+                    gw = __all_sync(0xffffffffu, gw);
+                    if (!gw) {
+                        ok = false;
+                        break;
+                    }
 #pragma unroll
-                    for (int i = 0; i < kBatch; ++i) {
-                        const bool in = i0 + i < kPieces && r0 + (i0 + i) * kStep < C::B_ROWS;
-                        if (in) *reinterpret_cast<uint4 *>(dst_of(i0 + i)) = int8x8_to_bf16x8(w8[i]);
+                    for (int i = 0; i < kPieces; ++i) {
+                        const bool in = r0 + i * kStep < C::B_ROWS;
+                        if (in) *reinterpret_cast<uint4 *>(dst_of(i)) = int8x8_to_bf16x8(w8[i]);
+                    }
+                } else {
+#pragma unroll
+                    for (int i0 = 0; i0 < kPieces; i0 += kBatch) {
+                        uint2 w8[kBatch];
+#pragma unroll
+                        for (int i = 0; i < kBatch; ++i) {
+                            const bool in =
+                                i0 + i < kPieces && r0 + (i0 + i) * kStep < C::B_ROWS;
+                            w8[i] = in ? *reinterpret_cast<const uint2 *>(src + (i0 + i) * kStep *
+                                                                          kBK)
+                                       : make_uint2(0u, 0u);
+                        }
+#pragma unroll
+                        for (int i = 0; i < kBatch; ++i) {
+                            const bool in =
+                                i0 + i < kPieces && r0 + (i0 + i) * kStep < C::B_ROWS;
+                            if (in)
+                                *reinterpret_cast<uint4 *>(dst_of(i0 + i)) =
+                                    int8x8_to_bf16x8(w8[i]);
+                        }
                     }
                 }
                 fence_proxy_async_smem();  // the tensor core reads what we wrote
                 // every converter thread arrives as soon as its own stores are
                 // fenced (one arrival per warp after __syncwarp measured 3-5 %
-                // slower); QR: the int8 tile is free again, and the leader's
-                // thread 0 also arms the peer's 16-byte signal
+                // slower); QR: the leader's thread 0 also arms the peer's
+                // 16-byte signal
                 if constexpr (QR) {
-                    mbar_arrive(qempty_bar(qs));
                     if (leader && tid == 0)
                         mbar_arrive_expect_tx(cfull_bar(stage), 16u);
                     else
@@ -1188,12 +1224,7 @@ __global__ void __launch_bounds__(Cfg<MODE, I8, MH, P>::THREADS, 1)
                     mbar_arrive(cfull_bar(cstage));
                 }
               }
-                if constexpr (QR) {
-                    if (++qs == QS) {
-                        qs = 0;
-                        qph ^= 1u;
-                    }
-                } else {
+                if constexpr (!QR) {
                     if (++cstage == CS) {
                         cstage = 0;
                         cph ^= 1u;
