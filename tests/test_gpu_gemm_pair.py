@@ -38,6 +38,10 @@ CASES = [
     ("down_carry_int8", ds.EPI_DOWN, 257, 512, 512, True, {"acc_load": 1, "acc_final": 1}),
     ("down_partial_bf16", ds.EPI_DOWN, 257, 512, 512, False, {"acc_load": 0, "acc_final": 0}),
     ("store_f32_tiny", ds.EPI_STORE_F32, 1, 32, 64, False, {}),
+    # fewer K-steps than converter groups and than ring stages
+    ("store_int8_k64", ds.EPI_STORE_BF16, 300, 512, 64, True, {}),
+    ("swiglu_int8_k192", ds.EPI_SWIGLU, 200, 384, 192, True, {}),
+    ("down_int8_k128", ds.EPI_DOWN, 300, 256, 128, True, {"acc_load": 1, "acc_final": 1}),
 ]
 
 
