@@ -1118,8 +1118,10 @@ __global__ void __launch_bounds__(Cfg<MODE, I8, MH, P>::THREADS, 1)
         // rows of a converted-B tile; 16-byte chunk c of row r lands at chunk
         // c ^ (r % 8) of the row (the 128-byte swizzle), rows in 8-row groups
         // of 1024 bytes.  One-CTA tiles: from the TMA stage into the
-        // converted-B ring; QR: from the int8 ring into the B half of the
-        // A + B stage, once the MMAs that read that stage's last use are done.
+        // converted-B ring; QR: in place, from the upper half of the A + B
+        // stage's B slot (where the int8 tile landed once the MMAs of the
+        // stage's previous use were done) over the whole slot.  Group g of
+        // CONV_GROUPS converts the CTA's K-steps j with j % CONV_GROUPS == g.
         const int tid_all =
             (QR ? warp - 8 : (warp - 8) - (warp > 9) - (warp > 13)) * 32 + lane;
         const int grp = tid_all / int(kGroupThreads);
@@ -1149,8 +1151,8 @@ __global__ void __launch_bounds__(Cfg<MODE, I8, MH, P>::THREADS, 1)
                                    : tiles + C::OFF_C + cstage * C::C_BYTES;
                 // Thread tid owns pieces of 8 int8: rows r = tid / 8 + kStep i
                 // (kStep = the group's threads / 8; the last piece is ragged),
-                // chunk c = tid % 8.  Loads are batched ahead of the
-                // conversions so their latency overlaps.
+                // chunk c = tid % 8.  Loads go ahead of the conversions so
+                // their latency overlaps (one-CTA: in batches; QR: all).
                 constexpr int kStep = int(kGroupThreads) / 8;
                 constexpr int kPieces = (C::B_ROWS + kStep - 1) / kStep;
                 constexpr int kBatch = kPieces < 6 ? kPieces : 6;
