@@ -92,11 +92,11 @@ struct GemmParams {
 constexpr int kLoraRows = 128;                    // rows of a half's L tile
 constexpr int kLoraStageBytes = (kBM + kLoraRows) * kBK * 2;
 
-// MH: 128-row halves of the M tile.  MH = 2 (int8 B, no LoRA) runs two
-// M = 128 MMAs per K-step on one converted B tile, which halves the int8
-// conversion per multiply-add (the conversion's ALU throughput bounds the
-// int8 main loop); the N tile is halved so that both halves' accumulators
-// still fit TMEM twice.
+// MH: 128-row halves of the M tile of a one-CTA tile.  MH = 2 runs two
+// M = 128 MMAs per K-step on one converted int8 B tile (half the conversion
+// per multiply-add, with the N tile halved so that both halves'
+// accumulators fit TMEM twice); no launch uses it now that launches without
+// LoRA run on pair tiles, and LoRA launches use MH = 1.
 //
 // P (pair): a cluster of two CTAs computes a 256 x 256 output tile (SwiGLU:
 // 256 rows x 128 features of gate and of up) with M = 256, N = 256 MMAs
