@@ -80,6 +80,11 @@ def parse_args(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-rows", type=int, default=256,
                     help="token rows in the oracle's timed sample")
+    ap.add_argument("--oracle", choices=("sample", "full"), default="sample",
+                    help="--impl reference: time the oracle on a row sample of "
+                         "the workload, or on the whole block (every token)")
+    ap.add_argument("--cpu-threads", type=int, default=0,
+                    help="BLAS threads of the oracle (0: every core of the process)")
     return ap.parse_args(argv)
 
 
@@ -204,6 +209,20 @@ def replica_throughput(units_per_rank: float, world: int, ms_max: float) -> floa
     return units_per_rank * world / (ms_max / 1e3)
 
 
+def block_flops(T: int, D: int, F: int) -> int:
+    """Algorithmic flops of one block: the Q, K, V projections (6 D^2 per
+    token, Q counted once), the O projection (2 D^2), the SwiGLU MLP (6 D F)
+    and the two attention contractions (4 T D per query token).  Norms,
+    softmax and elementwise work are not counted."""
+    return T * (8 * D * D + 6 * D * F) + 4 * T * T * D
+
+
+def step_stats(ms_list):
+    """Median, min and max of per-step milliseconds."""
+    return {"median": round(statistics.median(ms_list), 4),
+            "min": round(min(ms_list), 4), "max": round(max(ms_list), 4)}
+
+
 def cpu_cores():
     try:
         return len(os.sched_getaffinity(0))
@@ -295,6 +314,48 @@ def cpu_sample(cfg, inp, rows_n, steps=1, warmup=0, qk=None, loras=None):
     return value, per_step, sample, times
 
 
+def cpu_full(cfg, inp, steps=1, warmup=0):
+    """Time the float64 oracle on the whole workload: every block over all T
+    tokens (unchunked), plus the final layer when the workload has one.
+    Throughput = blocks x T / time."""
+    from oracle import block as ob
+
+    H = cfg["heads"]
+    x0 = inp.x.double().numpy()
+    blocks = []
+    for bw, mod in zip(inp.blocks, inp.mods):
+        if bw.int8:
+            w = ob.DitWeights(**{k: ob.dequant_int8(v.numpy(), bw.scales[k].numpy())
+                                 for k, v in bw.named().items()})
+        else:
+            w = ob.DitWeights(**{k: v.double().numpy() for k, v in bw.named().items()})
+        blocks.append((w, mod.double().numpy()))
+    wf = None
+    if inp.wf is not None:
+        wf = (ob.dequant_int8(inp.wf.numpy(), inp.wf_scale.numpy())
+              if inp.wf_scale is not None else inp.wf.double().numpy())
+        mod_f = inp.mod_f.double().numpy()
+
+    def one():
+        t0 = time.perf_counter()
+        x = x0
+        for w, mod in blocks:
+            x = ob.dit_block(x, w, mod, H)
+        if wf is not None:
+            ob.final_layer(x, wf, mod_f)
+        return time.perf_counter() - t0
+
+    for _ in range(warmup):
+        one()
+    times = [one() for _ in range(steps)]
+    per_step = sum(times) / len(times)
+    value = len(blocks) * cfg["T"] / per_step
+    sample = (f"whole workload: {len(blocks)} block(s) x {cfg['T']} tokens, unchunked"
+              + (", final layer" if wf is not None else "")
+              + ", float64 numpy oracle")
+    return value, per_step, sample, times
+
+
 # ------------------------------------------------------------------ GPU leg
 
 def run_ours(args, rank, world, local_rank):
@@ -303,7 +364,6 @@ def run_ours(args, rank, world, local_rank):
 
     from memory_bounded_video_gb300 import build as dbuild
     from memory_bounded_video_gb300 import ditstream, runner, synth
-    from oracle import block as ob
 
     cfg = dict(synth.WORKLOADS[args.workload])
     if args.mlp_chunk is not None:
@@ -335,8 +395,12 @@ def run_ours(args, rank, world, local_rank):
     stream = torch.cuda.current_stream()
     mem0 = torch.cuda.memory_allocated()
     torch.cuda.reset_peak_memory_stats()
-    for _ in range(args.warmup):
+
+    def step():
         stack.forward(x, dev, stream, qk=dqk, lora=dls)
+
+    for _ in range(args.warmup):
+        step()
     stack.check(stream)
     peak_fwd = torch.cuda.max_memory_allocated() - mem0
 
@@ -344,40 +408,55 @@ def run_ours(args, rank, world, local_rank):
         if world > 1:
             dist.barrier()
 
-    stack.plan.profile_enable(True)
-    stack.plan.profile_read()
+    def timed_steps(k, fn):
+        """Run fn() k times with a CUDA event on `stream` between steps;
+        returns the per-step ms and the total ms (first event to last)."""
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(k + 1)]
+        barrier()
+        torch.cuda.synchronize()
+        ev[0].record(stream)
+        for i in range(k):
+            fn()
+            ev[i + 1].record(stream)
+        torch.cuda.synchronize()
+        barrier()
+        return ([ev[i].elapsed_time(ev[i + 1]) for i in range(k)],
+                ev[0].elapsed_time(ev[k]))
+
     try:
         uuid = "GPU-" + str(torch.cuda.get_device_properties(local_rank).uuid)
     except Exception:
         uuid = None
+
+    # headline: no per-kernel instrumentation, one event between steps
     clocks = ClockSampler(uuid)
     clocks.start()
-    barrier()
-    torch.cuda.synchronize()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(args.steps):
-        stack.forward(x, dev, stream, qk=dqk, lora=dls)
-    e1.record(stream)
-    torch.cuda.synchronize()
-    barrier()
+    per_step, ms = timed_steps(args.steps, step)
     clk = clocks.stop()
-    ms = e0.elapsed_time(e1)
+    stack.check(stream)
+    ms = max_over_ranks(ms, world, dev_name)
+
+    # second pass of the same steps with every launch bracketed by events:
+    # the per-kernel breakdown and the dominant kernel's roofline
+    stack.plan.profile_enable(True)
+    stack.plan.profile_read()
+    per_step_prof, ms_prof = timed_steps(args.steps, step)
     prof = stack.plan.profile_read()
     stack.plan.profile_enable(False)
     stack.check(stream)
-    ms = max_over_ranks(ms, world, dev_name)
 
     blocks = cfg["blocks"]
     tokens_per_step = blocks * T
     value = replica_throughput(tokens_per_step * args.steps, world, ms)
     ms_per_step = ms / args.steps
-    flops_step = blocks * ob.block_flops(T, D, F)
+    flops_step = blocks * block_flops(T, D, F)
     if args.lora:  # u = x A^T and the u B^T K-steps of the five adapted linears
         flops_step += blocks * T * 2 * args.lora * (9 * D + 3 * F)
     peaks, peak_src = load_peaks()
     tflops = flops_step / (ms_per_step / 1e3) / 1e12
+    # the kernels run at the bench's clocks, not at the power-capped clock of
+    # the sustained cuBLAS loop: the burst figure is the denominator
+    tpeak = peaks["bf16_tflops"]
 
     # per-kernel breakdown and the dominant kernel's roofline
     kernels = {}
@@ -386,25 +465,31 @@ def run_ours(args, rank, world, local_rank):
         if v["launches"]:
             kernels[k] = dict(launches=v["launches"], ms=round(v["ms"], 4),
                               share=round(v["ms"] / total_k, 4))
+            if v["unit"] == "flops":
+                kernels[k]["tflops"] = round(v["work"] / (v["ms"] / 1e3) / 1e12, 1)
+            else:
+                kernels[k]["gbs"] = round(v["work"] / (v["ms"] / 1e3) / 1e9, 1)
     dom = max(prof, key=lambda k: prof[k]["ms"])
     d = prof[dom]
     if d["unit"] == "flops":
         achieved = d["work"] / (d["ms"] / 1e3) / 1e12
-        peak = peaks["bf16_tflops_sustained"]
-        roof = dict(bound="tensor", achieved=round(achieved, 2), peak=peak,
-                    unit="TFLOP/s", frac=round(achieved / peak, 4))
-        peak_note = f"bf16_tflops_sustained of {peak_src}"
+        roof = dict(bound="tensor", achieved=round(achieved, 2), peak=tpeak,
+                    unit="TFLOP/s", frac=round(achieved / tpeak, 4))
+        peak_note = f"bf16_tflops (burst) of {peak_src}"
     else:
         achieved = d["work"] / (d["ms"] / 1e3) / 1e9
         peak = peaks["hbm_gbs"]
         roof = dict(bound="hbm", achieved=round(achieved, 1), peak=peak,
                     unit="GB/s", frac=round(achieved / peak, 4))
         peak_note = f"hbm_gbs of {peak_src}"
+    roof["traffic"] = traffic_for(dom, args.workload)
     roof["kernel"] = dom
     roof["launch_ms"] = round(d["ms"] / d["launches"], 4)
     roof["work_per_launch"] = d["work"] / d["launches"]
     roof["peak_source"] = peak_note
-    roof["traffic"] = traffic_for(dom, args.workload)
+    roof["timing"] = ("CUDA events around every launch on the launching stream, "
+                      "in a second pass of the same steps (the headline pass "
+                      "runs without them)")
 
     line = {
         "metric": "DiT-block tokens/s @32k tokens, % BF16 tensor peak, "
@@ -413,6 +498,7 @@ def run_ours(args, rank, world, local_rank):
         "unit": "block-tokens/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(ms_per_step, 4),
+        "step_ms": step_stats(per_step),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16 (fp32 accumulate, fp32 residual)",
         "data": "synthetic (seeded N(0,1) tokens, N(0,0.02) weights)",
@@ -433,14 +519,18 @@ def run_ours(args, rank, world, local_rank):
                                                      / 2**30, 4) if scratch else None),
                    "parallelism": f"replicas x{world}"},
         "tflops": round(tflops, 2),
-        "tensor_peak_frac": round(tflops / peaks["bf16_tflops_sustained"], 4),
-        "tensor_peak_frac_burst": round(tflops / peaks["bf16_tflops"], 4),
+        "tensor_peak_frac": round(tflops / tpeak, 4),
+        "tensor_peak_frac_sustained": round(tflops / peaks["bf16_tflops_sustained"], 4),
+        "peak_source": f"bf16_tflops (burst) of {peak_src}",
         "peak_activation_gib": round(stack.plan.workspace_bytes() / 2**30, 4),
         "activation_beyond_kv_gib": round(
             (stack.plan.workspace_bytes() - (0 if args.kv_offload else 4 * T * D)) / 2**30, 4),
         "measured_forward_alloc_gib": round(peak_fwd / 2**30, 4),
         "roofline": roof,
         "kernels": kernels,
+        "instrumented_pass": {"ms_per_step": round(ms_prof / args.steps, 4),
+                              "step_ms": step_stats(per_step_prof),
+                              "kernel_ms_per_step": round(total_k / args.steps, 4)},
         "gpu_launches": int(sum(v["launches"] for v in prof.values())),
         "clocks": clk,
     }
@@ -453,7 +543,7 @@ def run_ours(args, rank, world, local_rank):
         x_host = inp.x.pin_memory()
         res_shape = (T, 64) if cfg["final"] else (T, D)
         out_host = torch.empty(res_shape, dtype=torch.float32).pin_memory()
-        k_e2e = max(1, min(args.steps, 5))
+        k_e2e = max(20, args.steps)
 
         def e2e_run(k):
             stack.forward_host([x_host] * k, dev, [out_host] * k, stream,
@@ -462,7 +552,24 @@ def run_ours(args, rank, world, local_rank):
         e2e_run(2)
         torch.cuda.synchronize()
         stack.check()
+        # the host -> device copy of one step's tokens alone, on a side stream
+        cs = torch.cuda.Stream()
+        xd = torch.empty_like(dev.x)
+        c0 = torch.cuda.Event(enable_timing=True)
+        c1 = torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        with torch.cuda.stream(cs):
+            c0.record(cs)
+            for _ in range(5):
+                xd.copy_(x_host, non_blocking=True)
+            c1.record(cs)
+        torch.cuda.synchronize()
+        h2d_ms = c0.elapsed_time(c1) / 5
+        del xd
+        clocks_e = ClockSampler(uuid)
+        clocks_e.start()
         barrier()
+        torch.cuda.synchronize()
         f0 = torch.cuda.Event(enable_timing=True)
         f1 = torch.cuda.Event(enable_timing=True)
         f0.record(stream)
@@ -470,6 +577,8 @@ def run_ours(args, rank, world, local_rank):
         f1.record(stream)
         torch.cuda.synchronize()
         barrier()
+        clk_e = clocks_e.stop()
+        stack.check()
         ms_e2e = max_over_ranks(f0.elapsed_time(f1), world, dev_name)
         line["e2e"] = {"value": round(replica_throughput(tokens_per_step * k_e2e, world,
                                                          ms_e2e), 1),
@@ -477,9 +586,13 @@ def run_ours(args, rank, world, local_rank):
                        "h2d_bytes_per_step": 4 * T * D,
                        "d2h_bytes_per_step": 4 * res_shape[0] * res_shape[1],
                        "steps": k_e2e,
+                       "ms_per_step": round(ms_e2e / k_e2e, 4),
+                       "h2d_ms_per_step_alone": round(h2d_ms, 4),
+                       "clocks": clk_e,
                        "copies": "pinned host memory; step i+1's input copied in and step "
                                  "i-1's result copied out on a copy stream during step i's "
-                                 "kernels (DitStack.forward_host)"}
+                                 "kernels (DitStack.forward_host); the first step's copy-in "
+                                 "is not overlapped"}
 
     # int8 workloads: the same plan and inputs with the bf16 weight scratch
     # bound (weights expanded ahead of the GEMMs instead of converted in
@@ -489,20 +602,11 @@ def run_ours(args, rank, world, local_rank):
                           device=dev_name)
         stack.plan.bind_weight_scratch(buf)
         for _ in range(2):
-            stack.forward(x, dev, stream, qk=dqk, lora=dls)
+            step()
         stack.check(stream)
-        barrier()
-        torch.cuda.synchronize()
-        a0 = torch.cuda.Event(enable_timing=True)
-        a1 = torch.cuda.Event(enable_timing=True)
-        a0.record(stream)
-        for _ in range(args.steps):
-            stack.forward(x, dev, stream, qk=dqk, lora=dls)
-        a1.record(stream)
-        torch.cuda.synchronize()
-        barrier()
+        per_alt, ms_alt = timed_steps(args.steps, step)
         stack.check(stream)
-        ms_alt = max_over_ranks(a0.elapsed_time(a1), world, dev_name) / args.steps
+        ms_alt = max_over_ranks(ms_alt, world, dev_name) / args.steps
         stack.plan.bind_weight_scratch(None)
         del buf
         tf_alt = flops_step / (ms_alt / 1e3) / 1e12
@@ -511,10 +615,11 @@ def run_ours(args, rank, world, local_rank):
                     "scratch ahead of the GEMMs instead of converted in the GEMM "
                     "main loop; same output bits",
             "ms_per_step": round(ms_alt, 4),
+            "step_ms": step_stats(per_alt),
             "value": round(replica_throughput(tokens_per_step, world, ms_alt), 1),
             "unit": "block-tokens/s",
             "tflops": round(tf_alt, 2),
-            "tensor_peak_frac": round(tf_alt / peaks["bf16_tflops_sustained"], 4),
+            "tensor_peak_frac": round(tf_alt / tpeak, 4),
             "scratch_gib": round(stack.plan.weight_scratch_bytes() / 2**30, 4)}
 
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -538,9 +643,14 @@ def run_reference(args):
     if args.lora:
         loras = [synth.make_lora(cfg["D"], cfg["F"], args.lora, seed=i)
                  for i in range(cfg["blocks"])]
-    value, per_step, sample, times = cpu_sample(cfg, inp, args.cpu_rows,
-                                                steps=args.steps,
-                                                warmup=args.warmup, qk=qk, loras=loras)
+    if args.oracle == "full":
+        value, per_step, sample, times = cpu_full(cfg, inp, steps=args.steps,
+                                                  warmup=args.warmup)
+    else:
+        value, per_step, sample, times = cpu_sample(cfg, inp, args.cpu_rows,
+                                                    steps=args.steps,
+                                                    warmup=args.warmup, qk=qk,
+                                                    loras=loras)
     T = cfg["T"]
     return {
         "impl": "reference",
@@ -559,8 +669,9 @@ def run_reference(args):
                                     f"q/k rmsnorm + {args.qk} rotary"),
                    "lora_rank": args.lora or None},
         "cpu_baseline": {"value": round(value, 3), "unit": "block-tokens/s",
-                         "cores": cpu_cores(), "kind": "oracle",
-                         "sample": sample},
+                         "cores": args.cpu_threads or cpu_cores(), "kind": "oracle",
+                         "sample": sample,
+                         "seconds_per_step": step_stats(times)},
         "e2e": {"value": round(value, 3), "unit": "block-tokens/s",
                 "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -568,6 +679,9 @@ def run_reference(args):
 
 def main(argv=None):
     args = parse_args(argv)
+    if args.cpu_threads:  # before numpy's BLAS starts its thread pool
+        for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+            os.environ[var] = str(args.cpu_threads)
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))

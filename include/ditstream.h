@@ -350,15 +350,21 @@ DIT_API dit_status_t dit_block_forward_ex(const dit_plan_t *plan, float *x,
  *   - Plans whose dit_block_workspace_bytes exceeds that size are rejected
  *     with DIT_ERR_WORKSPACE_TOO_SMALL before anything is launched.
  *   - The first call on a device sets up the scratch address for that
- *     device (with that device current); make that first call before any
- *     stream capture.
+ *     device (with that device current) and clears the scratch's header;
+ *     make that first call before any stream capture.  Under lazy module
+ *     loading (the CUDA default) the driver reserves the 64 MiB array on
+ *     that first call, so the device's free memory drops by that much then;
+ *     later calls reserve nothing.
  *   - All calls share one scratch, which keeps the last call's contents:
  *     calls whose work overlaps on the GPU (concurrent streams, several
- *     host threads) race and give wrong results.  Serialise them.
- *   - The scratch's header (status word, attention hand-off flags) is
- *     cleared at the start of each call; a bounded device wait that runs
- *     out is recorded there but not reported (dit_block_sync_status reads
- *     the plan's bound workspace only).
+ *     host threads) race and give wrong results.  Serialise them.  The plan
+ *     is only read: ordinary calls on the same plan (with its own bound
+ *     workspace) do not interfere with static ones.
+ *   - Each call clears the scratch's hand-off flags; its status word is
+ *     kept.  A bounded device wait that runs out in a static call is
+ *     recorded there and reported (and cleared) by the next
+ *     dit_block_sync_status on that device, for any plan.
+ *   - No per-kernel timing is recorded, whatever the plan's profiling flag.
  *   - Calls no cudaMalloc/cudaFree or any other allocating routine.
  * Errors: as dit_block_forward, plus DIT_ERR_WORKSPACE_TOO_SMALL and
  * DIT_ERR_UNSUPPORTED_ARCH. */
@@ -370,7 +376,10 @@ DIT_API dit_status_t dit_block_forward_static(const dit_plan_t *plan, float *x,
 
 /* Synchronise `stream`, read and clear the plan's device status word (after
  * a failure also the attention hand-off flags, which a launch that gave up
- * may have left set).  Returns DIT_OK, DIT_ERR_TIMEOUT or DIT_ERR_CUDA. */
+ * may have left set).  Once a dit_block_forward_static call has set up the
+ * current device, the static scratch's status word is read and cleared the
+ * same way, so a wait that ran out in any static call on this device is
+ * reported here.  Returns DIT_OK, DIT_ERR_TIMEOUT or DIT_ERR_CUDA. */
 DIT_API dit_status_t dit_block_sync_status(const dit_plan_t *plan, dit_stream_t stream);
 
 /* Final layer (output head), fp32 arithmetic, unsliced:

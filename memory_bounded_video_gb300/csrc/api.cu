@@ -119,10 +119,10 @@ bool gemm_split_on() {
 }
 
 // Launch `fn` (returning a dit_status_t) bracketed by profiling events when
-// the plan has profiling enabled.
+// a plan is given and has profiling enabled.
 template <class Fn>
 dit_status_t timed(dit_plan *p, cudaStream_t st, int kind, double work, Fn &&fn) {
-    if (!p->prof) return fn();
+    if (!p || !p->prof) return fn();
     cudaEvent_t ev[2];
     for (int i = 0; i < 2; ++i) {
         if (p->pool_used == p->pool.size()) {
@@ -501,12 +501,20 @@ dit_status_t dit_block_forward_qk(const dit_plan_t *cp, float *x, const dit_bloc
     return dit_block_forward_ex(cp, x, w, mod, qk, nullptr, stream);
 }
 
-dit_status_t dit_block_forward_ex(const dit_plan_t *cp, float *x, const dit_block_weights_t *w,
-                                  const float *mod, const dit_qk_t *qk,
-                                  const dit_block_lora_t *lora, dit_stream_t stream) {
-    // the plan is logically const; only its profiling record changes
-    dit_plan *p = const_cast<dit_plan *>(cp);
-    if (!p || !x || !w || !mod) return DIT_ERR_INVALID_ARG;
+}  // extern "C"
+
+namespace ds {
+
+// The block schedule over the scratch at `ws` (the plan's bound workspace,
+// or the library's static scratch), with per-kernel timing recorded in the
+// plan only when `prof` is set; the plan itself is not modified otherwise.
+dit_status_t block_forward(const dit_plan *cp, uint8_t *ws, bool prof, float *x,
+                           const dit_block_weights_t *w, const float *mod, const dit_qk_t *qk,
+                           const dit_block_lora_t *lora, dit_stream_t stream) {
+    if (!cp || !x || !w || !mod) return DIT_ERR_INVALID_ARG;
+    const dit_plan *p = cp;
+    // the timing record is the one part of the plan a forward may change
+    dit_plan *tp = prof ? const_cast<dit_plan *>(cp) : nullptr;
     if (qk) {
         if (!qk->rope_cos != !qk->rope_sin) return DIT_ERR_INVALID_ARG;
         if ((qk->q_norm || qk->k_norm) && !(qk->eps > 0.0f)) return DIT_ERR_INVALID_ARG;
@@ -523,7 +531,7 @@ dit_status_t dit_block_forward_ex(const dit_plan_t *cp, float *x, const dit_bloc
             if (!aligned16(l->a) || !aligned16(l->b)) return DIT_ERR_ALIGN;
         }
     }
-    if (!p->ws || (p->kvb && !p->kv_host)) return DIT_ERR_NO_WORKSPACE;
+    if (!ws || (p->kvb && !p->kv_host)) return DIT_ERR_NO_WORKSPACE;
     if (!w->wqkv || !w->wo || !w->wgate || !w->wup || !w->wdown) return DIT_ERR_INVALID_ARG;
     if (!aligned16(x) || !aligned16(mod) || !aligned16(w->wqkv) || !aligned16(w->wo) ||
         !aligned16(w->wgate) || !aligned16(w->wup) || !aligned16(w->wdown))
@@ -548,35 +556,35 @@ dit_status_t dit_block_forward_ex(const dit_plan_t *cp, float *x, const dit_bloc
     const int64_t T = p->T;
     const int D = p->D, F = p->F;
     const int64_t Dl = D;
-    int *status = reinterpret_cast<int *>(p->ws);
+    int *status = reinterpret_cast<int *>(ws);
     // the GEMMs' hand-off space for split tiles (flags shared with the
     // attention's: every launch leaves the flags it used zero)
-    const AttnSplit gsplit{reinterpret_cast<int *>(p->ws + kFlagsOffset),
-                           reinterpret_cast<float *>(p->ws + p->off_gsplit),
+    const AttnSplit gsplit{reinterpret_cast<int *>(ws + kFlagsOffset),
+                           reinterpret_cast<float *>(ws + p->off_gsplit),
                            gemm_split_on() ? p->gsplit_slots : 0, 0};
     // K [T, D] and V^T [D, T_pad]: in the workspace, or (offload) in the
     // host buffer, written there by pass one through its device mapping
-    void *K = p->kvb ? static_cast<void *>(p->kv_host) : static_cast<void *>(p->ws + p->off_k);
+    void *K = p->kvb ? static_cast<void *>(p->kv_host) : static_cast<void *>(ws + p->off_k);
     void *Vt = p->kvb ? static_cast<void *>(p->kv_host + 2 * size_t(T) * size_t(D))
-                      : static_cast<void *>(p->ws + p->off_vt);
-    void *a = p->ws + p->off_a;
-    void *Q = p->ws + p->off_q;
-    void *b = p->ws + p->off_b;
-    void *h = p->ws + p->off_h;
-    float *acc = reinterpret_cast<float *>(p->ws + p->off_acc);
-    void *u_q = p->ws + p->off_uq;
-    void *u_o = p->ws + p->off_uo;
-    void *u_g = p->ws + p->off_ug;
-    void *u_u = p->ws + p->off_uu;
-    void *u_d = p->ws + p->off_ud;
-    float *u_dc = reinterpret_cast<float *>(p->ws + p->off_udc);
+                      : static_cast<void *>(ws + p->off_vt);
+    void *a = ws + p->off_a;
+    void *Q = ws + p->off_q;
+    void *b = ws + p->off_b;
+    void *h = ws + p->off_h;
+    float *acc = reinterpret_cast<float *>(ws + p->off_acc);
+    void *u_q = ws + p->off_uq;
+    void *u_o = ws + p->off_uo;
+    void *u_g = ws + p->off_ug;
+    void *u_u = ws + p->off_uu;
+    void *u_d = ws + p->off_ud;
+    float *u_dc = reinterpret_cast<float *>(ws + p->off_udc);
     const float *shift1 = mod, *scale1 = mod + Dl, *gate1 = mod + 2 * Dl;
     const float *shift2 = mod + 3 * Dl, *scale2 = mod + 4 * Dl, *gate2 = mod + 5 * Dl;
     const uint8_t *wqkv = static_cast<const uint8_t *>(w->wqkv);
     const void *wo_m = w->wo;
     dit_status_t r;
     auto expand_into = [&](const void *q, int64_t n, uint8_t *dst) -> dit_status_t {
-        return timed(p, st, DIT_K_EXPAND, 3.0 * n,
+        return timed(tp, st, DIT_K_EXPAND, 3.0 * n,
                      [&] { return launch_expand_int8(q, n, dst, st); });
     };
     if (expand) {  // attention-phase weights: Wqkv [3D, D], Wo [D, D]
@@ -623,7 +631,7 @@ dit_status_t dit_block_forward_ex(const dit_plan_t *cp, float *x, const dit_bloc
             g.acc_load = load;
             g.acc_final = 0;
         }
-        return timed(p, st, DIT_K_LORA_U, 2.0 * rows * l.rank * K_,
+        return timed(tp, st, DIT_K_LORA_U, 2.0 * rows * l.rank * K_,
                      [&] { return launch_gemm(g, status, st, &gsplit); });
     };
     // LoRA K-steps of a GEMM: u [rows, rank] and rows row0.. of the prepared B
@@ -664,7 +672,7 @@ dit_status_t dit_block_forward_ex(const dit_plan_t *cp, float *x, const dit_bloc
     const int64_t n_kb = kvb ? (T + kvb - 1) / kvb : 0;
     const int64_t n_total = kvb ? n_kb * ((T + p->ca - 1) / p->ca) : 0;
     cudaStream_t cs = p->copy_stream;
-    auto slot_k = [&](int slot) { return p->ws + p->off_ring + size_t(slot) * p->ring_slot; };
+    auto slot_k = [&](int slot) { return ws + p->off_ring + size_t(slot) * p->ring_slot; };
     auto slot_vt = [&](int slot) { return slot_k(slot) + 2 * size_t(kvb) * size_t(D); };
     uint8_t *hK = static_cast<uint8_t *>(K);
     uint8_t *hVt = static_cast<uint8_t *>(Vt);  // offload: V^T blocks [n_kb][D][kvb]
@@ -687,7 +695,7 @@ dit_status_t dit_block_forward_ex(const dit_plan_t *cp, float *x, const dit_bloc
     // pass 1: K and V of every token
     for (int64_t s = 0; s < T; s += p->ca) {
         const int64_t rows = (T - s < p->ca) ? T - s : p->ca;
-        if ((r = timed(p, st, DIT_K_MODLN, 6.0 * rows * D,
+        if ((r = timed(tp, st, DIT_K_MODLN, 6.0 * rows * D,
                        [&] { return launch_modln(x + s * Dl, rows, D, shift1, scale1, a, st); })) !=
             DIT_OK)
             return r;
@@ -736,7 +744,7 @@ dit_status_t dit_block_forward_ex(const dit_plan_t *cp, float *x, const dit_bloc
             if (on(l_qkv))
                 attach(g, 0, static_cast<const uint8_t *>(u_q) + 2 * (t0 - s) * l_qkv.rank,
                        l_qkv, Dl);
-            if ((r = timed(p, st, DIT_K_GEMM_KV, 2.0 * sr * 2 * D * D + lflops(l_qkv, sr, 2 * D),
+            if ((r = timed(tp, st, DIT_K_GEMM_KV, 2.0 * sr * 2 * D * D + lflops(l_qkv, sr, 2 * D),
                            [&] { return launch_gemm(g, status, st, &gsplit); })) != DIT_OK)
                 return r;
             if (kvb && (t1 % kvb == 0 || t1 == T)) {  // block b complete
@@ -756,8 +764,8 @@ dit_status_t dit_block_forward_ex(const dit_plan_t *cp, float *x, const dit_bloc
         }
     }
     // the attention's hand-off space for split units
-    const AttnSplit split{reinterpret_cast<int *>(p->ws + kFlagsOffset),
-                          reinterpret_cast<float *>(p->ws + p->off_split), p->split_slots, 0};
+    const AttnSplit split{reinterpret_cast<int *>(ws + kFlagsOffset),
+                          reinterpret_cast<float *>(ws + p->off_split), p->split_slots, 0};
     int64_t kv_c = 0;  // blocks of pass two consumed so far
     // pass two's first block; the copy stream is in order, so it follows
     // pass one's copies to the host
@@ -765,7 +773,7 @@ dit_status_t dit_block_forward_ex(const dit_plan_t *cp, float *x, const dit_bloc
     // pass 2: Q per slab, attention against all keys, O-projection into x
     for (int64_t s = 0; s < T; s += p->ca) {
         const int64_t rows = (T - s < p->ca) ? T - s : p->ca;
-        if ((r = timed(p, st, DIT_K_MODLN, 6.0 * rows * D,
+        if ((r = timed(tp, st, DIT_K_MODLN, 6.0 * rows * D,
                        [&] { return launch_modln(x + s * Dl, rows, D, shift1, scale1, a, st); })) !=
             DIT_OK)
             return r;
@@ -787,12 +795,12 @@ dit_status_t dit_block_forward_ex(const dit_plan_t *cp, float *x, const dit_bloc
         g.rope_pos0 = s;  // rotary position of the slab's first token
         set_qk(g, 0);
         if (on(l_qkv)) attach(g, 0, u_q, l_qkv, 0);
-        if ((r = timed(p, st, DIT_K_GEMM_Q, 2.0 * rows * D * D + lflops(l_qkv, rows, D),
+        if ((r = timed(tp, st, DIT_K_GEMM_Q, 2.0 * rows * D * D + lflops(l_qkv, rows, D),
                        [&] { return launch_gemm(g, status, st, &gsplit); })) != DIT_OK)
             return r;
         // O_s overwrites a_s (dead once Q_s exists)
         if (!kvb) {
-            if ((r = timed(p, st, DIT_K_ATTENTION, 4.0 * rows * double(T) * D, [&] {
+            if ((r = timed(tp, st, DIT_K_ATTENTION, 4.0 * rows * double(T) * D, [&] {
                      return launch_attention(Q, rows, D, K, D, Vt, p->t_pad, T, p->heads,
                                              p->head_dim, a, D, status, st, nullptr, &split);
                  })) != DIT_OK)
@@ -804,11 +812,11 @@ dit_status_t dit_block_forward_ex(const dit_plan_t *cp, float *x, const dit_bloc
                 const int64_t kb = (T - b * kvb < kvb) ? T - b * kvb : kvb;
                 cudaError_t e = cudaStreamWaitEvent(st, p->ev_filled[slot], 0);
                 if (e != cudaSuccess) return cuda_fail(e);
-                AttnState as{reinterpret_cast<float *>(p->ws + p->off_ost),
-                             reinterpret_cast<float *>(p->ws + p->off_mst),
-                             reinterpret_cast<float *>(p->ws + p->off_lst), Dl, b == 0,
+                AttnState as{reinterpret_cast<float *>(ws + p->off_ost),
+                             reinterpret_cast<float *>(ws + p->off_mst),
+                             reinterpret_cast<float *>(ws + p->off_lst), Dl, b == 0,
                              b == n_kb - 1};
-                if ((r = timed(p, st, DIT_K_ATTENTION, 4.0 * rows * double(kb) * D, [&] {
+                if ((r = timed(tp, st, DIT_K_ATTENTION, 4.0 * rows * double(kb) * D, [&] {
                          return launch_attention(Q, rows, D, slot_k(slot), D, slot_vt(slot),
                                                  kvb, kb, p->heads, p->head_dim, a, D, status,
                                                  st, &as, &split);
@@ -835,7 +843,7 @@ dit_status_t dit_block_forward_ex(const dit_plan_t *cp, float *x, const dit_bloc
         o.ldx = D;
         o.gate = gate1;
         if (on(l_o)) attach(o, 0, u_o, l_o, 0);
-        if ((r = timed(p, st, DIT_K_GEMM_O, 2.0 * rows * D * D + lflops(l_o, rows, D),
+        if ((r = timed(tp, st, DIT_K_GEMM_O, 2.0 * rows * D * D + lflops(l_o, rows, D),
                        [&] { return launch_gemm(o, status, st, &gsplit); })) != DIT_OK)
             return r;
     }
@@ -856,7 +864,7 @@ dit_status_t dit_block_forward_ex(const dit_plan_t *cp, float *x, const dit_bloc
     }
     for (int64_t c = 0; c < T; c += p->cm) {
         const int64_t rows = (T - c < p->cm) ? T - c : p->cm;
-        if ((r = timed(p, st, DIT_K_MODLN, 6.0 * rows * D,
+        if ((r = timed(tp, st, DIT_K_MODLN, 6.0 * rows * D,
                        [&] { return launch_modln(x + c * Dl, rows, D, shift2, scale2, b, st); })) !=
             DIT_OK)
             return r;
@@ -884,7 +892,7 @@ dit_status_t dit_block_forward_ex(const dit_plan_t *cp, float *x, const dit_bloc
             g.ldo = p->fs;
             if (on(l_g)) attach(g, 0, u_g, l_g, f);
             if (on(l_u)) attach(g, 1, u_u, l_u, f);
-            if ((r = timed(p, st, DIT_K_GEMM_SWIGLU,
+            if ((r = timed(tp, st, DIT_K_GEMM_SWIGLU,
                            4.0 * rows * fw * D + lflops(l_g, rows, fw) + lflops(l_u, rows, fw),
                            [&] { return launch_gemm(g, status, st, &gsplit); })) != DIT_OK)
                 return r;
@@ -912,7 +920,7 @@ dit_status_t dit_block_forward_ex(const dit_plan_t *cp, float *x, const dit_bloc
             d.ldx = D;
             d.gate = gate2;
             if (last && on(l_d)) attach(d, 0, u_d, l_d, 0);
-            if ((r = timed(p, st, DIT_K_GEMM_DOWN,
+            if ((r = timed(tp, st, DIT_K_GEMM_DOWN,
                            2.0 * rows * D * fw + (last ? lflops(l_d, rows, D) : 0.0),
                            [&] { return launch_gemm(d, status, st, &gsplit); })) != DIT_OK)
                 return r;
@@ -921,20 +929,37 @@ dit_status_t dit_block_forward_ex(const dit_plan_t *cp, float *x, const dit_bloc
     return DIT_OK;
 }
 
+}  // namespace ds
+
+extern "C" {
+
+dit_status_t dit_block_forward_ex(const dit_plan_t *p, float *x, const dit_block_weights_t *w,
+                                  const float *mod, const dit_qk_t *qk,
+                                  const dit_block_lora_t *lora, dit_stream_t stream) {
+    if (!p) return DIT_ERR_INVALID_ARG;
+    return block_forward(p, p->ws, p->prof, x, w, mod, qk, lora, stream);
+}
+
 dit_status_t dit_block_sync_status(const dit_plan_t *p, dit_stream_t stream) {
     if (!p) return DIT_ERR_INVALID_ARG;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     cudaError_t e = cudaStreamSynchronize(st);
     if (e != cudaSuccess) return cuda_fail(e);
-    if (!p->ws) return DIT_OK;
+    // the plan's workspace header, and the static scratch's when a static
+    // forward has set up the current device (shared by every static call)
     int v = 0;
-    e = cudaMemcpyAsync(&v, p->ws, sizeof(int), cudaMemcpyDeviceToHost, st);
-    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
-    // after a failure the hand-off flags may be left set: clear them with
-    // the status word
-    if (e == cudaSuccess && v != 0) e = cudaMemsetAsync(p->ws, 0, kHeaderBytes, st);
-    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
-    if (e != cudaSuccess) return cuda_fail(e);
+    for (uint8_t *hdr : {p->ws, reinterpret_cast<uint8_t *>(static_status_word())}) {
+        if (!hdr) continue;
+        int s = 0;
+        e = cudaMemcpyAsync(&s, hdr, sizeof(int), cudaMemcpyDeviceToHost, st);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+        // after a failure the hand-off flags may be left set: clear them with
+        // the status word
+        if (e == cudaSuccess && s != 0) e = cudaMemsetAsync(hdr, 0, kHeaderBytes, st);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+        if (e != cudaSuccess) return cuda_fail(e);
+        if (v == 0) v = s;
+    }
     return v == 0 ? DIT_OK : (v == DIT_ERR_TIMEOUT ? DIT_ERR_TIMEOUT : DIT_ERR_CUDA);
 }
 

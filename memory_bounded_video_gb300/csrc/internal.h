@@ -127,6 +127,17 @@ dit_status_t launch_final(const float *x, int64_t T, int D, const void *wf,
 // bf16 copy of n int8 values (exact); n % 16 == 0, both 16-byte aligned.
 dit_status_t launch_expand_int8(const void *q, int64_t n, void *out, cudaStream_t s);
 
+// The block forward over the scratch at `ws` (a bound workspace or the
+// static scratch); per-kernel timing goes to the plan's record only when
+// `prof` is set, and the plan is not otherwise modified.
+dit_status_t block_forward(const dit_plan *p, uint8_t *ws, bool prof, float *x,
+                           const dit_block_weights_t *w, const float *mod, const dit_qk_t *qk,
+                           const dit_block_lora_t *lora, dit_stream_t stream);
+
+// Device address of the static scratch's status word on the current device,
+// or null when no static forward has set that device up yet.
+int *static_status_word();
+
 inline bool aligned16(const void *p) {
     return (reinterpret_cast<uintptr_t>(p) & 15u) == 0;
 }

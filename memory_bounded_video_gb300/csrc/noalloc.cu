@@ -8,20 +8,62 @@
 // dit_block_forward, but its scratch (the plan's workspace: K/V of all tokens
 // plus the chunk-sized slabs) is a file-scope device array of fixed size
 // instead of caller-bound memory.
+#include <atomic>
+#include <mutex>
+
 #include "internal.h"
 
 namespace {
 
 constexpr size_t kStaticScratchBytes = size_t(64) << 20;  // 64 MiB
+static_assert(kStaticScratchBytes == DIT_STATIC_SCRATCH_BYTES, "header and library agree");
 
 // Device scratch shared by every call in the process; every device that
 // loads this module holds it until the process exits.
 static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
 
 constexpr int kMaxDevices = 64;
-void *g_scratch_addr[kMaxDevices] = {};  // device address, per device
+// Device address of g_static_scratch per device (null until set up).
+std::atomic<void *> g_scratch_addr[kMaxDevices];
+std::mutex g_setup_mu;
+
+// Address of the scratch on device `dev` (current), setting it up on first
+// use: the symbol's host-side name is not a device address, so the runtime
+// is asked for it, and the header (status word and hand-off flags) is
+// cleared on `st`.
+dit_status_t scratch_for(int dev, cudaStream_t st, uint8_t **out) {
+    void *ptr = g_scratch_addr[dev].load(std::memory_order_acquire);
+    if (!ptr) {
+        std::lock_guard<std::mutex> lock(g_setup_mu);
+        ptr = g_scratch_addr[dev].load(std::memory_order_relaxed);
+        if (!ptr) {
+            int major = 0, minor = 0;
+            cudaError_t e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+            if (e == cudaSuccess)
+                e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+            if (e != cudaSuccess) return ds::cuda_fail(e);
+            if (major != 10 || minor != 3) return DIT_ERR_UNSUPPORTED_ARCH;
+            e = cudaGetSymbolAddress(&ptr, g_static_scratch);
+            if (e == cudaSuccess) e = cudaMemsetAsync(ptr, 0, ds::kHeaderBytes, st);
+            if (e != cudaSuccess) return ds::cuda_fail(e);
+            g_scratch_addr[dev].store(ptr, std::memory_order_release);
+        }
+    }
+    *out = static_cast<uint8_t *>(ptr);
+    return DIT_OK;
+}
 
 }  // namespace
+
+namespace ds {
+
+int *static_status_word() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    return static_cast<int *>(g_scratch_addr[dev].load(std::memory_order_acquire));
+}
+
+}  // namespace ds
 
 extern "C" dit_status_t dit_block_forward_static(const dit_plan_t *plan, float *x,
                                                  const dit_block_weights_t *w,
@@ -33,39 +75,15 @@ extern "C" dit_status_t dit_block_forward_static(const dit_plan_t *plan, float *
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return ds::cuda_fail(e);
     if (dev < 0 || dev >= kMaxDevices) return DIT_ERR_INVALID_ARG;
-    if (!g_scratch_addr[dev]) {
-        // Set-up, once per device, with that device current: the symbol's
-        // host-side name is not a device address; ask the runtime for it.
-        int major = 0, minor = 0;
-        e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
-        if (e == cudaSuccess)
-            e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
-        if (e != cudaSuccess) return ds::cuda_fail(e);
-        if (major != 10 || minor != 3) return DIT_ERR_UNSUPPORTED_ARCH;
-        void *ptr = nullptr;
-        e = cudaGetSymbolAddress(&ptr, g_static_scratch);
-        if (e != cudaSuccess) return ds::cuda_fail(e);
-        g_scratch_addr[dev] = ptr;
-    }
-    uint8_t *scratch = static_cast<uint8_t *>(g_scratch_addr[dev]);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    // Only the header (the status word and the attention's hand-off flags)
-    // must start at zero: every other region is written before it is read
-    // within one forward.
-    e = cudaMemsetAsync(scratch, 0, ds::kHeaderBytes, st);
+    uint8_t *scratch = nullptr;
+    dit_status_t r = scratch_for(dev, st, &scratch);
+    if (r != DIT_OK) return r;
+    // The hand-off flags must start at zero (a launch that gave up may have
+    // left some set); every other region is written before it is read within
+    // one forward.  The status word is kept, so that a wait that ran out in
+    // an earlier call stays visible to dit_block_sync_status.
+    e = cudaMemsetAsync(scratch + ds::kFlagsOffset, 0, ds::kHeaderBytes - ds::kFlagsOffset, st);
     if (e != cudaSuccess) return ds::cuda_fail(e);
-    // Run the ordinary schedule with the plan pointed at the static scratch
-    // for the duration of the (host-side, asynchronous) enqueue.
-    dit_plan *p = const_cast<dit_plan *>(plan);
-    uint8_t *saved_ws = p->ws;
-    const size_t saved_bytes = p->ws_bytes;
-    const bool saved_prof = p->prof;
-    p->ws = scratch;
-    p->ws_bytes = kStaticScratchBytes;
-    p->prof = false;
-    const dit_status_t r = dit_block_forward(p, x, w, modulation, stream);
-    p->ws = saved_ws;
-    p->ws_bytes = saved_bytes;
-    p->prof = saved_prof;
-    return r;
+    return ds::block_forward(plan, scratch, false, x, w, modulation, nullptr, nullptr, stream);
 }

@@ -94,6 +94,7 @@ def test_status_strings(lib):
 @pytest.mark.parametrize("args,status", [
     ((0, 256, 4, 704, 128, 128), ds.ERR_INVALID_ARG),       # T = 0
     ((512, 250, 4, 704, 128, 128), ds.ERR_INVALID_ARG),     # D % 128
+    ((512, 320, 5, 704, 128, 128), ds.ERR_INVALID_ARG),     # D % 128 with d = 64
     ((512, 256, 3, 704, 128, 128), ds.ERR_INVALID_ARG),     # D % heads
     ((512, 256, 8, 704, 128, 128), ds.ERR_INVALID_ARG),     # d = 32
     ((512, 256, 4, 700, 128, 128), ds.ERR_INVALID_ARG),     # ffn % 64

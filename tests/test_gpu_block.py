@@ -185,3 +185,40 @@ def test_auto_planned_chunks_give_the_same_bits():
     plan.forward(x, dev.blocks[0].struct, dev.blocks[0].mod)
     assert plan.sync_status() == ds.OK
     assert torch.equal(x, x_ref)
+
+
+_AUTO_REF = {}
+
+
+def _auto_ref(inp):
+    """Float64 oracle output of the seed-6 T=4096 block (computed once)."""
+    if "x" not in _AUTO_REF:
+        _AUTO_REF["x"] = ob.dit_block(inp.x.double().numpy(), weights64(inp.blocks[0]),
+                                      inp.mods[0].double().numpy(), inp.meta["heads"])
+    return _AUTO_REF["x"]
+
+
+@pytest.mark.parametrize("budget_mib,sliced", [(19, False), (24, True), (30, False),
+                                               (40, True), (60, False)])
+def test_auto_planned_forward_matches_oracle(budget_mib, sliced):
+    # "Proposal: Generic memory-aware streaming execution for transformer
+    # models" (Automatic chunk sizing): the chosen chunks are the one new
+    # thing on this path, so the auto-planned forward is checked against the
+    # float64 oracle under budgets that pick different chunks, with and
+    # without FFN feature slicing (ragged chunks included: T = 4096 is not a
+    # multiple of 896, 1408 or 2688)
+    inp = synth.make_workload("dit_T4096_D1024", seed=6)
+    T, D = inp.x.shape
+    budget = budget_mib * 2**20
+    plan = ds.block_plan_auto(T, D, 16, 2816, budget)
+    info = plan.info()
+    assert plan.workspace_bytes() <= budget
+    assert (info["ffn_slice"] < 2816) == sliced, info
+    dev = runner.upload(inp)
+    ws = torch.empty(plan.workspace_bytes(), dtype=torch.uint8, device="cuda")
+    plan.bind_workspace(ws)
+    x = dev.x.clone()
+    plan.forward(x, dev.blocks[0].struct, dev.blocks[0].mod)
+    assert plan.sync_status() == ds.OK
+    rel, mx, br = compare(x.cpu().numpy(), _auto_ref(inp), inp.x.double().numpy())
+    assert rel <= REL_L2 and mx <= MAX_ABS and br <= BRANCH_REL_L2, (info, rel, mx, br)
