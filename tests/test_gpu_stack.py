@@ -263,3 +263,27 @@ def test_forward_host_pipeline_matches_per_batch_forwards(final):
             assert torch.equal(oh.view(torch.int32), ref.view(torch.int32))
         for o in outs:
             o.fill_(float("nan"))
+
+
+def test_final_layer_rows_with_large_offsets():
+    # rows with a large common offset and rows of very different spread: the
+    # head's statistics come from sums of the row shifted by its first
+    # element, which must hold its accuracy when the offset dwarfs the spread
+    T, D = 777, 1024
+    g = torch.Generator().manual_seed(11)
+    x = torch.randn(T, D, generator=g)
+    x *= torch.exp(torch.randn(T, 1, generator=g))          # spread 0.1 .. 10
+    x += torch.randn(T, 1, generator=g) * 100.0             # offsets ~ 100
+    x[5] += 1.0e4
+    wf = (torch.randn(64, D, generator=g) * 0.02).float()
+    mod = (torch.randn(2, D, generator=g) * 0.1).float()
+    plan = ds.block_plan(T, D, 8, 704, 0, 0)
+    out = torch.full((T, 64), float("nan"), device="cuda")
+    plan.final_forward(x.cuda(), wf.cuda(), None, mod.cuda(), out)
+    torch.cuda.synchronize()
+    ref = ob.final_layer(x.double().numpy(), wf.double().numpy(), mod.double().numpy())
+    got = out.cpu().double().numpy()
+    # the same fp32 bound as the plain rows (after LN every row's output is
+    # of the same size, whatever its offset and spread)
+    assert np.isfinite(got).all()
+    assert np.abs(got - ref).max() <= 1e-4 * np.abs(ref).max()
