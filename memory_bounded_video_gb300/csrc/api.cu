@@ -971,7 +971,8 @@ dit_status_t dit_final_forward(const dit_plan_t *cp, const float *x, const void 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const double bytes = 4.0 * double(p->T) * p->D + 4.0 * 64 * p->D + 4.0 * 64 * double(p->T);
     return timed(p, st, DIT_K_FINAL, bytes, [&] {
-        return launch_final(x, p->T, p->D, wf, wf_scale, mod_f, out, st);
+        return launch_final(x, p->T, p->D, wf, wf_scale, mod_f, out,
+                            p->ws ? reinterpret_cast<int *>(p->ws) : nullptr, st);
     });
 }
 

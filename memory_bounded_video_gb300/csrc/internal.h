@@ -120,9 +120,11 @@ dit_status_t launch_attention(const void *q, int64_t Tq, int64_t ldq, const void
                               const AttnState *state = nullptr,
                               const AttnSplit *split = nullptr);
 
+// dev_status: where a bounded wait that ran out records DIT_ERR_TIMEOUT (may
+// be null).
 dit_status_t launch_final(const float *x, int64_t T, int D, const void *wf,
                           const float *wf_scale, const float *mod_f, float *out,
-                          cudaStream_t s);
+                          int *dev_status, cudaStream_t s);
 
 // bf16 copy of n int8 values (exact); n % 16 == 0, both 16-byte aligned.
 dit_status_t launch_expand_int8(const void *q, int64_t n, void *out, cudaStream_t s);

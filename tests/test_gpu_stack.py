@@ -81,8 +81,9 @@ def test_final_layer_matches_oracle(int8):
     torch.cuda.synchronize()
     ref = ob.final_layer(inp.x.double().numpy(), final64(inp), inp.mod_f.double().numpy())
     got = out.cpu().double().numpy()
-    # fp32 arithmetic over D terms
-    assert np.abs(got - ref).max() <= 1e-4 * max(1.0, np.abs(ref).max())
+    # fp32-level arithmetic over D terms (an fp32 FMA loop and the split
+    # tf32 tensor-core products with fp32 partial sums both land near 2e-6)
+    assert np.abs(got - ref).max() <= 1e-5 * max(1.0, np.abs(ref).max())
 
 
 def test_final_layer_rows_are_independent_of_T():
@@ -286,4 +287,4 @@ def test_final_layer_rows_with_large_offsets():
     # the same fp32 bound as the plain rows (after LN every row's output is
     # of the same size, whatever its offset and spread)
     assert np.isfinite(got).all()
-    assert np.abs(got - ref).max() <= 1e-4 * np.abs(ref).max()
+    assert np.abs(got - ref).max() <= 1e-5 * np.abs(ref).max()
