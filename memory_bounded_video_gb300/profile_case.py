@@ -5,7 +5,7 @@
     python -m memory_bounded_video_gb300.profile_case attention --Tq 2048 \\
         --T 8192 --heads 4 --head-dim 128 --reps 3 [--no-split]
     python -m memory_bounded_video_gb300.profile_case modln --M 8192 --D 3072
-    python -m memory_bounded_video_gb300.profile_case final --M 8192 --D 3072
+    python -m memory_bounded_video_gb300.profile_case final --M 8192 --D 3072 [--int8]
     python -m memory_bounded_video_gb300.profile_case expand --M 8192 --D 3072
 
 ``gemm --scaled`` runs the bf16 main loop on int8 values with per-row scales
@@ -103,12 +103,17 @@ def modln_case(a):
 
 def final_case(a):
     x = torch.randn(a.M, a.D, device="cuda")
-    wf = torch.randn(64, a.D, device="cuda") * 0.02
+    if a.int8:  # int8 W_f with one fp32 scale per output row
+        wf = torch.randint(-127, 128, (64, a.D), device="cuda", dtype=torch.int8)
+        ws = torch.full((64,), 0.02 / 127, device="cuda")
+    else:
+        wf = torch.randn(64, a.D, device="cuda") * 0.02
+        ws = None
     mod_f = torch.randn(2, a.D, device="cuda") * 0.1
     out = torch.empty(a.M, 64, device="cuda")
     plan = ds.block_plan(a.M, a.D, a.D // 128, 128, 0, 0)
-    keep = (x, wf, mod_f, out, plan)
-    return (lambda: plan.final_forward(x, wf, None, mod_f, out)), 4 * a.M * a.D, keep
+    keep = (x, wf, ws, mod_f, out, plan)
+    return (lambda: plan.final_forward(x, wf, ws, mod_f, out)), 4 * a.M * a.D, keep
 
 
 def expand_case(a):
