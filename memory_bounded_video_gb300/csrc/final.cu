@@ -22,24 +22,24 @@
 // tensor memory by two tcgen05.mma.kind::tf32 per k step: hi_z [W'hi; W'lo]
 // (N = 128: hi_z W'hi and hi_z W'lo side by side) and lo_z W'hi (N = 64,
 // onto hi_z W'hi); the dropped lo_z W'lo term is below 2^-22 of each
-// product.  The tensor
-// memory accumulator only ever holds a partial sum over 128 values of k: the
-// partials are added in fp32 registers, round-to-nearest, so the long sum
-// over D is not left to the accumulator (accumulating all of D there
-// measured 25 times the error of an fp32 FMA loop against the float64
-// oracle).  Statistics, modulation, the final combination and the output
-// are fp32 CUDA-core work.
+// product.  The tensor-memory accumulator only ever holds a partial sum over
+// 128 values of k: the partials are added in fp32 registers, round-to-
+// nearest, so the long sum over D is not left to the accumulator
+// (accumulating all of D there measured 25 times the error of an fp32 FMA
+// loop against the float64 oracle).  Statistics, modulation, the final
+// combination and the output are fp32 CUDA-core work.
 //
 // Persistent CTAs, one per SM, over 128-row tiles (the MMA's M = 128, N = 64
 // outputs).  Warps 0..7 stage: per 32-wide k chunk they copy their pieces of
 // x and W_f from global memory into a raw shared-memory ring (cp.async, two
-// chunks ahead), read them back, shift, gather the row
-// sums, modulate, split and store the four operand tiles of a shared-memory
-// ring stage in the 128-byte-swizzle K-major layout; warps 8..11 (one
-// accumulator row per thread, 168 registers each like the stagers) add each
-// finished partial from tensor memory (two 64-column buffers, owned by warp
-// 8) into registers and, after a tile's last partial, combine and write
-// out; warp 8's lane 0 also issues the MMAs.
+// chunks ahead), read them back, shift, gather the row sums, modulate, split
+// and store the four operand tiles of a shared-memory ring stage in the
+// 128-byte-swizzle K-major layout.  Warps 8..11 (one accumulator row per
+// thread) add each finished partial from tensor memory (two 128-column
+// buffers, allocated by warp 8) into registers and, after a tile's last
+// partial, combine and write out; warp 8's lane 0 also issues the MMAs.
+// Twelve warps (three per SM sub-partition) leave each thread up to 168
+// registers; a thirteenth warp for the MMAs would cap every thread at 128.
 #include "internal.h"
 #include "ptx.cuh"
 
