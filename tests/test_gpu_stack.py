@@ -288,3 +288,24 @@ def test_final_layer_rows_with_large_offsets():
     # of the same size, whatever its offset and spread)
     assert np.isfinite(got).all()
     assert np.abs(got - ref).max() <= 1e-5 * np.abs(ref).max()
+
+
+@pytest.mark.parametrize("int8", [False, True])
+def test_final_layer_several_tiles_per_cta(int8):
+    # more 128-row tiles than multiprocessors (every CTA of the persistent
+    # grid runs two or three tiles, the last one ragged), against the full
+    # oracle: the tile loop's hand-over of the statistics and the
+    # tensor-memory partial-sum buffers from one tile to the next
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    T, D = 128 * (2 * sms + 5) + 77, 512
+    inp = synth.make_inputs(T, D, 4, 704, seed=21, int8=int8, final=True, jitter=True,
+                            blocks=0)
+    dev = runner.upload(inp)
+    plan = ds.block_plan(T, D, 4, 704, 0, 0)
+    out = torch.full((T, 64), float("nan"), device="cuda")
+    plan.final_forward(dev.x, dev.wf, dev.wf_scale, dev.mod_f, out)
+    torch.cuda.synchronize()
+    ref = ob.final_layer(inp.x.double().numpy(), final64(inp), inp.mod_f.double().numpy())
+    got = out.cpu().double().numpy()
+    assert np.isfinite(got).all()
+    assert np.abs(got - ref).max() <= 1e-5 * max(1.0, np.abs(ref).max())
