@@ -451,3 +451,25 @@ def test_plan_auto_slices_the_ffn_only_when_needed(lib):
     if info["ffn_slice"] < F:
         unsliced = ds.block_plan(T, D, H, F, info["mlp_chunk"], info["attn_chunk"])
         assert unsliced.workspace_bytes() > attn_4096
+
+
+def test_final_forward_validates_before_launch(lib):
+    # argument and alignment errors come back before any CUDA call (the
+    # pointers below are never dereferenced)
+    h = ctypes.c_void_p()
+    assert lib.dit_block_plan(1000, 256, 4, 704, 0, 0, ctypes.byref(h)) == ds.OK
+    try:
+        ok_ptr = ctypes.c_void_p(0x10000)
+        bad_ptr = ctypes.c_void_p(0x10004)  # not 16-byte aligned
+        assert lib.dit_final_forward(None, ok_ptr, ok_ptr, None, ok_ptr, ok_ptr,
+                                     None) == ds.ERR_INVALID_ARG
+        for i in range(4):  # x, wf, mod_f, out missing in turn
+            args = [ok_ptr, ok_ptr, None, ok_ptr, ok_ptr]
+            args[[0, 1, 3, 4][i]] = None
+            assert lib.dit_final_forward(h, *args, None) == ds.ERR_INVALID_ARG
+        for i in range(4):  # x, wf, mod_f, out misaligned in turn
+            args = [ok_ptr, ok_ptr, None, ok_ptr, ok_ptr]
+            args[[0, 1, 3, 4][i]] = bad_ptr
+            assert lib.dit_final_forward(h, *args, None) == ds.ERR_ALIGN
+    finally:
+        lib.dit_block_plan_destroy(h)
