@@ -164,6 +164,31 @@ def test_headline_stack_T32768_full_size():
         assert torch.equal(out, results[0][1])
 
 
+def test_headline_stack_chunk_sweep_T32768_is_bit_identical():
+    """The 32k int8 stack's chunk sweep: mlp and attention chunks of every
+    power of two from 256 to 32768 tokens (and two unequal pairs) give the
+    same residual and final-layer bits."""
+    name = "dit4_int8_final_T32768_D3072"
+    inp = synth.make_workload(name, seed=1)
+    T, D = inp.x.shape
+    dev = runner.upload(inp)
+    stream = torch.cuda.current_stream()
+    ref = None
+    for cm, ca in [(c, c) for c in (256, 512, 1024, 2048, 4096, 8192, 16384, 32768)] + \
+                  [(256, 32768), (32768, 512)]:
+        st = runner.DitStack(T, D, 24, 8192, cm, ca)
+        x = dev.x.clone()
+        out = st.forward(x, dev, stream)
+        st.check()
+        if ref is None:
+            assert torch.isfinite(out).all()
+            ref = (x, out)
+        else:
+            assert torch.equal(x, ref[0]), (cm, ca)
+            assert torch.equal(out, ref[1]), (cm, ca)
+        del st
+
+
 # ---------------------------------------------------------------- weight scratch
 
 def test_int8_to_bf16_is_exact():
