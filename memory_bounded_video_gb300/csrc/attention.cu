@@ -23,12 +23,13 @@
 //                 tensor core works on one tile while the other's softmax runs
 //   warps 4..7    softmax of tile A, one query row per thread
 //   warps 8..11   softmax of tile B
-// Softmax per key tile: the row max from S (TMEM), P = exp2(S*log2e/sqrt(d)
-// - m) as bf16 written back into the first 64 columns of the same TMEM
-// region (P is the A operand of the PV MMA, read straight from tensor
-// memory, so P never touches shared memory), the running sum l.  The reference max m is only moved when
-// the tile max exceeds it by more than 8 (log2 units); then the row of O is
-// rescaled in TMEM.  Otherwise P may reach 2^8, which bf16 and the fp32
+// Softmax per key tile: the S row into registers (one tensor-memory load
+// latency for the whole tile), its max, P = exp2(S*log2e/sqrt(d) - m) as
+// bf16 written back into the first 64 columns of the same TMEM region (P is
+// the A operand of the PV MMA, read straight from tensor memory, so P never
+// touches shared memory), the running sum l.  The reference max m is only
+// moved when the tile max exceeds it by more than 8 (log2 units); then the
+// row of O is rescaled in TMEM.  Otherwise P may reach 2^8, which bf16 and the fp32
 // accumulator represent without loss of range; O / l is unchanged in exact
 // arithmetic.
 //
@@ -89,58 +90,57 @@ DEV float ex2(float x) {
     return y;
 }
 
-// Row max of one S tile (128 fp32 columns from TMEM); keys >= nvalid masked.
+// The whole S row of a tile (128 fp32 columns) into registers: four loads
+// in flight, one wait (a wait covers every earlier load of the thread, so
+// loads waited for one by one would each pay the full latency).
+DEV void tile_load(uint32_t saddr, uint32_t (&s)[kBKV]) {
+#pragma unroll
+    for (int c0 = 0; c0 < kBKV; c0 += 32)
+        tmem_ld32(saddr + c0, *reinterpret_cast<uint32_t(*)[32]>(s + c0));
+#pragma unroll
+    for (int c0 = 0; c0 < kBKV; c0 += 32) tmem_ld_wait(*reinterpret_cast<uint32_t(*)[32]>(s + c0));
+}
+
+// Row max of a tile held in registers; keys >= nvalid masked.
 template <bool MASK>
-DEV float tile_max(uint32_t saddr, int nvalid) {
+DEV float row_max(const uint32_t (&s)[kBKV], int nvalid) {
     float m0 = -INFINITY, m1 = -INFINITY, m2 = -INFINITY, m3 = -INFINITY;
 #pragma unroll
-    for (int c0 = 0; c0 < kBKV; c0 += 32) {
-        uint32_t r[32];
-        tmem_ld32(saddr + c0, r);
-        tmem_ld_wait(r);
-#pragma unroll
-        for (int c = 0; c < 32; c += 4) {
-            float v0 = __uint_as_float(r[c]), v1 = __uint_as_float(r[c + 1]);
-            float v2 = __uint_as_float(r[c + 2]), v3 = __uint_as_float(r[c + 3]);
-            if (MASK) {
-                if (c0 + c >= nvalid) v0 = -INFINITY;
-                if (c0 + c + 1 >= nvalid) v1 = -INFINITY;
-                if (c0 + c + 2 >= nvalid) v2 = -INFINITY;
-                if (c0 + c + 3 >= nvalid) v3 = -INFINITY;
-            }
-            m0 = fmaxf(m0, v0);
-            m1 = fmaxf(m1, v1);
-            m2 = fmaxf(m2, v2);
-            m3 = fmaxf(m3, v3);
+    for (int c = 0; c < kBKV; c += 4) {
+        float v0 = __uint_as_float(s[c]), v1 = __uint_as_float(s[c + 1]);
+        float v2 = __uint_as_float(s[c + 2]), v3 = __uint_as_float(s[c + 3]);
+        if (MASK) {
+            if (c >= nvalid) v0 = -INFINITY;
+            if (c + 1 >= nvalid) v1 = -INFINITY;
+            if (c + 2 >= nvalid) v2 = -INFINITY;
+            if (c + 3 >= nvalid) v3 = -INFINITY;
         }
+        m0 = fmaxf(m0, v0);
+        m1 = fmaxf(m1, v1);
+        m2 = fmaxf(m2, v2);
+        m3 = fmaxf(m3, v3);
     }
     return fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
 }
 
-// P = exp2(S * sl2 - m) for one row, as bf16 written over the consumed S
-// columns (keys 2i, 2i+1 -> column i), returns the sum of the fp32
-// probabilities.  The scale-and-shift and the four running sums use packed
-// two-lane fp32 instructions (each lane rounds as the scalar instruction
-// would, in the same order), which cuts the instructions the softmax issues
-// per score: the softmax is bound by issue, not by the exponential unit.  Chunk c (keys 32c..32c+31) is read before its P (columns
-// 16c..16c+15) is written, so the write never clobbers unread S.
+// P = exp2(S * sl2 - m) of a tile held in registers, as bf16 written over
+// the tile's S columns in tensor memory (keys 2i, 2i+1 -> column i); returns
+// the sum of the fp32 probabilities.  The scale-and-shift and the four
+// running sums use packed two-lane fp32 instructions (each lane rounds as the
+// scalar instruction would, in the same order), which cuts the instructions
+// the softmax issues per score.
 template <bool MASK>
-DEV float tile_exp(uint32_t saddr, float sl2, float m, int nvalid) {
+DEV float row_exp(const uint32_t (&s)[kBKV], uint32_t saddr, float sl2, float m, int nvalid) {
     uint64_t s01 = 0, s23 = 0;  // (s0, s1), (s2, s3): four running sums
     const uint64_t sl2x2 = (uint64_t(__float_as_uint(sl2)) << 32) | __float_as_uint(sl2);
     const uint64_t negm2 = (uint64_t(__float_as_uint(-m)) << 32) | __float_as_uint(-m);
 #pragma unroll
     for (int c0 = 0; c0 < kBKV; c0 += 32) {
-        uint32_t r[32];
-        tmem_ld32(saddr + c0, r);
-        tmem_ld_wait(r);
         uint32_t pk[16];
 #pragma unroll
         for (int c = 0; c < 32; c += 4) {
-            // x = s * sl2 - m for two scores per instruction (each lane rounds
-            // as a scalar fma would)
-            uint64_t x01 = (uint64_t(r[c + 1]) << 32) | r[c];
-            uint64_t x23 = (uint64_t(r[c + 3]) << 32) | r[c + 2];
+            uint64_t x01 = (uint64_t(s[c0 + c + 1]) << 32) | s[c0 + c];
+            uint64_t x23 = (uint64_t(s[c0 + c + 3]) << 32) | s[c0 + c + 2];
             asm("fma.rn.f32x2 %0, %0, %1, %2;" : "+l"(x01) : "l"(sl2x2), "l"(negm2));
             asm("fma.rn.f32x2 %0, %0, %1, %2;" : "+l"(x23) : "l"(sl2x2), "l"(negm2));
             float p0 = ex2(__uint_as_float(uint32_t(x01)));
@@ -519,9 +519,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 tc_fence_after();
                 const bool masked = (j == n_kv - 1) && last_valid < kBKV;
+                // the tile's S row in registers: one load latency for the max
+                // and the exponentials together
+                uint32_t sr[kBKV];
+                tile_load(saddr, sr);
                 const float mx =
-                    (masked ? tile_max<true>(saddr, last_valid) : tile_max<false>(saddr, kBKV)) *
-                    sl2;
+                    (masked ? row_max<true>(sr, last_valid) : row_max<false>(sr, kBKV)) * sl2;
+                float alpha = 1.0f;
+                bool rescale = false;
                 if (jj == 0 && fresh) {  // no reference max yet: the tile's own
                     m = mx;
                 } else if (__any_sync(0xffffffffu, mx > m + kRescaleLog2)) {
@@ -531,7 +536,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // and are multiplied by exactly 1, so each row's result
                     // depends on that row alone.
                     const float m_new = (mx > m + kRescaleLog2) ? mx : m;
-                    const float alpha = ex2(m - m_new);
+                    alpha = ex2(m - m_new);
+                    m = m_new;
+                    rescale = true;
+                }
+                const float sum = masked ? row_exp<true>(sr, saddr, sl2, m, last_valid)
+                                         : row_exp<false>(sr, saddr, sl2, m, kBKV);
+                if (rescale) {
+                    // O is rescaled after P is written (the S row is out of
+                    // the registers by then); the PV MMA that accumulates
+                    // onto O waits for this thread's arrival below
 #pragma unroll
                     for (int c0 = 0; c0 < HD; c0 += 32) {
                         uint32_t r[32];
@@ -543,10 +557,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tmem_st32_sync(oaddr + c0, r);
                     }
                     l *= alpha;
-                    m = m_new;
                 }
-                const float sum = masked ? tile_exp<true>(saddr, sl2, m, last_valid)
-                                         : tile_exp<false>(saddr, sl2, m, kBKV);
                 l += sum;
                 tmem_st_wait();    // P is in tensor memory before the PV MMA reads it
                 tc_fence_before(); // S/O/P accesses finish before the next MMAs
