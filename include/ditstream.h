@@ -387,7 +387,14 @@ DIT_API dit_status_t dit_block_sync_status(const dit_plan_t *plan, dit_stream_t 
  * x [T, D] fp32; mod_f [2, D] fp32 (shift_f, scale_f); W_f [64, D] fp32 when
  * wf_scale == NULL, else int8 with fp32 scales [64]; out [T, 64] fp32.
  * "LayerStream: H3 Chunking" ("How the slicing works"): the fp32 output head
- * runs stock.  Uses the plan's T and D only; needs no workspace. */
+ * runs stock.  Uses the plan's T and D only; needs no workspace (when one is
+ * bound, a bounded device wait that runs out is recorded in its status word
+ * and reported by dit_block_sync_status).  Arithmetic is fp32-level: the
+ * statistics and the output in fp32, the D-long contraction on the tensor
+ * cores as three products of operands split into two tf32 parts each, with
+ * fp32 partial sums over 128 values of k.  Asynchronous on `stream`.
+ * Errors: DIT_ERR_INVALID_ARG (null pointer, D not a multiple of 32),
+ * DIT_ERR_ALIGN (a pointer not 16-byte aligned), DIT_ERR_CUDA. */
 DIT_API dit_status_t dit_final_forward(const dit_plan_t *plan, const float *x,
                                const void *wf, const float *wf_scale,
                                const float *mod_f, float *out,
