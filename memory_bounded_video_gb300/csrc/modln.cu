@@ -101,7 +101,18 @@ dit_status_t run(const float *x, int64_t rows, const float *shift, const float *
     constexpr int W = warps_per_row<NV>();
     constexpr int RB = kWarpsPerBlock / W;
     const int64_t blocks_needed = (rows + RB - 1) / RB;
-    const int64_t cap = int64_t(sm_count()) * 8;
+    // one wave of resident blocks, each looping over row groups: a second,
+    // partial wave of block launches measured 4 % slower (24.8 against 23.7
+    // us for 8192 x 3072)
+    static int per_sm = 0;  // the same value from any thread
+    if (!per_sm) {
+        int n = 0;
+        const cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+            &n, modln_cast_kernel<NV, W>, 32 * kWarpsPerBlock, 0);
+        if (e != cudaSuccess) return cuda_fail(e);
+        per_sm = n > 0 ? n : 1;
+    }
+    const int64_t cap = int64_t(sm_count()) * per_sm;
     const int grid = int(blocks_needed < cap ? blocks_needed : cap);
     modln_cast_kernel<NV, W><<<grid, 32 * kWarpsPerBlock, 0, s>>>(
         x, rows, shift, scale, reinterpret_cast<__nv_bfloat16 *>(out));
