@@ -177,7 +177,7 @@ struct Cfg {
     static constexpr int OUT_COLS = BN;       // output columns per tile
     static constexpr int SLOT_FLOATS = MH * kBM * HALF_COLS;  // one CTA's accumulator
     // barriers (up to byte 384), TMEM slot, abort flag; this CTA's work list
-    // at byte 384; completion-signal bytes at 448
+    // at byte 384
     static constexpr int BAR_BYTES = 512;
     static constexpr int SMEM_BYTES = OFF_T + T_BYTES + BAR_BYTES + 1024;
     static_assert(2 * STAGES + 32 <= 48 && CSTAGES <= 8,
@@ -657,12 +657,10 @@ __global__ void __launch_bounds__(Cfg<MODE, I8, MH, P>::THREADS, 1)
     // bars: full[S], empty[S], cfull[8], cempty[8] (QR: qfull), qempty[8]
     // (QR: the converter groups' load-before-store barriers),
     // tfull[2], tempty[2], drain, handed (split accumulator written); then the
-    // TMEM slot and the abort flag; this CTA's work list at byte 384; 16
-    // bytes at byte 448 (QR: the completion-signal copy's source/target)
+    // TMEM slot and the abort flag; this CTA's work list at byte 384
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * S + 30);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     AttnCta *cs_smem = reinterpret_cast<AttnCta *>(reinterpret_cast<uint8_t *>(bars) + 384);
-    const uint32_t sig = smem_u32(bars) + 448u;
     // work unit owner: the CTA, or the cluster pair; rank 0 of a pair issues
     // the MMAs for both
     const int cta = P ? int(cluster_id_x()) : int(blockIdx.x);
@@ -695,8 +693,8 @@ __global__ void __launch_bounds__(Cfg<MODE, I8, MH, P>::THREADS, 1)
             mbar_init(empty_bar(s), 1);
             // QR: stage s ready: the A producer's arrival with the A tile's
             // bytes, the converters' arrivals, and at the pair's leader the
-            // peer's 16-byte signal
-            if (QR) mbar_init(cfull_bar(s), kGroupThreads + 1);
+            // peer's forwarded arrival
+            if (QR) mbar_init(cfull_bar(s), kGroupThreads + 1 + (leader ? 1 : 0));
         }
         for (int s = 0; s < CS; ++s) {
             mbar_init(cfull_bar(s), kGroupThreads);
@@ -1003,25 +1001,35 @@ __global__ void __launch_bounds__(Cfg<MODE, I8, MH, P>::THREADS, 1)
                     mbar_wait_quiet(qfull_bar(int(i % S)), uint32_t((i / S) & 1), kWaitLimitNs);
             }
         }
-    } else if (warp == 3 && QR) {
+    } else if (QR && (warp == 1 || warp == 3)) {
         if (!leader && lane == 0) {
-            // ---------------------------------------------- forwarder (QR)
+            // ---------------------------------------------- forwarders (QR)
             // the pair's second CTA: once its converters have filled the B
-            // half of stage s and its A tile has landed there, send the leader
-            // a 16-byte copy that completes on the leader's converted-B
-            // barrier.  The bulk-copy engine carries it; the thread does not
-            // wait for it.
-            int stage = 0;
+            // half of stage s and its A tile has landed there, arrive on the
+            // leader's barrier of the stage.  A remote arrival holds its
+            // thread for several hundred ns, so two otherwise idle warps (1,
+            // the MMA issuer at the leader; 3) take the K-steps in turn.  (A
+            // 16-byte bulk copy completing on the leader's barrier, which
+            // does not hold the thread, took 1.5-2.3 us to land, queued
+            // behind this CTA's tile loads; the down projection's launch of
+            // 8192 x 3072 x 8192 ran 1 % slower with it.  A cluster-scope
+            // release held each arriving thread so long that two forwarders
+            // fell behind: the SwiGLU launch took 0.72 ms against 0.51.)
+            const int mine = warp == 3 ? 0 : 1;
+            int stage = 0, turn = 0;
             uint32_t ph = 0;
             bool ok = true;
             for (int idx = 0; idx < cs.count && ok; ++idx) {
                 const AttnItem it = attn_item(p.g, cs, cta, idx);
                 for (int kb = it.k0; kb < it.k1; ++kb) {
-                    if (!mbar_wait(cfull_bar(stage), ph, wc)) {
-                        ok = false;
-                        break;
+                    if (turn == mine) {
+                        if (!mbar_wait(cfull_bar(stage), ph, wc)) {
+                            ok = false;
+                            break;
+                        }
+                        mbar_arrive_remote(lead(cfull_bar(stage)));
                     }
-                    bulk_signal_remote(lead(sig), sig, 16u, lead(cfull_bar(stage)));
+                    turn ^= 1;
                     if (++stage == S) {
                         stage = 0;
                         ph ^= 1u;
@@ -1215,16 +1223,8 @@ __global__ void __launch_bounds__(Cfg<MODE, I8, MH, P>::THREADS, 1)
                 fence_proxy_async_smem();  // the tensor core reads what we wrote
                 // every converter thread arrives as soon as its own stores are
                 // fenced (one arrival per warp after __syncwarp measured 3-5 %
-                // slower); QR: the leader's thread 0 also arms the peer's
-                // 16-byte signal
-                if constexpr (QR) {
-                    if (leader && tid == 0)
-                        mbar_arrive_expect_tx(cfull_bar(stage), 16u);
-                    else
-                        mbar_arrive(cfull_bar(stage));
-                } else {
-                    mbar_arrive(cfull_bar(cstage));
-                }
+                // slower)
+                mbar_arrive(cfull_bar(QR ? stage : cstage));
               }
                 if constexpr (!QR) {
                     if (++cstage == CS) {

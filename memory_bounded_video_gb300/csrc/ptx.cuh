@@ -207,21 +207,6 @@ DEV void tma_load_2d_pair(uint32_t dst, const CUtensorMap *m, uint32_t cluster_b
         : "memory");
 }
 
-// Completion signal to another CTA of the cluster through the bulk-copy
-// engine: `bytes` (a multiple of 16) copied from this CTA's shared memory
-// `src` to `dst` in the other CTA (mapa_shared address), completing them on
-// that CTA's barrier `cluster_bar`.  The issuing thread does not wait for
-// it, unlike a remote mbarrier arrival; the copy follows the shared-memory
-// writes this thread (or its warp, after __syncwarp) fenced to the async
-// proxy before it.
-DEV void bulk_signal_remote(uint32_t dst, uint32_t src, uint32_t bytes, uint32_t cluster_bar) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, "
-        "[%3];" ::"r"(dst),
-        "r"(src), "r"(bytes), "r"(cluster_bar)
-        : "memory");
-}
-
 // ------------------------------------------------------------ tcgen05
 // G = 1: this CTA's tensor memory.  G = 2: the same columns in both CTAs of
 // a cluster pair, for MMAs issued with cta_group::2; one warp of each CTA of
