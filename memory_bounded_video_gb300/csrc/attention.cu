@@ -47,6 +47,11 @@ constexpr int kBQ = 128;    // queries per tile
 constexpr int kBKV = 128;   // keys per tile
 constexpr int kThreads = 384;
 constexpr float kRescaleLog2 = 8.0f;
+// 2^kRescaleLog2: a row whose probabilities against its reference max sum to
+// at most this has no score above that max + kRescaleLog2 (each probability
+// is at most the fp32 sum of all of them, which are >= 0)
+constexpr float kRescaleSum = 256.0f;
+static_assert(kRescaleSum == 256.0f && kRescaleLog2 == 8.0f, "kRescaleSum = 2^kRescaleLog2");
 
 template <int HD>
 struct ACfg {
@@ -519,29 +524,48 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 tc_fence_after();
                 const bool masked = (j == n_kv - 1) && last_valid < kBKV;
-                // the tile's S row in registers: one load latency for the max
-                // and the exponentials together
+                // the tile's S row in registers: one load latency for the
+                // exponentials and, when needed, the max
                 uint32_t sr[kBKV];
                 tile_load(saddr, sr);
-                const float mx =
-                    (masked ? row_max<true>(sr, last_valid) : row_max<false>(sr, kBKV)) * sl2;
                 float alpha = 1.0f;
                 bool rescale = false;
+                float sum;
                 if (jj == 0 && fresh) {  // no reference max yet: the tile's own
-                    m = mx;
-                } else if (__any_sync(0xffffffffu, mx > m + kRescaleLog2)) {
-                    // Move the reference max of the rows that need it: O_row *=
-                    // 2^(m - m_new), l likewise.  The branch is warp-uniform (the
-                    // TMEM accesses are warp-collective); the other rows keep m
-                    // and are multiplied by exactly 1, so each row's result
-                    // depends on that row alone.
-                    const float m_new = (mx > m + kRescaleLog2) ? mx : m;
-                    alpha = ex2(m - m_new);
-                    m = m_new;
-                    rescale = true;
-                }
-                const float sum = masked ? row_exp<true>(sr, saddr, sl2, m, last_valid)
+                    m = (masked ? row_max<true>(sr, last_valid) : row_max<false>(sr, kBKV)) * sl2;
+                    sum = masked ? row_exp<true>(sr, saddr, sl2, m, last_valid)
+                                 : row_exp<false>(sr, saddr, sl2, m, kBKV);
+                } else {
+                    // P against the reference max first.  A row can need its
+                    // max moved (a score above m + kRescaleLog2) only if its
+                    // probabilities sum to more than kRescaleSum, so the
+                    // tile max is computed only for warps with such a row;
+                    // the rows that move their max are exactly those the
+                    // max-first order moves, and their P is redone.
+                    sum = masked ? row_exp<true>(sr, saddr, sl2, m, last_valid)
+                                 : row_exp<false>(sr, saddr, sl2, m, kBKV);
+                    if (__any_sync(0xffffffffu, sum > kRescaleSum)) {
+                        const float mx =
+                            (masked ? row_max<true>(sr, last_valid) : row_max<false>(sr, kBKV)) *
+                            sl2;
+                        if (__any_sync(0xffffffffu, mx > m + kRescaleLog2)) {
+                            // Move the reference max of the rows that need it:
+                            // O_row *= 2^(m - m_new), l likewise.  The branch
+                            // is warp-uniform (the TMEM accesses are
+                            // warp-collective); the other rows keep m, their P
+                            // and sum are recomputed unchanged and they are
+                            // multiplied by exactly 1, so each row's result
+                            // depends on that row alone.
+                            const float m_new = (mx > m + kRescaleLog2) ? mx : m;
+                            alpha = ex2(m - m_new);
+                            m = m_new;
+                            rescale = true;
+                            tmem_st_wait();  // the first P is stored before it is overwritten
+                            sum = masked ? row_exp<true>(sr, saddr, sl2, m, last_valid)
                                          : row_exp<false>(sr, saddr, sl2, m, kBKV);
+                        }
+                    }
+                }
                 if (rescale) {
                     // O is rescaled after P is written (the S row is out of
                     // the registers by then); the PV MMA that accumulates

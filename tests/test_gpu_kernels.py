@@ -249,6 +249,57 @@ def test_attention_matches_oracle(Tq, T, H, hd, sharp):
     assert np.abs(got - ref).max() < 2e-2 * max(1.0, np.abs(ref).max())
 
 
+# The running reference max moves only when a row's score exceeds it by more
+# than 8 (log2 units).  The kernel computes P against the current max first
+# and takes the tile max only for warps where some row's probabilities sum to
+# more than 2^8: a later key tile whose scores sit 7.48 above the first
+# tile's max (sum far above 2^8, max not moved) and one 8.66 above (max
+# moved, O and l rescaled, P redone).  Every query row scores key j as
+# q . k_j / 8 = b_j with q = (8, 0, ...) and k_j = (b_j, 0, ...).
+@pytest.mark.parametrize("b1", [9.1875, 10.0], ids=["sum_over_256_max_kept", "max_moved"])
+def test_attention_later_tile_above_the_reference_max(b1):
+    H, hd, Tq, T = 1, 64, 256, 3 * 128 + 17
+    g = gen(23)
+    q = torch.zeros(Tq, hd)
+    q[:, 0] = 8.0
+    k = torch.zeros(T, hd)
+    k[0, 0] = 4.0              # first tile: max score 4, the others 0
+    k[128:256, 0] = b1         # second tile: every score b1
+    k[256:, 0] = -2.0          # third tile and the ragged tail: small
+    q, k = q.to(torch.bfloat16), k.to(torch.bfloat16)
+    v = randn(g, T, hd).to(torch.bfloat16)
+    o = run_attention(q, k, v, H, hd)
+    ref = ob.mha_attention(f64(q), f64(k), f64(v), H)
+    got = f64(o)
+    assert np.linalg.norm(got - ref) / np.linalg.norm(ref) < 1e-2
+    assert np.abs(got - ref).max() < 2e-2
+
+
+# Random scores with single keys planted in a later tile that score far above
+# every earlier key for a few rows of a warp only: those rows move their max,
+# the warp's other rows keep theirs (multiplied by exactly 1).
+def test_attention_max_moves_for_some_rows_of_a_warp():
+    H, hd, Tq, T = 2, 128, 256, 1000
+    D = H * hd
+    g = gen(24)
+    q = randn(g, Tq, D).to(torch.bfloat16)
+    k = randn(g, T, D)
+    rows = [3, 17, 40, 130, 255]
+    for i, r in enumerate(rows):
+        for h in range(H):
+            k[3 * 128 + 5 + i, h * hd:(h + 1) * hd] = 1.5 * q[r, h * hd:(h + 1) * hd].float()
+    k = k.to(torch.bfloat16)
+    v = randn(g, T, D).to(torch.bfloat16)
+    o = run_attention(q, k, v, H, hd)
+    ref = ob.mha_attention(f64(q), f64(k), f64(v), H)
+    got = f64(o)
+    assert np.linalg.norm(got - ref) / np.linalg.norm(ref) < 1e-2
+    assert np.abs(got - ref).max() < 2e-2 * max(1.0, np.abs(ref).max())
+    # the planted rows are dominated by their planted key
+    for i, r in enumerate(rows):
+        np.testing.assert_allclose(got[r], f64(v)[3 * 128 + 5 + i], atol=2e-2)
+
+
 def test_attention_rows_do_not_depend_on_slab():
     g = gen(21)
     H, hd, T = 2, 128, 700
