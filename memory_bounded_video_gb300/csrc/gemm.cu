@@ -104,11 +104,9 @@ constexpr int kLoraStageBytes = (kBM + kLoraRows) * kBK * 2;
 // of A and half of the B rows (the N-block's first or second 128 rows; for
 // SwiGLU the gate or the up tile) and keeps its 128 rows x 256 columns of the
 // accumulator in its own tensor memory, so its epilogue is the MH = 1 one.
-// Per K-step a CTA then moves 64 KB through shared memory for bf16 B (TMA
-// writes of A and its B half, the MMA's reads of both) against 96 KB for the
-// one-CTA 128 x 256 tile, and 80 KB against 128 KB for int8 B with MH = 2:
-// the one-CTA tiles' main loops are bound by that traffic (78-80 % tensor
-// pipe activity for bf16).
+// Per K-step a CTA then stages half the B rows of the one-CTA 128 x 256
+// tile for the same multiply-adds, and an int8 CTA converts half as many;
+// the one-CTA tiles' main loops ran at 78-80 % tensor-pipe activity for bf16.
 template <int MODE, bool I8, int MH = 1, bool P = false>
 struct Cfg {
     static_assert(!P || MH == 1, "pair tiles hold one 128-row half per CTA");
