@@ -255,13 +255,14 @@ def test_attention_matches_oracle(Tq, T, H, hd, sharp):
 # more than 2^8: a later key tile whose scores sit 7.48 above the first
 # tile's max (sum far above 2^8, max not moved) and one 8.66 above (max
 # moved, O and l rescaled, P redone).  Every query row scores key j as
-# q . k_j / 8 = b_j with q = (8, 0, ...) and k_j = (b_j, 0, ...).
+# q . k_j / sqrt(d) = b_j with q = (sqrt(d), 0, ...) and k_j = (b_j, 0, ...).
+@pytest.mark.parametrize("hd", [64, 128])
 @pytest.mark.parametrize("b1", [9.1875, 10.0], ids=["sum_over_256_max_kept", "max_moved"])
-def test_attention_later_tile_above_the_reference_max(b1):
-    H, hd, Tq, T = 1, 64, 256, 3 * 128 + 17
+def test_attention_later_tile_above_the_reference_max(b1, hd):
+    H, Tq, T = 1, 256, 3 * 128 + 17
     g = gen(23)
     q = torch.zeros(Tq, hd)
-    q[:, 0] = 8.0
+    q[:, 0] = hd ** 0.5  # q . k / sqrt(hd) = k[0]
     k = torch.zeros(T, hd)
     k[0, 0] = 4.0              # first tile: max score 4, the others 0
     k[128:256, 0] = b1         # second tile: every score b1
@@ -278,8 +279,9 @@ def test_attention_later_tile_above_the_reference_max(b1):
 # Random scores with single keys planted in a later tile that score far above
 # every earlier key for a few rows of a warp only: those rows move their max,
 # the warp's other rows keep theirs (multiplied by exactly 1).
-def test_attention_max_moves_for_some_rows_of_a_warp():
-    H, hd, Tq, T = 2, 128, 256, 1000
+@pytest.mark.parametrize("hd", [64, 128])
+def test_attention_max_moves_for_some_rows_of_a_warp(hd):
+    H, Tq, T = 2, 256, 1000
     D = H * hd
     g = gen(24)
     q = randn(g, Tq, D).to(torch.bfloat16)
