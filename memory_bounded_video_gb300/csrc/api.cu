@@ -202,7 +202,8 @@ void layout(dit_plan *p) {
     // hand-off state of the attention's split units, when a slab has enough
     // (query pair, head) units to leave a partial wave on some device
     const int64_t units = (int64_t(p->ca) + 255) / 256 * p->heads;
-    p->split_slots = units < (int64_t(1) << 30) ? attn_slots_needed(int(units)) : 0;
+    p->split_slots =
+        units < (int64_t(1) << 30) ? attn_slots_needed(int(units), 1 << 20, kAttnSplitSlots, true) : 0;
     p->off_split = 0;
     if (p->split_slots) {
         p->off_split = attn_end;
@@ -1047,7 +1048,7 @@ dit_status_t dit_attention_schedule(int units, int n_kv, int max_ctas, int slots
                                     int *n_split, int *items, int64_t cap, int64_t *n_items) {
     if (units <= 0 || n_kv <= 0 || max_ctas <= 0 || slots < 0 || cap < 0)
         return DIT_ERR_INVALID_ARG;
-    const AttnGrid g = attn_grid(units, n_kv, max_ctas, slots);
+    const AttnGrid g = attn_grid(units, n_kv, max_ctas, slots, true);
     if (n_cta) *n_cta = g.n_cta;
     if (n_split) *n_split = g.n_pc;
     int64_t n = 0;

@@ -790,7 +790,7 @@ dit_status_t run(const void *q, int64_t Tq, int64_t ldq, const void *k, int64_t 
     int max_cta = sm_count();
     if (split && split->max_ctas > 0 && split->max_ctas < max_cta) max_cta = split->max_ctas;
     const int slots = (split && split->flags && split->state) ? split->slots : 0;
-    p.g = attn_grid(p.n_qpairs * heads, p.n_kv, max_cta, slots);
+    p.g = attn_grid(p.n_qpairs * heads, p.n_kv, max_cta, slots, true);
     if (p.g.n_pc > 0) {
         p.split_flags = split->flags;
         p.split_state = split->state;

@@ -21,6 +21,15 @@
 // at most F when n_pc <= R * F, since a unit then spans at most F + 1
 // ranges, or when every unit is cut into the same q <= F + 1 aligned ranges;
 // a larger position is clamped to F (correct, only slower).
+//
+// When R is small against G (few CTAs could share it), the attention takes
+// one whole unit per CTA into the shared part as well (extended split): the
+// R + G units after the first (F - 1) G are cut into G equal ranges, each
+// longer than a unit and shorter than two, so a range is the end of one unit
+// (piece A), at most one whole unit, and the start of another (piece B), and
+// every CTA carries about the mean load.  Each cut unit then spans two
+// ranges: its start is piece B of CTA c, run first, and its end piece A of
+// CTA c + 1, run last, so no CTA waits either.
 #pragma once
 
 #include <stdint.h>
@@ -48,14 +57,15 @@ struct AttnGrid {
     int units, n_kv, n_cta;
     int full;           // whole units per CTA (split mode); 0: round robin
     int n_pc;           // CTAs sharing the remainder (0: no split)
-    int64_t rem_tiles;  // remainder key tiles R * n_kv
+    int64_t rem_tiles;  // remainder key tiles R * n_kv ((R + G) * n_kv extended)
     int rem_u0;         // first remainder unit, full * n_cta
+    int ext;            // extended split: ranges between one and two units long
 };
 
 // Grid and split for U units of n_kv key tiles on at most max_cta CTAs;
 // slots: state slots available (0: no split; slot c is used by CTAs c - 1
-// and c, for 0 < c < n_pc).
-DS_HD AttnGrid attn_grid(int units, int n_kv, int max_cta, int slots) {
+// and c, for 0 < c < n_pc); extend: the extended split may be chosen.
+DS_HD AttnGrid attn_grid(int units, int n_kv, int max_cta, int slots, bool extend = false) {
     AttnGrid g{};
     g.units = units;
     g.n_kv = n_kv;
@@ -86,6 +96,19 @@ DS_HD AttnGrid attn_grid(int units, int n_kv, int max_cta, int slots) {
             g.rem_tiles = int64_t(R) * n_kv;
             g.rem_u0 = F * g.n_cta;
         }
+        // extended split: at least two whole units per CTA (one stays whole
+        // after one goes into the shared part), a slot per CTA, and a busiest
+        // CTA shorter by more than n_kv / 16 key tiles
+        const int64_t cur = g.n_pc ? int64_t(F) * n_kv + longest : int64_t(F + 1) * n_kv;
+        const int64_t G = g.n_cta;
+        const int64_t ext_max = int64_t(F - 1) * n_kv + (int64_t(R + G) * n_kv + G - 1) / G;
+        if (extend && F >= 2 && G <= slots && ext_max + n_kv / 16 < cur) {
+            g.full = F - 1;
+            g.n_pc = g.n_cta;
+            g.rem_tiles = int64_t(R + G) * n_kv;
+            g.rem_u0 = (F - 1) * g.n_cta;
+            g.ext = 1;
+        }
     }
     return g;
 }
@@ -97,10 +120,11 @@ constexpr int kAttnMinSms = 128, kAttnMaxSms = 160;
 // State slots that `units` units of n_kv key tiles may need on any device
 // with kAttnMinSms..kAttnMaxSms multiprocessors when at most `cap` slots
 // are available (0: none would split).
-inline int attn_slots_needed(int units, int n_kv = 1 << 20, int cap = kAttnSplitSlots) {
+inline int attn_slots_needed(int units, int n_kv = 1 << 20, int cap = kAttnSplitSlots,
+                             bool extend = false) {
     int need = 0;
     for (int sm = kAttnMinSms; sm <= kAttnMaxSms; ++sm) {
-        const AttnGrid g = attn_grid(units, n_kv, sm, cap);
+        const AttnGrid g = attn_grid(units, n_kv, sm, cap, extend);
         if (g.n_pc > need) need = g.n_pc;
     }
     return need;
@@ -138,6 +162,7 @@ inline int gemm_slots_needed(int units, int k_steps, bool pair) {
 struct AttnCta {
     int count;  // items
     int has_a, has_b, pos_a;
+    int has_m, m_u;  // extended split: a whole unit between pieces A and B
     AttnItem a, b;
 };
 
@@ -161,14 +186,22 @@ DS_HD AttnCta attn_cta(const AttnGrid &g, int c) {
     s.a.src = s.a.k0 > 0 ? c : -1;
     s.a.dst = s.a.k1 < nkv ? c + 1 : -1;
     if (hi > (ja + 1) * nkv) {  // the range goes on into the next unit
+        int64_t jb = ja + 1;
+        if (hi - jb * nkv > nkv) {  // extended: a whole unit, then the next
+            s.has_m = 1;
+            s.m_u = int(g.rem_u0 + jb);
+            ++jb;
+        }
         s.has_b = 1;
-        s.b.u = s.a.u + 1;
+        s.b.u = int(g.rem_u0 + jb);
         s.b.k0 = 0;
-        s.b.k1 = int(hi - (ja + 1) * nkv);
+        s.b.k1 = int(hi - jb * nkv);
         s.b.src = -1;
         s.b.dst = s.b.k1 < nkv ? c + 1 : -1;
     }
-    if (s.a.k0 > 0) {
+    if (g.ext) {
+        s.pos_a = g.full + s.has_m;  // after every whole unit
+    } else if (s.a.k0 > 0) {
         // chain position: CTAs before c whose ranges hold keys of unit ja;
         // the first is the one whose range holds its key tile 0
         const int64_t first = ((ja * nkv + 1) * g.n_pc - 1) / g.rem_tiles;
@@ -176,7 +209,7 @@ DS_HD AttnCta attn_cta(const AttnGrid &g, int c) {
         if (pos > g.full) pos = g.full;
         s.pos_a = int(pos);
     }
-    s.count += s.has_a + s.has_b;
+    s.count += s.has_a + s.has_b + s.has_m;
     return s;
 }
 
@@ -192,7 +225,7 @@ DS_HD AttnItem attn_item(const AttnGrid &g, const AttnCta &s, int c, int idx) {
         if (i > s.pos_a) --i;
     }
     AttnItem w;
-    w.u = c + i * g.n_cta;
+    w.u = (s.has_m && i == g.full) ? s.m_u : c + i * g.n_cta;
     w.k0 = 0;
     w.k1 = g.n_kv;
     w.src = w.dst = -1;

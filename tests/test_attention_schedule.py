@@ -22,25 +22,35 @@ def lib():
 
 
 def grid(units, n_kv, max_cta, slots):
-    """(CTAs, CTAs sharing the remainder, whole units each, remainder units),
-    restating the documented rule: F = U // G whole units per CTA and the
-    R = U % G remaining units cut into n ranges, n the larger of
-    min(G, R*F, R*n_kv) (any ranges of at least n_kv / F tiles) and R*q,
-    q = min(F + 1, G // R, n_kv) (q aligned ranges per unit), or, when that
-    exceeds the slots, min(the first, slots); used when the longest range,
-    ceil(R * n_kv / n), is shorter than a unit."""
+    """(CTAs, CTAs sharing the remainder, whole units each, remainder units,
+    whole units each without the extension), restating the documented rule:
+    F = U // G whole units per CTA and the R = U % G remaining units cut into
+    n ranges, n the larger of min(G, R*F, R*n_kv) (any ranges of at least
+    n_kv / F tiles) and R*q, q = min(F + 1, G // R, n_kv) (q aligned ranges
+    per unit), or, when that exceeds the slots, min(the first, slots); used
+    when the longest range, ceil(R * n_kv / n), is shorter than a unit.  The
+    extended split (F >= 2, G <= slots) instead cuts the last R + G units
+    into G ranges, leaving F - 1 whole units per CTA, when that makes the
+    busiest CTA's load, (F - 1) * n_kv + ceil((R + G) * n_kv / G), shorter
+    by more than n_kv // 16 key tiles."""
     G = max(1, min(units, max_cta))
     F, R = divmod(units, G)
     if R == 0:
-        return G, 0, F, 0
+        return G, 0, F, 0, F
     n1 = min(G, R * F, R * n_kv)
     q = min(F + 1, G // R, n_kv)
     n = max(n1, R * q)
     if n > slots:
         n = min(n1, slots)
-    if n > 0 and -(-R * n_kv // n) < n_kv:
-        return G, n, F, R
-    return G, 0, F, R
+    longest = -(-R * n_kv // n) if n > 0 else n_kv
+    split = n > 0 and longest < n_kv
+    cur = F * n_kv + longest if split else (F + 1) * n_kv
+    ext_max = (F - 1) * n_kv + -(-(R + G) * n_kv // G)
+    if F >= 2 and G <= slots and ext_max + n_kv // 16 < cur:
+        return G, G, F - 1, R + G, F
+    if split:
+        return G, n, F, R, F
+    return G, 0, F, R, F
 
 
 CASES = [
@@ -76,7 +86,7 @@ def by_cta(items):
 @pytest.mark.parametrize("units,n_kv,max_cta,slots", CASES)
 def test_schedule_covers_every_key_tile_once_as_chains(units, n_kv, max_cta, slots):
     n_cta, n_split, items = ds.attention_schedule(units, n_kv, max_cta, slots)
-    G, n_pc, F, R = grid(units, n_kv, max_cta, slots)
+    G, n_pc, F, R, _ = grid(units, n_kv, max_cta, slots)
     assert (n_cta, n_split) == (G, n_pc)
     pieces = {}
     for c, i, u, k0, k1, src, dst in items:
@@ -108,7 +118,7 @@ def test_schedule_never_waits_and_balances_key_tiles(units, n_kv, max_cta, slots
     in time; an item that continues a unit must not start before the piece
     before it has ended on the CTA before."""
     n_cta, n_split, items = ds.attention_schedule(units, n_kv, max_cta, slots)
-    G, n_pc, F, R = grid(units, n_kv, max_cta, slots)
+    G, n_pc, F, R, F0 = grid(units, n_kv, max_cta, slots)
     per = by_cta(items)
     start, end = {}, {}
     for c, its in per.items():
@@ -124,7 +134,7 @@ def test_schedule_never_waits_and_balances_key_tiles(units, n_kv, max_cta, slots
     assert sum(loads) == units * n_kv
     if n_pc:
         assert max(loads) == F * n_kv + -(-R * n_kv // n_pc)
-        assert max(loads) < (F + 1) * n_kv  # shorter than with a last wave
+        assert max(loads) < (F0 + 1) * n_kv  # shorter than with a last wave
     else:
         assert max(loads) == -(-units // n_cta) * n_kv
 
@@ -139,6 +149,23 @@ def test_schedule_of_the_32k_token_slab():
     for c, i, u, k0, k1, src, dst in items:
         loads[c] = loads.get(c, 0) + k1 - k0
     assert max(loads.values()) == 1332 and min(loads.values()) == 1280
+
+
+def test_schedule_of_the_32k_token_slab_on_152_sms():
+    # the same slab on 152 SMs: 768 units are 5.05 waves, and the 8 left over
+    # could be cut into at most 48 ranges (1323 key tiles on the busiest SM
+    # against a mean of 1293.5); the extended split cuts the last 160 units
+    # into 152 ranges of 269-270 key tiles after 4 whole units per CTA
+    n_cta, n_split, items = ds.attention_schedule(768, 256, 152, 160)
+    assert (n_cta, n_split) == (152, 152)
+    loads, count = {}, {}
+    for c, i, u, k0, k1, src, dst in items:
+        loads[c] = loads.get(c, 0) + k1 - k0
+        count[c] = count.get(c, 0) + 1
+    assert max(loads.values()) == 1294 and min(loads.values()) == 1293
+    assert max(count.values()) <= 7
+    # without the extension (as the GEMMs split): 48 ranges, 1323 tiles
+    assert ds.attention_schedule(768, 256, 152, 151)[1] == 48
 
 
 def test_plan_workspace_holds_the_hand_off_space():
