@@ -27,9 +27,14 @@
 // R + G units after the first (F - 1) G are cut into G equal ranges, each
 // longer than a unit and shorter than two, so a range is the end of one unit
 // (piece A), at most one whole unit, and the start of another (piece B), and
-// every CTA carries about the mean load.  Each cut unit then spans two
-// ranges: its start is piece B of CTA c, run first, and its end piece A of
-// CTA c + 1, run last, so no CTA waits either.
+// every CTA carries about the mean load.  A CTA runs its whole units first
+// (all CTAs in step, so those sharing a head share its K/V tiles in L2),
+// then piece B, the whole unit, and piece A last.  Each cut unit spans two
+// ranges, its start piece B of CTA c and its end piece A of CTA c + 1; with
+// W whole-unit tiles per CTA, B ends at W + |B| and A starts at W + L - |A|
+// on the next CTA (L its range's length), so since |B| + |A| = n_kv <= L no
+// CTA waits.  (Running B first instead let the CTAs' whole units drift apart
+// by up to a unit and doubled the launch's DRAM reads.)
 #pragma once
 
 #include <stdint.h>
@@ -200,7 +205,7 @@ DS_HD AttnCta attn_cta(const AttnGrid &g, int c) {
         s.b.dst = s.b.k1 < nkv ? c + 1 : -1;
     }
     if (g.ext) {
-        s.pos_a = g.full + s.has_m;  // after every whole unit
+        s.pos_a = g.full + s.has_b + s.has_m;  // last
     } else if (s.a.k0 > 0) {
         // chain position: CTAs before c whose ranges hold keys of unit ja;
         // the first is the one whose range holds its key tile 0
@@ -216,6 +221,29 @@ DS_HD AttnCta attn_cta(const AttnGrid &g, int c) {
 // Item idx (0 <= idx < count) of CTA c, in processing order.
 DS_HD AttnItem attn_item(const AttnGrid &g, const AttnCta &s, int c, int idx) {
     int i = idx;
+    AttnItem w;
+    w.k0 = 0;
+    w.k1 = g.n_kv;
+    w.src = w.dst = -1;
+    if (g.ext) {  // whole units, piece B, the range's whole unit, piece A
+        if (i < g.full) {
+            w.u = c + i * g.n_cta;
+            return w;
+        }
+        i -= g.full;
+        if (s.has_b) {
+            if (i == 0) return s.b;
+            --i;
+        }
+        if (s.has_m) {
+            if (i == 0) {
+                w.u = s.m_u;
+                return w;
+            }
+            --i;
+        }
+        return s.a;
+    }
     if (s.has_b) {
         if (i == 0) return s.b;
         --i;
@@ -224,11 +252,7 @@ DS_HD AttnItem attn_item(const AttnGrid &g, const AttnCta &s, int c, int idx) {
         if (i == s.pos_a) return s.a;
         if (i > s.pos_a) --i;
     }
-    AttnItem w;
-    w.u = (s.has_m && i == g.full) ? s.m_u : c + i * g.n_cta;
-    w.k0 = 0;
-    w.k1 = g.n_kv;
-    w.src = w.dst = -1;
+    w.u = c + i * g.n_cta;
     return w;
 }
 
