@@ -101,13 +101,13 @@ DS_HD AttnGrid attn_grid(int units, int n_kv, int max_cta, int slots, bool exten
             g.rem_tiles = int64_t(R) * n_kv;
             g.rem_u0 = F * g.n_cta;
         }
-        // extended split: at least two whole units per CTA (one stays whole
-        // after one goes into the shared part), a slot per CTA, and a busiest
-        // CTA shorter by more than n_kv / 16 key tiles
+        // extended split: at least one whole unit per CTA to move into the
+        // shared part, a slot per CTA, and a busiest CTA shorter by more than
+        // n_kv / 16 key tiles
         const int64_t cur = g.n_pc ? int64_t(F) * n_kv + longest : int64_t(F + 1) * n_kv;
         const int64_t G = g.n_cta;
         const int64_t ext_max = int64_t(F - 1) * n_kv + (int64_t(R + G) * n_kv + G - 1) / G;
-        if (extend && F >= 2 && G <= slots && ext_max + n_kv / 16 < cur) {
+        if (extend && F >= 1 && G <= slots && ext_max + n_kv / 16 < cur) {
             g.full = F - 1;
             g.n_pc = g.n_cta;
             g.rem_tiles = int64_t(R + G) * n_kv;

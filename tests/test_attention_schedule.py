@@ -29,7 +29,7 @@ def grid(units, n_kv, max_cta, slots):
     n_kv / F tiles) and R*q, q = min(F + 1, G // R, n_kv) (q aligned ranges
     per unit), or, when that exceeds the slots, min(the first, slots); used
     when the longest range, ceil(R * n_kv / n), is shorter than a unit.  The
-    extended split (F >= 2, G <= slots) instead cuts the last R + G units
+    extended split (F >= 1, G <= slots) instead cuts the last R + G units
     into G ranges, leaving F - 1 whole units per CTA, when that makes the
     busiest CTA's load, (F - 1) * n_kv + ceil((R + G) * n_kv / G), shorter
     by more than n_kv // 16 key tiles."""
@@ -46,7 +46,7 @@ def grid(units, n_kv, max_cta, slots):
     split = n > 0 and longest < n_kv
     cur = F * n_kv + longest if split else (F + 1) * n_kv
     ext_max = (F - 1) * n_kv + -(-(R + G) * n_kv // G)
-    if F >= 2 and G <= slots and ext_max + n_kv // 16 < cur:
+    if F >= 1 and G <= slots and ext_max + n_kv // 16 < cur:
         return G, G, F - 1, R + G, F
     if split:
         return G, n, F, R, F
@@ -169,9 +169,7 @@ def test_schedule_of_the_32k_token_slab_on_152_sms():
 
 
 def test_plan_workspace_holds_the_hand_off_space():
-    # a 8192-query slab of 24 heads needs hand-off slots, a 4096-token block
-    # of 16 heads (256 units, one per SM and a remainder too large to cut)
-    # does not
+    # a 8192-query slab of 24 heads needs hand-off slots
     big = ds.block_plan(32768, 3072, 24, 8192, 8192, 8192)
     small = ds.block_plan(4096, 1024, 16, 2816, 4096, 4096)
     slots = max(grid(768, 1 << 20, sm, 160)[1] for sm in range(128, 161))
@@ -189,9 +187,16 @@ def test_plan_workspace_holds_the_hand_off_space():
     assert ds.attention_schedule(768, 48, 152, 64)[1] == 48
     assert ds.attention_schedule(1536, 48, 152, 64)[1] == 64
     assert big.workspace_bytes() == max(attn, mlp) + g
-    assert max(grid(256, 1 << 20, sm, 160)[1] for sm in range(128, 161)) == 0
-    assert small.workspace_bytes() == (1024 + 4 * 4096 * 1024 + 2 * 4096 * 1024
-                                       + 2 * 4096 * 2816
+    # the 4096-token block: 256 units, one whole unit per CTA and a remainder,
+    # split by the extended rule on every device size (160 slots of 64-wide
+    # state); its attention phase stays below the MLP phase, which sets the
+    # workspace
+    small_slots = max(grid(256, 1 << 20, sm, 160)[1] for sm in range(128, 161))
+    assert small_slots == 160
+    small_attn = (1024 + 4 * 4096 * 1024 + 4 * 4096 * 1024 + small_slots * 256 * 66 * 4)
+    small_mlp = 1024 + 4 * 4096 * 1024 + 2 * 4096 * 1024 + 2 * 4096 * 2816
+    assert small_attn < small_mlp
+    assert small.workspace_bytes() == (small_mlp
                                        + gemm_region(4096, 1024, 2816, 4096, 4096, 2816))
 
 

@@ -199,14 +199,14 @@ def _auto_ref(inp):
 
 
 @pytest.mark.parametrize("budget_mib,sliced", [(19, False), (24, True), (30, False),
-                                               (40, True), (60, False)])
+                                               (44, True), (60, False)])
 def test_auto_planned_forward_matches_oracle(budget_mib, sliced):
     # "Proposal: Generic memory-aware streaming execution for transformer
     # models" (Automatic chunk sizing): the chosen chunks are the one new
     # thing on this path, so the auto-planned forward is checked against the
     # float64 oracle under budgets that pick different chunks, with and
     # without FFN feature slicing (ragged chunks included: T = 4096 is not a
-    # multiple of 896, 1408 or 2688)
+    # multiple of 384, 896, 1408 or 2816)
     inp = synth.make_workload("dit_T4096_D1024", seed=6)
     T, D = inp.x.shape
     budget = budget_mib * 2**20
