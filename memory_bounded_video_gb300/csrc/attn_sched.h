@@ -23,7 +23,8 @@
 // a larger position is clamped to F (correct, only slower).
 //
 // When R is small against G (few CTAs could share it), the attention takes
-// one whole unit per CTA into the shared part as well (extended split): the
+// one whole unit per CTA into the shared part as well (extended split; with
+// F = 1 that leaves no whole unit before the pieces): the
 // R + G units after the first (F - 1) G are cut into G equal ranges, each
 // longer than a unit and shorter than two, so a range is the end of one unit
 // (piece A), at most one whole unit, and the start of another (piece B), and
