@@ -3,8 +3,10 @@ units into key ranges handed from CTA to CTA must not change a bit.
 
 Each case caps the CTA count so that, at sizes that run in milliseconds, the
 remainder units are cut into chains of several ranges (ranges aligned to the
-units and ranges that straddle two of them), including a ragged last key
-tile and peaked softmax rows whose reference max moves across a hand-off.
+units and ranges that straddle two of them; in the extended split, ranges
+longer than a unit, one of them holding a whole unit between two pieces),
+including a ragged last key tile and peaked softmax rows whose reference max
+moves across a hand-off.
 The split result is compared bit for bit with the unsplit launch (one whole
 unit per CTA turn), whose agreement with the float64 oracle is checked in
 test_gpu_kernels.py, and once more here against the oracle directly."""
@@ -48,6 +50,9 @@ CASES = [
     (2048, 1000, 3, 128, 7, 6.0),    # peaked rows: the max moves after a hand-off
     (1500, 3000, 4, 64, 9, 1.0),     # ragged queries and keys, d = 64
     (4096, 4096, 2, 128, 10, 1.0),   # four aligned ranges per cut unit
+    (512, 1500, 6, 64, 5, 6.0),      # extended split: a CTA's range holds a unit's
+    (512, 1500, 6, 128, 5, 1.0),     #   end, a whole unit and another's start
+    (256, 2000, 9, 128, 7, 1.0),     # extended split with one whole unit per CTA
     (8192, 8192, 6, 128, 0, 1.0),    # all SMs: one whole unit each + a cut remainder
     (8192, 32768, 24, 128, 0, 1.0),  # the 32k-token slab of the default workload
 ]
