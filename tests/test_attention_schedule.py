@@ -71,6 +71,13 @@ CASES = [
 _rng = random.Random(11)
 CASES += [(_rng.randint(1, 400), _rng.randint(1, 40), _rng.randint(1, 40), 40)
           for _ in range(60)]
+# few units left over (where the extended split applies): U = F * G + R with
+# R small against G
+_rng2 = random.Random(12)
+for _ in range(40):
+    _g = _rng2.randint(2, 40)
+    CASES.append((_rng2.randint(1, 6) * _g + _rng2.randint(1, max(1, _g // 4)),
+                  _rng2.randint(1, 64), _g, 40))
 
 
 def by_cta(items):
