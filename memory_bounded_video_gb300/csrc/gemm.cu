@@ -146,7 +146,7 @@ struct Cfg {
     // stages deep (6 with the fp32 epilogue tile) instead of 5 beside a
     // 7-stage int8 ring.  The conversion of a stage can start only when the
     // MMA of the stage's previous use is done, and the ring's depth is what
-    // hides that chain (conversion, proxy fence, the peer's signal, the MMA
+    // hides that chain (conversion, proxy fence, the peer's arrival, the MMA
     // and its commit).
     // TMA ring: bf16: A + B; int8 one-CTA: A + int8 B; QR: A + converted B
     // (the A tile completes on the converted-B barrier, so the MMA issuer
