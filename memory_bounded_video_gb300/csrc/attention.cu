@@ -8,9 +8,10 @@
 //
 // Persistent: one CTA per SM works through a list of (unit, key range)
 // items (attn_sched.h), where a unit is one head and one pair of query tiles;
-// the last, partial wave of units is cut into key ranges shared by all CTAs,
-// handing the softmax state from CTA to CTA, so that every SM gets the same
-// number of key tiles.
+// the last, partial wave of units (with one more whole unit per CTA when few
+// are left over) is cut into key ranges shared by the CTAs, handing the
+// softmax state from CTA to CTA, so that every SM gets about the same number
+// of key tiles.
 //
 // Roles (384 threads):
 //   warp 0        TMA: per item both Q tiles, then K_j and V_j^T tiles
@@ -24,14 +25,16 @@
 //   warps 4..7    softmax of tile A, one query row per thread
 //   warps 8..11   softmax of tile B
 // Softmax per key tile: the S row into registers (one tensor-memory load
-// latency for the whole tile), its max, P = exp2(S*log2e/sqrt(d) - m) as
-// bf16 written back into the first 64 columns of the same TMEM region (P is
-// the A operand of the PV MMA, read straight from tensor memory, so P never
-// touches shared memory), the running sum l.  The reference max m is only
-// moved when the tile max exceeds it by more than 8 (log2 units); then the
-// row of O is rescaled in TMEM.  Otherwise P may reach 2^8, which bf16 and the fp32
-// accumulator represent without loss of range; O / l is unchanged in exact
-// arithmetic.
+// latency for the whole tile), P = exp2(S*log2e/sqrt(d) - m) against the
+// running reference max m as bf16 written back into the first 64 columns of
+// the same TMEM region (P is the A operand of the PV MMA, read straight from
+// tensor memory, so P never touches shared memory), the running sum l.  The
+// reference max m is only moved when the tile max exceeds it by more than 8
+// (log2 units); then the row of O is rescaled in TMEM and the tile's P
+// recomputed.  The tile max is taken only where it can matter: a row whose
+// probabilities sum to at most 2^8 has no score above m + 8.  Otherwise P may
+// reach 2^8, which bf16 and the fp32 accumulator represent without loss of
+// range; O / l is unchanged in exact arithmetic.
 //
 // V arrives transposed (V^T [H*d, T], written so by the K/V projection's
 // epilogue), which makes both MMAs K-major in both operands.
