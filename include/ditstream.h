@@ -162,9 +162,10 @@ DIT_API dit_status_t dit_block_plan_info(const dit_plan_t *plan, int64_t *T, int
  * each region rounded up to 1 KiB, plus the LoRA regions when the plan has a
  * LoRA rank (dit_block_plan_set_lora_rank).  The attention's hand-off state
  * is that of dit_attention_ex: slots x 1024 * (head_dim + 2) bytes, slots the
- * most CTAs that would share the partial last wave of ceil(C_a / 256) * heads
- * units on a device of 128 to 160 multiprocessors (0 when no such device
- * would split; at most 160).  The GEMMs' is that of dit_gemm_ex: 128 KiB per
+ * most CTAs that would share the split part (the partial last wave, or with
+ * the extended split one range per CTA) of ceil(C_a / 256) * heads units on
+ * a device of 128 to 160 multiprocessors (0 when no such device would split;
+ * at most 160).  The GEMMs' is that of dit_gemm_ex: 128 KiB per
  * slot, slots the most that any of the plan's GEMM launches (K/V, Q, O,
  * gate/up, down, at full and ragged chunk and slice sizes, in either tile
  * shape) would use on such a device, at most 64.  K/V for all tokens is the floor that grows with T ("Where
@@ -585,10 +586,11 @@ DIT_API dit_status_t dit_attention(const void *q, int64_t Tq, int64_t ldq,
 
 /* dit_attention with the persistent kernel's work split.  The (query pair,
  * head) units of a launch are spread over at most max_ctas CTAs (0: one per
- * multiprocessor); the units that would form a last, partial wave are cut
- * into key ranges shared by all CTAs, each range continuing the running max,
- * sum and fp32 output of the range before it, so that every CTA gets the
- * same number of key tiles.  Key tiles are still visited in ascending order
+ * multiprocessor); the units that would form a last, partial wave (and,
+ * when few are left over, one more whole unit per CTA) are cut into key
+ * ranges shared by the CTAs, each range continuing the running max, sum and
+ * fp32 output of the range before it, so that every CTA gets about the same
+ * number of key tiles.  Key tiles are still visited in ascending order
  * with the same arithmetic: the result equals dit_attention bit for bit.
  * split_ws: device memory of dit_attention_split_bytes(head_dim, slots)
  * bytes, 16-byte aligned, zero before its first use (the call leaves it so
